@@ -1,0 +1,174 @@
+"""CPU float64 oracle for fused softmax cross-entropy.
+
+TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the
+benchmark's CPU-baseline leg may import this package. The CUDA library never
+links or calls it, and this package imports nothing from the CUDA library:
+the two share no code. The arithmetic lives in ``ce_oracle.c`` (plain C,
+double precision, single-threaded); this module compiles it with gcc and
+marshals numpy arrays in and out.
+
+Logit storage: ``"f64"``, ``"f32"``, or ``"bf16"`` given as the raw uint16
+bit patterns (the oracle decodes them exactly).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ce_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libceoracle.so")
+
+_DTYPES = {"f64": 0, "f32": 1, "bf16": 2}
+_NP_STORAGE = {"f64": np.float64, "f32": np.float32, "bf16": np.uint16}
+REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compiles ce_oracle.c into a shared object next to it (no fast-math:
+    IEEE double semantics are part of the oracle's definition)."""
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off",
+             "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"],
+            check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i64 = ctypes.c_int64
+            d = ctypes.c_double
+            lib.orc_ce_forward.argtypes = [P, ctypes.c_int, i64, i64, P, P, i64, d, d, d,
+                                           ctypes.c_int, P, P, P, P, P]
+            lib.orc_ce_forward.restype = ctypes.c_int
+            lib.orc_ce_rows.argtypes = [P, ctypes.c_int, i64, i64, P, P, i64, d, d, d,
+                                        ctypes.c_int, P, i64, P, P, P, P, P, P, P]
+            lib.orc_ce_rows.restype = ctypes.c_int
+            lib.orc_ce_backward.argtypes = [P, i64, i64, P, ctypes.c_int]
+            lib.orc_ce_backward.restype = None
+            lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.orc_bf16_to_double.restype = d
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _prep(x, dtype, target, weight):
+    if dtype not in _DTYPES:
+        raise ValueError(f"unknown logit storage {dtype!r}")
+    x = np.ascontiguousarray(x, dtype=_NP_STORAGE[dtype])
+    if x.ndim != 2:
+        raise ValueError("logits must be 2-D (rows, V)")
+    target = np.ascontiguousarray(target, dtype=np.int64).reshape(-1)
+    if target.shape[0] != x.shape[0]:
+        raise ValueError("target must have one entry per row")
+    if weight is not None:
+        weight = np.ascontiguousarray(weight, dtype=np.float64).reshape(-1)
+        if weight.shape[0] != x.shape[1]:
+            raise ValueError("weight must have V entries")
+    return x, target, weight
+
+
+def _check(rc):
+    if rc == 1:
+        raise OracleError("invalid argument")
+    if rc == 2:
+        raise OracleError("target out of range")
+    if rc != 0:
+        raise OracleError(f"oracle error {rc}")
+
+
+def forward(x, target, *, dtype="f64", weight=None, ignore_index=-100,
+            label_smoothing=0.0, lse_square_scale=0.0, softcap=None,
+            reduction="mean", want_grad=True):
+    """Whole-batch forward. Returns a dict with ``loss``, ``z_loss``, ``acc``
+    (scalars, or [rows] arrays for reduction "none"), ``pred`` [rows] int64
+    and ``grad`` [rows, V] float64 (the gradient of the reduced loss with
+    respect to the logits) or None."""
+    lib = _load()
+    x, target, weight = _prep(x, dtype, target, weight)
+    rows, V = x.shape
+    red = REDUCTIONS[reduction]
+    n_out = rows if red == 0 else 1
+    loss = np.zeros(n_out, np.float64)
+    zl = np.zeros(n_out, np.float64)
+    acc = np.zeros(n_out, np.float64)
+    pred = np.zeros(rows, np.int64)
+    grad = np.empty((rows, V), np.float64) if want_grad else None
+    rc = lib.orc_ce_forward(_ptr(x), _DTYPES[dtype], rows, V, _ptr(target), _ptr(weight),
+                            int(ignore_index), float(label_smoothing),
+                            float(lse_square_scale),
+                            float(softcap) if softcap is not None else 0.0, red,
+                            _ptr(loss), _ptr(zl), _ptr(acc), _ptr(pred), _ptr(grad))
+    _check(rc)
+    if red != 0:
+        loss, zl, acc = loss[0], zl[0], acc[0]
+    return {"loss": loss, "z_loss": zl, "acc": acc, "pred": pred, "grad": grad}
+
+
+def rows(x, target, row_idx, *, dtype="f64", weight=None, ignore_index=-100,
+         label_smoothing=0.0, lse_square_scale=0.0, softcap=None,
+         reduction="mean", want_grad=True):
+    """Selected rows of a batch: per-row (unreduced) loss, z-loss, pred,
+    0/1 correctness and the reduction-scaled gradient rows, plus the batch
+    denominators ``D`` and ``n_valid``."""
+    lib = _load()
+    x, target, weight = _prep(x, dtype, target, weight)
+    nrows, V = x.shape
+    idx = np.ascontiguousarray(row_idx, dtype=np.int64).reshape(-1)
+    k = idx.shape[0]
+    loss = np.zeros(k, np.float64)
+    zl = np.zeros(k, np.float64)
+    pred = np.zeros(k, np.int64)
+    corr = np.zeros(k, np.float64)
+    grad = np.empty((k, V), np.float64) if want_grad else None
+    D = ctypes.c_double(0.0)
+    nv = ctypes.c_int64(0)
+    rc = lib.orc_ce_rows(_ptr(x), _DTYPES[dtype], nrows, V, _ptr(target), _ptr(weight),
+                         int(ignore_index), float(label_smoothing),
+                         float(lse_square_scale),
+                         float(softcap) if softcap is not None else 0.0,
+                         REDUCTIONS[reduction], _ptr(idx), k, _ptr(loss), _ptr(zl),
+                         _ptr(pred), _ptr(corr), _ptr(grad), ctypes.byref(D),
+                         ctypes.byref(nv))
+    _check(rc)
+    return {"loss": loss, "z_loss": zl, "pred": pred, "correct": corr, "grad": grad,
+            "D": D.value, "n_valid": nv.value}
+
+
+def backward(grad, grad_output):
+    """Scales a stored gradient in place by grad_output: a scalar, or one
+    value per row."""
+    lib = _load()
+    grad = np.ascontiguousarray(grad, dtype=np.float64)
+    go = np.ascontiguousarray(np.atleast_1d(grad_output), dtype=np.float64)
+    per_row = 1 if go.shape[0] == grad.shape[0] and go.shape[0] != 1 else 0
+    lib.orc_ce_backward(_ptr(grad), grad.shape[0], grad.shape[1], _ptr(go), per_row)
+    return grad
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().orc_bf16_to_double(int(bits) & 0xFFFF)
