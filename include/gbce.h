@@ -1,0 +1,162 @@
+/*
+ * gbce.h - C ABI of the GB300 fused softmax cross-entropy library
+ * (libgbce.so, built for sm_103a).
+ *
+ * One call computes, for every row i of a (rows, V) logit matrix x, the
+ * cross-entropy loss against an integer target, and (optionally) writes the
+ * gradient of the reduced loss in place over x. Backward then only scales
+ * the stored gradient by grad_output.
+ *
+ * Definitions followed (page title, section):
+ *  - "Kernel Profile: CrossEntropy (Tier 3 - Fused/Complex)" (Liger-Kernel),
+ *    §Forward Pass: inputs _input (B*T, V), target (B*T,), weight (V,) or
+ *    none, ignore_index, label_smoothing, reduction "mean" | "sum" | "none",
+ *    softcap; outputs loss (scalar, or (B*T,) for "none"), z_loss,
+ *    token_accuracy, predicted_tokens; exp and log run in fp32.
+ *    §Backward Pass: the gradient is computed during the forward and stored
+ *    in the _input tensor; backward scales it by grad_output.
+ *    §Module Parameters: ignore_index = -100 by default, lse_square_scale.
+ *    §Key Patterns: max-shifted log-sum-exp; the loss combines CE, the
+ *    label-smoothing loss and the z-loss, each contributing to the gradient.
+ *  - tenstorrent/tt-mlir pull request #9324 "[tt-crank] fuse cross entropy
+ *    onto the ttml cross_entropy_fw/bw composites", review comments: the
+ *    mean divides by total_weight; a batch whose rows are all ignored keeps
+ *    the NaN forward loss and gets exactly zero gradients.
+ *
+ * Per row, with z = softcap(x) = s * tanh(x / s) (s > 0) or z = x,
+ * lse = log sum_j exp(z_j), p = exp(z - lse), target t, class weights w
+ * (all 1 when weight is NULL), W = sum_j w_j, eps = label_smoothing and
+ * lam = lse_square_scale:
+ *
+ *   loss_i = (1 - eps) * w_t * (lse - z_t)
+ *          + (eps / V) * sum_j w_j * (lse - z_j)
+ *          + lam * lse^2                         (z_loss_i = lam * lse^2)
+ *   dlogits_ik = scale * [ (1 - eps) * w_t * (p_k - [k == t])
+ *                        + (eps / V) * (W * p_k - w_k)
+ *                        + 2 * lam * lse * p_k ] * dz_k/dx_k
+ *
+ * with scale = 1 / D for "mean" and 1 otherwise, D = sum of w_{t_i} over the
+ * rows whose target is not ignore_index. A row whose target equals
+ * ignore_index has loss 0, z_loss 0, predicted token -1 and a gradient of
+ * exact +0; its logits are never read. Reductions: "sum" adds the rows,
+ * "mean" divides the sums by D (so a batch with every row ignored gives a
+ * NaN loss, NaN z_loss and zero gradients), "none" returns per-row values.
+ * Accuracy is n_correct / n_valid for "sum"/"mean" (NaN with no valid row)
+ * and a 0/1 value per row for "none"; a row is correct when its argmax
+ * (over the raw logits, lowest index on ties) equals its target.
+ *
+ * Arithmetic: fp32 in registers for every input dtype; gradients are
+ * rounded to nearest-even into the logit dtype. Partial sums of the scalar
+ * outputs are combined in a fixed order, so results are run-to-run
+ * deterministic.
+ *
+ * Threading and streams: every call is asynchronous on `stream` (NULL is
+ * the legacy default stream). All pointers are device pointers owned by
+ * the caller. The library keeps a small scratch area per (device, stream),
+ * allocated with cudaMalloc on the first call for that pair and kept until
+ * the process exits; make that first call outside any CUDA graph capture.
+ * Calls on the same stream are ordered; calls on different streams use
+ * different scratch areas.
+ */
+#ifndef GBCE_H
+#define GBCE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* ce_stream_t;
+
+typedef enum {
+    CE_OK = 0,
+    CE_ERR_INVALID_ARG = 1,   /* argument check failed; nothing was enqueued */
+    CE_ERR_UNSUPPORTED = 2,   /* valid arguments outside what is implemented */
+    CE_ERR_CUDA = 3,          /* a CUDA runtime call failed (see ce_last_error) */
+    CE_ERR_TARGET_RANGE = 4,  /* the device saw a target outside [0, V) that is not ignore_index */
+    CE_ERR_TIMEOUT = 5        /* a bounded device wait gave up; that call's outputs are invalid */
+} ce_status;
+
+typedef enum { CE_F32 = 0, CE_BF16 = 1 } ce_dtype;
+
+typedef enum { CE_RED_NONE = 0, CE_RED_SUM = 1, CE_RED_MEAN = 2 } ce_reduction;
+
+enum {
+    CE_FLAG_GRAD = 1,        /* write dlogits in place over logits */
+    CE_FLAG_Z_LOSS = 2,      /* write z_loss */
+    CE_FLAG_ACC = 4,         /* write token accuracy to acc */
+    CE_FLAG_PRED = 8,        /* write predicted tokens to pred */
+    CE_FLAG_TARGET_I64 = 16  /* target is int64 (default int32) */
+};
+
+/*
+ * ce_fwd - fused forward (and, with CE_FLAG_GRAD, the in-forward gradient).
+ *
+ * logits       [rows, V] row-major, dtype `dtype` (CE_F32 or CE_BF16). With
+ *              CE_FLAG_GRAD it is overwritten by dlogits (d loss / d logits
+ *              of the reduced loss; for "none", of the sum of the row
+ *              losses). The fast path needs a 16-byte aligned base and
+ *              V * sizeof(dtype) a multiple of 16; other shapes take a
+ *              slower general path with the same results.
+ * rows, V      rows >= 0, 1 <= V < 2^31.
+ * target       [rows] int32 (int64 with CE_FLAG_TARGET_I64). A value equal
+ *              to ignore_index marks an ignored row. A value outside [0, V)
+ *              that is not ignore_index is an error: that row is treated as
+ *              ignored and CE_ERR_TARGET_RANGE is recorded for
+ *              ce_device_status.
+ * weight       [V] fp32 class weights, or NULL for all ones.
+ * label_smoothing   in [0, 1].
+ * lse_square_scale  finite; 0 turns the z-loss term off.
+ * softcap      0 turns softcapping off; > 0 is the cap s; negative or
+ *              non-finite values are invalid.
+ * reduction    CE_RED_NONE, CE_RED_SUM or CE_RED_MEAN.
+ * flags        CE_FLAG_* bits.
+ * loss         fp32, [rows] for CE_RED_NONE else [1]. Required.
+ * z_loss       same shape as loss; required with CE_FLAG_Z_LOSS.
+ * acc          same shape as loss; required with CE_FLAG_ACC.
+ * pred         [rows] int64 (-1 on ignored rows); required with CE_FLAG_PRED.
+ * stream       CUDA stream of the launch.
+ *
+ * rows == 0: "mean" writes NaN to loss (and z_loss), "sum" writes 0, acc
+ * gets NaN. Returns CE_OK when the work was enqueued; CE_ERR_INVALID_ARG or
+ * CE_ERR_UNSUPPORTED with nothing enqueued; CE_ERR_CUDA on a failed launch.
+ */
+ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V,
+                 const void* target, const float* weight, int64_t ignore_index,
+                 float label_smoothing, float lse_square_scale, float softcap,
+                 int reduction, uint32_t flags, float* loss, float* z_loss,
+                 float* acc, int64_t* pred, ce_stream_t stream);
+
+/*
+ * ce_bwd - backward (§Backward Pass: the stored gradient times
+ * grad_output): dlogits *= grad_output, in place.
+ *
+ * grad_output  fp32 device pointer: one value (grad_per_row == 0) or one per
+ *              row (grad_per_row != 0, for reduction "none").
+ * dlogits      [rows, V] in dtype, the buffer ce_fwd wrote with CE_FLAG_GRAD.
+ * The kernel reads grad_output on the device; rows whose factor is exactly
+ * 1.0 are left untouched, since multiplying by one changes nothing.
+ */
+ce_status ce_bwd(const float* grad_output, int grad_per_row, void* dlogits,
+                 int dtype, int64_t rows, int64_t V, ce_stream_t stream);
+
+/*
+ * ce_device_status - synchronizes `stream`, then reads and clears the
+ * device-side error word of that stream's scratch area. Returns CE_OK,
+ * CE_ERR_TARGET_RANGE, CE_ERR_TIMEOUT or CE_ERR_CUDA.
+ */
+ce_status ce_device_status(ce_stream_t stream);
+
+/* Static text for a status code. */
+const char* ce_status_string(ce_status status);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char* ce_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBCE_H */

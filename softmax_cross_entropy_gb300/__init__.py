@@ -1,0 +1,183 @@
+"""GB300-native fused softmax cross-entropy (forward + in-forward gradient).
+
+    loss = cross_entropy(logits, target, weight=None, ignore_index=-100,
+                         lse_square_scale=0.0, label_smoothing=0.0,
+                         reduction="mean", softcap=None, return_z_loss=False,
+                         return_token_accuracy=False,
+                         return_predicted_tokens=False)
+
+The arguments and outputs are those of the Liger-Kernel cross-entropy kernel
+profile (§Forward Pass, §Module Parameters). ``logits`` is a 2-D (B*T, V)
+CUDA tensor in float32 or bfloat16; ``target`` holds int32 or int64 labels.
+When ``logits.requires_grad`` the forward writes the gradient of the reduced
+loss over ``logits`` itself (§Backward Pass: the gradient-in-forward trick),
+so the logits' values are gone after the call and backward only scales that
+buffer by grad_output. Every step runs in the CUDA kernels of libgbce.so
+(see include/gbce.h); PyTorch supplies device memory, streams and autograd.
+"""
+from __future__ import annotations
+
+from collections import namedtuple
+
+import torch
+
+from . import _lib
+from ._lib import CEError, ce_bwd, ce_device_status, ce_fwd, ce_last_error, ce_status_string
+
+__all__ = ["cross_entropy", "CrossEntropyLoss", "CrossEntropyFunction", "CrossEntropyOutput",
+           "CEError", "device_status", "ce_fwd", "ce_bwd", "ce_device_status",
+           "ce_status_string", "ce_last_error"]
+
+CrossEntropyOutput = namedtuple("CrossEntropyOutput",
+                                ["loss", "z_loss", "token_accuracy", "predicted_tokens"])
+
+_REDUCTIONS = {"none": _lib.CE_RED_NONE, "sum": _lib.CE_RED_SUM, "mean": _lib.CE_RED_MEAN}
+_DTYPES = {torch.float32: _lib.CE_F32, torch.bfloat16: _lib.CE_BF16}
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_inputs(logits, target, weight):
+    if not isinstance(logits, torch.Tensor) or logits.dim() != 2:
+        raise ValueError("logits must be a 2-D (B*T, V) tensor; flatten the batch dimensions "
+                         "first (class dimension last)")
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor")
+    if logits.dtype not in _DTYPES:
+        raise TypeError(f"logits dtype {logits.dtype} is not supported (float32, bfloat16)")
+    if target.dim() != 1 or target.shape[0] != logits.shape[0]:
+        raise ValueError("target must be 1-D with one label per row of logits")
+    if target.dtype not in (torch.int32, torch.int64):
+        raise TypeError("target must be int32 or int64")
+    if target.device != logits.device:
+        raise ValueError("target must be on the logits' device")
+    if weight is not None:
+        if weight.dim() != 1 or weight.shape[0] != logits.shape[1]:
+            raise ValueError("weight must have shape (V,)")
+        if weight.device != logits.device:
+            raise ValueError("weight must be on the logits' device")
+
+
+def _forward(logits, target, weight, ignore_index, lse_square_scale, label_smoothing,
+             reduction, softcap, want_grad, want_z, want_acc, want_pred):
+    """Runs ce_fwd; returns (loss, z_loss, acc, pred). Writes dlogits over
+    logits when want_grad."""
+    rows, V = logits.shape
+    dev = logits.device
+    red = _REDUCTIONS[reduction]
+    out_shape = (rows,) if red == _lib.CE_RED_NONE else ()
+    f32 = dict(dtype=torch.float32, device=dev)
+    loss = torch.empty(out_shape, **f32)
+    z_loss = torch.empty(out_shape, **f32) if want_z else None
+    acc = torch.empty(out_shape, **f32) if want_acc else None
+    pred = torch.empty((rows,), dtype=torch.int64, device=dev) if want_pred else None
+    flags = ((_lib.CE_FLAG_GRAD if want_grad else 0) | (_lib.CE_FLAG_Z_LOSS if want_z else 0) |
+             (_lib.CE_FLAG_ACC if want_acc else 0) | (_lib.CE_FLAG_PRED if want_pred else 0) |
+             (_lib.CE_FLAG_TARGET_I64 if target.dtype == torch.int64 else 0))
+    w = None if weight is None else weight.to(torch.float32).contiguous()
+    with torch.cuda.device(dev):
+        rc = ce_fwd(_ptr(logits), _DTYPES[logits.dtype], rows, V, _ptr(target), _ptr(w),
+                    int(ignore_index), float(label_smoothing), float(lse_square_scale),
+                    float(softcap) if softcap is not None else 0.0, red, flags, _ptr(loss),
+                    _ptr(z_loss), _ptr(acc), _ptr(pred), _stream(dev))
+    if rc != _lib.CE_OK:
+        raise CEError(rc, "ce_fwd")
+    return loss, z_loss, acc, pred
+
+
+class CrossEntropyFunction(torch.autograd.Function):
+    """Autograd wrapper: forward stores the gradient in the logits buffer;
+    backward scales it by grad_output (ce_bwd) and returns that buffer."""
+
+    @staticmethod
+    def forward(ctx, logits, target, weight, ignore_index, lse_square_scale, label_smoothing,
+                reduction, softcap, return_z_loss, return_acc, return_pred):
+        want_grad = logits.requires_grad
+        loss, z_loss, acc, pred = _forward(logits, target, weight, ignore_index,
+                                           lse_square_scale, label_smoothing, reduction,
+                                           softcap, want_grad, return_z_loss, return_acc,
+                                           return_pred)
+        ctx.reduction = reduction
+        if want_grad:
+            ctx.save_for_backward(logits.detach())  # now holds dlogits
+        extras = [t for t in (z_loss, acc, pred) if t is not None]
+        if extras:
+            ctx.mark_non_differentiable(*extras)
+        return loss, z_loss, acc, pred
+
+    @staticmethod
+    def backward(ctx, grad_loss, *unused):
+        (dlogits,) = ctx.saved_tensors
+        rows, V = dlogits.shape
+        g = grad_loss.to(torch.float32).contiguous()
+        per_row = 1 if ctx.reduction == "none" else 0
+        with torch.cuda.device(dlogits.device):
+            rc = ce_bwd(_ptr(g), per_row, _ptr(dlogits), _DTYPES[dlogits.dtype], rows, V,
+                        _stream(dlogits.device))
+        if rc != _lib.CE_OK:
+            raise CEError(rc, "ce_bwd")
+        return dlogits, None, None, None, None, None, None, None, None, None, None
+
+
+def cross_entropy(logits, target, weight=None, ignore_index=-100, lse_square_scale=0.0,
+                  label_smoothing=0.0, reduction="mean", softcap=None, return_z_loss=False,
+                  return_token_accuracy=False, return_predicted_tokens=False):
+    """Fused softmax cross-entropy. Returns the loss tensor, or a
+    CrossEntropyOutput(loss, z_loss, token_accuracy, predicted_tokens) when
+    any return_* flag is set (unrequested fields are None)."""
+    _check_inputs(logits, target, weight)
+    if reduction not in _REDUCTIONS:
+        raise ValueError(f"reduction must be one of {sorted(_REDUCTIONS)}")
+    if not 0.0 <= label_smoothing <= 1.0:
+        raise ValueError("label_smoothing must lie in [0, 1]")
+    if softcap is not None and not softcap > 0:
+        raise ValueError("softcap must be positive or None")
+    if not logits.is_contiguous():
+        logits = logits.contiguous()
+    target = target.contiguous()
+    loss, z_loss, acc, pred = CrossEntropyFunction.apply(
+        logits, target, weight, ignore_index, lse_square_scale, label_smoothing, reduction,
+        softcap, return_z_loss, return_token_accuracy, return_predicted_tokens)
+    if return_z_loss or return_token_accuracy or return_predicted_tokens:
+        return CrossEntropyOutput(loss, z_loss, acc, pred)
+    return loss
+
+
+class CrossEntropyLoss(torch.nn.Module):
+    """Module form of cross_entropy with the profile's constructor
+    parameters (§Module Parameters)."""
+
+    def __init__(self, weight=None, ignore_index=-100, lse_square_scale=0.0,
+                 label_smoothing=0.0, reduction="mean", softcap=None, return_z_loss=False,
+                 return_token_accuracy=False, return_predicted_tokens=False):
+        super().__init__()
+        self.weight = weight
+        self.ignore_index = ignore_index
+        self.lse_square_scale = lse_square_scale
+        self.label_smoothing = label_smoothing
+        self.reduction = reduction
+        self.softcap = softcap
+        self.return_z_loss = return_z_loss
+        self.return_token_accuracy = return_token_accuracy
+        self.return_predicted_tokens = return_predicted_tokens
+
+    def forward(self, logits, target):
+        return cross_entropy(logits, target, self.weight, self.ignore_index,
+                             self.lse_square_scale, self.label_smoothing, self.reduction,
+                             self.softcap, self.return_z_loss, self.return_token_accuracy,
+                             self.return_predicted_tokens)
+
+
+def device_status(device=None) -> int:
+    """Synchronizes the current stream of `device` and returns (and clears)
+    the library's device-side error status for it (CE_OK when clean)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+        torch.device(device)
+    with torch.cuda.device(dev):
+        return ce_device_status(_stream(dev))

@@ -1,0 +1,82 @@
+"""ctypes binding of libgbce.so: the C ABI declared in include/gbce.h, under
+the same names, taking integers for device pointers and streams. Argument
+marshalling only; every step of the computation runs in the library's CUDA
+kernels. There is no fallback: loading fails loudly if the library has not
+been built (``python -m softmax_cross_entropy_gb300.build``)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgbce.so")
+
+CE_OK, CE_ERR_INVALID_ARG, CE_ERR_UNSUPPORTED, CE_ERR_CUDA, CE_ERR_TARGET_RANGE, \
+    CE_ERR_TIMEOUT = range(6)
+CE_F32, CE_BF16 = 0, 1
+CE_RED_NONE, CE_RED_SUM, CE_RED_MEAN = 0, 1, 2
+CE_FLAG_GRAD, CE_FLAG_Z_LOSS, CE_FLAG_ACC, CE_FLAG_PRED, CE_FLAG_TARGET_I64 = 1, 2, 4, 8, 16
+
+# (name, restype, argtypes) for every symbol include/gbce.h declares
+_P, _I, _I64, _U32, _F = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32,
+                          ctypes.c_float)
+SIGNATURES = {
+    "ce_fwd": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P, _P, _P, _P]),
+    "ce_bwd": (_I, [_P, _I, _P, _I, _I64, _I64, _P]),
+    "ce_device_status": (_I, [_P]),
+    "ce_status_string": (ctypes.c_char_p, [_I]),
+    "ce_last_error": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = load()
+        msg = lib.ce_status_string(status).decode()
+        detail = lib.ce_last_error().decode()
+        super().__init__(f"{where}: {msg}" + (f" ({detail})" if detail else ""))
+        self.status = status
+
+
+def load():
+    """Loads libgbce.so once and declares its signatures."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build the CUDA library first with "
+                    "`python -m softmax_cross_entropy_gb300.build`")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def ce_fwd(logits, dtype, rows, V, target, weight, ignore_index, label_smoothing,
+           lse_square_scale, softcap, reduction, flags, loss, z_loss, acc, pred, stream):
+    return load().ce_fwd(logits, dtype, rows, V, target, weight, ignore_index,
+                         label_smoothing, lse_square_scale, softcap, reduction, flags,
+                         loss, z_loss, acc, pred, stream)
+
+
+def ce_bwd(grad_output, grad_per_row, dlogits, dtype, rows, V, stream):
+    return load().ce_bwd(grad_output, grad_per_row, dlogits, dtype, rows, V, stream)
+
+
+def ce_device_status(stream):
+    return load().ce_device_status(stream)
+
+
+def ce_status_string(status):
+    return load().ce_status_string(status).decode()
+
+
+def ce_last_error():
+    return load().ce_last_error().decode()

@@ -1,0 +1,392 @@
+// C ABI of libgbce.so: argument checks, library-owned scratch, the choice
+// of kernel variant and launch shape, and the launches themselves. The
+// definitions the calls implement are stated in include/gbce.h.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "ce_kernels.cuh"
+#include "gbce.h"
+
+namespace gbce {
+namespace {
+
+thread_local std::string g_last_error;
+
+ce_status cuda_failure(cudaError_t e, const char* what) {
+    g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return CE_ERR_CUDA;
+}
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int smem_per_sm = 0;
+    int smem_optin = 0;
+};
+
+// A launch plan for one (device, dtype, V, variant): which kernel, how many
+// CTAs per row, ring depth, dynamic shared memory and the resident grid.
+struct Plan {
+    const void* fn = nullptr;
+    bool staged = false;
+    int nt = 0;
+    int cluster = 1;
+    int stages = 0;
+    int slice_vec = 0;
+    size_t smem = 0;
+    int64_t max_units = 0;  // resident CTAs (cluster == 1) or clusters
+};
+
+using PlanKey = std::tuple<int, int, int64_t, bool, bool, int>;
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::pair<int, uintptr_t>, Scratch*> g_scratch;
+std::map<PlanKey, Plan> g_plans;
+
+int env_int(const char* name, int fallback) {
+    const char* v = std::getenv(name);
+    return (v && *v) ? std::atoi(v) : fallback;
+}
+
+ce_status device_info(int dev, DeviceInfo* out) {
+    auto it = g_devices.find(dev);
+    if (it != g_devices.end()) {
+        *out = it->second;
+        return CE_OK;
+    }
+    DeviceInfo d;
+    cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaDeviceGetAttribute");
+    g_devices[dev] = d;
+    *out = d;
+    return CE_OK;
+}
+
+// Scratch for (device, stream): allocated and zeroed on first use, on the
+// caller's stream so the zeroing is ordered before the first kernel.
+ce_status scratch_for(int dev, cudaStream_t st, Scratch** out) {
+    const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(st));
+    auto it = g_scratch.find(key);
+    if (it != g_scratch.end()) {
+        *out = it->second;
+        return CE_OK;
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, kScratchBytes);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaMalloc(scratch)");
+    e = cudaMemsetAsync(p, 0, kScratchBytes, st);
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        return cuda_failure(e, "cudaMemsetAsync(scratch)");
+    }
+    g_scratch[key] = static_cast<Scratch*>(p);
+    *out = static_cast<Scratch*>(p);
+    return CE_OK;
+}
+
+const void* staged_fn(int dtype, int cfg, bool softcap, bool wsmooth) {
+    if (dtype == CE_BF16)
+        return softcap ? staged_kernel_bf16_softcap(cfg, wsmooth)
+                       : staged_kernel_bf16_plain(cfg, wsmooth);
+    return softcap ? staged_kernel_f32_softcap(cfg, wsmooth) : staged_kernel_f32_plain(cfg, wsmooth);
+}
+
+// Tries the staged kernel with `C` CTAs per row. Returns false when the
+// shape does not fit (then the caller tries another C or the general path).
+bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, const DeviceInfo& dev,
+                Plan* out, ce_status* err) {
+    const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
+    const int64_t ve = 16 / bytes;
+    const int64_t vec_row = V / ve;
+    const int64_t per = (vec_row + C - 1) / C;
+    if (C > 1 && per * (C - 1) >= vec_row) return false;  // a CTA would own nothing
+    int cfg = -1;
+    for (int i = 0; i < kNumStagedCfgs; ++i)
+        if (static_cast<int64_t>(kStagedCfgs[i].nt) * kStagedCfgs[i].nv >= per) {
+            cfg = i;
+            break;
+        }
+    if (cfg < 0) return false;
+    const void* fn = staged_fn(dtype, cfg, softcap, wsmooth);
+    if (!fn) return false;
+    const int nt = kStagedCfgs[cfg].nt;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) {
+        *err = cuda_failure(e, "cudaFuncGetAttributes");
+        return false;
+    }
+    const size_t stage_bytes = static_cast<size_t>(per) * 16;
+    const size_t wbytes = wsmooth ? static_cast<size_t>(per) * ve * 4 : 0;
+    const size_t max_dyn = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
+    if (2 * stage_bytes + wbytes > max_dyn) return false;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(max_dyn));
+    if (e != cudaSuccess) {
+        *err = cuda_failure(e, "cudaFuncSetAttribute");
+        return false;
+    }
+    // Largest occupancy the registers allow, then the deepest ring that keeps it.
+    int occ2 = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, fn, nt, 2 * stage_bytes + wbytes);
+    if (e != cudaSuccess) {
+        *err = cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        return false;
+    }
+    if (occ2 < 1) return false;
+    int stages = 2;
+    const int max_stages = std::min(kMaxStages, env_int("GBCE_MAX_STAGES", kMaxStages));
+    for (int s = 3; s <= max_stages; ++s) {
+        const size_t dyn = s * stage_bytes + wbytes;
+        if (dyn > max_dyn) break;
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, nt, dyn) != cudaSuccess ||
+            occ < occ2)
+            break;
+        stages = s;
+    }
+    const size_t smem = stages * stage_bytes + wbytes;
+    int64_t units = static_cast<int64_t>(occ2) * dev.sm_count;
+    if (C > 1) {
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(static_cast<unsigned>(C * dev.sm_count));
+        lc.blockDim = dim3(static_cast<unsigned>(nt));
+        lc.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(C);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        lc.attrs = &attr;
+        lc.numAttrs = 1;
+        int ncl = 0;
+        e = cudaOccupancyMaxActiveClusters(&ncl, fn, &lc);
+        if (e != cudaSuccess) {
+            *err = cuda_failure(e, "cudaOccupancyMaxActiveClusters");
+            return false;
+        }
+        if (ncl < 1) return false;
+        units = ncl;
+    }
+    units = std::min<int64_t>(units, kMaxPartials);
+    out->fn = fn;
+    out->staged = true;
+    out->nt = nt;
+    out->cluster = C;
+    out->stages = stages;
+    out->slice_vec = static_cast<int>(per);
+    out->smem = smem;
+    out->max_units = units;
+    return true;
+}
+
+ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth, bool aligned,
+                    Plan* out) {
+    const int forced = env_int("GBCE_CLUSTER", 0);  // tuning: force CTAs per row (1,2,4,8)
+    const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth, forced);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) {
+        *out = it->second;
+        return CE_OK;
+    }
+    DeviceInfo dev;
+    ce_status rc = device_info(devid, &dev);
+    if (rc != CE_OK) return rc;
+    Plan p;
+    const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
+    if (aligned && (V * bytes) % 16 == 0 && forced >= 0) {
+        for (int C : {1, 2, 4, 8}) {
+            if (forced && C != forced) continue;
+            rc = CE_OK;
+            if (try_staged(dtype, V, softcap, wsmooth, C, dev, &p, &rc)) break;
+            if (rc != CE_OK) return rc;
+        }
+    }
+    if (!p.staged) {
+        p.fn = generic_kernel(dtype, softcap);
+        p.nt = kGenericThreads;
+        p.max_units = std::min<int64_t>(static_cast<int64_t>(dev.sm_count) * 8, kMaxPartials);
+    }
+    g_plans[key] = p;
+    *out = p;
+    return CE_OK;
+}
+
+ce_status launch(const void* fn, int grid, int nt, size_t smem, int cluster, cudaStream_t st,
+                 void* arg) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    lc.blockDim = dim3(static_cast<unsigned>(nt));
+    lc.dynamicSmemBytes = smem;
+    lc.stream = st;
+    cudaLaunchAttribute attr;
+    if (cluster > 1) {
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        lc.attrs = &attr;
+        lc.numAttrs = 1;
+    }
+    void* args[] = {arg};
+    cudaError_t e = cudaLaunchKernelExC(&lc, fn, args);
+    if (e != cudaSuccess) return cuda_failure(e, "kernel launch");
+    return CE_OK;
+}
+
+bool finite(float v) { return std::isfinite(v); }
+
+}  // namespace
+}  // namespace gbce
+
+using namespace gbce;
+
+extern "C" ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V, const void* target,
+                            const float* weight, int64_t ignore_index, float label_smoothing,
+                            float lse_square_scale, float softcap, int reduction, uint32_t flags,
+                            float* loss, float* z_loss, float* acc, int64_t* pred,
+                            ce_stream_t stream) {
+    const uint32_t known =
+        CE_FLAG_GRAD | CE_FLAG_Z_LOSS | CE_FLAG_ACC | CE_FLAG_PRED | CE_FLAG_TARGET_I64;
+    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_INVALID_ARG;
+    if (rows < 0 || V <= 0) return CE_ERR_INVALID_ARG;
+    if (V > INT32_MAX - 16) return CE_ERR_UNSUPPORTED;
+    if (reduction != CE_RED_NONE && reduction != CE_RED_SUM && reduction != CE_RED_MEAN)
+        return CE_ERR_INVALID_ARG;
+    if (flags & ~known) return CE_ERR_INVALID_ARG;
+    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return CE_ERR_INVALID_ARG;
+    if (!finite(lse_square_scale)) return CE_ERR_INVALID_ARG;
+    if (!finite(softcap) || softcap < 0.f) return CE_ERR_INVALID_ARG;
+    if (!loss) return CE_ERR_INVALID_ARG;
+    if ((flags & CE_FLAG_Z_LOSS) && !z_loss) return CE_ERR_INVALID_ARG;
+    if ((flags & CE_FLAG_ACC) && !acc) return CE_ERR_INVALID_ARG;
+    if ((flags & CE_FLAG_PRED) && !pred) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && (!logits || !target)) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && V > INT64_MAX / rows / 4) return CE_ERR_INVALID_ARG;
+    if (rows == 0 && reduction == CE_RED_NONE) return CE_OK;  // nothing to write
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Scratch* scratch = nullptr;
+    ce_status rc = scratch_for(dev, st, &scratch);
+    if (rc != CE_OK) return rc;
+
+    FwdArgs a = {};
+    a.x = logits;
+    a.rows = rows;
+    a.V = V;
+    a.target = target;
+    a.tgt64 = (flags & CE_FLAG_TARGET_I64) ? 1 : 0;
+    a.weight = weight;
+    a.ignore_index = ignore_index;
+    a.eps = label_smoothing;
+    a.lam = lse_square_scale;
+    const bool sc = softcap > 0.f;
+    a.softcap = sc ? softcap : 0.f;
+    a.sc_k2 = sc ? 2.f * kLog2e / softcap : 0.f;
+    a.sc_slog2e = sc ? softcap * kLog2e : 0.f;
+    a.reduction = reduction;
+    a.grad = (flags & CE_FLAG_GRAD) ? 1 : 0;
+    a.want_z = (flags & CE_FLAG_Z_LOSS) ? 1 : 0;
+    a.want_acc = (flags & CE_FLAG_ACC) ? 1 : 0;
+    a.want_pred = (flags & CE_FLAG_PRED) ? 1 : 0;
+    a.loss = loss;
+    a.zloss = z_loss;
+    a.acc = acc;
+    a.pred = pred;
+    a.timeout_ns = static_cast<uint64_t>(env_int("GBCE_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
+    a.scratch = scratch;
+
+    const bool wsmooth = weight != nullptr && label_smoothing > 0.f;
+    const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16) == 0;
+    Plan p;
+    rc = make_plan(dev, dtype, V, sc, wsmooth, aligned, &p);
+    if (rc != CE_OK) return rc;
+    if (rows == 0) {
+        // empty batch: the general kernel with one CTA writes the scalars
+        const void* fn = generic_kernel(dtype, sc);
+        return launch(fn, 1, kGenericThreads, 0, 1, st, &a);
+    }
+    const int64_t units = std::min<int64_t>(rows, p.max_units);
+    if (p.staged) {
+        a.slice_vec = p.slice_vec;
+        a.stages = p.stages;
+        return launch(p.fn, static_cast<int>(units * p.cluster), p.nt, p.smem, p.cluster, st, &a);
+    }
+    return launch(p.fn, static_cast<int>(units), p.nt, 0, 1, st, &a);
+}
+
+extern "C" ce_status ce_bwd(const float* grad_output, int grad_per_row, void* dlogits, int dtype,
+                            int64_t rows, int64_t V, ce_stream_t stream) {
+    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_INVALID_ARG;
+    if (rows < 0 || V <= 0) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && (!grad_output || !dlogits)) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && V > INT64_MAX / rows / 4) return CE_ERR_INVALID_ARG;
+    if (rows == 0) return CE_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    DeviceInfo info;
+    ce_status rc = device_info(dev, &info);
+    if (rc != CE_OK) return rc;
+    const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
+    BwdArgs b = {};
+    b.g = grad_output;
+    b.per_row = grad_per_row ? 1 : 0;
+    b.x = dlogits;
+    b.rows = rows;
+    b.V = V;
+    b.vec_ok = ((V * bytes) % 16 == 0 && reinterpret_cast<uintptr_t>(dlogits) % 16 == 0) ? 1 : 0;
+    const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(info.sm_count) * 8);
+    return launch(bwd_kernel(dtype), static_cast<int>(grid), kBwdThreads, 0, 1,
+                  reinterpret_cast<cudaStream_t>(stream), &b);
+}
+
+extern "C" ce_status ce_device_status(ce_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaStreamSynchronize");
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    auto it = g_scratch.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(st)));
+    if (it == g_scratch.end()) return CE_OK;
+    unsigned status = 0;
+    e = cudaMemcpyAsync(&status, &it->second->status, sizeof status, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&it->second->status, 0, sizeof status, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_failure(e, "reading the device status");
+    if (status & kDevErrTimeout) return CE_ERR_TIMEOUT;
+    if (status & kDevErrTarget) return CE_ERR_TARGET_RANGE;
+    return CE_OK;
+}
+
+extern "C" const char* ce_status_string(ce_status s) {
+    switch (s) {
+    case CE_OK: return "ok";
+    case CE_ERR_INVALID_ARG: return "invalid argument";
+    case CE_ERR_UNSUPPORTED: return "unsupported argument combination";
+    case CE_ERR_CUDA: return "CUDA runtime error";
+    case CE_ERR_TARGET_RANGE: return "target index outside [0, V) that is not ignore_index";
+    case CE_ERR_TIMEOUT: return "bounded device wait timed out";
+    }
+    return "unknown status";
+}
+
+extern "C" const char* ce_last_error(void) { return g_last_error.c_str(); }

@@ -1,0 +1,19 @@
+// Instantiations of the staged forward kernel: f32 logits, no softcap.
+#include "ce_fwd_staged.cuh"
+
+namespace gbce {
+
+const void* staged_kernel_f32_plain(int cfg_index, bool wsmooth) {
+#define GBCE_PICK(I, NT, NV)                                                     \
+    if (cfg_index == I)                                                          \
+        return wsmooth ? (const void*)&ce_fwd_staged<float, NT, NV, false, true> \
+                       : (const void*)&ce_fwd_staged<float, NT, NV, false, false>;
+    GBCE_PICK(0, 128, 4)
+    GBCE_PICK(1, 256, 4)
+    GBCE_PICK(2, 512, 4)
+    GBCE_PICK(3, 512, 8)
+#undef GBCE_PICK
+    return nullptr;
+}
+
+}  // namespace gbce

@@ -1,0 +1,213 @@
+// General-path forward kernel and the backward kernel.
+//
+// The general forward handles what the staged kernel does not: rows whose
+// byte length is not a multiple of 16 or that start unaligned, vocabularies
+// larger than eight CTAs can stage, and the empty batch. One CTA owns a row
+// at a time and makes three passes over it in global memory (max and
+// argmax; exp-sum and smoothing sum; gradient), so the second and third
+// reads come from L2 when the row fits. Same arithmetic and outputs as the
+// staged kernel (Liger-Kernel cross-entropy kernel profile, §Forward Pass
+// and §Key Patterns).
+//
+// Backward (same profile, §Backward Pass): the forward already stored the
+// gradient, so backward multiplies it by grad_output, in place.
+#include <climits>
+
+#include "ce_kernels.cuh"
+
+namespace gbce {
+
+template <typename T, bool SOFTCAP>
+__global__ void __launch_bounds__(kGenericThreads)
+ce_fwd_generic(const __grid_constant__ FwdArgs a) {
+    using VT = Vec<T>;
+    constexpr int NT = kGenericThreads;
+    constexpr int NW = NT / 32;
+    __shared__ float red_m[NW];
+    __shared__ int red_i[NW];
+    __shared__ float red_s[NW];
+    __shared__ float red_z[NW];
+    __shared__ float red_p[NW];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const bool wsmooth = a.weight != nullptr && a.eps > 0.f;
+
+    float D = 0.f, W = static_cast<float>(a.V);
+    int n_valid = 0;
+    if (a.reduction != kRedNone || wsmooth) denominators<NT>(a, wsmooth, red_p, D, n_valid, W);
+    const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;
+    const float inv_V = 1.f / static_cast<float>(a.V);
+
+    double accL = 0.0, accZ = 0.0;
+    long long accC = 0;
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        const int64_t t = load_target(a, r);
+        const bool counts = row_counts(a, t);
+        const int64_t base = r * a.V;
+        if (tid == 0 && t != a.ignore_index && !counts) atomicOr(&a.scratch->status, kDevErrTarget);
+        if (!counts) {
+            if (a.grad)
+                for (int64_t j = tid; j < a.V; j += NT) VT::store1(a.x, base + j, 0.f);
+            if (tid == 0) {
+                if (a.reduction == kRedNone) {
+                    a.loss[r] = 0.f;
+                    if (a.want_z) a.zloss[r] = 0.f;
+                    if (a.want_acc) a.acc[r] = 0.f;
+                }
+                if (a.want_pred) a.pred[r] = -1;
+            }
+            continue;
+        }
+        const float xt = tid == 0 ? VT::load1(a.x, base + t) : 0.f;
+        const float wt = a.weight ? __ldg(a.weight + t) : 1.f;
+
+        // pass 1: max and first argmax of the raw logits
+        float tmax = -INFINITY;
+        int tidx = INT_MAX;
+        for (int64_t j = tid; j < a.V; j += NT) {
+            const float v = VT::load1(a.x, base + j);
+            if (v > tmax) {
+                tmax = v;
+                tidx = static_cast<int>(j);
+            }
+        }
+        warp_argmax(tmax, tidx);
+        if (lane == 0) {
+            red_m[warp] = tmax;
+            red_i[warp] = tidx;
+        }
+        __syncthreads();
+        float mraw = red_m[0];
+        int amax = red_i[0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) {
+            if (red_m[w] > mraw || (red_m[w] == mraw && red_i[w] < amax)) {
+                mraw = red_m[w];
+                amax = red_i[w];
+            }
+        }
+        const float mz = SOFTCAP ? a.softcap * tanh_from_scaled(mraw * a.sc_k2) : mraw;
+        const float shift = mz == -INFINITY ? 0.f : mz;
+        const float Ls = shift * kLog2e;
+
+        // pass 2: sum of exp(z - shift) and the smoothing sum
+        float S = 0.f, SZ = 0.f;
+        for (int64_t j = tid; j < a.V; j += NT) {
+            const float v = VT::load1(a.x, base + j);
+            float e, zc;
+            if (SOFTCAP) {
+                zc = tanh_from_scaled(v * a.sc_k2);
+                e = ex2(fmaf(zc, a.sc_slog2e, -Ls));
+            } else {
+                zc = v;
+                e = ex2(fmaf(v, kLog2e, -Ls));
+            }
+            S += e;
+            SZ = wsmooth ? fmaf(__ldg(a.weight + j), zc, SZ) : SZ + zc;
+        }
+        S = warp_sum(S);
+        SZ = warp_sum(SZ);
+        if (lane == 0) {
+            red_s[warp] = S;
+            red_z[warp] = SZ;
+        }
+        __syncthreads();
+        S = 0.f;
+        SZ = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            S += red_s[w];
+            SZ += red_z[w];
+        }
+        const float lse = (S > 0.f ? shift : -INFINITY) + logf(S);
+
+        if (tid == 0) {
+            const float zt = SOFTCAP ? a.softcap * tanh_from_scaled(xt * a.sc_k2) : xt;
+            const float swz = SOFTCAP ? a.softcap * SZ : SZ;
+            float zl;
+            const float l = row_loss(a, lse, zt, wt, W, swz, zl);
+            const bool correct = static_cast<int64_t>(amax) == t;
+            if (a.reduction == kRedNone) {
+                a.loss[r] = l;
+                if (a.want_z) a.zloss[r] = zl;
+                if (a.want_acc) a.acc[r] = correct ? 1.f : 0.f;
+            } else {
+                accL += static_cast<double>(l);
+                accZ += static_cast<double>(zl);
+                accC += correct ? 1 : 0;
+            }
+            if (a.want_pred) a.pred[r] = amax;
+        }
+
+        // pass 3: gradient in place (each thread rewrites only what it reads)
+        if (a.grad) {
+            const float c0 = ex2((shift - lse) * kLog2e);
+            const float Wn = wsmooth ? W * inv_V : 1.f;
+            const float Ac = scale * ((1.f - a.eps) * wt + a.eps * Wn + 2.f * a.lam * lse) * c0;
+            const float Bc = -scale * a.eps * inv_V;
+            const float tfix = -scale * (1.f - a.eps) * wt;
+            for (int64_t j = tid; j < a.V; j += NT) {
+                const float v = VT::load1(a.x, base + j);
+                float e, th = 0.f;
+                if (SOFTCAP) {
+                    th = tanh_from_scaled(v * a.sc_k2);
+                    e = ex2(fmaf(th, a.sc_slog2e, -Ls));
+                } else {
+                    e = ex2(fmaf(v, kLog2e, -Ls));
+                }
+                float g = fmaf(Ac, e, wsmooth ? Bc * __ldg(a.weight + j) : Bc);
+                if (j == t) g += tfix;
+                if (SOFTCAP) g *= fmaf(-th, th, 1.f);
+                VT::store1(a.x, base + j, g);
+            }
+        }
+    }
+    if (a.reduction != kRedNone && tid == 0)
+        finish_scalars(a, blockIdx.x, gridDim.x, accL, accZ, accC, D, n_valid);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kBwdThreads) ce_bwd_scale(const __grid_constant__ BwdArgs a) {
+    using VT = Vec<T>;
+    constexpr int VE = VT::N;
+    if (!a.per_row && __ldg(a.g) == 1.f) return;  // multiplying by one changes nothing
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        const float g = a.per_row ? __ldg(a.g + r) : __ldg(a.g);
+        if (g == 1.f) continue;
+        if (a.vec_ok) {
+            uint4* row = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.x) + r * a.V);
+            const int64_t nv = a.V / VE;
+#pragma unroll 4
+            for (int64_t v = threadIdx.x; v < nv; v += kBwdThreads) {
+                float f[VE];
+                VT::unpack(row[v], f);
+#pragma unroll
+                for (int j = 0; j < VE; ++j) f[j] *= g;
+                row[v] = VT::pack(f);
+            }
+        } else {
+            for (int64_t j = threadIdx.x; j < a.V; j += kBwdThreads)
+                VT::store1(a.x, r * a.V + j, VT::load1(a.x, r * a.V + j) * g);
+        }
+    }
+}
+
+const void* generic_kernel(int dtype, bool softcap) {
+    if (dtype == 0)
+        return softcap ? (const void*)&ce_fwd_generic<float, true>
+                       : (const void*)&ce_fwd_generic<float, false>;
+    if (dtype == 1)
+        return softcap ? (const void*)&ce_fwd_generic<__nv_bfloat16, true>
+                       : (const void*)&ce_fwd_generic<__nv_bfloat16, false>;
+    return nullptr;
+}
+
+const void* bwd_kernel(int dtype) {
+    if (dtype == 0) return (const void*)&ce_bwd_scale<float>;
+    if (dtype == 1) return (const void*)&ce_bwd_scale<__nv_bfloat16>;
+    return nullptr;
+}
+
+}  // namespace gbce
