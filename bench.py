@@ -1,0 +1,451 @@
+"""Benchmark: fused softmax cross-entropy forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pass of the whole hot path over one batch: ce_fwd with the
+in-place gradient, then ce_bwd with grad_output = 1 (the loss.backward()
+case; the backward kernel leaves a factor of exactly 1 alone). The workload
+is the Liger cross-entropy profile's benchmark point with the largest
+vocabulary: rows = B*T = 4096 (B=8, T=512), V = 131072, bf16 logits
+N(0, 3^2), 5% of targets ignore_index, mean reduction. The metric is HBM
+throughput over the algorithmic bytes (one read and one write of the logits
+plus the targets) and rows/s; the V sweep of the same profile is reported
+beside it.
+
+Timing: W eager warm-up steps, then exactly K steps replayed from a captured
+CUDA graph, bracketed by a barrier and device synchronisation and timed with
+CUDA events on the launching stream; the maximum over ranks is reported.
+Steps cycle over a pool of device input buffers; each buffer is larger than
+L2 or the pool is deep enough that a buffer is evicted before its reuse, and
+L2 is flushed before the timed region. The pool is filled with the seeded
+logits before the timed region; the in-place gradient of a step becomes the
+next input of that buffer (the work per step does not depend on the values).
+
+--impl reference times the CPU float64 oracle on the host cores, on a
+bounded sample of the same workload, and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "CE fwd+bwd HBM GB/s (% of peak) and rows/s, B*T=4096, V=4k-131k bf16"
+ROWS, V_MAIN = 4096, 131072
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def algorithmic_bytes(rows, V, elem_bytes, target_bytes=4):
+    """One read and one write of the logits plus the targets."""
+    return rows * (2 * V * elem_bytes + target_bytes)
+
+
+def workload_desc(V):
+    return (f"rows=4096 (B=8, T=512) x V={V} bf16 logits N(0,3^2), 5% ignore_index, "
+            f"mean, fused fwd+bwd with in-place dlogits, grad_output=1")
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "softmax_cross_entropy_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_key):
+    """DRAM bytes per launch of the forward kernel from the committed ncu
+    summary, or None if absent or taken on other kernel sources."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    ent = d.get("workloads", {}).get(workload_key)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, interval_ms=50):
+        self.proc = None
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "window": "warm-up and timed steps"}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class GpuRunner:
+    def __init__(self, case, device, torch):
+        from softmax_cross_entropy_gb300 import _lib
+        self.torch, self.lib, self.case, self.dev = torch, _lib, case, device
+        x16 = np.ascontiguousarray(case.x).view(np.int16)
+        self.host = torch.from_numpy(x16).view(torch.bfloat16).pin_memory()
+        self.host_t = torch.from_numpy(case.target).pin_memory()
+        self.pristine = self.host.to(device)
+        self.target = self.host_t.to(device)
+        self.nbytes = self.pristine.numel() * 2
+        self.pool = max(2, min(16, math.ceil(3 * L2_BYTES / self.nbytes) + 1))
+        self.bufs = [torch.empty_like(self.pristine) for _ in range(self.pool)]
+        self.loss = torch.empty(1, dtype=torch.float32, device=device)
+        self.one = torch.ones(1, dtype=torch.float32, device=device)
+        self.half = torch.full((1,), 0.5, dtype=torch.float32, device=device)
+        self.flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+        self.stream = torch.cuda.Stream(device)
+
+    def fwd(self, x, st):
+        L = self.lib
+        rc = L.ce_fwd(x.data_ptr(), L.CE_BF16, self.case.rows, self.case.V,
+                      self.target.data_ptr(), None, self.case.ignore_index, 0.0, 0.0, 0.0,
+                      L.CE_RED_MEAN, L.CE_FLAG_GRAD, self.loss.data_ptr(), None, None, None, st)
+        if rc != 0:
+            raise RuntimeError(f"ce_fwd: {L.ce_status_string(rc)} {L.ce_last_error()}")
+
+    def bwd(self, x, g, st):
+        L = self.lib
+        rc = L.ce_bwd(g.data_ptr(), 0, x.data_ptr(), L.CE_BF16, self.case.rows, self.case.V, st)
+        if rc != 0:
+            raise RuntimeError(f"ce_bwd: {L.ce_status_string(rc)} {L.ce_last_error()}")
+
+    def refill(self):
+        for b in self.bufs:
+            b.copy_(self.pristine)
+        self.flush_buf.fill_(1.0)
+
+    def capture(self, steps, body):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.stream):
+            with torch.cuda.graph(g, stream=self.stream):
+                st = self.stream.cuda_stream
+                for k in range(steps):
+                    body(self.bufs[k % self.pool], st)
+        return g
+
+    def time_graph(self, g, barrier):
+        torch = self.torch
+        self.refill()
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            g.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        return e0.elapsed_time(e1) / 1e3
+
+    def warmup(self, steps):
+        st = self.stream.cuda_stream
+        with self.torch.cuda.stream(self.stream):
+            for k in range(steps):
+                b = self.bufs[k % self.pool]
+                b.copy_(self.pristine)
+                self.fwd(b, st)
+                self.bwd(b, self.one, st)
+        self.torch.cuda.synchronize(self.dev)
+        s = self.lib.ce_device_status(st)
+        if s != 0:
+            raise RuntimeError(f"device status after warm-up: {self.lib.ce_status_string(s)}")
+
+    def e2e(self, steps, barrier):
+        """Through the C ABI from pinned host memory: per step, copy the
+        logits and targets in, run forward + backward, read the loss back."""
+        torch = self.torch
+        out = torch.empty(1, dtype=torch.float32).pin_memory()
+        x = self.bufs[0]
+        st = self.stream.cuda_stream
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(steps):
+                x.copy_(self.host, non_blocking=True)
+                self.target.copy_(self.host_t, non_blocking=True)
+                self.fwd(x, st)
+                self.bwd(x, self.one, st)
+                out.copy_(self.loss, non_blocking=True)
+            e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        h2d = self.host.numel() * 2 + self.host_t.numel() * 4
+        return e0.elapsed_time(e1) / 1e3, h2d, 4
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    from softmax_cross_entropy_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    barrier()
+    build.build()
+
+    K, W = args.steps, args.warmup
+    peak, peak_kind = measured_peak()
+    sampler = ClockSampler(local) if rank == 0 else None
+
+    # ---- headline workload
+    case = workloads.vsweep(V=V_MAIN, rows=ROWS, seed=rank)
+    runner = GpuRunner(case, device, torch)
+    if sampler:
+        sampler.start()
+    runner.warmup(W)
+    g_step = runner.capture(K, lambda b, st: (runner.fwd(b, st), runner.bwd(b, runner.one, st)))
+    g_fwd = runner.capture(K, lambda b, st: runner.fwd(b, st))
+    t_step = max_over_ranks(runner.time_graph(g_step, barrier))
+    t_fwd = max_over_ranks(runner.time_graph(g_fwd, barrier))
+    clocks = sampler.stop() if sampler else None
+    g_bwd = runner.capture(K, lambda b, st: runner.bwd(b, runner.half, st))
+    t_bwd = max_over_ranks(runner.time_graph(g_bwd, barrier))
+    t_e2e, h2d, d2h = runner.e2e(K, barrier)
+    t_e2e = max_over_ranks(t_e2e)
+    del g_step, g_fwd, g_bwd
+
+    bytes_step = algorithmic_bytes(case.rows, case.V, 2)
+    value = world * bytes_step * K / t_step / 1e9
+    achieved = bytes_step / (t_fwd / K) / 1e9
+    traffic = recorded_traffic(f"vsweep_V{V_MAIN}")
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(t_step / K * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,3^2) bf16 logits, uniform targets, 5% ignored)",
+        "config": {"workload": workload_desc(V_MAIN), "rows": ROWS, "V": V_MAIN,
+                   "parallelism": f"dp{world} (independent row shards, no collective)",
+                   "l2": f"inputs larger than L2 (pool of {runner.pool} x "
+                         f"{runner.nbytes / 2**30:.2f} GiB buffers), L2 flushed before the "
+                         f"timed region",
+                   "timing": "CUDA graph of K steps, CUDA events on the launching stream"},
+        "rows_per_s": round(world * case.rows * K / t_step, 1),
+        "elements_per_s": round(world * case.rows * case.V * K / t_step, 1),
+        "frac_of_peak": round(value / world / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "ce_fwd_staged (forward with in-place gradient)",
+                     "bytes_per_launch": bytes_step,
+                     "avg_launch_us": round(t_fwd / K * 1e6, 2)},
+        "e2e": {"value": round(world * bytes_step * K / t_e2e / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(t_e2e / K * 1e3, 4)},
+        "gpu_launches": 2 * K,
+        "bwd_scale_g_ne_1": {"value": round(bytes_step * K / t_bwd / 1e9, 1), "unit": "GB/s",
+                             "us_per_launch": round(t_bwd / K * 1e6, 2)},
+    }
+    del runner
+    torch.cuda.empty_cache()
+
+    # ---- the V sweep of the same profile (context beside the headline)
+    if not args.no_sweep:
+        sweep = []
+        for V in workloads.VSWEEP:
+            c = workloads.vsweep(V=V, rows=ROWS, seed=rank)
+            r = GpuRunner(c, device, torch)
+            r.warmup(max(W, 3))
+            ks = K
+            g1 = r.capture(ks, lambda b, st: (r.fwd(b, st), r.bwd(b, r.one, st)))
+            t = max_over_ranks(r.time_graph(g1, barrier))
+            by = algorithmic_bytes(c.rows, c.V, 2)
+            sweep.append({"V": V, "GB/s": round(by * ks / t / 1e9, 1),
+                          "frac": round(by * ks / t / 1e9 / peak, 4),
+                          "us_per_step": round(t / ks * 1e6, 2),
+                          "rows_per_s": round(c.rows * ks / t, 1)})
+            del g1, r
+            torch.cuda.empty_cache()
+        line["sweep"] = sweep
+
+    if clocks:
+        line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ oracle arm
+
+def oracle_rate(case, seconds, chunk=16, max_rows=None):
+    """Times the oracle (forward with gradient) on successive row chunks of
+    the workload until `seconds` have passed. Returns (GB/s, rows, secs)."""
+    import oracle
+    oracle.build()
+    rows_done, t_used = 0, 0.0
+    limit = case.rows if max_rows is None else min(case.rows, max_rows)
+    while rows_done < limit and t_used < seconds:
+        r1 = min(limit, rows_done + chunk)
+        sub = case.x[rows_done:r1]
+        tg = case.target[rows_done:r1]
+        t0 = time.perf_counter()
+        oracle.forward(sub, tg, dtype=case.dtype, weight=case.weight, **case.options())
+        t_used += time.perf_counter() - t0
+        rows_done = r1
+    by = algorithmic_bytes(rows_done, case.V, 2)
+    return by / t_used / 1e9, rows_done, t_used
+
+
+def cpu_baseline(case, seconds):
+    gbs, rows, secs = oracle_rate(case, seconds)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} of {case.rows} rows (V={case.V}) of the same workload, "
+                      f"{secs:.1f} s single-threaded float64 oracle with gradient"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return  # the oracle arm runs on rank 0 only
+    case = workloads.vsweep(V=V_MAIN, rows=ROWS)
+    K, W = args.steps, args.warmup
+    per_step_rows = 8
+    times = []
+    import oracle
+    oracle.build()
+    for k in range(W + K):
+        r0 = (k * per_step_rows) % case.rows
+        sub, tg = case.x[r0:r0 + per_step_rows], case.target[r0:r0 + per_step_rows]
+        t0 = time.perf_counter()
+        oracle.forward(sub, tg, dtype="bf16", **case.options())
+        dt = time.perf_counter() - t0
+        if k >= W:
+            times.append(dt)
+    total = sum(times)
+    by = algorithmic_bytes(per_step_rows, case.V, 2) * K
+    value = by / total / 1e9
+    sample = (f"{per_step_rows} rows of V={case.V} per step (rows=4096 workload), "
+              f"float64 oracle with gradient, single thread")
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": K,
+        "warmup": W, "ms_per_step": round(total / K * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": workload_desc(V_MAIN), "rows": ROWS, "V": V_MAIN},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -96,28 +97,28 @@ ce_status scratch_for(int dev, cudaStream_t st, Scratch** out) {
 }
 
 const void* staged_fn(int dtype, int cfg, bool softcap, bool wsmooth) {
-    if (dtype == CE_BF16)
-        return softcap ? staged_kernel_bf16_softcap(cfg, wsmooth)
-                       : staged_kernel_bf16_plain(cfg, wsmooth);
-    return softcap ? staged_kernel_f32_softcap(cfg, wsmooth) : staged_kernel_f32_plain(cfg, wsmooth);
+    if (dtype == CE_BF16) {
+        if (softcap)
+            return wsmooth ? staged_kernel_bf16_softcap_wsmooth(cfg)
+                           : staged_kernel_bf16_softcap_plain(cfg);
+        return wsmooth ? staged_kernel_bf16_nocap_wsmooth(cfg) : staged_kernel_bf16_nocap_plain(cfg);
+    }
+    if (softcap)
+        return wsmooth ? staged_kernel_f32_softcap_wsmooth(cfg) : staged_kernel_f32_softcap_plain(cfg);
+    return wsmooth ? staged_kernel_f32_nocap_wsmooth(cfg) : staged_kernel_f32_nocap_plain(cfg);
 }
 
-// Tries the staged kernel with `C` CTAs per row. Returns false when the
-// shape does not fit (then the caller tries another C or the general path).
-bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, const DeviceInfo& dev,
-                Plan* out, ce_status* err) {
+// Evaluates the staged kernel with shape `cfg` and `C` CTAs per row.
+// Returns false when the combination does not fit (then other candidates or
+// the general path are tried); `occ` receives the CTAs per SM.
+bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, int cfg,
+                const DeviceInfo& dev, Plan* out, int* occ, ce_status* err) {
     const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
     const int64_t ve = 16 / bytes;
     const int64_t vec_row = V / ve;
     const int64_t per = (vec_row + C - 1) / C;
     if (C > 1 && per * (C - 1) >= vec_row) return false;  // a CTA would own nothing
-    int cfg = -1;
-    for (int i = 0; i < kNumStagedCfgs; ++i)
-        if (static_cast<int64_t>(kStagedCfgs[i].nt) * kStagedCfgs[i].nv >= per) {
-            cfg = i;
-            break;
-        }
-    if (cfg < 0) return false;
+    if (static_cast<int64_t>(kStagedCfgs[cfg].nt) * kStagedCfgs[cfg].nv < per) return false;
     const void* fn = staged_fn(dtype, cfg, softcap, wsmooth);
     if (!fn) return false;
     const int nt = kStagedCfgs[cfg].nt;
@@ -133,6 +134,8 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, const D
     if (2 * stage_bytes + wbytes > max_dyn) return false;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(max_dyn));
+    if (e == cudaSuccess && C > 8)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) {
         *err = cuda_failure(e, "cudaFuncSetAttribute");
         return false;
@@ -146,13 +149,13 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, const D
     }
     if (occ2 < 1) return false;
     int stages = 2;
-    const int max_stages = std::min(kMaxStages, env_int("GBCE_MAX_STAGES", kMaxStages));
+    const int max_stages = std::max(2, std::min(kMaxStages, env_int("GBCE_MAX_STAGES", kMaxStages)));
     for (int s = 3; s <= max_stages; ++s) {
         const size_t dyn = s * stage_bytes + wbytes;
         if (dyn > max_dyn) break;
-        int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, nt, dyn) != cudaSuccess ||
-            occ < occ2)
+        int o = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, nt, dyn) != cudaSuccess ||
+            o < occ2)
             break;
         stages = s;
     }
@@ -173,7 +176,8 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, const D
         int ncl = 0;
         e = cudaOccupancyMaxActiveClusters(&ncl, fn, &lc);
         if (e != cudaSuccess) {
-            *err = cuda_failure(e, "cudaOccupancyMaxActiveClusters");
+            // a cluster size this device cannot schedule: not a candidate
+            cudaGetLastError();
             return false;
         }
         if (ncl < 1) return false;
@@ -188,13 +192,18 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, const D
     out->slice_vec = static_cast<int>(per);
     out->smem = smem;
     out->max_units = units;
+    *occ = occ2;
     return true;
 }
 
 ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth, bool aligned,
                     Plan* out) {
-    const int forced = env_int("GBCE_CLUSTER", 0);  // tuning: force CTAs per row (1,2,4,8)
-    const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth, forced);
+    // Tuning overrides: GBCE_CLUSTER forces the CTAs per row (1, 2, 4, 8 or
+    // 16; -1 forces the general path) and GBCE_CFG the CTA shape index.
+    const int forced_c = env_int("GBCE_CLUSTER", 0);
+    const int forced_cfg = env_int("GBCE_CFG", -1);
+    const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth,
+                      forced_c * 64 + forced_cfg);
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
         *out = it->second;
@@ -203,23 +212,48 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     DeviceInfo dev;
     ce_status rc = device_info(devid, &dev);
     if (rc != CE_OK) return rc;
-    Plan p;
+    Plan best;
     const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
-    if (aligned && (V * bytes) % 16 == 0 && forced >= 0) {
-        for (int C : {1, 2, 4, 8}) {
-            if (forced && C != forced) continue;
-            rc = CE_OK;
-            if (try_staged(dtype, V, softcap, wsmooth, C, dev, &p, &rc)) break;
-            if (rc != CE_OK) return rc;
+    if (aligned && (V * bytes) % 16 == 0 && forced_c >= 0) {
+        // Candidates: every shape and cluster size that fits. Prefer at
+        // least two resident CTAs per SM (latency hiding across rows), then
+        // the fewest CTAs per row (cheaper cluster merges), then the deeper
+        // ring.
+        long best_score = -1;
+        for (int C : {1, 2, 4, 8, 16}) {
+            if (forced_c && C != forced_c) continue;
+            for (int cfg = 0; cfg < kNumStagedCfgs; ++cfg) {
+                if (forced_cfg >= 0 && cfg != forced_cfg) continue;
+                Plan p;
+                int occ = 0;
+                rc = CE_OK;
+                if (!try_staged(dtype, V, softcap, wsmooth, C, cfg, dev, &p, &occ, &rc)) {
+                    if (rc != CE_OK) return rc;
+                    continue;
+                }
+                const long score = std::min(occ, 2) * 100000L + (16 - C) * 1000L +
+                                   p.stages * 10L + (kNumStagedCfgs - cfg);
+                if (score > best_score) {
+                    best_score = score;
+                    best = p;
+                }
+            }
         }
     }
-    if (!p.staged) {
-        p.fn = generic_kernel(dtype, softcap);
-        p.nt = kGenericThreads;
-        p.max_units = std::min<int64_t>(static_cast<int64_t>(dev.sm_count) * 8, kMaxPartials);
+    if (!best.staged) {
+        best.fn = generic_kernel(dtype, softcap);
+        best.nt = kGenericThreads;
+        best.max_units = std::min<int64_t>(static_cast<int64_t>(dev.sm_count) * 8, kMaxPartials);
     }
-    g_plans[key] = p;
-    *out = p;
+    if (env_int("GBCE_VERBOSE", 0))
+        std::fprintf(stderr,
+                     "gbce plan: dtype=%d V=%lld softcap=%d wsmooth=%d -> %s nt=%d C=%d "
+                     "stages=%d slice_vec=%d smem=%zu units=%lld\n",
+                     dtype, static_cast<long long>(V), softcap ? 1 : 0, wsmooth ? 1 : 0,
+                     best.staged ? "staged" : "general", best.nt, best.cluster, best.stages,
+                     best.slice_vec, best.smem, static_cast<long long>(best.max_units));
+    g_plans[key] = best;
+    *out = best;
     return CE_OK;
 }
 

@@ -9,23 +9,25 @@
 // reduced loss written in place over the logits.
 //
 // GB300 design (not the pages' one-program-per-row, two-pass loop):
-//  * Row ownership. A thread-block cluster of C CTAs (C = 1, 2, 4 or 8)
-//    owns a row; CTA c owns a contiguous slice of slice_vec 16-byte vectors.
-//    The grid is persistent: cluster k handles rows k, k + n_clusters, ...
+//  * Row ownership. A thread-block cluster of C CTAs (C = 1 ... 16) owns a
+//    row; CTA c owns a contiguous slice of slice_vec 16-byte vectors. The
+//    grid is persistent: cluster k handles rows k, k + n_clusters, ...
 //  * One HBM read per element. Thread 0 of every CTA keeps a ring of
 //    `stages` shared-memory buffers filled by 1-D bulk asynchronous copies
 //    (cp.async.bulk, completion counted on an mbarrier) for the next rows,
 //    so loads of later rows overlap the compute and stores of this one.
 //    Ignored rows are never loaded.
 //  * Registers. Each thread copies its vectors of the staged slice into
-//    registers once; the buffer goes back to the copy engine right after
-//    the first block barrier. exp(z - m) (or tanh(x/s) under softcap) is
-//    cached per element, so the gradient pass needs no second load and no
-//    second exponential (one more under softcap).
-//  * Reductions. Warp shuffles, then a fixed-order pass over the warps'
-//    shared-memory partials; across the cluster one exchange per row
-//    through distributed shared memory combines (local max, sum of exp,
-//    argmax, smoothing sum) with the online-softmax rescaling.
+//    registers; the buffer goes back to the copy engine after the row's one
+//    block barrier. exp(z - m) (or tanh(x/s) under softcap) is kept per
+//    element, so the gradient needs no second load and no second
+//    exponential (one more under softcap).
+//  * One barrier per row. Each thread forms online-softmax statistics of
+//    its own elements (its max, sum of exp, smoothing sum, argmax); warps
+//    merge them with shuffles; one __syncthreads publishes the warp
+//    records; across the cluster one barrier.cluster makes the CTA records
+//    readable through distributed shared memory, and every warp merges
+//    them itself. Merges rescale sums to the larger max.
 //  * One HBM write per element: the gradient is packed to the logit dtype
 //    and stored with 16-byte coalesced stores over the row it came from.
 //  * Scalars. Per-row outputs are written by the cluster's rank 0; sums
@@ -33,6 +35,7 @@
 #pragma once
 
 #include <climits>
+#include <type_traits>
 
 #include "ce_kernels.cuh"
 
@@ -49,13 +52,9 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
 
     extern __shared__ __align__(128) unsigned char dyn[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
-    __shared__ float red_m[NW];
-    __shared__ int red_i[NW];
-    __shared__ float red_s[NW];
-    __shared__ float red_z[NW];
+    __shared__ __align__(16) RowStats red[2][NW];     // warp records, by row parity
+    __shared__ __align__(16) float rec[2][8];         // this CTA's record, by exchange parity
     __shared__ float red_p[NW];
-    __shared__ __align__(16) float rec[2][8];
-    __shared__ float bc[8];
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -106,9 +105,9 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
     }
 
     // ---- prologue (overlaps the first copies): denominators, weight slice
-    float D = 0.f, W = static_cast<float>(a.V);
+    float D = 0.f;
     int n_valid = 0;
-    if (a.reduction != kRedNone || WSMOOTH) denominators<NT>(a, WSMOOTH, red_p, D, n_valid, W);
+    if (a.reduction != kRedNone) denominators<NT>(a, red_p, D, n_valid);
     if (WSMOOTH) {
         // transposed [j][v] so that a warp reading element j of its vectors
         // touches consecutive words
@@ -118,6 +117,7 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
     }
     const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;  // unused when D == 0
     const float inv_V = 1.f / static_cast<float>(a.V);
+    const bool smooth = a.eps != 0.f;
 
     const bool leader = crank == 0 && tid == 0;
     double accL = 0.0, accZ = 0.0;
@@ -163,7 +163,7 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
             continue;
         }
 
-        // ---- 1. registers from the stage; local max and first argmax of raw x
+        // ---- 1. registers from the stage; the thread's max and first argmax
         const uint4* stg = reinterpret_cast<const uint4*>(dyn + static_cast<size_t>(s) * slice_bytes);
         uint4 xr[NV];
         float tmax = -INFINITY;
@@ -182,7 +182,7 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
                 xr[k] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        int tidx = INT_MAX;
+        RowStats st = empty_stats();
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             if (k == tk) {
@@ -191,14 +191,69 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
                 const int base = static_cast<int>((vbeg + tid + k * NT) * VE);
 #pragma unroll
                 for (int j = VE - 1; j >= 0; --j)
-                    if (f[j] == tmax) tidx = base + j;
+                    if (f[j] == tmax) st.idx = base + j;
             }
         }
-        warp_argmax(tmax, tidx);
-        if (lane == 0) {
-            red_m[warp] = tmax;
-            red_i[warp] = tidx;
+        st.xmax = tmax;
+
+        // ---- 2. exp(z - shift) once per element, relative to the thread's max
+        const float shift = tk < 0 ? 0.f
+                            : (SOFTCAP ? a.softcap * tanh_from_scaled(tmax * a.sc_k2) : tmax);
+        float cc[NV][VE];
+        float S = 0.f, SZ = 0.f, Wn = 0.f;
+        auto exp_pass = [&](auto with_sums) {
+            constexpr bool kSums = decltype(with_sums)::value;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int v = tid + k * NT;
+                if (v < nvec) {
+                    float f[VE];
+                    VT::unpack(xr[k], f);
+#pragma unroll
+                    for (int j = 0; j < VE; ++j) {
+                        float d;
+                        if (SOFTCAP) {
+                            const float th = tanh_from_scaled(f[j] * a.sc_k2);
+                            d = fmaf(th, a.softcap, -shift);
+                            cc[k][j] = th;
+                        } else {
+                            d = f[j] - shift;
+                        }
+                        const float e = ex2(d * kLog2e);
+                        if (!SOFTCAP) cc[k][j] = e;
+                        S += e;
+                        if (kSums) {
+                            if (WSMOOTH) {
+                                const float w = wsl[j * a.slice_vec + v];
+                                SZ = fmaf(w, d, SZ);
+                                Wn += w;
+                            } else {
+                                SZ += d;
+                            }
+                        }
+                    }
+                    if (kSums && !WSMOOTH) Wn += static_cast<float>(VE);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VE; ++j) cc[k][j] = 0.f;
+                }
+            }
+        };
+        if (smooth)
+            exp_pass(std::true_type{});
+        else
+            exp_pass(std::false_type{});
+        if (tk >= 0) {
+            st.m = shift;
+            st.S = S;
+            st.SZ = SZ;
+            st.Wn = Wn;
         }
+
+        // ---- 3. merge: warp butterfly, one block barrier, CTA records
+        warp_stats_allreduce<32>(st);
+        const int rp = static_cast<int>(it & 1);
+        if (lane == 0) red[rp][warp] = st;
         {
             const bool f = __syncthreads_or(!ok) != 0;
             if (f && !failed) fail_it = it;
@@ -206,122 +261,43 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
         }
         // every thread holds its vectors: hand the stage back to the copy engine
         if (tid == 0 && !failed && r + stages * ncl < a.rows) issue(r + stages * ncl, s);
-        float mraw = red_m[0];
-        int amax = red_i[0];
+        RowStats tot = red[rp][0];
 #pragma unroll
-        for (int w = 1; w < NW; ++w) {
-            const float v = red_m[w];
-            const int i = red_i[w];
-            if (v > mraw || (v == mraw && i < amax)) {
-                mraw = v;
-                amax = i;
-            }
-        }
+        for (int w = 1; w < NW; ++w) stats_merge(tot, red[rp][w]);
 
-        // ---- 2. exp(z - shift) once per element, sum, smoothing sum
-        const float mz = SOFTCAP ? a.softcap * tanh_from_scaled(mraw * a.sc_k2) : mraw;
-        const float shift = mz == -INFINITY ? 0.f : mz;
-        const float Ls = shift * kLog2e;
-        float cc[NV][VE];
-        float S = 0.f, SZ = 0.f;
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int v = tid + k * NT;
-            if (v < nvec) {
-                float f[VE];
-                VT::unpack(xr[k], f);
-#pragma unroll
-                for (int j = 0; j < VE; ++j) {
-                    float e, zc;
-                    if (SOFTCAP) {
-                        const float th = tanh_from_scaled(f[j] * a.sc_k2);
-                        e = ex2(fmaf(th, a.sc_slog2e, -Ls));
-                        cc[k][j] = th;
-                        zc = th;  // sum of z = s * sum of tanh
-                    } else {
-                        e = ex2(fmaf(f[j], kLog2e, -Ls));
-                        cc[k][j] = e;
-                        zc = f[j];
-                    }
-                    S += e;
-                    SZ = WSMOOTH ? fmaf(wsl[j * a.slice_vec + v], zc, SZ) : SZ + zc;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < VE; ++j) cc[k][j] = 0.f;
-            }
-        }
-        S = warp_sum(S);
-        SZ = warp_sum(SZ);
-        if (lane == 0) {
-            red_s[warp] = S;
-            red_z[warp] = SZ;
-        }
-        __syncthreads();
-        S = 0.f;
-        SZ = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            S += red_s[w];
-            SZ += red_z[w];
-        }
-
-        // ---- 3. combine over the cluster (distributed shared memory)
-        float M = S > 0.f ? shift : -INFINITY;
-        float Stot = S, SZtot = SZ;
-        int am = amax;
+        // ---- 4. merge over the cluster through distributed shared memory
         if (csize > 1) {
             const int slot = xchg & 1;
             ++xchg;
             if (tid == 0) {
-                rec[slot][0] = M;
-                rec[slot][1] = S;
-                rec[slot][2] = mraw;
-                rec[slot][3] = __int_as_float(amax);
-                rec[slot][4] = SZ;
+                rec[slot][0] = tot.m;
+                rec[slot][1] = tot.S;
+                rec[slot][2] = tot.SZ;
+                rec[slot][3] = tot.Wn;
+                rec[slot][4] = tot.xmax;
+                rec[slot][5] = __int_as_float(tot.idx);
             }
             cluster_sync();
-            if (warp == 0) {
-                float m_c = -INFINITY, s_c = 0.f, r_c = -INFINITY, z_c = 0.f;
-                int i_c = INT_MAX;
-                if (lane < static_cast<int>(csize)) {
-                    const uint32_t ra = map_to_rank(smem_u32(&rec[slot][0]), lane);
-                    const float4 q0 = ld_dsmem_f4(ra);
-                    const float4 q1 = ld_dsmem_f4(ra + 16);
-                    m_c = q0.x;
-                    s_c = q0.y;
-                    r_c = q0.z;
-                    i_c = __float_as_int(q0.w);
-                    z_c = q1.x;
-                }
-                float Mx = m_c;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
-                float term = s_c > 0.f ? s_c * ex2((m_c - Mx) * kLog2e) : 0.f;
-                term = warp_sum(term);
-                z_c = warp_sum(z_c);
-                warp_argmax(r_c, i_c);
-                if (lane == 0) {
-                    bc[0] = Mx;
-                    bc[1] = term;
-                    bc[2] = __int_as_float(i_c);
-                    bc[3] = z_c;
-                }
+            RowStats cs = empty_stats();
+            if (lane < static_cast<int>(csize)) {
+                const uint32_t ra = map_to_rank(smem_u32(&rec[slot][0]), lane);
+                const float4 q0 = ld_dsmem_f4(ra);
+                const float4 q1 = ld_dsmem_f4(ra + 16);
+                cs = RowStats{q0.x, q0.y, q0.z, q0.w, q1.x, __float_as_int(q1.y)};
             }
-            __syncthreads();
-            M = bc[0];
-            Stot = bc[1];
-            am = __float_as_int(bc[2]);
-            SZtot = bc[3];
+            warp_stats_allreduce<32>(cs);
+            tot = cs;
         }
-        const float lse = M + logf(Stot);
+        const float M = tot.m;
+        const float logS = logf(tot.S);
+        const int am = tot.idx;
 
-        // ---- 4. per-row outputs (rank 0 of the cluster)
+        // ---- 5. per-row outputs (rank 0 of the cluster)
         if (leader) {
             const float zt = SOFTCAP ? a.softcap * tanh_from_scaled(xt * a.sc_k2) : xt;
-            const float swz = SOFTCAP ? a.softcap * SZtot : SZtot;
             float zl;
-            const float l = row_loss(a, lse, zt, wt, W, swz, zl);
+            const float l = row_loss(a, M, logS, zt, wt, WSMOOTH ? tot.Wn : static_cast<float>(a.V),
+                                     tot.SZ, zl);
             const bool correct = static_cast<int64_t>(am) == t;
             if (a.reduction == kRedNone) {
                 a.loss[r] = l;
@@ -335,12 +311,13 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
             if (a.want_pred) a.pred[r] = am;
         }
 
-        // ---- 5. gradient in place:
+        // ---- 6. gradient in place:
         //   scale * [ (1-eps) w_t (p - onehot) + (eps/V)(W p - w) + 2 lam lse p ] * dz/dx
         if (a.grad && !failed) {
-            const float c0 = ex2((shift - lse) * kLog2e);  // p = e * c0
-            const float Wn = WSMOOTH ? W * inv_V : 1.f;
+            const float lse = M + logS;
+            const float Wn = WSMOOTH ? tot.Wn * inv_V : 1.f;
             const float A = scale * ((1.f - a.eps) * wt + a.eps * Wn + 2.f * a.lam * lse);
+            const float c0 = ex2((shift - M) * kLog2e) / tot.S;  // p = e * c0
             const float Ac = A * c0;
             const float Bc = -scale * a.eps * inv_V;
             const float tfix = -scale * (1.f - a.eps) * wt;
@@ -355,8 +332,8 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
                     float g[VE];
 #pragma unroll
                     for (int j = 0; j < VE; ++j) {
-                        const float e =
-                            SOFTCAP ? ex2(fmaf(cc[k][j], a.sc_slog2e, -Ls)) : cc[k][j];
+                        const float e = SOFTCAP ? ex2(fmaf(cc[k][j], a.softcap, -shift) * kLog2e)
+                                                : cc[k][j];
                         const float b = WSMOOTH ? Bc * wsl[j * a.slice_vec + v] : Bc;
                         g[j] = fmaf(Ac, e, b);
                     }

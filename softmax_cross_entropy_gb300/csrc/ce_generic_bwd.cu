@@ -34,9 +34,9 @@ ce_fwd_generic(const __grid_constant__ FwdArgs a) {
     const int warp = tid >> 5;
     const bool wsmooth = a.weight != nullptr && a.eps > 0.f;
 
-    float D = 0.f, W = static_cast<float>(a.V);
+    float D = 0.f;
     int n_valid = 0;
-    if (a.reduction != kRedNone || wsmooth) denominators<NT>(a, wsmooth, red_p, D, n_valid, W);
+    if (a.reduction != kRedNone) denominators<NT>(a, red_p, D, n_valid);
     const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;
     const float inv_V = 1.f / static_cast<float>(a.V);
 
@@ -88,46 +88,47 @@ ce_fwd_generic(const __grid_constant__ FwdArgs a) {
                 amax = red_i[w];
             }
         }
-        const float mz = SOFTCAP ? a.softcap * tanh_from_scaled(mraw * a.sc_k2) : mraw;
-        const float shift = mz == -INFINITY ? 0.f : mz;
-        const float Ls = shift * kLog2e;
+        // the row max of z (softcap is monotone); every difference below is
+        // taken against it before scaling, which keeps them exact or nearly so
+        const float M = SOFTCAP ? a.softcap * tanh_from_scaled(mraw * a.sc_k2) : mraw;
+        const float shift = M == -INFINITY ? 0.f : M;
 
-        // pass 2: sum of exp(z - shift) and the smoothing sum
-        float S = 0.f, SZ = 0.f;
+        // pass 2: S = sum exp(z - M), SZ = sum w (z - M), W = sum w
+        float S = 0.f, SZ = 0.f, Wn = 0.f;
         for (int64_t j = tid; j < a.V; j += NT) {
             const float v = VT::load1(a.x, base + j);
-            float e, zc;
-            if (SOFTCAP) {
-                zc = tanh_from_scaled(v * a.sc_k2);
-                e = ex2(fmaf(zc, a.sc_slog2e, -Ls));
-            } else {
-                zc = v;
-                e = ex2(fmaf(v, kLog2e, -Ls));
-            }
-            S += e;
-            SZ = wsmooth ? fmaf(__ldg(a.weight + j), zc, SZ) : SZ + zc;
+            const float d = SOFTCAP ? fmaf(tanh_from_scaled(v * a.sc_k2), a.softcap, -shift)
+                                    : v - shift;
+            S += ex2(d * kLog2e);
+            const float w = wsmooth ? __ldg(a.weight + j) : 1.f;
+            SZ = fmaf(w, d, SZ);
+            Wn += w;
         }
         S = warp_sum(S);
         SZ = warp_sum(SZ);
+        Wn = warp_sum(Wn);
         if (lane == 0) {
             red_s[warp] = S;
             red_z[warp] = SZ;
+            red_p[warp] = Wn;
         }
         __syncthreads();
         S = 0.f;
         SZ = 0.f;
+        Wn = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
             S += red_s[w];
             SZ += red_z[w];
+            Wn += red_p[w];
         }
-        const float lse = (S > 0.f ? shift : -INFINITY) + logf(S);
+        const float logS = logf(S);
 
         if (tid == 0) {
             const float zt = SOFTCAP ? a.softcap * tanh_from_scaled(xt * a.sc_k2) : xt;
-            const float swz = SOFTCAP ? a.softcap * SZ : SZ;
             float zl;
-            const float l = row_loss(a, lse, zt, wt, W, swz, zl);
+            const float l = row_loss(a, shift, logS, zt, wt,
+                                     wsmooth ? Wn : static_cast<float>(a.V), SZ, zl);
             const bool correct = static_cast<int64_t>(amax) == t;
             if (a.reduction == kRedNone) {
                 a.loss[r] = l;
@@ -143,26 +144,29 @@ ce_fwd_generic(const __grid_constant__ FwdArgs a) {
 
         // pass 3: gradient in place (each thread rewrites only what it reads)
         if (a.grad) {
-            const float c0 = ex2((shift - lse) * kLog2e);
-            const float Wn = wsmooth ? W * inv_V : 1.f;
-            const float Ac = scale * ((1.f - a.eps) * wt + a.eps * Wn + 2.f * a.lam * lse) * c0;
+            const float lse = shift + logS;
+            const float Wf = wsmooth ? Wn * inv_V : 1.f;
+            const float Ac =
+                scale * ((1.f - a.eps) * wt + a.eps * Wf + 2.f * a.lam * lse) / S;
             const float Bc = -scale * a.eps * inv_V;
             const float tfix = -scale * (1.f - a.eps) * wt;
             for (int64_t j = tid; j < a.V; j += NT) {
                 const float v = VT::load1(a.x, base + j);
-                float e, th = 0.f;
+                float d, th = 0.f;
                 if (SOFTCAP) {
                     th = tanh_from_scaled(v * a.sc_k2);
-                    e = ex2(fmaf(th, a.sc_slog2e, -Ls));
+                    d = fmaf(th, a.softcap, -shift);
                 } else {
-                    e = ex2(fmaf(v, kLog2e, -Ls));
+                    d = v - shift;
                 }
-                float g = fmaf(Ac, e, wsmooth ? Bc * __ldg(a.weight + j) : Bc);
+                float g = fmaf(Ac, ex2(d * kLog2e), wsmooth ? Bc * __ldg(a.weight + j) : Bc);
                 if (j == t) g += tfix;
                 if (SOFTCAP) g *= fmaf(-th, th, 1.f);
                 VT::store1(a.x, base + j, g);
             }
         }
+        // red_s, red_z, red_p are read above; the next row writes them only
+        // after its first barrier, which every thread reaches after reading
     }
     if (a.reduction != kRedNone && tid == 0)
         finish_scalars(a, blockIdx.x, gridDim.x, accL, accZ, accC, D, n_valid);

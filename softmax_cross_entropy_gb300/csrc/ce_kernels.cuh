@@ -83,13 +83,12 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* sh) {
     return r;
 }
 
-// Prologue: the mean denominator D = sum of w[t_i] over counted rows, the
-// counted-row number, and (for weighted label smoothing) W = sum_j w_j.
-// Every CTA computes them in the same fixed order, so all CTAs hold
-// bit-identical values without any inter-CTA communication.
+// Prologue: the mean denominator D = sum of w[t_i] over counted rows and the
+// counted-row number. Every CTA computes them in the same fixed order, so
+// all CTAs hold bit-identical values without inter-CTA communication.
 template <int NT>
-__device__ __forceinline__ void denominators(const FwdArgs& a, bool need_W, float* sh,
-                                             float& D, int& n_valid, float& W) {
+__device__ __forceinline__ void denominators(const FwdArgs& a, float* sh, float& D,
+                                             int& n_valid) {
     float d = 0.f;
     int n = 0;
     for (int64_t i = threadIdx.x; i < a.rows; i += NT) {
@@ -101,36 +100,92 @@ __device__ __forceinline__ void denominators(const FwdArgs& a, bool need_W, floa
     }
     D = block_sum_fixed<NT>(d, sh);
     __syncthreads();
-    {
-        // integer count through the same fixed tree (exact)
-        int v = n;
+    int v = n;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if ((threadIdx.x & 31) == 0) reinterpret_cast<int*>(sh)[threadIdx.x >> 5] = v;
-        __syncthreads();
-        int r = 0;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) reinterpret_cast<int*>(sh)[threadIdx.x >> 5] = v;
+    __syncthreads();
+    int r = 0;
 #pragma unroll
-        for (int w = 0; w < NT / 32; ++w) r += reinterpret_cast<int*>(sh)[w];
-        n_valid = r;
-        __syncthreads();
+    for (int w = 0; w < NT / 32; ++w) r += reinterpret_cast<int*>(sh)[w];
+    n_valid = r;
+    __syncthreads();
+    if (!a.weight) D = static_cast<float>(n_valid);  // exact count
+}
+
+// Online softmax statistics of a set of elements of one row, relative to a
+// reference m (the largest z of the set): S = sum exp(z - m),
+// SZ = sum w (z - m), Wn = sum w (the element count without weights), and
+// the first argmax (xmax, idx) of the raw logits. An empty set has
+// m = -inf. Sets are merged with the usual rescaling.
+struct RowStats {
+    float m, S, SZ, Wn, xmax;
+    int idx;
+};
+
+__device__ __forceinline__ RowStats empty_stats() {
+    return RowStats{-INFINITY, 0.f, 0.f, 0.f, -INFINITY, 0x7fffffff};
+}
+
+// a <- a (+) b. The result does not depend on the order of a and b, bit
+// for bit (every product and sum is rounded explicitly, per side), so the
+// lanes of a butterfly reduction and the CTAs of a cluster agree exactly.
+__device__ __forceinline__ void stats_merge(RowStats& a, const RowStats& b) {
+    if (b.xmax > a.xmax || (b.xmax == a.xmax && b.idx < a.idx)) {
+        a.xmax = b.xmax;
+        a.idx = b.idx;
     }
-    if (!a.weight) D = static_cast<float>(n_valid);
-    W = static_cast<float>(a.V);
-    if (need_W) {
-        float s = 0.f;
-        for (int64_t j = threadIdx.x; j < a.V; j += NT) s += __ldg(a.weight + j);
-        W = block_sum_fixed<NT>(s, sh);
-        __syncthreads();
+    if (b.m == -INFINITY) return;
+    if (a.m == -INFINITY) {
+        a.m = b.m;
+        a.S = b.S;
+        a.SZ = b.SZ;
+        a.Wn = b.Wn;
+        return;
+    }
+    const float M = fmaxf(a.m, b.m);
+    const float da = __fsub_rn(a.m, M);
+    const float db = __fsub_rn(b.m, M);
+    a.S = __fadd_rn(__fmul_rn(a.S, ex2(__fmul_rn(da, kLog2e))),
+                    __fmul_rn(b.S, ex2(__fmul_rn(db, kLog2e))));
+    a.SZ = __fadd_rn(__fmaf_rn(a.Wn, da, a.SZ), __fmaf_rn(b.Wn, db, b.SZ));
+    a.Wn = __fadd_rn(a.Wn, b.Wn);
+    a.m = M;
+}
+
+__device__ __forceinline__ RowStats shfl_xor_stats(const RowStats& v, int o) {
+    RowStats r;
+    r.m = __shfl_xor_sync(0xffffffffu, v.m, o);
+    r.S = __shfl_xor_sync(0xffffffffu, v.S, o);
+    r.SZ = __shfl_xor_sync(0xffffffffu, v.SZ, o);
+    r.Wn = __shfl_xor_sync(0xffffffffu, v.Wn, o);
+    r.xmax = __shfl_xor_sync(0xffffffffu, v.xmax, o);
+    r.idx = __shfl_xor_sync(0xffffffffu, v.idx, o);
+    return r;
+}
+
+// Butterfly all-reduce over the low `width` lanes groups (width a power of
+// two); every lane ends with the same bits.
+template <int WIDTH>
+__device__ __forceinline__ void warp_stats_allreduce(RowStats& v) {
+#pragma unroll
+    for (int o = WIDTH / 2; o > 0; o >>= 1) {
+        const RowStats b = shfl_xor_stats(v, o);
+        stats_merge(v, b);
     }
 }
 
-// Per-row loss from the row's scalars:
-//   (1-eps) w_t (lse - z_t) + (eps/V) (W lse - sum_j w_j z_j) + lam lse^2
-__device__ __forceinline__ float row_loss(const FwdArgs& a, float lse, float zt, float wt,
-                                          float W, float swz, float& zl) {
+// Per-row loss from the row's merged statistics (M = max z, S = sum
+// exp(z - M), SZ = sum w (z - M), W = sum w):
+//   (1-eps) w_t (lse - z_t) + (eps/V) sum_j w_j (lse - z_j) + lam lse^2
+// with lse - z_t = (M - z_t) + log S and
+// sum_j w_j (lse - z_j) = W log S - SZ, which keeps every difference small.
+__device__ __forceinline__ float row_loss(const FwdArgs& a, float M, float logS, float zt,
+                                          float wt, float W, float SZ, float& zl) {
+    const float lse = M + logS;
     zl = a.lam * lse * lse;
-    const float ce = wt * (lse - zt);
-    const float sm = (W * lse - swz) / static_cast<float>(a.V);
+    const float ce = wt * ((M - zt) + logS);
+    const float sm = (W * logS - SZ) / static_cast<float>(a.V);
     return (1.f - a.eps) * ce + a.eps * sm + zl;
 }
 
@@ -171,13 +226,16 @@ __device__ __forceinline__ void finish_scalars(const FwdArgs& a, int64_t slot, i
 // ---------------------------------------------------------------- variants
 
 // Staged-kernel shapes: threads per CTA and 16-byte vectors each thread
-// keeps in registers. A CTA holds at most nt * nv vectors of one row.
+// keeps in registers. A CTA holds at most nt * nv vectors of one row; with
+// at most 128 registers a thread, 512 / nt CTAs fit on an SM by registers.
 struct StagedCfg {
     int nt;
     int nv;
 };
-constexpr int kNumStagedCfgs = 4;
-constexpr StagedCfg kStagedCfgs[kNumStagedCfgs] = {{128, 4}, {256, 4}, {512, 4}, {512, 8}};
+constexpr int kNumStagedCfgs = 6;
+constexpr StagedCfg kStagedCfgs[kNumStagedCfgs] = {{128, 4}, {128, 8}, {256, 4},
+                                                   {256, 8}, {512, 4}, {512, 8}};
+constexpr int kMaxCluster = 16;
 constexpr int kMaxStages = 8;
 constexpr int kGenericThreads = 256;
 constexpr int kBwdThreads = 256;
@@ -194,10 +252,14 @@ struct BwdArgs {
 // Kernel entry points by variant, for cudaLaunchKernelExC and the occupancy
 // API (nullptr for an unknown variant). Forward kernels take one FwdArgs,
 // the backward kernel one BwdArgs, both by value.
-const void* staged_kernel_bf16_plain(int cfg_index, bool wsmooth);
-const void* staged_kernel_bf16_softcap(int cfg_index, bool wsmooth);
-const void* staged_kernel_f32_plain(int cfg_index, bool wsmooth);
-const void* staged_kernel_f32_softcap(int cfg_index, bool wsmooth);
+const void* staged_kernel_bf16_nocap_plain(int cfg);
+const void* staged_kernel_bf16_nocap_wsmooth(int cfg);
+const void* staged_kernel_bf16_softcap_plain(int cfg);
+const void* staged_kernel_bf16_softcap_wsmooth(int cfg);
+const void* staged_kernel_f32_nocap_plain(int cfg);
+const void* staged_kernel_f32_nocap_wsmooth(int cfg);
+const void* staged_kernel_f32_softcap_plain(int cfg);
+const void* staged_kernel_f32_softcap_wsmooth(int cfg);
 const void* generic_kernel(int dtype, bool softcap);
 const void* bwd_kernel(int dtype);
 

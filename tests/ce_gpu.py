@@ -1,0 +1,161 @@
+"""Helpers for the GPU parity tests: move a workload case to the device, run
+the CUDA path through the C ABI, run the oracle on the same bits, and the
+tolerances the comparisons use."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import workloads
+
+# Tolerances. The headline bounds: fp32 loss rel 1e-5 and dlogits abs 1e-6;
+# bf16 dlogits abs 4e-3 with the loss (fp32-accumulated) rel 1e-4;
+# predicted tokens and accuracy exact. Because mean-scaled gradients are
+# small, the gradient checks add a relative bound as well: a bf16 gradient
+# must be within one bf16 unit in the last place of the oracle value (the
+# kernel computes in fp32 and rounds once), an fp32 gradient within 1e-5
+# relative plus 1e-6 of the largest gradient magnitude of the batch.
+# The bf16 absolute bound applies where |gradient| < 0.5: above that, the
+# nearest bf16 value itself can lie more than 4e-3 from the exact one
+# (half a unit in the last place is 2^-8 at magnitude 1, 2^-7 at 2), and
+# the one-ulp bound governs.
+LOSS_RTOL = {"f32": 1e-5, "bf16": 1e-4}
+GRAD_ATOL = {"f32": 1e-6, "bf16": 4e-3}
+
+
+def to_device(case, device="cuda"):
+    import torch
+    if case.dtype == "bf16":
+        x = torch.from_numpy(np.ascontiguousarray(case.x).view(np.int16)).view(torch.bfloat16)
+    else:
+        x = torch.from_numpy(np.ascontiguousarray(case.x))
+    x = x.to(device)
+    t = torch.from_numpy(np.ascontiguousarray(case.target)).to(device)
+    w = None if case.weight is None else torch.from_numpy(case.weight).to(device)
+    return x, t, w
+
+
+def run_cuda(case, *, grad=True, want_z=False, want_acc=False, want_pred=False, x=None,
+             target=None, reduction=None, stream=None):
+    """Calls ce_fwd through the C ABI. Returns a dict of numpy outputs plus
+    the device logits buffer (holding dlogits when grad)."""
+    import torch
+    from softmax_cross_entropy_gb300 import _lib
+    dev_x, dev_t, dev_w = to_device(case)
+    if x is not None:
+        dev_x = x
+    if target is not None:
+        dev_t = target
+    red = reduction or case.reduction
+    rows, V = case.rows, case.V
+    n = rows if red == "none" else 1
+    f32 = dict(dtype=torch.float32, device=dev_x.device)
+    loss = torch.full((n,), float("nan"), **f32)
+    zl = torch.full((n,), float("nan"), **f32) if want_z else None
+    acc = torch.full((n,), float("nan"), **f32) if want_acc else None
+    pred = torch.full((rows,), -7, dtype=torch.int64, device=dev_x.device) if want_pred else None
+    flags = ((_lib.CE_FLAG_GRAD if grad else 0) | (_lib.CE_FLAG_Z_LOSS if want_z else 0) |
+             (_lib.CE_FLAG_ACC if want_acc else 0) | (_lib.CE_FLAG_PRED if want_pred else 0) |
+             (_lib.CE_FLAG_TARGET_I64 if dev_t.dtype == torch.int64 else 0))
+    st = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    rc = _lib.ce_fwd(dev_x.data_ptr(), _lib.CE_BF16 if case.dtype == "bf16" else _lib.CE_F32,
+                     rows, V, dev_t.data_ptr(), None if dev_w is None else dev_w.data_ptr(),
+                     case.ignore_index, case.label_smoothing, case.lse_square_scale,
+                     case.softcap or 0.0, {"none": 0, "sum": 1, "mean": 2}[red], flags,
+                     loss.data_ptr(), None if zl is None else zl.data_ptr(),
+                     None if acc is None else acc.data_ptr(),
+                     None if pred is None else pred.data_ptr(), st)
+    assert rc == _lib.CE_OK, (_lib.ce_status_string(rc), _lib.ce_last_error())
+    status = _lib.ce_device_status(st)
+    out = {"status": status, "x": dev_x,
+           "loss": loss.cpu().numpy().astype(np.float64),
+           "z_loss": None if zl is None else zl.cpu().numpy().astype(np.float64),
+           "acc": None if acc is None else acc.cpu().numpy().astype(np.float64),
+           "pred": None if pred is None else pred.cpu().numpy()}
+    if red != "none":
+        for k in ("loss", "z_loss", "acc"):
+            if out[k] is not None:
+                out[k] = out[k][0]
+    return out
+
+
+def grad_rows_f64(dev_x, rows_idx=None):
+    import torch
+    g = dev_x if rows_idx is None else dev_x[torch.as_tensor(rows_idx, device=dev_x.device)]
+    return g.float().cpu().numpy().astype(np.float64)
+
+
+def oracle_full(case, reduction=None, want_grad=True):
+    import oracle
+    opts = case.options()
+    if reduction:
+        opts["reduction"] = reduction
+    return oracle.forward(case.x, case.target, dtype=case.dtype, weight=case.weight,
+                          want_grad=want_grad, **opts)
+
+
+def oracle_rows(case, idx, reduction=None, want_grad=True):
+    import oracle
+    opts = case.options()
+    if reduction:
+        opts["reduction"] = reduction
+    return oracle.rows(case.x, case.target, idx, dtype=case.dtype, weight=case.weight,
+                       want_grad=want_grad, **opts)
+
+
+def assert_loss_close(got, want, dtype, what="loss"):
+    if isinstance(want, float) and math.isnan(want):
+        assert math.isnan(got), f"{what}: expected NaN, got {got}"
+        return
+    np.testing.assert_allclose(got, want, rtol=LOSS_RTOL[dtype], atol=1e-30, err_msg=what)
+
+
+def assert_rowloss_close(got, want, dtype, what="row loss"):
+    # per-row values: relative bound plus a small absolute floor for rows
+    # whose loss is near zero
+    np.testing.assert_allclose(got, want, rtol=LOSS_RTOL[dtype], atol=LOSS_RTOL[dtype] * 1e-2,
+                               err_msg=what)
+
+
+def assert_grad_close(got, want, dtype, what="dlogits"):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape
+    err = np.abs(got - want)
+    small = np.abs(want) < 0.5 if dtype == "bf16" else np.ones(want.shape, bool)
+    emax = err[small].max(initial=0.0)
+    assert emax <= GRAD_ATOL[dtype], f"{what}: max abs err {emax}"
+    if dtype == "bf16":
+        # one bf16 ulp of the oracle value (2^-7 relative covers the binade
+        # edge), plus the fp32 compute noise near zero
+        gmax = np.abs(want).max(initial=0.0)
+        bound = np.abs(want) * 2.0 ** -7 + 1e-6 * gmax + 1e-30
+    else:
+        gmax = np.abs(want).max(initial=0.0)
+        bound = 1e-5 * np.abs(want) + 1e-6 * gmax + 1e-30
+    bad = err > bound
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} elements out of bound; first at {tuple(i)}: "
+                             f"got {got[tuple(i)]!r} want {want[tuple(i)]!r}")
+
+
+def sample_rows(case, n=24, seed=0):
+    """A fixed sample of row indices: some valid, some ignored, first and
+    last rows."""
+    rng = np.random.default_rng(seed)
+    rows = case.rows
+    idx = set(rng.choice(rows, size=min(n, rows), replace=False).tolist())
+    idx.update({0, rows - 1})
+    ign = np.nonzero(case.target == case.ignore_index)[0]
+    if ign.size:
+        idx.add(int(ign[0]))
+    return np.array(sorted(idx), np.int64)
+
+
+
+
+__all__ = ["to_device", "run_cuda", "grad_rows_f64", "oracle_full", "oracle_rows",
+           "assert_loss_close", "assert_rowloss_close", "assert_grad_close", "sample_rows",
+           "workloads"]

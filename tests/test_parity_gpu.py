@@ -1,0 +1,355 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU
+float64 oracle on the same seeded inputs.
+
+Small and medium shapes are compared element by element over the whole
+batch. At the full workload sizes (the launch configuration the benchmark
+times), every scalar and per-row output is compared with the oracle over the
+whole batch, and the gradient on a fixed sample of rows; ignored rows are
+checked to be exact zeros everywhere."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import workloads
+from ce_gpu import (assert_grad_close, assert_loss_close, assert_rowloss_close, grad_rows_f64,
+                    oracle_full, oracle_rows, run_cuda, sample_rows, to_device)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from softmax_cross_entropy_gb300 import build, _lib
+    build.build()
+    _lib.load()
+
+
+def check_full(case, *, want_z=False, want_acc=False, want_pred=False, reduction=None):
+    red = reduction or case.reduction
+    out = run_cuda(case, want_z=want_z, want_acc=want_acc, want_pred=want_pred, reduction=red)
+    ref = oracle_full(case, reduction=red)
+    assert out["status"] == 0
+    if red == "none":
+        assert_rowloss_close(out["loss"], ref["loss"], case.dtype)
+        if want_z:
+            assert_rowloss_close(out["z_loss"], ref["z_loss"], case.dtype, "z_loss")
+        if want_acc:
+            assert np.array_equal(out["acc"], ref["acc"])
+    else:
+        assert_loss_close(out["loss"], ref["loss"], case.dtype)
+        if want_z:
+            assert_loss_close(out["z_loss"], ref["z_loss"], case.dtype, "z_loss")
+        if want_acc:
+            assert out["acc"] == np.float32(ref["acc"]) or (
+                math.isnan(out["acc"]) and math.isnan(ref["acc"]))
+    if want_pred:
+        assert np.array_equal(out["pred"], ref["pred"])
+    assert_grad_close(grad_rows_f64(out["x"]), ref["grad"], case.dtype)
+    return out, ref
+
+
+def check_sampled(case, *, want_z=False, want_acc=False, want_pred=True, reduction=None):
+    red = reduction or case.reduction
+    out = run_cuda(case, want_z=want_z, want_acc=want_acc, want_pred=want_pred, reduction=red)
+    assert out["status"] == 0
+    ref = oracle_full(case, reduction=red, want_grad=False)
+    if red == "none":
+        assert_rowloss_close(out["loss"], ref["loss"], case.dtype)
+    else:
+        assert_loss_close(out["loss"], ref["loss"], case.dtype)
+    if want_z:
+        f = assert_rowloss_close if red == "none" else assert_loss_close
+        f(out["z_loss"], ref["z_loss"], case.dtype, "z_loss")
+    if want_acc:
+        assert np.array_equal(np.float32(out["acc"]), np.float32(ref["acc"]))
+    if want_pred:
+        assert np.array_equal(out["pred"], ref["pred"])
+    idx = sample_rows(case)
+    rr = oracle_rows(case, idx, reduction=red)
+    assert_grad_close(grad_rows_f64(out["x"], idx), rr["grad"], case.dtype)
+    ign = np.nonzero(case.target == case.ignore_index)[0]
+    if ign.size:
+        g = out["x"][torch.as_tensor(ign, device=out["x"].device)]
+        assert bool((g.view(torch.int16 if case.dtype == "bf16" else torch.int32) == 0).all())
+    return out, ref
+
+
+# ------------------------------------------------------------------ workloads
+
+def test_small_config():
+    check_full(workloads.small(), want_acc=True, want_pred=True)
+
+
+@pytest.mark.parametrize("V", workloads.VSWEEP)
+def test_vsweep_reduced_rows(V):
+    check_full(workloads.vsweep(V=V, rows=96), want_acc=True, want_pred=True)
+
+
+@pytest.mark.parametrize("V", workloads.VSWEEP)
+def test_vsweep_full_size(V):
+    check_sampled(workloads.vsweep(V=V), want_acc=True)
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum"])
+def test_tt_fp32_full_size(reduction):
+    check_sampled(workloads.tt_fp32(reduction=reduction), want_acc=True)
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum"])
+def test_tt_fp32_reduced_rows(reduction):
+    check_full(workloads.tt_fp32(rows=40, reduction=reduction), want_acc=True, want_pred=True)
+
+
+def test_tt_fp32_all_ignored():
+    case = workloads.tt_fp32(variant="all_ignored")
+    m = run_cuda(case, want_acc=True, want_pred=True)
+    assert math.isnan(m["loss"]) and math.isnan(m["acc"])
+    assert bool((m["x"].view(torch.int32) == 0).all())  # every gradient is +0
+    assert (m["pred"] == -1).all()
+    s = run_cuda(case.with_(reduction="sum"))
+    assert s["loss"] == 0.0
+
+
+def test_tt_fp32_nonfinite_in_ignored_rows():
+    plain = workloads.tt_fp32(rows=300)
+    bad = workloads.tt_fp32(rows=300, variant="nonfinite_ignored")
+    assert np.array_equal(plain.target, bad.target)
+    assert not np.isfinite(bad.x).all()
+    for red in ("mean", "sum"):
+        a = run_cuda(plain.with_(reduction=red), want_pred=True)
+        b = run_cuda(bad.with_(reduction=red), want_pred=True)
+        assert a["loss"] == b["loss"]
+        assert np.array_equal(a["pred"], b["pred"])
+        assert torch.equal(a["x"], b["x"])  # valid rows identical, ignored rows +0
+    ref = oracle_full(bad)
+    assert_loss_close(run_cuda(bad)["loss"], ref["loss"], "f32")
+
+
+def test_softcap_zloss_reduced_rows():
+    check_full(workloads.softcap_z(rows=64), want_z=True, want_acc=True, want_pred=True)
+
+
+def test_softcap_zloss_full_size():
+    check_sampled(workloads.softcap_z(), want_z=True, want_acc=True)
+
+
+@pytest.mark.parametrize("reduction", ["none", "mean"])
+def test_weighted_reduced_rows(reduction):
+    check_full(workloads.weighted(rows=257, reduction=reduction), want_acc=True,
+               want_pred=True)
+
+
+@pytest.mark.parametrize("reduction", ["none", "mean"])
+def test_weighted_full_size(reduction):
+    check_sampled(workloads.weighted(reduction=reduction), want_acc=True)
+
+
+# ------------------------------------------------------------------ shapes and options
+
+EDGE_SHAPES = [(1, 1), (3, 2), (5, 3), (63, 127), (4, 4097), (2, 8191), (17, 8), (9, 16),
+               (33, 64), (7, 1000), (65, 4096), (3, 262144)]
+OPTION_SETS = [
+    dict(),
+    dict(label_smoothing=0.2, lse_square_scale=1e-3),
+    dict(softcap=5.0, label_smoothing=0.1),
+    dict(weight=True, label_smoothing=0.3, reduction="sum"),
+    dict(weight=True, reduction="none", lse_square_scale=1e-2),
+]
+
+
+@pytest.mark.parametrize("rows,V", EDGE_SHAPES)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("opt", range(len(OPTION_SETS)))
+def test_edge_shapes(rows, V, dtype, opt):
+    if rows * V > 2_000_000 and opt > 1:
+        pytest.skip("large shape covered by the first option sets")
+    case = workloads.random_case(1000 + rows * 7 + V, rows, V, dtype=dtype,
+                                 **dict(OPTION_SETS[opt]))
+    check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("dtype,V,rows", [("bf16", 16384, 203), ("f32", 8192, 77),
+                                          ("bf16", 32000, 50), ("bf16", 131072, 37)])
+def test_forced_cluster_sizes(monkeypatch, cluster, dtype, V, rows):
+    monkeypatch.setenv("GBCE_CLUSTER", str(cluster))
+    for opts in (dict(), dict(weight=True, label_smoothing=0.1, softcap=20.0,
+                               lse_square_scale=1e-3)):
+        case = workloads.random_case(7 + cluster, rows, V, dtype=dtype, **opts)
+        check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+@pytest.mark.parametrize("cfg", range(6))
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_forced_cta_shapes(monkeypatch, cfg, dtype):
+    # every CTA shape of the staged kernel, with the smallest cluster it fits
+    monkeypatch.setenv("GBCE_CFG", str(cfg))
+    case = workloads.random_case(40 + cfg, 150, 8192, dtype=dtype, label_smoothing=0.05,
+                                 lse_square_scale=1e-4)
+    check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+def test_general_path_forced(monkeypatch):
+    monkeypatch.setenv("GBCE_CLUSTER", "-1")  # skip the staged kernel
+    case = workloads.random_case(11, 70, 8192, dtype="bf16", weight=True, label_smoothing=0.1,
+                                 softcap=20.0, lse_square_scale=1e-3)
+    check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+def test_unaligned_base_pointer():
+    case = workloads.random_case(12, 31, 1024, dtype="bf16", label_smoothing=0.1)
+    x, _, _ = to_device(case)
+    buf = torch.empty(x.numel() + 1, dtype=x.dtype, device=x.device)
+    view = buf[1:].view(case.rows, case.V)
+    view.copy_(x)
+    assert view.data_ptr() % 16 != 0
+    out = run_cuda(case, x=view, want_pred=True)
+    ref = oracle_full(case)
+    assert_loss_close(out["loss"], ref["loss"], "bf16")
+    assert np.array_equal(out["pred"], ref["pred"])
+    assert_grad_close(grad_rows_f64(view), ref["grad"], "bf16")
+
+
+def test_argmax_ties_across_cta_slices():
+    rows, V = 48, 131072
+    case = workloads.vsweep(V=V, rows=rows)
+    x = workloads.bf16_bits_to_f32(case.x).copy()
+    top = np.float32(64.0)
+    cols = [(32767, 32768), (40000, 100000), (131071, 5), (65536, 65535), (98304, 98303)]
+    for r in range(rows):
+        a, b = cols[r % len(cols)]
+        x[r, a] = top
+        x[r, b] = top
+    case = case.with_(x=workloads.f32_to_bf16_bits(x))
+    out = run_cuda(case, want_pred=True, want_acc=True)
+    ref = oracle_full(case, want_grad=False)
+    valid = case.target != case.ignore_index
+    assert np.array_equal(out["pred"], ref["pred"])
+    expect = np.array([min(cols[r % len(cols)]) for r in range(rows)])
+    assert np.array_equal(out["pred"][valid], expect[valid])
+
+
+def test_int64_targets():
+    case = workloads.random_case(13, 50, 4096, dtype="bf16", label_smoothing=0.1)
+    x, t, _ = to_device(case)
+    out = run_cuda(case, target=t.to(torch.int64), want_pred=True)
+    ref = oracle_full(case)
+    assert_loss_close(out["loss"], ref["loss"], "bf16")
+    assert np.array_equal(out["pred"], ref["pred"])
+    assert_grad_close(grad_rows_f64(out["x"]), ref["grad"], "bf16")
+
+
+def test_custom_ignore_index():
+    case = workloads.random_case(14, 64, 512, dtype="f32", ignore_frac=0.0)
+    case.target[::3] = 7
+    case = case.with_(ignore_index=7)
+    check_full(case, want_acc=True, want_pred=True)
+
+
+def test_out_of_range_target_is_reported_and_ignored():
+    from softmax_cross_entropy_gb300 import _lib
+    case = workloads.random_case(15, 20, 256, dtype="f32", ignore_frac=0.0)
+    bad = case.target.copy()
+    bad[4] = 256
+    bad[9] = -3
+    out = run_cuda(case.with_(target=bad), want_pred=True)
+    assert out["status"] == _lib.CE_ERR_TARGET_RANGE
+    as_ignored = bad.copy()
+    as_ignored[[4, 9]] = case.ignore_index
+    ref = oracle_full(case.with_(target=as_ignored))
+    assert_loss_close(out["loss"], ref["loss"], "f32")
+    assert_grad_close(grad_rows_f64(out["x"]), ref["grad"], "f32")
+    assert out["pred"][4] == -1 and out["pred"][9] == -1
+    # the status word is cleared by the read
+    assert run_cuda(case)["status"] == 0
+
+
+def test_empty_batch():
+    case = workloads.random_case(16, 0, 64, dtype="f32")
+    m = run_cuda(case, want_acc=True, want_z=True)
+    assert math.isnan(m["loss"]) and math.isnan(m["z_loss"]) and math.isnan(m["acc"])
+    s = run_cuda(case.with_(reduction="sum"))
+    assert s["loss"] == 0.0
+
+
+def test_forward_only_leaves_logits_untouched():
+    case = workloads.vsweep(V=65536, rows=64)
+    x, _, _ = to_device(case)
+    before = x.clone()
+    out = run_cuda(case, x=x, grad=False, want_pred=True)
+    assert torch.equal(x, before)
+    ref = oracle_full(case, want_grad=False)
+    assert_loss_close(out["loss"], ref["loss"], "bf16")
+    assert np.array_equal(out["pred"], ref["pred"])
+
+
+def test_deterministic():
+    case = workloads.softcap_z(rows=300)
+    a = run_cuda(case, want_z=True)
+    b = run_cuda(case, want_z=True)
+    assert a["loss"] == b["loss"] and a["z_loss"] == b["z_loss"]
+    assert torch.equal(a["x"], b["x"])
+
+
+# ------------------------------------------------------------------ backward
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 4096), ("f32", 1000), ("bf16", 131072)])
+def test_backward_scales_stored_gradient(dtype, V):
+    import oracle
+    from softmax_cross_entropy_gb300 import _lib
+    rows = 24
+    case = workloads.random_case(17, rows, V, dtype=dtype, reduction="none")
+    out = run_cuda(case)
+    g = out["x"]
+    stored = grad_rows_f64(g)
+    dt = _lib.CE_BF16 if dtype == "bf16" else _lib.CE_F32
+    st = torch.cuda.current_stream().cuda_stream
+    one = torch.ones(1, device="cuda")
+    assert _lib.ce_bwd(one.data_ptr(), 0, g.data_ptr(), dt, rows, V, st) == 0
+    np.testing.assert_array_equal(grad_rows_f64(g), stored)  # factor 1: untouched
+    go = torch.from_numpy(np.random.default_rng(0).uniform(-2, 2, rows).astype(np.float32))
+    go[3] = 1.0
+    assert _lib.ce_bwd(go.cuda().data_ptr(), 1, g.data_ptr(), dt, rows, V, st) == 0
+    torch.cuda.synchronize()
+    want = oracle.backward(oracle_full(case)["grad"], go.numpy().astype(np.float64))
+    assert_grad_close(grad_rows_f64(g), want, dtype)
+    half = torch.full((1,), 0.5, device="cuda")
+    before = grad_rows_f64(g)
+    assert _lib.ce_bwd(half.data_ptr(), 0, g.data_ptr(), dt, rows, V, st) == 0
+    np.testing.assert_array_equal(grad_rows_f64(g), before * 0.5)
+
+
+def test_autograd_api_matches_c_abi():
+    import softmax_cross_entropy_gb300 as ce
+    case = workloads.weighted(rows=129, V=32000)
+    x, t, w = to_device(case)
+    x.requires_grad_(True)
+    out = ce.cross_entropy(x, t, weight=w, label_smoothing=case.label_smoothing,
+                           return_token_accuracy=True, return_predicted_tokens=True)
+    (out.loss * 3.0).backward()
+    ref = oracle_full(case)
+    assert_loss_close(float(out.loss), ref["loss"], "bf16")
+    assert np.array_equal(out.predicted_tokens.cpu().numpy(), ref["pred"])
+    assert_grad_close(grad_rows_f64(x.grad), 3.0 * ref["grad"], "bf16")
+    assert ce.device_status() == 0
+
+
+def test_module_reduction_none_backward():
+    import softmax_cross_entropy_gb300 as ce
+    case = workloads.random_case(18, 40, 2048, dtype="f32", reduction="none",
+                                 lse_square_scale=1e-3)
+    x, t, _ = to_device(case)
+    x.requires_grad_(True)
+    loss = ce.CrossEntropyLoss(reduction="none", lse_square_scale=1e-3)(x, t)
+    go = torch.linspace(-1, 1, 40, device="cuda")
+    loss.backward(go)
+    import oracle
+    ref = oracle_full(case)
+    assert_rowloss_close(loss.detach().cpu().numpy(), ref["loss"], "f32")
+    want = oracle.backward(ref["grad"], go.cpu().numpy().astype(np.float64))
+    assert_grad_close(grad_rows_f64(x.grad), want, "f32")
