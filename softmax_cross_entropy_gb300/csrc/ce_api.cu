@@ -33,8 +33,11 @@ struct DeviceInfo {
 
 // A launch plan for one (device, dtype, V, variant): which kernel, how many
 // CTAs per row, ring depth, dynamic shared memory and the resident grid.
+enum class Kind { General, Staged, Stream };
+
 struct Plan {
     const void* fn = nullptr;
+    Kind kind = Kind::General;
     bool staged = false;
     int nt = 0;
     int cluster = 1;
@@ -42,6 +45,8 @@ struct Plan {
     int slice_vec = 0;
     size_t smem = 0;
     int64_t max_units = 0;  // resident CTAs (cluster == 1) or clusters
+    // streaming kernel layout
+    int ng = 0, sg = 0, chunk_vec = 0, nchunk = 0, resident = 0;
 };
 
 using PlanKey = std::tuple<int, int, int64_t, bool, bool, int>;
@@ -196,14 +201,84 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, int cfg
     return true;
 }
 
+// The streaming kernel's layout: a row that fits twice in a group's share of
+// the ring stays resident; otherwise one group streams it twice.
+bool try_stream(int dtype, int64_t V, bool softcap, const DeviceInfo& dev, Plan* out,
+                ce_status* err) {
+    const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
+    const int64_t vec_row = V * bytes / 16;
+    const void* fn = stream_kernel(dtype, softcap);
+    if (!fn) return false;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) {
+        *err = cuda_failure(e, "cudaFuncGetAttributes");
+        return false;
+    }
+    const size_t ring_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(ring_max));
+    if (e != cudaSuccess) {
+        *err = cuda_failure(e, "cudaFuncSetAttribute");
+        return false;
+    }
+    const int force_ng = env_int("GBCE_STREAM_GROUPS", 0);
+    Plan p;
+    // resident: chunks of at most 32 KB, at least two rows per group
+    const int64_t rchunk = std::min<int64_t>(vec_row, 2048);
+    const int64_t rn = (vec_row + rchunk - 1) / rchunk;
+    for (int ng = kStreamMaxGroups; ng >= 1 && !p.ng; ng >>= 1) {
+        if (force_ng && ng != force_ng) continue;
+        for (int64_t sg = 3 * rn; sg >= 2 * rn; --sg) {
+            if (ng * sg > kStreamMaxSlots) continue;
+            if (static_cast<size_t>(ng * sg * rchunk * 16) > ring_max) continue;
+            p.ng = ng;
+            p.sg = static_cast<int>(sg);
+            p.chunk_vec = static_cast<int>(rchunk);
+            p.nchunk = static_cast<int>(rn);
+            p.resident = 1;
+            break;
+        }
+    }
+    if (!p.ng || env_int("GBCE_STREAM_TWICE", 0)) {
+        // streaming: 16 KB slots, one group, as deep a ring as fits
+        p = Plan();
+        p.ng = 1;
+        p.chunk_vec = static_cast<int>(std::min<int64_t>(vec_row, 1024));
+        p.nchunk = static_cast<int>((vec_row + p.chunk_vec - 1) / p.chunk_vec);
+        p.sg = static_cast<int>(std::min<size_t>(kStreamMaxSlots,
+                                                 ring_max / (static_cast<size_t>(p.chunk_vec) * 16)));
+        p.resident = 0;
+        if (p.sg < 2) return false;
+    }
+    p.fn = fn;
+    p.kind = Kind::Stream;
+    p.nt = 32 * (kStreamWarps + 1);
+    p.smem = static_cast<size_t>(p.ng) * p.sg * p.chunk_vec * 16;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, p.nt, p.smem);
+    if (e != cudaSuccess) {
+        *err = cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        return false;
+    }
+    if (occ < 1) return false;
+    p.max_units = std::min<int64_t>(static_cast<int64_t>(occ) * dev.sm_count, kMaxPartials);
+    *out = p;
+    return true;
+}
+
 ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth, bool aligned,
                     Plan* out) {
     // Tuning overrides: GBCE_CLUSTER forces the CTAs per row (1, 2, 4, 8 or
     // 16; -1 forces the general path) and GBCE_CFG the CTA shape index.
     const int forced_c = env_int("GBCE_CLUSTER", 0);
     const int forced_cfg = env_int("GBCE_CFG", -1);
+    // GBCE_KERNEL: 1 staged, 2 streaming, 3 general (0: automatic)
+    const int forced_kind = env_int("GBCE_KERNEL", 0);
     const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth,
-                      forced_c * 64 + forced_cfg);
+                      (forced_kind * 64 + forced_c) * 64 + forced_cfg +
+                          1000000 * env_int("GBCE_STREAM_GROUPS", 0) +
+                          100000000 * env_int("GBCE_STREAM_TWICE", 0));
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
         *out = it->second;
@@ -214,7 +289,12 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     if (rc != CE_OK) return rc;
     Plan best;
     const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
-    if (aligned && (V * bytes) % 16 == 0 && forced_c >= 0) {
+    const bool fast_ok = aligned && (V * bytes) % 16 == 0 && forced_c >= 0 && forced_kind != 3;
+    if (fast_ok && !wsmooth && forced_kind != 1) {
+        rc = CE_OK;
+        if (!try_stream(dtype, V, softcap, dev, &best, &rc) && rc != CE_OK) return rc;
+    }
+    if (fast_ok && best.kind == Kind::General && forced_kind != 2) {
         // Candidates: every shape and cluster size that fits. Prefer at
         // least two resident CTAs per SM (latency hiding across rows), then
         // the fewest CTAs per row (cheaper cluster merges), then the deeper
@@ -236,11 +316,12 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
                 if (score > best_score) {
                     best_score = score;
                     best = p;
+                    best.kind = Kind::Staged;
                 }
             }
         }
     }
-    if (!best.staged) {
+    if (best.kind == Kind::General) {
         best.fn = generic_kernel(dtype, softcap);
         best.nt = kGenericThreads;
         best.max_units = std::min<int64_t>(static_cast<int64_t>(dev.sm_count) * 8, kMaxPartials);
@@ -248,10 +329,14 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     if (env_int("GBCE_VERBOSE", 0))
         std::fprintf(stderr,
                      "gbce plan: dtype=%d V=%lld softcap=%d wsmooth=%d -> %s nt=%d C=%d "
-                     "stages=%d slice_vec=%d smem=%zu units=%lld\n",
+                     "stages=%d slice_vec=%d smem=%zu units=%lld ng=%d sg=%d chunk_vec=%d "
+                     "nchunk=%d resident=%d\n",
                      dtype, static_cast<long long>(V), softcap ? 1 : 0, wsmooth ? 1 : 0,
-                     best.staged ? "staged" : "general", best.nt, best.cluster, best.stages,
-                     best.slice_vec, best.smem, static_cast<long long>(best.max_units));
+                     best.kind == Kind::Stream ? "stream"
+                                               : (best.kind == Kind::Staged ? "staged" : "general"),
+                     best.nt, best.cluster, best.stages, best.slice_vec, best.smem,
+                     static_cast<long long>(best.max_units), best.ng, best.sg, best.chunk_vec,
+                     best.nchunk, best.resident);
     g_plans[key] = best;
     *out = best;
     return CE_OK;
@@ -356,7 +441,15 @@ extern "C" ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V, co
         return launch(fn, 1, kGenericThreads, 0, 1, st, &a);
     }
     const int64_t units = std::min<int64_t>(rows, p.max_units);
-    if (p.staged) {
+    if (p.kind == Kind::Stream) {
+        a.ng = p.ng;
+        a.sg = p.sg;
+        a.chunk_vec = p.chunk_vec;
+        a.nchunk = p.nchunk;
+        a.resident = p.resident;
+        return launch(p.fn, static_cast<int>(units), p.nt, p.smem, 1, st, &a);
+    }
+    if (p.kind == Kind::Staged) {
         a.slice_vec = p.slice_vec;
         a.stages = p.stages;
         return launch(p.fn, static_cast<int>(units * p.cluster), p.nt, p.smem, p.cluster, st, &a);

@@ -54,6 +54,12 @@ struct FwdArgs {
     // layout of the staged kernel
     int slice_vec;  // 16-byte vectors of one row owned by one CTA
     int stages;     // depth of the shared-memory ring
+    // layout of the streaming kernel
+    int ng;         // row groups per CTA
+    int sg;         // ring slots per group
+    int chunk_vec;  // 16-byte vectors per ring slot
+    int nchunk;     // slots one row occupies
+    int resident;   // 1: a row stays in its slots for both passes
     uint64_t timeout_ns;
     Scratch* scratch;
 };
@@ -86,9 +92,21 @@ __device__ __forceinline__ float block_sum_fixed(float v, float* sh) {
 // Prologue: the mean denominator D = sum of w[t_i] over counted rows and the
 // counted-row number. Every CTA computes them in the same fixed order, so
 // all CTAs hold bit-identical values without inter-CTA communication.
-template <int NT>
-__device__ __forceinline__ void denominators(const FwdArgs& a, float* sh, float& D,
-                                             int& n_valid) {
+struct CtaSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// Barrier over the first `n` threads of the CTA (named barrier `id`).
+struct NamedSync {
+    int id, n;
+    __device__ __forceinline__ void operator()() const {
+        asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+    }
+};
+
+template <int NT, typename Sync = CtaSync>
+__device__ __forceinline__ void denominators(const FwdArgs& a, float* sh, float& D, int& n_valid,
+                                             Sync sync = Sync()) {
     float d = 0.f;
     int n = 0;
     for (int64_t i = threadIdx.x; i < a.rows; i += NT) {
@@ -98,18 +116,24 @@ __device__ __forceinline__ void denominators(const FwdArgs& a, float* sh, float&
             ++n;
         }
     }
-    D = block_sum_fixed<NT>(d, sh);
-    __syncthreads();
+    d = warp_sum(d);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = d;
+    sync();
+    float dd = 0.f;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) dd += sh[w];
+    D = dd;
+    sync();
     int v = n;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if ((threadIdx.x & 31) == 0) reinterpret_cast<int*>(sh)[threadIdx.x >> 5] = v;
-    __syncthreads();
+    sync();
     int r = 0;
 #pragma unroll
     for (int w = 0; w < NT / 32; ++w) r += reinterpret_cast<int*>(sh)[w];
     n_valid = r;
-    __syncthreads();
+    sync();
     if (!a.weight) D = static_cast<float>(n_valid);  // exact count
 }
 
@@ -260,6 +284,10 @@ const void* staged_kernel_f32_nocap_plain(int cfg);
 const void* staged_kernel_f32_nocap_wsmooth(int cfg);
 const void* staged_kernel_f32_softcap_plain(int cfg);
 const void* staged_kernel_f32_softcap_wsmooth(int cfg);
+const void* stream_kernel(int dtype, bool softcap);
+constexpr int kStreamWarps = 16;      // consumer warps of the streaming kernel
+constexpr int kStreamMaxSlots = 48;   // ring slots (all groups) of the streaming kernel
+constexpr int kStreamMaxGroups = 8;
 const void* generic_kernel(int dtype, bool softcap);
 const void* bwd_kernel(int dtype);
 
