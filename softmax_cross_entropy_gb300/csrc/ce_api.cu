@@ -201,62 +201,82 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, int cfg
     return true;
 }
 
-// The streaming kernel's layout: a row that fits twice in a group's share of
-// the ring stays resident; otherwise one group streams it twice.
+// The streaming kernel's layout. NW consumer warps (8 by default, with 8
+// vectors a thread a slot, or 16 with 4). A slot holds VPT vectors
+// for each thread of a group (or the whole row when it is shorter). A row
+// that fits in one slot with room for two more stays resident, with as many
+// row groups as the ring holds; otherwise one group of all consumer warps
+// streams the row twice.
 bool try_stream(int dtype, int64_t V, bool softcap, const DeviceInfo& dev, Plan* out,
                 ce_status* err) {
     const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
     const int64_t vec_row = V * bytes / 16;
-    const void* fn = stream_kernel(dtype, softcap);
-    if (!fn) return false;
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
-    if (e != cudaSuccess) {
-        *err = cuda_failure(e, "cudaFuncGetAttributes");
-        return false;
-    }
-    const size_t ring_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(ring_max));
-    if (e != cudaSuccess) {
-        *err = cuda_failure(e, "cudaFuncSetAttribute");
-        return false;
-    }
     const int force_ng = env_int("GBCE_STREAM_GROUPS", 0);
+    const bool force_twice = env_int("GBCE_STREAM_TWICE", 0) != 0;
+    const int nw = env_int("GBCE_STREAM_WARPS", 8) == 16 ? 16 : 8;
+    const int vpt_res = nw == 8 ? 8 : 4;  // the two compiled shapes
     Plan p;
-    // resident: chunks of at most 32 KB, at least two rows per group
-    const int64_t rchunk = std::min<int64_t>(vec_row, 2048);
-    const int64_t rn = (vec_row + rchunk - 1) / rchunk;
-    for (int ng = kStreamMaxGroups; ng >= 1 && !p.ng; ng >>= 1) {
-        if (force_ng && ng != force_ng) continue;
-        for (int64_t sg = 3 * rn; sg >= 2 * rn; --sg) {
-            if (ng * sg > kStreamMaxSlots) continue;
-            if (static_cast<size_t>(ng * sg * rchunk * 16) > ring_max) continue;
-            p.ng = ng;
-            p.sg = static_cast<int>(sg);
-            p.chunk_vec = static_cast<int>(rchunk);
-            p.nchunk = static_cast<int>(rn);
-            p.resident = 1;
-            break;
+    const void* fn = nullptr;
+    size_t ring_max = 0;
+    auto prepare = [&](int vpt) -> bool {
+        fn = stream_kernel(dtype, softcap, vpt, nw);
+        if (!fn) return false;
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+        if (e == cudaSuccess) {
+            ring_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(ring_max));
+        }
+        if (e != cudaSuccess) {
+            *err = cuda_failure(e, "stream kernel attributes");
+            return false;
+        }
+        return true;
+    };
+    if (!force_twice) {
+        if (!prepare(vpt_res)) return false;
+        for (int ng = kStreamMaxGroups; ng >= 1 && !p.ng; ng >>= 1) {
+            if (force_ng && ng != force_ng) continue;
+            if (nw % ng) continue;
+            const int64_t cap = static_cast<int64_t>(vpt_res) * 32 * (nw / ng);
+            const int64_t nchunk = (vec_row + cap - 1) / cap;
+            const int64_t cvec = nchunk == 1 ? vec_row : cap;
+            for (int64_t sg = 3 * nchunk; sg >= 2 * nchunk; --sg) {
+                if (ng * sg > kStreamMaxSlots) continue;
+                if (static_cast<size_t>(ng * sg * cvec * 16) > ring_max) continue;
+                p.ng = ng;
+                p.sg = static_cast<int>(sg);
+                p.chunk_vec = static_cast<int>(cvec);
+                p.nchunk = static_cast<int>(nchunk);
+                p.resident = 1;
+                break;
+            }
         }
     }
-    if (!p.ng || env_int("GBCE_STREAM_TWICE", 0)) {
-        // streaming: 16 KB slots, one group, as deep a ring as fits
+    if (!p.ng) {
+        const int vpt = vpt_res;
+        if (!prepare(vpt)) return false;
         p = Plan();
-        p.ng = 1;
-        p.chunk_vec = static_cast<int>(std::min<int64_t>(vec_row, 1024));
+        // one group by default; GBCE_STREAM_GROUPS splits the warps into
+        // groups that stream different rows
+        p.ng = (force_ng > 0 && nw % force_ng == 0) ? force_ng : 1;
+        p.chunk_vec =
+            static_cast<int>(std::min<int64_t>(vec_row, 32 * (nw / p.ng) * vpt));
         p.nchunk = static_cast<int>((vec_row + p.chunk_vec - 1) / p.chunk_vec);
-        p.sg = static_cast<int>(std::min<size_t>(kStreamMaxSlots,
-                                                 ring_max / (static_cast<size_t>(p.chunk_vec) * 16)));
+        p.sg = static_cast<int>(std::min<size_t>(
+            kStreamMaxSlots / p.ng, ring_max / (static_cast<size_t>(p.ng) * p.chunk_vec * 16)));
+        const int want_slots = env_int("GBCE_STREAM_SLOTS", 0);
+        if (want_slots >= 2) p.sg = std::min(p.sg, want_slots);
         p.resident = 0;
         if (p.sg < 2) return false;
     }
     p.fn = fn;
     p.kind = Kind::Stream;
-    p.nt = 32 * (kStreamWarps + 1);
+    p.nt = 32 * (nw + 1);
     p.smem = static_cast<size_t>(p.ng) * p.sg * p.chunk_vec * 16;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, p.nt, p.smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, p.nt, p.smem);
     if (e != cudaSuccess) {
         *err = cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         return false;
@@ -278,7 +298,9 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth,
                       (forced_kind * 64 + forced_c) * 64 + forced_cfg +
                           1000000 * env_int("GBCE_STREAM_GROUPS", 0) +
-                          100000000 * env_int("GBCE_STREAM_TWICE", 0));
+                          100000000 * env_int("GBCE_STREAM_TWICE", 0) +
+                          13 * env_int("GBCE_STREAM_SLOTS", 0) +
+                          17 * env_int("GBCE_STREAM_WARPS", 0));
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
         *out = it->second;
@@ -320,6 +342,11 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
                 }
             }
         }
+    }
+    if ((forced_kind == 1 && best.kind != Kind::Staged) ||
+        (forced_kind == 2 && best.kind != Kind::Stream)) {
+        g_last_error = "the kernel forced by GBCE_KERNEL cannot run this shape";
+        return CE_ERR_UNSUPPORTED;
     }
     if (best.kind == Kind::General) {
         best.fn = generic_kernel(dtype, softcap);

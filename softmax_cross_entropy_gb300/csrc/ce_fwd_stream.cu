@@ -40,91 +40,228 @@ constexpr uint32_t kStreamCopyChunk = 32768;
 
 __device__ __forceinline__ int64_t imin64(int64_t x, int64_t y) { return x < y ? x : y; }
 
+// z = softcap(x) for a pair of logits.
+template <bool SOFTCAP>
+__device__ __forceinline__ float2 capped2(float x0, float x1, const FwdArgs& a) {
+    if (!SOFTCAP) return make_float2(x0, x1);
+    return make_float2(a.softcap * tanh_from_scaled(x0 * a.sc_k2),
+                       a.softcap * tanh_from_scaled(x1 * a.sc_k2));
+}
+
+// exp2 arguments (z - m) * log2(e) for a pair. bf16 logits use one packed
+// FFMA against the rounded m*log2(e) (that rounding is common to a thread's
+// terms); fp32 logits subtract first.
+template <typename T>
+__device__ __forceinline__ float2 exp_arg2(float2 z, float m, float mL) {
+    if (sizeof(T) == 2) return ffma2(z, make_float2(kLog2e, kLog2e), make_float2(-mL, -mL));
+    return fmul2(fadd2(z, make_float2(-m, -m)), make_float2(kLog2e, kLog2e));
+}
+
 // Row statistics of one thread during pass 1 (see RowStats): the running
-// reference m (the largest z seen), S = sum exp(z - m), the running sum of
-// z for label smoothing, the element count, and the first argmax of x.
-template <typename T, bool SOFTCAP>
+// reference m (the largest z seen; a finite sentinel before the first
+// element), S = sum exp(z - m), the running sum of z for label smoothing, the
+// element count, and the first vector holding the largest raw logit.
+// add_chunk takes the thread's VPT vectors of one ring slot at once: one
+// max and one rescale per slot, then VPT independent exp-sum chains of
+// packed pairs.
+template <typename T, bool SOFTCAP, int VPT>
 struct PassOne {
     using VT = Vec<T>;
     static constexpr int VE = VT::N;
-    float m = -INFINITY, mL = 0.f, S = 0.f, sumz = 0.f, n = 0.f, xmax = -INFINITY;
-    int idx = INT_MAX;
+    float m = -3.0e38f, mL = -3.0e38f * kLog2e, S = 0.f, sumz = 0.f, xmax = -INFINITY;
+    int best = INT_MAX, nel = 0;  // best: first element index of the largest raw logit
 
-    // exp argument: bf16 logits use one FFMA (the rounding of m*log2e is
-    // common to a thread's terms); fp32 logits subtract first.
-    __device__ __forceinline__ float arg(float z) const {
-        if (sizeof(T) == 2) return fmaf(z, kLog2e, -mL);
-        return (z - m) * kLog2e;
-    }
-
-    __device__ __forceinline__ void add(const uint4& q, int col0, const FwdArgs& a,
-                                        bool smooth) {
-        float f[VE];
-        VT::unpack(q, f);
-        const float vm = VT::vmax(q);
-        if (vm > xmax) {  // first occurrence of a new thread maximum
-            xmax = vm;
-            int j0 = VE - 1;
+    // q[k] is vector vidx0 + k * stride; unless FULL, it exists only when
+    // vidx0 + k * stride < vend (the thread's vectors of the slot, in
+    // increasing index order).
+    template <bool FULL>
+    __device__ __forceinline__ void add_chunk(const uint4 (&q)[VPT], int vidx0, int vend,
+                                              int stride, const FwdArgs& a, bool smooth) {
+        float cm = -INFINITY;
+        int ck = 0;
+        int nk = 0;
 #pragma unroll
-            for (int j = VE - 1; j >= 0; --j)
-                if (f[j] == vm) j0 = j;
-            idx = col0 + j0;
-            const float mz = SOFTCAP ? a.softcap * tanh_from_scaled(vm * a.sc_k2) : vm;
-            if (mz > m) {
-                if (S > 0.f) S *= ex2((m - mz) * kLog2e);
-                m = mz;
-                mL = mz * kLog2e;
+        for (int k = 0; k < VPT; ++k) {
+            if (FULL || vidx0 + k * stride < vend) {
+                ++nk;
+                const float vm = VT::vmax(q[k]);
+                const bool b = vm > cm;
+                cm = b ? vm : cm;
+                ck = b ? k : ck;
             }
         }
+        const bool better = cm > xmax;
+        if (__any_sync(0xffffffffu, better)) {
+            // a new thread maximum (frequent at a row's start, rare later):
+            // find its first element in the vector that holds it
+            if (better) {
+                uint4 qb = q[0];
 #pragma unroll
-        for (int j = 0; j < VE; ++j) {
-            float z;
-            if (SOFTCAP) {
-                z = a.softcap * tanh_from_scaled(f[j] * a.sc_k2);
-            } else {
-                z = f[j];
+                for (int k = 1; k < VPT; ++k)
+                    if (k == ck) qb = q[k];
+                float fb[VE];
+                VT::unpack(qb, fb);
+                int j0 = VE - 1;
+#pragma unroll
+                for (int j = VE - 1; j >= 0; --j)
+                    if (fb[j] == cm) j0 = j;
+                xmax = cm;
+                best = (vidx0 + ck * stride) * VE + j0;
             }
-            S += ex2(arg(z));
-            if (smooth) sumz += z;
         }
-        n += static_cast<float>(VE);
+        const float mz = SOFTCAP ? a.softcap * tanh_from_scaled(cm * a.sc_k2) : cm;
+        const float mn = fmaxf(m, mz);
+        S *= ex2((m - mn) * kLog2e);
+        m = mn;
+        mL = fmaxf(mn, -1.0e30f) * kLog2e;
+        float2 sk[VPT], zk[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            sk[k] = make_float2(0.f, 0.f);
+            zk[k] = make_float2(0.f, 0.f);
+            if (FULL || vidx0 + k * stride < vend) {
+                float f[VE];
+                VT::unpack(q[k], f);
+#pragma unroll
+                for (int j = 0; j < VE; j += 2) {
+                    const float2 z = capped2<SOFTCAP>(f[j], f[j + 1], a);
+                    const float2 ar = exp_arg2<T>(z, m, mL);
+                    sk[k] = fadd2(sk[k], make_float2(ex2(ar.x), ex2(ar.y)));
+                    if (smooth) zk[k] = fadd2(zk[k], z);
+                }
+            }
+        }
+        float2 acc = sk[0], zacc = zk[0];
+#pragma unroll
+        for (int k = 1; k < VPT; ++k) {
+            acc = fadd2(acc, sk[k]);
+            if (smooth) zacc = fadd2(zacc, zk[k]);
+        }
+        S += acc.x + acc.y;
+        if (smooth) sumz += zacc.x + zacc.y;
+        nel += nk * VE;
     }
 
-    __device__ __forceinline__ RowStats stats(bool smooth) const {
-        RowStats r = empty_stats();
-        r.xmax = xmax;
-        r.idx = idx;
-        if (m != -INFINITY) {
-            r.m = m;
-            r.S = S;
-            r.Wn = n;
-            r.SZ = smooth ? sumz - n * m : 0.f;
+};
+
+// Row statistics of a warp or group, all relative to M = softcap(X), the
+// largest z: S = sum exp(z - M), SZ = sum (z - M) (label smoothing), n the
+// element count, X the largest raw logit and I its first index.
+struct RowSums {
+    float M, S, SZ, n, X;
+    int I;
+};
+
+template <bool SOFTCAP>
+__device__ __forceinline__ float capped1(float x, const FwdArgs& a) {
+    return SOFTCAP ? a.softcap * tanh_from_scaled(x * a.sc_k2) : x;
+}
+
+// Two-phase merge over the lanes of a warp, each lane holding (m, S, SZ, n,
+// x, i) relative to its own m: a butterfly on the raw maximum (with the first
+// index on ties), one rescale per lane, then a butterfly of plain sums. Every
+// lane ends with the same bits.
+template <bool SOFTCAP>
+__device__ __forceinline__ RowSums warp_merge(float m, float S, float SZ, float n, float x, int i,
+                                              bool smooth, const FwdArgs& a) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ox = __shfl_xor_sync(0xffffffffu, x, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        if (ox > x || (ox == x && oi < i)) {
+            x = ox;
+            i = oi;
         }
-        return r;
+    }
+    const float M = capped1<SOFTCAP>(x, a);
+    const bool live = S > 0.f && M != -INFINITY;
+    float s = live ? S * ex2((m - M) * kLog2e) : 0.f;
+    float sz = (smooth && live) ? fmaf(n, m - M, SZ) : 0.f;
+    float nn = n;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (smooth) sz += __shfl_xor_sync(0xffffffffu, sz, o);
+        nn += __shfl_xor_sync(0xffffffffu, nn, o);
+    }
+    return RowSums{M, s, sz, nn, x, i};
+}
+
+// Pass 2 for the thread's VPT vectors of one slot: gradient
+// As * exp(z - M) + Bc (times dz/dx under softcap), packed and stored.
+template <typename T, bool SOFTCAP, int VPT, bool FULL>
+__device__ __forceinline__ void grad_chunk(const uint4* ch, uint4* outv, int tg, int nv, int GT,
+                                           float M, float ML, float As, float Bc,
+                                           const FwdArgs& a) {
+    using VT = Vec<T>;
+    constexpr int VE = VT::N;
+    uint4 q[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+        if (FULL || tg + k * GT < nv) q[k] = ch[tg + k * GT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        if (FULL || tg + k * GT < nv) {
+            float f[VE], gr[VE];
+            VT::unpack(q[k], f);
+#pragma unroll
+            for (int j = 0; j < VE; j += 2) {
+                float2 fac = make_float2(1.f, 1.f);
+                float2 z = make_float2(f[j], f[j + 1]);
+                if (SOFTCAP) {
+                    const float t0 = tanh_from_scaled(f[j] * a.sc_k2);
+                    const float t1 = tanh_from_scaled(f[j + 1] * a.sc_k2);
+                    fac = make_float2(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
+                    z = make_float2(a.softcap * t0, a.softcap * t1);
+                }
+                const float2 ar = exp_arg2<T>(z, M, ML);
+                float2 g = ffma2(make_float2(As, As), make_float2(ex2(ar.x), ex2(ar.y)),
+                                 make_float2(Bc, Bc));
+                if (SOFTCAP) g = fmul2(g, fac);
+                gr[j] = g.x;
+                gr[j + 1] = g.y;
+            }
+            outv[k * GT] = VT::pack(gr);
+        }
+    }
+}
+
+// Ring position of a group: slot within the group's slots and the phase bit
+// of its current use, advanced without division.
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int sg) {
+        if (++slot == sg) {
+            slot = 0;
+            phase ^= 1u;
+        }
     }
 };
 
 }  // namespace
 
-template <typename T, bool SOFTCAP>
-__global__ void __launch_bounds__(32 * (kStreamWarps + 1), 1)
+// NW consumer warps plus the producer warp; the register file is split
+// across the SM's four sub-partitions, so 17 warps allow 96 registers a
+// thread and 9 warps allow 168.
+template <typename T, bool SOFTCAP, int VPT, int NW>
+__global__ void __launch_bounds__(32 * (NW + 1), 1)
 ce_fwd_stream(const __grid_constant__ FwdArgs a) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;
-    constexpr int NW = kStreamWarps;
     constexpr int NTC = 32 * NW;  // consumer threads
 
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full_bar[kStreamMaxSlots];
     __shared__ __align__(8) uint64_t empty_bar[kStreamMaxSlots];
-    __shared__ __align__(16) RowStats grec[kStreamMaxGroups][2][NW];
+    __shared__ __align__(16) RowSums grec[kStreamMaxGroups][2][NW];
     __shared__ float red_p[NW];
     __shared__ double gpart_l[kStreamMaxGroups], gpart_z[kStreamMaxGroups];
-    __shared__ long long gpart_c[kStreamMaxGroups];
     __shared__ int s_failed;
     __shared__ float s_D;
     __shared__ int s_nvalid;
-    __shared__ uint32_t s_issued[kStreamMaxSlots];  // last issued use of a slot, +1
+    __shared__ uint32_t s_issued[kStreamMaxSlots];  // 0, or 2 + phase of the last use
+    __shared__ int s_correct[kStreamMaxGroups];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -146,6 +283,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
             mbar_init(smem_u32(&empty_bar[i]), static_cast<uint32_t>(G));
             s_issued[i] = 0;
         }
+        for (int g = 0; g < kStreamMaxGroups; ++g) s_correct[g] = 0;
         s_failed = 0;
         fence_mbar_init();
     }
@@ -156,9 +294,13 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
         if (lane == 0) {
             const uint64_t pol_keep = l2_evict_last_policy();
             const uint64_t pol_once = l2_evict_first_policy();
-            uint32_t seq[kStreamMaxGroups];
+            int pslot[kStreamMaxGroups];
+            uint32_t pphase[kStreamMaxGroups];
 #pragma unroll
-            for (int g = 0; g < kStreamMaxGroups; ++g) seq[g] = 0;
+            for (int k = 0; k < kStreamMaxGroups; ++k) {
+                pslot[k] = 0;
+                pphase[k] = 0;
+            }
             bool failed = false;
             int g = 0;
             for (int64_t r = cid; r < a.rows && !failed; r += ncta) {
@@ -168,12 +310,20 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                 const int passes = a.resident ? 1 : 2;
                 for (int p = 0; p < passes && !failed; ++p) {
                     for (int c = 0; c < nchunk; ++c) {
-                        uint32_t sq = 0;
+                        int ls = 0;
+                        uint32_t ph = 0;
 #pragma unroll
-                        for (int k = 0; k < kStreamMaxGroups; ++k)
-                            if (k == gg) sq = seq[k]++;
-                        const int slot = gg * sg + static_cast<int>(sq % sg);
-                        const uint32_t ph = (sq / sg) & 1u;
+                        for (int k = 0; k < kStreamMaxGroups; ++k) {
+                            if (k == gg) {
+                                ls = pslot[k];
+                                ph = pphase[k];
+                                if (++pslot[k] == sg) {
+                                    pslot[k] = 0;
+                                    pphase[k] ^= 1u;
+                                }
+                            }
+                        }
+                        const int slot = gg * sg + ls;
                         if (!mbar_wait_bounded(smem_u32(&empty_bar[slot]), ph ^ 1u,
                                                a.timeout_ns)) {
                             failed = true;
@@ -191,7 +341,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                         for (uint32_t off = 0; off < bytes; off += kStreamCopyChunk)
                             bulk_g2s(dst + off, src + off, min(kStreamCopyChunk, bytes - off), fb,
                                      pol);
-                        s_issued[slot] = sq + 1;
+                        s_issued[slot] = 2u + ph;  // nonzero: used; low bit: phase of the last use
                     }
                 }
             }
@@ -221,22 +371,28 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
         const bool gleader = tid == g * GT;
         double accL = 0.0, accZ = 0.0;
         long long accC = 0;
-        uint32_t seq = 0;
+        RingPos pos;
         bool failed = false;
         int rp = 0;
+        const int vrow = static_cast<int>(vec_row);
+        // the thread of the group that handles vector v of a row (pass 1 and
+        // pass 2 use the same assignment)
+        // (GT is a power of two and every slot but a lone one spans a
+        // multiple of GT vectors)
+        auto owner_of = [&](int v) { return v & (GT - 1); };
 
         for (int64_t r = cid + static_cast<int64_t>(g) * ncta; r < a.rows;
              r += static_cast<int64_t>(ng) * ncta) {
             const int64_t t = load_target(a, r);
             const bool counts = row_counts(a, t);
+            T* xrow = reinterpret_cast<T*>(a.x) + r * a.V;
+            uint4* rowv = reinterpret_cast<uint4*>(xrow);
             if (gleader && t != a.ignore_index && !counts)
                 atomicOr(&a.scratch->status, kDevErrTarget);
             if (!counts) {
                 // Ignored row: exact +0 gradient, zero per-row outputs, pred -1.
-                if (a.grad) {
-                    uint4* rowv = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.x) + r * a.V);
-                    for (int64_t v = tg; v < vec_row; v += GT) rowv[v] = make_uint4(0u, 0u, 0u, 0u);
-                }
+                if (a.grad)
+                    for (int v = tg; v < vrow; v += GT) rowv[v] = make_uint4(0u, 0u, 0u, 0u);
                 if (gleader) {
                     if (a.reduction == kRedNone) {
                         a.loss[r] = 0.f;
@@ -247,47 +403,62 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                 }
                 continue;
             }
+            const int tvec = static_cast<int>(t / VE);
+            const bool t_owner = tg == owner_of(tvec);
             float xt = 0.f;
-            if (gleader) xt = VT::load1(a.x, r * a.V + t);  // before any store to this row
+            if (gleader || t_owner) xt = VT::load1(xrow, t);  // before any store to this row
             const float wt = a.weight ? __ldg(a.weight + t) : 1.f;
 
             // ---- pass 1: thread statistics over the row's slots
-            PassOne<T, SOFTCAP> st;
-            const uint32_t seq0 = seq;
-            for (int c = 0; c < nchunk; ++c, ++seq) {
-                const int slot = g * sg + static_cast<int>(seq % sg);
-                if (!failed && !mbar_wait_bounded(smem_u32(&full_bar[slot]), (seq / sg) & 1u,
+            PassOne<T, SOFTCAP, VPT> st;
+            const RingPos pos0 = pos;
+            for (int c = 0, v0 = 0; c < nchunk; ++c, v0 += chunk_vec) {
+                const int slot = g * sg + pos.slot;
+                if (!failed && !mbar_wait_bounded(smem_u32(&full_bar[slot]), pos.phase,
                                                   a.timeout_ns)) {
                     failed = true;
                     atomicOr(&a.scratch->status, kDevErrTimeout);
                 }
                 const uint4* ch = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * chunk_bytes);
-                const int64_t v0 = static_cast<int64_t>(c) * chunk_vec;
-                const int nv = static_cast<int>(imin64(chunk_vec, vec_row - v0));
-                for (int v = tg; v < nv; v += GT)
-                    st.add(ch[v], static_cast<int>((v0 + v) * VE), a, smooth);
+                const int nv = min(chunk_vec, vrow - v0);
+                // this thread's vectors of the slot: tg, tg + GT, ... below nv
+                uint4 q[VPT];
+                if (nv == VPT * GT) {
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k) q[k] = ch[tg + k * GT];
+                    st.template add_chunk<true>(q, v0 + tg, v0 + nv, GT, a, smooth);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k)
+                        if (tg + k * GT < nv) q[k] = ch[tg + k * GT];
+                    st.template add_chunk<false>(q, v0 + tg, v0 + nv, GT, a, smooth);
+                }
                 if (!a.resident) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
                 }
+                pos.next(sg);
             }
 
-            // ---- merge: warp butterfly, one group barrier, lane-parallel group merge
-            RowStats ws = st.stats(smooth);
-            warp_stats_allreduce<32>(ws);
-            if (lane == 0) grec[g][rp][wg] = ws;
+            // ---- merge: warp, then one group barrier, then the group's warp records
+            const RowSums wsum = warp_merge<SOFTCAP>(
+                st.m, st.S, smooth ? st.sumz - static_cast<float>(st.nel) * st.m : 0.f,
+                static_cast<float>(st.nel), st.xmax, st.best, smooth, a);
+            if (lane == 0) grec[g][rp][wg] = wsum;
             group_sync();
-            RowStats tot = lane < G ? grec[g][rp][lane] : empty_stats();
-            warp_stats_allreduce<32>(tot);
+            const RowSums rec = lane < G ? grec[g][rp][lane]
+                                         : RowSums{-INFINITY, 0.f, 0.f, 0.f, -INFINITY, INT_MAX};
+            const RowSums tot = warp_merge<SOFTCAP>(rec.M, rec.S, rec.SZ, rec.n, rec.X, rec.I,
+                                                    smooth, a);
             rp ^= 1;
-            const float M = tot.m;
+            const float M = tot.M;
             const float logS = logf(tot.S);
 
             if (gleader) {
                 const float zt = SOFTCAP ? a.softcap * tanh_from_scaled(xt * a.sc_k2) : xt;
                 float zl;
                 const float l = row_loss(a, M, logS, zt, wt, static_cast<float>(a.V), tot.SZ, zl);
-                const bool correct = static_cast<int64_t>(tot.idx) == t;
+                const bool correct = tot.I < vrow * VE && static_cast<int64_t>(tot.I) == t;
                 if (a.reduction == kRedNone) {
                     a.loss[r] = l;
                     if (a.want_z) a.zloss[r] = zl;
@@ -297,65 +468,56 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                     accZ += static_cast<double>(zl);
                     accC += correct ? 1 : 0;
                 }
-                if (a.want_pred) a.pred[r] = tot.idx;
+                if (a.want_pred) a.pred[r] = tot.I < vrow * VE ? tot.I : -1;
             }
 
             // ---- pass 2: gradient in place
             //   scale * [ (1-eps) w_t (p - onehot) + (eps/V)(V p - 1) + 2 lam lse p ] * dz/dx
+            // The one-hot term is added by the owner of the target's vector,
+            // which rewrites that element after storing the vector.
             const float lse = M + logS;
             const float As = scale * ((1.f - a.eps) * wt + a.eps + 2.f * a.lam * lse) / tot.S;
             const float Bc = -scale * a.eps * inv_V;
-            const float tfix = -scale * (1.f - a.eps) * wt;
             const float ML = M * kLog2e;
-            const int64_t tvec = t / VE;
-            const int tj = static_cast<int>(t % VE);
-            uint4* rowv = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.x) + r * a.V);
-            if (a.resident) seq = seq0;
-            for (int c = 0; c < nchunk; ++c, ++seq) {
-                const int slot = g * sg + static_cast<int>(seq % sg);
+            if (a.resident) pos = pos0;
+            for (int c = 0, v0 = 0; c < nchunk; ++c, v0 += chunk_vec) {
+                const int slot = g * sg + pos.slot;
                 if (!a.resident && !failed &&
-                    !mbar_wait_bounded(smem_u32(&full_bar[slot]), (seq / sg) & 1u, a.timeout_ns)) {
+                    !mbar_wait_bounded(smem_u32(&full_bar[slot]), pos.phase, a.timeout_ns)) {
                     failed = true;
                     atomicOr(&a.scratch->status, kDevErrTimeout);
                 }
                 const uint4* ch = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * chunk_bytes);
-                const int64_t v0 = static_cast<int64_t>(c) * chunk_vec;
-                const int nv = static_cast<int>(imin64(chunk_vec, vec_row - v0));
+                const int nv = min(chunk_vec, vrow - v0);
                 if (a.grad && !failed) {
-                    for (int v = tg; v < nv; v += GT) {
-                        float f[VE], gr[VE], th[VE];
-                        VT::unpack(ch[v], f);
-#pragma unroll
-                        for (int j = 0; j < VE; ++j) {
-                            float z = f[j];
-                            if (SOFTCAP) {
-                                th[j] = tanh_from_scaled(f[j] * a.sc_k2);
-                                z = a.softcap * th[j];
-                            }
-                            const float e = sizeof(T) == 2 ? ex2(fmaf(z, kLog2e, -ML))
-                                                           : ex2((z - M) * kLog2e);
-                            gr[j] = fmaf(As, e, Bc);
-                        }
-                        if (v0 + v == tvec) {
-#pragma unroll
-                            for (int j = 0; j < VE; ++j)
-                                if (j == tj) gr[j] += tfix;
-                        }
-                        if (SOFTCAP) {
-#pragma unroll
-                            for (int j = 0; j < VE; ++j) gr[j] *= fmaf(-th[j], th[j], 1.f);
-                        }
-                        rowv[v0 + v] = VT::pack(gr);
-                    }
+                    if (nv == VPT * GT)
+                        grad_chunk<T, SOFTCAP, VPT, true>(ch, rowv + v0 + tg, tg, nv, GT, M, ML,
+                                                          As, Bc, a);
+                    else
+                        grad_chunk<T, SOFTCAP, VPT, false>(ch, rowv + v0 + tg, tg, nv, GT, M, ML,
+                                                           As, Bc, a);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+                pos.next(sg);
+            }
+            if (a.grad && !failed && t_owner) {
+                float e, fac = 1.f;
+                if (SOFTCAP) {
+                    const float th = tanh_from_scaled(xt * a.sc_k2);
+                    fac = fmaf(-th, th, 1.f);
+                    e = ex2((a.softcap * th - M) * kLog2e);
+                } else {
+                    e = ex2((xt - M) * kLog2e);
+                }
+                const float gt = (fmaf(As, e, Bc) - scale * (1.f - a.eps) * wt) * fac;
+                VT::store1(xrow, t, gt);
             }
         }
         if (gleader) {
             gpart_l[g] = accL;
             gpart_z[g] = accZ;
-            gpart_c[g] = accC;
+            s_correct[g] = static_cast<int>(accC);
         }
         if (failed && lane == 0) s_failed = 1;
     }
@@ -366,8 +528,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
         // last issued use of every slot
         for (int i = 0; i < ng * sg; ++i) {
             const uint32_t used = s_issued[i];
-            if (used) (void)mbar_wait_bounded(smem_u32(&full_bar[i]), ((used - 1) / sg) & 1u,
-                                              a.timeout_ns);
+            if (used) (void)mbar_wait_bounded(smem_u32(&full_bar[i]), used & 1u, a.timeout_ns);
         }
     }
     if (a.reduction != kRedNone && tid == 0) {
@@ -376,19 +537,23 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
         for (int g = 0; g < ng; ++g) {
             L += gpart_l[g];
             Z += gpart_z[g];
-            C += gpart_c[g];
+            C += s_correct[g];
         }
         finish_scalars(a, cid, ncta, L, Z, C, s_D, s_nvalid);
     }
 }
 
-const void* stream_kernel(int dtype, bool softcap) {
-    if (dtype == 0)
-        return softcap ? (const void*)&ce_fwd_stream<float, true>
-                       : (const void*)&ce_fwd_stream<float, false>;
+const void* stream_kernel(int dtype, bool softcap, int vpt, int nw) {
+    // two shapes: 8 consumer warps with 8 vectors a thread a slot, or 16
+    // warps with 4 (both 1024 vectors per slot, both without spills)
+#define GBCE_STREAM(TT, SC)                                                     \
+    (nw == 8 && vpt == 8 ? (const void*)&ce_fwd_stream<TT, SC, 8, 8>            \
+                         : (nw == 16 && vpt == 4 ? (const void*)&ce_fwd_stream<TT, SC, 4, 16> \
+                                                 : nullptr))
+    if (dtype == 0) return softcap ? GBCE_STREAM(float, true) : GBCE_STREAM(float, false);
     if (dtype == 1)
-        return softcap ? (const void*)&ce_fwd_stream<__nv_bfloat16, true>
-                       : (const void*)&ce_fwd_stream<__nv_bfloat16, false>;
+        return softcap ? GBCE_STREAM(__nv_bfloat16, true) : GBCE_STREAM(__nv_bfloat16, false);
+#undef GBCE_STREAM
     return nullptr;
 }
 

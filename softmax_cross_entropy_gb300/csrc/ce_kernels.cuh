@@ -284,8 +284,7 @@ const void* staged_kernel_f32_nocap_plain(int cfg);
 const void* staged_kernel_f32_nocap_wsmooth(int cfg);
 const void* staged_kernel_f32_softcap_plain(int cfg);
 const void* staged_kernel_f32_softcap_wsmooth(int cfg);
-const void* stream_kernel(int dtype, bool softcap);
-constexpr int kStreamWarps = 16;      // consumer warps of the streaming kernel
+const void* stream_kernel(int dtype, bool softcap, int vpt, int nw);
 constexpr int kStreamMaxSlots = 48;   // ring slots (all groups) of the streaming kernel
 constexpr int kStreamMaxGroups = 8;
 const void* generic_kernel(int dtype, bool softcap);

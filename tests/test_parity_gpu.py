@@ -360,11 +360,14 @@ def test_module_reduction_none_backward():
 KINDS = {"staged": "1", "stream": "2", "general": "3"}
 
 
-@pytest.mark.parametrize("kind", sorted(KINDS))
+@pytest.mark.parametrize("kind", sorted(KINDS) + ["stream16"])
 @pytest.mark.parametrize("dtype,V,rows", [("bf16", 4096, 300), ("bf16", 32768, 90),
                                           ("f32", 8192, 77), ("bf16", 131072, 20),
                                           ("f32", 24, 33)])
 def test_kernel_kinds(monkeypatch, kind, dtype, V, rows):
+    if kind == "stream16":
+        monkeypatch.setenv("GBCE_STREAM_WARPS", "16")
+        kind = "stream"
     monkeypatch.setenv("GBCE_KERNEL", KINDS[kind])
     for opts in (dict(), dict(label_smoothing=0.1, softcap=20.0, lse_square_scale=1e-3),
                  dict(weight=True, reduction="none")):
@@ -372,21 +375,25 @@ def test_kernel_kinds(monkeypatch, kind, dtype, V, rows):
         check_full(case, want_z=True, want_acc=True, want_pred=True)
 
 
+@pytest.mark.parametrize("warps", [8, 16])
 @pytest.mark.parametrize("groups", [1, 2, 4, 8])
-def test_stream_groups(monkeypatch, groups):
+def test_stream_groups(monkeypatch, groups, warps):
     monkeypatch.setenv("GBCE_KERNEL", "2")
     monkeypatch.setenv("GBCE_STREAM_GROUPS", str(groups))
+    monkeypatch.setenv("GBCE_STREAM_WARPS", str(warps))
     case = workloads.random_case(70 + groups, 203, 2048, dtype="bf16", label_smoothing=0.1,
                                  lse_square_scale=1e-4)
     check_full(case, want_z=True, want_acc=True, want_pred=True)
 
 
+@pytest.mark.parametrize("warps", [8, 16])
 @pytest.mark.parametrize("dtype,V", [("bf16", 32768), ("f32", 20000), ("bf16", 8200)])
-def test_stream_twice_from_l2(monkeypatch, dtype, V):
+def test_stream_twice_from_l2(monkeypatch, dtype, V, warps):
     # rows streamed through the ring twice (the large-vocabulary mode), at
     # sizes the oracle checks whole
     monkeypatch.setenv("GBCE_KERNEL", "2")
     monkeypatch.setenv("GBCE_STREAM_TWICE", "1")
+    monkeypatch.setenv("GBCE_STREAM_WARPS", str(warps))
     for opts in (dict(), dict(label_smoothing=0.2, softcap=10.0)):
         case = workloads.random_case(80, 61, V, dtype=dtype, **opts)
         check_full(case, want_z=True, want_acc=True, want_pred=True)
