@@ -180,36 +180,12 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
-// Packed fp32 pairs (sm_100 and later issue one instruction for both lanes).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
+// Packed fp32 pairs: sm_100 and later issue one FFMA2 / FADD2 / FMUL2
+// instruction for both lanes (CUDA's float2 builtins, which the compiler
+// keeps in register pairs).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // tanh(y) from the identity tanh(y) = 1 - 2 / (exp(2y) + 1), with the
 // argument already multiplied by 2*log2(e): tanh_from_2ylog2e(2*y*log2e).
@@ -253,6 +229,21 @@ struct Vec<__nv_bfloat16> {
         __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
         return fmaxf(__low2float(m), __high2float(m));
     }
+    // Running maximum over whole vectors kept as a packed bf16 pair.
+    using MaxAcc = __nv_bfloat162;
+    __device__ __forceinline__ static MaxAcc max_init() {
+        return __halves2bfloat162(__ushort_as_bfloat16(0xFF80u), __ushort_as_bfloat16(0xFF80u));
+    }
+    __device__ __forceinline__ static MaxAcc max_fold(MaxAcc acc, const uint4& v) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
+        const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
+        return __hmax2(__hmax2(acc, a), __hmax2(__hmax2(b, c), d));
+    }
+    __device__ __forceinline__ static float max_value(MaxAcc acc) {
+        return fmaxf(__low2float(acc), __high2float(acc));
+    }
     __device__ __forceinline__ static float load1(const void* p, int64_t i) {
         const uint16_t b = reinterpret_cast<const uint16_t*>(p)[i];
         return __uint_as_float(static_cast<uint32_t>(b) << 16);
@@ -279,6 +270,14 @@ struct Vec<float> {
         return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
                      fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
     }
+    using MaxAcc = float;
+    __device__ __forceinline__ static MaxAcc max_init() { return -INFINITY; }
+    __device__ __forceinline__ static MaxAcc max_fold(MaxAcc acc, const uint4& v) {
+        return fmaxf(fmaxf(acc, __uint_as_float(v.x)),
+                     fmaxf(fmaxf(__uint_as_float(v.y), __uint_as_float(v.z)),
+                           __uint_as_float(v.w)));
+    }
+    __device__ __forceinline__ static float max_value(MaxAcc acc) { return acc; }
     __device__ __forceinline__ static float load1(const void* p, int64_t i) {
         return reinterpret_cast<const float*>(p)[i];
     }

@@ -77,28 +77,30 @@ struct PassOne {
     template <bool FULL>
     __device__ __forceinline__ void add_chunk(const uint4 (&q)[VPT], int vidx0, int vend,
                                               int stride, const FwdArgs& a, bool smooth) {
-        float cm = -INFINITY;
-        int ck = 0;
+        typename VT::MaxAcc macc = VT::max_init();
         int nk = 0;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             if (FULL || vidx0 + k * stride < vend) {
                 ++nk;
-                const float vm = VT::vmax(q[k]);
-                const bool b = vm > cm;
-                cm = b ? vm : cm;
-                ck = b ? k : ck;
+                macc = VT::max_fold(macc, q[k]);
             }
         }
+        const float cm = VT::max_value(macc);
         const bool better = cm > xmax;
         if (__any_sync(0xffffffffu, better)) {
             // a new thread maximum (frequent at a row's start, rare later):
-            // find its first element in the vector that holds it
+            // find the first vector and element that hold it
             if (better) {
-                uint4 qb = q[0];
+                int ck = VPT - 1;
+                uint4 qb = q[VPT - 1];
 #pragma unroll
-                for (int k = 1; k < VPT; ++k)
-                    if (k == ck) qb = q[k];
+                for (int k = VPT - 1; k >= 0; --k) {
+                    if ((FULL || vidx0 + k * stride < vend) && VT::vmax(q[k]) == cm) {
+                        ck = k;
+                        qb = q[k];
+                    }
+                }
                 float fb[VE];
                 VT::unpack(qb, fb);
                 int j0 = VE - 1;
