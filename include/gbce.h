@@ -130,6 +130,38 @@ ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V,
                  float* acc, int64_t* pred, ce_stream_t stream);
 
 /*
+ * ce_fwd_noalloc - ce_fwd for callers that cannot allocate device memory.
+ *
+ * The method has no counterpart for this call: it exists for code that may
+ * not call cudaMalloc, such as an allocator's own callbacks, a memory-capped
+ * sandbox, or a framework that forbids allocations once it has started.
+ * ce_fwd keeps a small scratch area per (device, stream) that it allocates on
+ * first use; this call instead uses one fixed device array compiled into the
+ * library (about 64 KB, held by every GPU that loads the library until the
+ * process exits) and allocates nothing.
+ *
+ * Arguments, outputs and results are those of ce_fwd. Differences:
+ *  - The scratch holds 2048 partial-sum slots, one per CTA (or cluster) of
+ *    the launch; a launch that would need more returns CE_ERR_UNSUPPORTED
+ *    and ce_last_error names the number. (On a GB300 no launch of this
+ *    library uses more than 8 slots per SM, 1216 in all.)
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call, on every stream, shares the same array. Each call clears
+ *    the part that must start at zero, but calls that overlap on the GPU
+ *    (different streams, or concurrent host threads) race on it; order
+ *    them on one stream or synchronise between them.
+ *  - Its device-side status word is cleared at the start of each call and
+ *    is not reported by ce_device_status.
+ */
+ce_status ce_fwd_noalloc(void* logits, int dtype, int64_t rows, int64_t V,
+                         const void* target, const float* weight, int64_t ignore_index,
+                         float label_smoothing, float lse_square_scale, float softcap,
+                         int reduction, uint32_t flags, float* loss, float* z_loss,
+                         float* acc, int64_t* pred, ce_stream_t stream);
+
+/*
  * ce_bwd - backward (§Backward Pass: the stored gradient times
  * grad_output): dlogits *= grad_output, in place.
  *

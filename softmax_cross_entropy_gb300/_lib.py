@@ -22,6 +22,8 @@ _P, _I, _I64, _U32, _F = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.
                           ctypes.c_float)
 SIGNATURES = {
     "ce_fwd": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P, _P, _P, _P]),
+    "ce_fwd_noalloc": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P, _P, _P,
+                            _P]),
     "ce_bwd": (_I, [_P, _I, _P, _I, _I64, _I64, _P]),
     "ce_device_status": (_I, [_P]),
     "ce_status_string": (ctypes.c_char_p, [_I]),
@@ -64,6 +66,13 @@ def ce_fwd(logits, dtype, rows, V, target, weight, ignore_index, label_smoothing
     return load().ce_fwd(logits, dtype, rows, V, target, weight, ignore_index,
                          label_smoothing, lse_square_scale, softcap, reduction, flags,
                          loss, z_loss, acc, pred, stream)
+
+
+def ce_fwd_noalloc(logits, dtype, rows, V, target, weight, ignore_index, label_smoothing,
+                   lse_square_scale, softcap, reduction, flags, loss, z_loss, acc, pred, stream):
+    return load().ce_fwd_noalloc(logits, dtype, rows, V, target, weight, ignore_index,
+                                 label_smoothing, lse_square_scale, softcap, reduction, flags,
+                                 loss, z_loss, acc, pred, stream)
 
 
 def ce_bwd(grad_output, grad_per_row, dlogits, dtype, rows, V, stream):

@@ -544,3 +544,102 @@ extern "C" const char* ce_status_string(ce_status s) {
 }
 
 extern "C" const char* ce_last_error(void) { return g_last_error.c_str(); }
+
+namespace gbce {
+
+// The forward call with scratch that the caller provides (the static-scratch
+// entry point in ce_noalloc.cu). Same checks, plan and launch as ce_fwd; the
+// launch is refused when its grid would need more partial slots than the
+// scratch holds. Allocates nothing.
+ce_status fwd_with_scratch(Scratch* scratch, int max_slots, void* logits, int dtype, int64_t rows,
+                           int64_t V, const void* target, const float* weight,
+                           int64_t ignore_index, float label_smoothing, float lse_square_scale,
+                           float softcap, int reduction, uint32_t flags, float* loss,
+                           float* z_loss, float* acc, int64_t* pred, cudaStream_t st) {
+    const uint32_t known =
+        CE_FLAG_GRAD | CE_FLAG_Z_LOSS | CE_FLAG_ACC | CE_FLAG_PRED | CE_FLAG_TARGET_I64;
+    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_INVALID_ARG;
+    if (rows < 0 || V <= 0) return CE_ERR_INVALID_ARG;
+    if (V > INT32_MAX - 16) return CE_ERR_UNSUPPORTED;
+    if (reduction != CE_RED_NONE && reduction != CE_RED_SUM && reduction != CE_RED_MEAN)
+        return CE_ERR_INVALID_ARG;
+    if (flags & ~known) return CE_ERR_INVALID_ARG;
+    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return CE_ERR_INVALID_ARG;
+    if (!finite(lse_square_scale)) return CE_ERR_INVALID_ARG;
+    if (!finite(softcap) || softcap < 0.f) return CE_ERR_INVALID_ARG;
+    if (!loss) return CE_ERR_INVALID_ARG;
+    if ((flags & CE_FLAG_Z_LOSS) && !z_loss) return CE_ERR_INVALID_ARG;
+    if ((flags & CE_FLAG_ACC) && !acc) return CE_ERR_INVALID_ARG;
+    if ((flags & CE_FLAG_PRED) && !pred) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && (!logits || !target)) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && V > INT64_MAX / rows / 4) return CE_ERR_INVALID_ARG;
+    if (!scratch || max_slots < 1) return CE_ERR_INVALID_ARG;
+    if (rows == 0 && reduction == CE_RED_NONE) return CE_OK;
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+
+    FwdArgs a = {};
+    a.x = logits;
+    a.rows = rows;
+    a.V = V;
+    a.target = target;
+    a.tgt64 = (flags & CE_FLAG_TARGET_I64) ? 1 : 0;
+    a.weight = weight;
+    a.ignore_index = ignore_index;
+    a.eps = label_smoothing;
+    a.lam = lse_square_scale;
+    const bool sc = softcap > 0.f;
+    a.softcap = sc ? softcap : 0.f;
+    a.sc_k2 = sc ? 2.f * kLog2e / softcap : 0.f;
+    a.sc_slog2e = sc ? softcap * kLog2e : 0.f;
+    a.reduction = reduction;
+    a.grad = (flags & CE_FLAG_GRAD) ? 1 : 0;
+    a.want_z = (flags & CE_FLAG_Z_LOSS) ? 1 : 0;
+    a.want_acc = (flags & CE_FLAG_ACC) ? 1 : 0;
+    a.want_pred = (flags & CE_FLAG_PRED) ? 1 : 0;
+    a.loss = loss;
+    a.zloss = z_loss;
+    a.acc = acc;
+    a.pred = pred;
+    a.timeout_ns = static_cast<uint64_t>(env_int("GBCE_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
+    a.scratch = scratch;
+
+    const bool wsmooth = weight != nullptr && label_smoothing > 0.f;
+    const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16) == 0;
+    Plan p;
+    ce_status rc = make_plan(dev, dtype, V, sc, wsmooth, aligned, &p);
+    if (rc != CE_OK) return rc;
+    const int64_t units = rows == 0 ? 1 : std::min<int64_t>(rows, p.max_units);
+    if (units > max_slots) {
+        g_last_error = "this launch needs " + std::to_string(units) +
+                       " partial-sum slots; the static scratch holds " + std::to_string(max_slots);
+        return CE_ERR_UNSUPPORTED;
+    }
+    // the scratch keeps the previous call's contents: the ticket and the
+    // status word must start at zero (partial slots are written before read)
+    e = cudaMemsetAsync(scratch, 0, 2 * sizeof(unsigned), st);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaMemsetAsync(scratch header)");
+    if (rows == 0) return launch(generic_kernel(dtype, sc), 1, kGenericThreads, 0, 1, st, &a);
+    if (p.kind == Kind::Stream) {
+        a.ng = p.ng;
+        a.sg = p.sg;
+        a.chunk_vec = p.chunk_vec;
+        a.nchunk = p.nchunk;
+        a.resident = p.resident;
+        return launch(p.fn, static_cast<int>(units), p.nt, p.smem, 1, st, &a);
+    }
+    if (p.kind == Kind::Staged) {
+        a.slice_vec = p.slice_vec;
+        a.stages = p.stages;
+        return launch(p.fn, static_cast<int>(units * p.cluster), p.nt, p.smem, p.cluster, st, &a);
+    }
+    return launch(p.fn, static_cast<int>(units), p.nt, 0, 1, st, &a);
+}
+
+// Records a CUDA error for ce_last_error (for the static-scratch entry point).
+ce_status record_cuda_failure(cudaError_t e, const char* what) { return cuda_failure(e, what); }
+
+}  // namespace gbce
