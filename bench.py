@@ -322,7 +322,7 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "ce_fwd_staged (forward with in-place gradient)",
+                     "kernel": "ce_fwd forward kernel with in-place gradient",
                      "bytes_per_launch": bytes_step,
                      "avg_launch_us": round(t_fwd / K * 1e6, 2)},
         "e2e": {"value": round(world * bytes_step * K / t_e2e / 1e9, 1), "unit": "GB/s",
@@ -429,6 +429,28 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_target(args):
+    """Profiling target (no timing): `--ncu-steps` eager forward + backward
+    steps of the workload, for an ncu capture of one forward launch
+    (`-k regex:ce_fwd -s 1 -c 1`)."""
+    import torch
+    from softmax_cross_entropy_gb300 import build
+    build.build()
+    device = torch.device("cuda", 0)
+    case = workloads.vsweep(V=args.V, rows=args.rows)
+    r = GpuRunner(case, device, torch)
+    st = r.stream.cuda_stream
+    with torch.cuda.stream(r.stream):
+        for k in range(args.ncu_steps):
+            b = r.bufs[k % r.pool]
+            b.copy_(r.pristine)
+            r.fwd(b, st)
+            r.bwd(b, r.one, st)
+    torch.cuda.synchronize(device)
+    print(json.dumps({"profile_target": workload_desc(args.V), "rows": args.rows,
+                      "steps": args.ncu_steps}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,7 +460,15 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ncu", action="store_true",
+                    help="run a few untimed steps as an ncu profiling target")
+    ap.add_argument("--ncu-steps", type=int, default=3)
+    ap.add_argument("--rows", type=int, default=ROWS, help="rows of the --ncu target")
+    ap.add_argument("--V", type=int, default=V_MAIN, help="vocabulary of the --ncu target")
     args = ap.parse_args()
+    if args.ncu:
+        run_profile_target(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
