@@ -362,7 +362,7 @@ ce_fwd_staged(const __grid_constant__ FwdArgs a) {
             (void)mbar_wait_bounded(smem_u32(&full_bar[j % stages]),
                                     static_cast<uint32_t>((j / stages) & 1), a.timeout_ns);
     }
-    if (a.reduction != kRedNone && leader)
+    if (a.reduction != kRedNone && crank == 0 && tid < 32)
         finish_scalars(a, cid, ncl, accL, accZ, accC, D, n_valid);
 }
 

@@ -533,7 +533,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
             if (used) (void)mbar_wait_bounded(smem_u32(&full_bar[i]), used & 1u, a.timeout_ns);
         }
     }
-    if (a.reduction != kRedNone && tid == 0) {
+    if (a.reduction != kRedNone && tid < 32) {
         double L = 0.0, Z = 0.0;
         long long C = 0;
         for (int g = 0; g < ng; ++g) {

@@ -168,7 +168,7 @@ ce_fwd_generic(const __grid_constant__ FwdArgs a) {
         // red_s, red_z, red_p are read above; the next row writes them only
         // after its first barrier, which every thread reaches after reading
     }
-    if (a.reduction != kRedNone && tid == 0)
+    if (a.reduction != kRedNone && tid < 32)
         finish_scalars(a, blockIdx.x, gridDim.x, accL, accZ, accC, D, n_valid);
 }
 

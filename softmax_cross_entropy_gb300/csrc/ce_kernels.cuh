@@ -109,6 +109,7 @@ __device__ __forceinline__ void denominators(const FwdArgs& a, float* sh, float&
                                              Sync sync = Sync()) {
     float d = 0.f;
     int n = 0;
+#pragma unroll 8
     for (int64_t i = threadIdx.x; i < a.rows; i += NT) {
         const int64_t t = load_target(a, i);
         if (row_counts(a, t)) {
@@ -214,28 +215,42 @@ __device__ __forceinline__ float row_loss(const FwdArgs& a, float M, float logS,
 }
 
 // Epilogue for "sum" and "mean": each participating CTA publishes its
-// partials; the last one to arrive (atomic ticket) adds them in index order
-// and writes the scalar outputs, then resets the ticket for the next call.
-// Called by one thread per participating CTA.
+// partials; the last one to arrive (atomic ticket) adds them and writes the
+// scalar outputs, then resets the ticket for the next call. Called by all 32
+// lanes of one warp of each participating CTA; lane 0 holds the CTA's
+// partials. In the last CTA, lane k adds the slots k, k + 32, ... in order
+// and a fixed butterfly combines the lanes, so the result does not depend on
+// which CTA finishes last (one dependent L2 read per slot in a single thread
+// would cost tens of microseconds at a thousand slots).
 __device__ __forceinline__ void finish_scalars(const FwdArgs& a, int64_t slot, int64_t nslots,
                                                double l, double z, long long nc, float D,
                                                int n_valid) {
     Scratch* s = a.scratch;
-    s->partials[slot].loss = l;
-    s->partials[slot].zloss = z;
-    s->partials[slot].n_correct = nc;
-    __threadfence();
-    const unsigned prev = atomicAdd(&s->ticket, 1u);
-    if (prev != static_cast<unsigned>(nslots - 1)) return;
+    const int lane = threadIdx.x & 31;
+    int last = 0;
+    if (lane == 0) {
+        s->partials[slot].loss = l;
+        s->partials[slot].zloss = z;
+        s->partials[slot].n_correct = nc;
+        __threadfence();
+        last = atomicAdd(&s->ticket, 1u) == static_cast<unsigned>(nslots - 1);
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __threadfence();
     double L = 0.0, Z = 0.0;
     long long C = 0;
-    for (int64_t c = 0; c < nslots; ++c) {
-        const volatile Partial* p = &s->partials[c];
-        L += p->loss;
-        Z += p->zloss;
-        C += p->n_correct;
+    for (int64_t c = lane; c < nslots; c += 32) {
+        L += __ldcg(&s->partials[c].loss);
+        Z += __ldcg(&s->partials[c].zloss);
+        C += __ldcg(&s->partials[c].n_correct);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        L += __shfl_xor_sync(0xffffffffu, L, o);
+        Z += __shfl_xor_sync(0xffffffffu, Z, o);
+        C += __shfl_xor_sync(0xffffffffu, C, o);
+    }
+    if (lane != 0) return;
     if (a.reduction == kRedMean) {
         // no counted row: 0/0 = NaN, as the mean of an empty set
         L = L / static_cast<double>(D);
