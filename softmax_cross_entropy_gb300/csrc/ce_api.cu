@@ -207,26 +207,38 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, int cfg
 // that fits in one slot with room for two more stays resident, with as many
 // row groups as the ring holds; otherwise one group of all consumer warps
 // streams the row twice.
-bool try_stream(int dtype, int64_t V, bool softcap, const DeviceInfo& dev, Plan* out,
+// ws: class weights with label smoothing; the kernel then keeps the V
+// weights in shared memory after the ring, which must leave room for at
+// least two slots.
+bool try_stream(int dtype, int64_t V, bool softcap, bool ws, const DeviceInfo& dev, Plan* out,
                 ce_status* err) {
     const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
     const int64_t vec_row = V * bytes / 16;
     const int force_ng = env_int("GBCE_STREAM_GROUPS", 0);
     const bool force_twice = env_int("GBCE_STREAM_TWICE", 0) != 0;
-    const int nw = env_int("GBCE_STREAM_WARPS", 8) == 16 ? 16 : 8;
+    // 16 consumer warps hide the longer per-element latency of softcap and
+    // of fp32 logits, and the row-end latency of short rows, better; long
+    // plain bf16 rows stream fastest with 8 (and the class-weighted
+    // smoothing kernel exists with 8 only). GBCE_STREAM_WARPS (8 or 16)
+    // overrides.
+    const int nw_env = env_int("GBCE_STREAM_WARPS", 0);
+    const int nw_auto = (softcap || dtype == CE_F32 || V * bytes <= 32768) ? 16 : 8;
+    const int nw = ws ? 8 : (nw_env == 8 || nw_env == 16 ? nw_env : nw_auto);
     const int vpt_res = nw == 8 ? 8 : 4;  // the two compiled shapes
+    const size_t wbytes = ws ? static_cast<size_t>((V * 4 + 15) / 16 * 16) : 0;
     Plan p;
     const void* fn = nullptr;
     size_t ring_max = 0;
     auto prepare = [&](int vpt) -> bool {
-        fn = stream_kernel(dtype, softcap, vpt, nw);
+        fn = ws ? stream_kernel_ws(dtype, softcap) : stream_kernel(dtype, softcap, vpt, nw);
         if (!fn) return false;
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, fn);
         if (e == cudaSuccess) {
-            ring_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
+            const size_t dyn_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
+            ring_max = dyn_max > wbytes ? dyn_max - wbytes : 0;
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(ring_max));
+                                     static_cast<int>(dyn_max));
         }
         if (e != cudaSuccess) {
             *err = cuda_failure(e, "stream kernel attributes");
@@ -260,9 +272,17 @@ bool try_stream(int dtype, int64_t V, bool softcap, const DeviceInfo& dev, Plan*
         p = Plan();
         // one group by default; GBCE_STREAM_GROUPS splits the warps into
         // groups that stream different rows
-        p.ng = (force_ng > 0 && nw % force_ng == 0) ? force_ng : 1;
+        p.ng = (force_ng > 0 && force_ng <= kStreamMaxGroups && nw % force_ng == 0) ? force_ng : 1;
         p.chunk_vec =
             static_cast<int>(std::min<int64_t>(vec_row, 32 * (nw / p.ng) * vpt));
+        if (ring_max / (static_cast<size_t>(p.ng) * p.chunk_vec * 16) < 3) {
+            // little room left by the weights: smaller slots (a multiple of
+            // the group's threads, as the vector ownership needs), three deep
+            const int gt = 32 * (nw / p.ng);
+            const int64_t fit = static_cast<int64_t>(ring_max / (3 * 16 * static_cast<size_t>(p.ng)));
+            const int64_t c = fit / gt * gt;
+            if (c >= gt && c < p.chunk_vec) p.chunk_vec = static_cast<int>(c);
+        }
         p.nchunk = static_cast<int>((vec_row + p.chunk_vec - 1) / p.chunk_vec);
         p.sg = static_cast<int>(std::min<size_t>(
             kStreamMaxSlots / p.ng, ring_max / (static_cast<size_t>(p.ng) * p.chunk_vec * 16)));
@@ -274,7 +294,7 @@ bool try_stream(int dtype, int64_t V, bool softcap, const DeviceInfo& dev, Plan*
     p.fn = fn;
     p.kind = Kind::Stream;
     p.nt = 32 * (nw + 1);
-    p.smem = static_cast<size_t>(p.ng) * p.sg * p.chunk_vec * 16;
+    p.smem = static_cast<size_t>(p.ng) * p.sg * p.chunk_vec * 16 + wbytes;
     int occ = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, p.nt, p.smem);
     if (e != cudaSuccess) {
@@ -312,9 +332,9 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     Plan best;
     const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
     const bool fast_ok = aligned && (V * bytes) % 16 == 0 && forced_c >= 0 && forced_kind != 3;
-    if (fast_ok && !wsmooth && forced_kind != 1) {
+    if (fast_ok && forced_kind != 1) {
         rc = CE_OK;
-        if (!try_stream(dtype, V, softcap, dev, &best, &rc) && rc != CE_OK) return rc;
+        if (!try_stream(dtype, V, softcap, wsmooth, dev, &best, &rc) && rc != CE_OK) return rc;
     }
     if (fast_ok && best.kind == Kind::General && forced_kind != 2) {
         // Candidates: every shape and cluster size that fits. Prefer at

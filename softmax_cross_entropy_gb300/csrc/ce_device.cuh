@@ -308,4 +308,18 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     }
 }
 
+// Warp-wide maximum of a float and minimum of an int in one instruction
+// each (redux.sync on sm_100-class GPUs); every lane gets the result.
+__device__ __forceinline__ float warp_max_f32(float v) {
+    float m;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+    return m;
+}
+
+__device__ __forceinline__ int warp_min_s32(int v) {
+    int m;
+    asm volatile("redux.sync.min.s32 %0, %1, 0xffffffff;" : "=r"(m) : "r"(v));
+    return m;
+}
+
 }  // namespace gbce

@@ -1,557 +1,18 @@
-// Fused softmax cross-entropy forward with the in-forward gradient: the
-// streaming kernel.
-//
-// Method (Liger-Kernel cross-entropy kernel profile, §Forward Pass,
-// §Backward Pass and §Key Patterns): per row a max-shifted log-sum-exp,
-// the NLL with ignore_index, class weights on the target term, label
-// smoothing and z-loss, the argmax, and the gradient of the reduced loss
-// written in place over the logits.
-//
-// GB300 design:
-//  * Warp specialisation. One producer warp keeps a ring of shared-memory
-//    slots filled with 1-D bulk asynchronous copies (completion counted on
-//    a `full` mbarrier per slot); 16 consumer warps compute, and each warp
-//    hands a slot back through an `empty` mbarrier when it is done with it.
-//  * Row groups. The consumer warps form ng groups; group g takes every
-//    ng-th row of the CTA's rows, with its own ring slots, so several rows
-//    are in flight per SM and one group's row-end merge overlaps the
-//    others' streaming.
-//  * Two passes per row. Pass 1 forms each thread's online-softmax
-//    statistics (running max, sum of exp relative to it, first argmax,
-//    smoothing sum); warps merge them with shuffles and the group with one
-//    named barrier. Pass 2 recomputes exp from the logits (the SFU issues
-//    about 30 ex2 per clock per SM, so the second exponential is cheap)
-//    and stores the gradient with 16-byte coalesced stores. When a row
-//    fits in the group's slots it stays there for both passes ("resident");
-//    otherwise the producer streams it twice, the first time with an L2
-//    evict-last hint so that the second read comes from L2, and HBM sees
-//    one read and one write per element.
-//  * Scalars. Per-row outputs come from the group leader; sums go through
-//    per-CTA partials and the last-CTA fixed-order epilogue.
-#include <climits>
-
-#include "ce_kernels.cuh"
+// Instantiations of the streaming forward kernel without class-weighted
+// label smoothing (see ce_fwd_stream.cuh).
+#include "ce_fwd_stream.cuh"
 
 namespace gbce {
 
-namespace {
-
-constexpr uint32_t kStreamCopyChunk = 32768;
-
-__device__ __forceinline__ int64_t imin64(int64_t x, int64_t y) { return x < y ? x : y; }
-
-// z = softcap(x) for a pair of logits.
-template <bool SOFTCAP>
-__device__ __forceinline__ float2 capped2(float x0, float x1, const FwdArgs& a) {
-    if (!SOFTCAP) return make_float2(x0, x1);
-    return make_float2(a.softcap * tanh_from_scaled(x0 * a.sc_k2),
-                       a.softcap * tanh_from_scaled(x1 * a.sc_k2));
-}
-
-// exp2 arguments (z - m) * log2(e) for a pair. bf16 logits use one packed
-// FFMA against the rounded m*log2(e) (that rounding is common to a thread's
-// terms); fp32 logits subtract first.
-template <typename T>
-__device__ __forceinline__ float2 exp_arg2(float2 z, float m, float mL) {
-    if (sizeof(T) == 2) return ffma2(z, make_float2(kLog2e, kLog2e), make_float2(-mL, -mL));
-    return fmul2(fadd2(z, make_float2(-m, -m)), make_float2(kLog2e, kLog2e));
-}
-
-// Row statistics of one thread during pass 1 (see RowStats): the running
-// reference m (the largest z seen; a finite sentinel before the first
-// element), S = sum exp(z - m), the running sum of z for label smoothing, the
-// element count, and the first vector holding the largest raw logit.
-// add_chunk takes the thread's VPT vectors of one ring slot at once: one
-// max and one rescale per slot, then VPT independent exp-sum chains of
-// packed pairs.
-template <typename T, bool SOFTCAP, int VPT>
-struct PassOne {
-    using VT = Vec<T>;
-    static constexpr int VE = VT::N;
-    float m = -3.0e38f, mL = -3.0e38f * kLog2e, S = 0.f, sumz = 0.f, xmax = -INFINITY;
-    int best = INT_MAX, nel = 0;  // best: first element index of the largest raw logit
-
-    // q[k] is vector vidx0 + k * stride; unless FULL, it exists only when
-    // vidx0 + k * stride < vend (the thread's vectors of the slot, in
-    // increasing index order).
-    template <bool FULL>
-    __device__ __forceinline__ void add_chunk(const uint4 (&q)[VPT], int vidx0, int vend,
-                                              int stride, const FwdArgs& a, bool smooth) {
-        typename VT::MaxAcc macc = VT::max_init();
-        int nk = 0;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            if (FULL || vidx0 + k * stride < vend) {
-                ++nk;
-                macc = VT::max_fold(macc, q[k]);
-            }
-        }
-        const float cm = VT::max_value(macc);
-        const bool better = cm > xmax;
-        if (__any_sync(0xffffffffu, better)) {
-            // a new thread maximum (frequent at a row's start, rare later):
-            // find the first vector and element that hold it
-            if (better) {
-                int ck = VPT - 1;
-                uint4 qb = q[VPT - 1];
-#pragma unroll
-                for (int k = VPT - 1; k >= 0; --k) {
-                    if ((FULL || vidx0 + k * stride < vend) && VT::vmax(q[k]) == cm) {
-                        ck = k;
-                        qb = q[k];
-                    }
-                }
-                float fb[VE];
-                VT::unpack(qb, fb);
-                int j0 = VE - 1;
-#pragma unroll
-                for (int j = VE - 1; j >= 0; --j)
-                    if (fb[j] == cm) j0 = j;
-                xmax = cm;
-                best = (vidx0 + ck * stride) * VE + j0;
-            }
-        }
-        const float mz = SOFTCAP ? a.softcap * tanh_from_scaled(cm * a.sc_k2) : cm;
-        const float mn = fmaxf(m, mz);
-        S *= ex2((m - mn) * kLog2e);
-        m = mn;
-        mL = fmaxf(mn, -1.0e30f) * kLog2e;
-        float2 sk[VPT], zk[VPT];
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            sk[k] = make_float2(0.f, 0.f);
-            zk[k] = make_float2(0.f, 0.f);
-            if (FULL || vidx0 + k * stride < vend) {
-                float f[VE];
-                VT::unpack(q[k], f);
-#pragma unroll
-                for (int j = 0; j < VE; j += 2) {
-                    const float2 z = capped2<SOFTCAP>(f[j], f[j + 1], a);
-                    const float2 ar = exp_arg2<T>(z, m, mL);
-                    sk[k] = fadd2(sk[k], make_float2(ex2(ar.x), ex2(ar.y)));
-                    if (smooth) zk[k] = fadd2(zk[k], z);
-                }
-            }
-        }
-        float2 acc = sk[0], zacc = zk[0];
-#pragma unroll
-        for (int k = 1; k < VPT; ++k) {
-            acc = fadd2(acc, sk[k]);
-            if (smooth) zacc = fadd2(zacc, zk[k]);
-        }
-        S += acc.x + acc.y;
-        if (smooth) sumz += zacc.x + zacc.y;
-        nel += nk * VE;
-    }
-
-};
-
-// Row statistics of a warp or group, all relative to M = softcap(X), the
-// largest z: S = sum exp(z - M), SZ = sum (z - M) (label smoothing), n the
-// element count, X the largest raw logit and I its first index.
-struct RowSums {
-    float M, S, SZ, n, X;
-    int I;
-};
-
-template <bool SOFTCAP>
-__device__ __forceinline__ float capped1(float x, const FwdArgs& a) {
-    return SOFTCAP ? a.softcap * tanh_from_scaled(x * a.sc_k2) : x;
-}
-
-// Two-phase merge over the lanes of a warp, each lane holding (m, S, SZ, n,
-// x, i) relative to its own m: a butterfly on the raw maximum (with the first
-// index on ties), one rescale per lane, then a butterfly of plain sums. Every
-// lane ends with the same bits.
-template <bool SOFTCAP>
-__device__ __forceinline__ RowSums warp_merge(float m, float S, float SZ, float n, float x, int i,
-                                              bool smooth, const FwdArgs& a) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ox = __shfl_xor_sync(0xffffffffu, x, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-        if (ox > x || (ox == x && oi < i)) {
-            x = ox;
-            i = oi;
-        }
-    }
-    const float M = capped1<SOFTCAP>(x, a);
-    const bool live = S > 0.f && M != -INFINITY;
-    float s = live ? S * ex2((m - M) * kLog2e) : 0.f;
-    float sz = (smooth && live) ? fmaf(n, m - M, SZ) : 0.f;
-    float nn = n;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (smooth) sz += __shfl_xor_sync(0xffffffffu, sz, o);
-        nn += __shfl_xor_sync(0xffffffffu, nn, o);
-    }
-    return RowSums{M, s, sz, nn, x, i};
-}
-
-// Pass 2 for the thread's VPT vectors of one slot: gradient
-// As * exp(z - M) + Bc (times dz/dx under softcap), packed and stored.
-template <typename T, bool SOFTCAP, int VPT, bool FULL>
-__device__ __forceinline__ void grad_chunk(const uint4* ch, uint4* outv, int tg, int nv, int GT,
-                                           float M, float ML, float As, float Bc,
-                                           const FwdArgs& a) {
-    using VT = Vec<T>;
-    constexpr int VE = VT::N;
-    uint4 q[VPT];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-        if (FULL || tg + k * GT < nv) q[k] = ch[tg + k * GT];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        if (FULL || tg + k * GT < nv) {
-            float f[VE], gr[VE];
-            VT::unpack(q[k], f);
-#pragma unroll
-            for (int j = 0; j < VE; j += 2) {
-                float2 fac = make_float2(1.f, 1.f);
-                float2 z = make_float2(f[j], f[j + 1]);
-                if (SOFTCAP) {
-                    const float t0 = tanh_from_scaled(f[j] * a.sc_k2);
-                    const float t1 = tanh_from_scaled(f[j + 1] * a.sc_k2);
-                    fac = make_float2(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
-                    z = make_float2(a.softcap * t0, a.softcap * t1);
-                }
-                const float2 ar = exp_arg2<T>(z, M, ML);
-                float2 g = ffma2(make_float2(As, As), make_float2(ex2(ar.x), ex2(ar.y)),
-                                 make_float2(Bc, Bc));
-                if (SOFTCAP) g = fmul2(g, fac);
-                gr[j] = g.x;
-                gr[j + 1] = g.y;
-            }
-            outv[k * GT] = VT::pack(gr);
-        }
-    }
-}
-
-// Ring position of a group: slot within the group's slots and the phase bit
-// of its current use, advanced without division.
-struct RingPos {
-    int slot = 0;
-    uint32_t phase = 0;
-    __device__ __forceinline__ void next(int sg) {
-        if (++slot == sg) {
-            slot = 0;
-            phase ^= 1u;
-        }
-    }
-};
-
-}  // namespace
-
-// NW consumer warps plus the producer warp; the register file is split
-// across the SM's four sub-partitions, so 17 warps allow 96 registers a
-// thread and 9 warps allow 168.
-template <typename T, bool SOFTCAP, int VPT, int NW>
-__global__ void __launch_bounds__(32 * (NW + 1), 1)
-ce_fwd_stream(const __grid_constant__ FwdArgs a) {
-    using VT = Vec<T>;
-    constexpr int VE = VT::N;
-    constexpr int NTC = 32 * NW;  // consumer threads
-
-    extern __shared__ __align__(128) unsigned char ring[];
-    __shared__ __align__(8) uint64_t full_bar[kStreamMaxSlots];
-    __shared__ __align__(8) uint64_t empty_bar[kStreamMaxSlots];
-    __shared__ __align__(16) RowSums grec[kStreamMaxGroups][2][NW];
-    __shared__ float red_p[NW];
-    __shared__ double gpart_l[kStreamMaxGroups], gpart_z[kStreamMaxGroups];
-    __shared__ int s_failed;
-    __shared__ float s_D;
-    __shared__ int s_nvalid;
-    __shared__ uint32_t s_issued[kStreamMaxSlots];  // 0, or 2 + phase of the last use
-    __shared__ int s_correct[kStreamMaxGroups];
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int ng = a.ng;
-    const int G = NW / ng;  // warps per group
-    const int GT = 32 * G;  // threads per group
-    const int sg = a.sg;
-    const int nchunk = a.nchunk;
-    const int chunk_vec = a.chunk_vec;
-    const uint32_t chunk_bytes = static_cast<uint32_t>(chunk_vec) * 16u;
-    const int64_t vec_row = a.V / VE;
-    const int64_t cid = blockIdx.x;
-    const int64_t ncta = gridDim.x;
-
-    if (tid == 0) {
-        for (int i = 0; i < ng * sg; ++i) {
-            mbar_init(smem_u32(&full_bar[i]), 1);
-            mbar_init(smem_u32(&empty_bar[i]), static_cast<uint32_t>(G));
-            s_issued[i] = 0;
-        }
-        for (int g = 0; g < kStreamMaxGroups; ++g) s_correct[g] = 0;
-        s_failed = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    if (warp == NW) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t pol_keep = l2_evict_last_policy();
-            const uint64_t pol_once = l2_evict_first_policy();
-            int pslot[kStreamMaxGroups];
-            uint32_t pphase[kStreamMaxGroups];
-#pragma unroll
-            for (int k = 0; k < kStreamMaxGroups; ++k) {
-                pslot[k] = 0;
-                pphase[k] = 0;
-            }
-            bool failed = false;
-            int g = 0;
-            for (int64_t r = cid; r < a.rows && !failed; r += ncta) {
-                const int gg = g;
-                g = (g + 1 == ng) ? 0 : g + 1;
-                if (!row_counts(a, load_target(a, r))) continue;
-                const int passes = a.resident ? 1 : 2;
-                for (int p = 0; p < passes && !failed; ++p) {
-                    for (int c = 0; c < nchunk; ++c) {
-                        int ls = 0;
-                        uint32_t ph = 0;
-#pragma unroll
-                        for (int k = 0; k < kStreamMaxGroups; ++k) {
-                            if (k == gg) {
-                                ls = pslot[k];
-                                ph = pphase[k];
-                                if (++pslot[k] == sg) {
-                                    pslot[k] = 0;
-                                    pphase[k] ^= 1u;
-                                }
-                            }
-                        }
-                        const int slot = gg * sg + ls;
-                        if (!mbar_wait_bounded(smem_u32(&empty_bar[slot]), ph ^ 1u,
-                                               a.timeout_ns)) {
-                            failed = true;
-                            break;
-                        }
-                        const int64_t v0 = static_cast<int64_t>(c) * chunk_vec;
-                        const uint32_t bytes =
-                            static_cast<uint32_t>(imin64(chunk_vec, vec_row - v0)) * 16u;
-                        const uint32_t fb = smem_u32(&full_bar[slot]);
-                        mbar_arrive_expect_tx(fb, bytes);
-                        const char* src = reinterpret_cast<const char*>(a.x) +
-                                          (r * a.V + v0 * VE) * static_cast<int64_t>(sizeof(T));
-                        const uint32_t dst = smem_u32(ring + static_cast<size_t>(slot) * chunk_bytes);
-                        const uint64_t pol = (!a.resident && p == 0) ? pol_keep : pol_once;
-                        for (uint32_t off = 0; off < bytes; off += kStreamCopyChunk)
-                            bulk_g2s(dst + off, src + off, min(kStreamCopyChunk, bytes - off), fb,
-                                     pol);
-                        s_issued[slot] = 2u + ph;  // nonzero: used; low bit: phase of the last use
-                    }
-                }
-            }
-            if (failed) {
-                atomicOr(&a.scratch->status, kDevErrTimeout);
-                s_failed = 1;
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ consumers
-        const NamedSync all_consumers{15, NTC};
-        float D = 0.f;
-        int n_valid = 0;
-        if (a.reduction != kRedNone) denominators<NTC>(a, red_p, D, n_valid, all_consumers);
-        if (tid == 0) {
-            s_D = D;
-            s_nvalid = n_valid;
-        }
-        const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;  // unused when D == 0
-        const float inv_V = 1.f / static_cast<float>(a.V);
-        const bool smooth = a.eps != 0.f;
-
-        const int g = warp / G;
-        const int wg = warp % G;
-        const int tg = tid - g * GT;
-        const NamedSync group_sync{1 + g, GT};
-        const bool gleader = tid == g * GT;
-        double accL = 0.0, accZ = 0.0;
-        long long accC = 0;
-        RingPos pos;
-        bool failed = false;
-        int rp = 0;
-        const int vrow = static_cast<int>(vec_row);
-        // the thread of the group that handles vector v of a row (pass 1 and
-        // pass 2 use the same assignment)
-        // (GT is a power of two and every slot but a lone one spans a
-        // multiple of GT vectors)
-        auto owner_of = [&](int v) { return v & (GT - 1); };
-
-        for (int64_t r = cid + static_cast<int64_t>(g) * ncta; r < a.rows;
-             r += static_cast<int64_t>(ng) * ncta) {
-            const int64_t t = load_target(a, r);
-            const bool counts = row_counts(a, t);
-            T* xrow = reinterpret_cast<T*>(a.x) + r * a.V;
-            uint4* rowv = reinterpret_cast<uint4*>(xrow);
-            if (gleader && t != a.ignore_index && !counts)
-                atomicOr(&a.scratch->status, kDevErrTarget);
-            if (!counts) {
-                // Ignored row: exact +0 gradient, zero per-row outputs, pred -1.
-                if (a.grad)
-                    for (int v = tg; v < vrow; v += GT) rowv[v] = make_uint4(0u, 0u, 0u, 0u);
-                if (gleader) {
-                    if (a.reduction == kRedNone) {
-                        a.loss[r] = 0.f;
-                        if (a.want_z) a.zloss[r] = 0.f;
-                        if (a.want_acc) a.acc[r] = 0.f;
-                    }
-                    if (a.want_pred) a.pred[r] = -1;
-                }
-                continue;
-            }
-            const int tvec = static_cast<int>(t / VE);
-            const bool t_owner = tg == owner_of(tvec);
-            float xt = 0.f;
-            if (gleader || t_owner) xt = VT::load1(xrow, t);  // before any store to this row
-            const float wt = a.weight ? __ldg(a.weight + t) : 1.f;
-
-            // ---- pass 1: thread statistics over the row's slots
-            PassOne<T, SOFTCAP, VPT> st;
-            const RingPos pos0 = pos;
-            for (int c = 0, v0 = 0; c < nchunk; ++c, v0 += chunk_vec) {
-                const int slot = g * sg + pos.slot;
-                if (!failed && !mbar_wait_bounded(smem_u32(&full_bar[slot]), pos.phase,
-                                                  a.timeout_ns)) {
-                    failed = true;
-                    atomicOr(&a.scratch->status, kDevErrTimeout);
-                }
-                const uint4* ch = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * chunk_bytes);
-                const int nv = min(chunk_vec, vrow - v0);
-                // this thread's vectors of the slot: tg, tg + GT, ... below nv
-                uint4 q[VPT];
-                if (nv == VPT * GT) {
-#pragma unroll
-                    for (int k = 0; k < VPT; ++k) q[k] = ch[tg + k * GT];
-                    st.template add_chunk<true>(q, v0 + tg, v0 + nv, GT, a, smooth);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < VPT; ++k)
-                        if (tg + k * GT < nv) q[k] = ch[tg + k * GT];
-                    st.template add_chunk<false>(q, v0 + tg, v0 + nv, GT, a, smooth);
-                }
-                if (!a.resident) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
-                }
-                pos.next(sg);
-            }
-
-            // ---- merge: warp, then one group barrier, then the group's warp records
-            const RowSums wsum = warp_merge<SOFTCAP>(
-                st.m, st.S, smooth ? st.sumz - static_cast<float>(st.nel) * st.m : 0.f,
-                static_cast<float>(st.nel), st.xmax, st.best, smooth, a);
-            if (lane == 0) grec[g][rp][wg] = wsum;
-            group_sync();
-            const RowSums rec = lane < G ? grec[g][rp][lane]
-                                         : RowSums{-INFINITY, 0.f, 0.f, 0.f, -INFINITY, INT_MAX};
-            const RowSums tot = warp_merge<SOFTCAP>(rec.M, rec.S, rec.SZ, rec.n, rec.X, rec.I,
-                                                    smooth, a);
-            rp ^= 1;
-            const float M = tot.M;
-            const float logS = logf(tot.S);
-
-            if (gleader) {
-                const float zt = SOFTCAP ? a.softcap * tanh_from_scaled(xt * a.sc_k2) : xt;
-                float zl;
-                const float l = row_loss(a, M, logS, zt, wt, static_cast<float>(a.V), tot.SZ, zl);
-                const bool correct = tot.I < vrow * VE && static_cast<int64_t>(tot.I) == t;
-                if (a.reduction == kRedNone) {
-                    a.loss[r] = l;
-                    if (a.want_z) a.zloss[r] = zl;
-                    if (a.want_acc) a.acc[r] = correct ? 1.f : 0.f;
-                } else {
-                    accL += static_cast<double>(l);
-                    accZ += static_cast<double>(zl);
-                    accC += correct ? 1 : 0;
-                }
-                if (a.want_pred) a.pred[r] = tot.I < vrow * VE ? tot.I : -1;
-            }
-
-            // ---- pass 2: gradient in place
-            //   scale * [ (1-eps) w_t (p - onehot) + (eps/V)(V p - 1) + 2 lam lse p ] * dz/dx
-            // The one-hot term is added by the owner of the target's vector,
-            // which rewrites that element after storing the vector.
-            const float lse = M + logS;
-            const float As = scale * ((1.f - a.eps) * wt + a.eps + 2.f * a.lam * lse) / tot.S;
-            const float Bc = -scale * a.eps * inv_V;
-            const float ML = M * kLog2e;
-            if (a.resident) pos = pos0;
-            for (int c = 0, v0 = 0; c < nchunk; ++c, v0 += chunk_vec) {
-                const int slot = g * sg + pos.slot;
-                if (!a.resident && !failed &&
-                    !mbar_wait_bounded(smem_u32(&full_bar[slot]), pos.phase, a.timeout_ns)) {
-                    failed = true;
-                    atomicOr(&a.scratch->status, kDevErrTimeout);
-                }
-                const uint4* ch = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * chunk_bytes);
-                const int nv = min(chunk_vec, vrow - v0);
-                if (a.grad && !failed) {
-                    if (nv == VPT * GT)
-                        grad_chunk<T, SOFTCAP, VPT, true>(ch, rowv + v0 + tg, tg, nv, GT, M, ML,
-                                                          As, Bc, a);
-                    else
-                        grad_chunk<T, SOFTCAP, VPT, false>(ch, rowv + v0 + tg, tg, nv, GT, M, ML,
-                                                           As, Bc, a);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
-                pos.next(sg);
-            }
-            if (a.grad && !failed && t_owner) {
-                float e, fac = 1.f;
-                if (SOFTCAP) {
-                    const float th = tanh_from_scaled(xt * a.sc_k2);
-                    fac = fmaf(-th, th, 1.f);
-                    e = ex2((a.softcap * th - M) * kLog2e);
-                } else {
-                    e = ex2((xt - M) * kLog2e);
-                }
-                const float gt = (fmaf(As, e, Bc) - scale * (1.f - a.eps) * wt) * fac;
-                VT::store1(xrow, t, gt);
-            }
-        }
-        if (gleader) {
-            gpart_l[g] = accL;
-            gpart_z[g] = accZ;
-            s_correct[g] = static_cast<int>(accC);
-        }
-        if (failed && lane == 0) s_failed = 1;
-    }
-    __syncthreads();
-
-    if (s_failed && tid == NW * 32) {
-        // drain copies that may still be in flight: wait (bounded) for the
-        // last issued use of every slot
-        for (int i = 0; i < ng * sg; ++i) {
-            const uint32_t used = s_issued[i];
-            if (used) (void)mbar_wait_bounded(smem_u32(&full_bar[i]), used & 1u, a.timeout_ns);
-        }
-    }
-    if (a.reduction != kRedNone && tid < 32) {
-        double L = 0.0, Z = 0.0;
-        long long C = 0;
-        for (int g = 0; g < ng; ++g) {
-            L += gpart_l[g];
-            Z += gpart_z[g];
-            C += s_correct[g];
-        }
-        finish_scalars(a, cid, ncta, L, Z, C, s_D, s_nvalid);
-    }
-}
-
 const void* stream_kernel(int dtype, bool softcap, int vpt, int nw) {
-    // two shapes: 8 consumer warps with 8 vectors a thread a slot, or 16
-    // warps with 4 (both 1024 vectors per slot, both without spills)
-#define GBCE_STREAM(TT, SC)                                                     \
-    (nw == 8 && vpt == 8 ? (const void*)&ce_fwd_stream<TT, SC, 8, 8>            \
-                         : (nw == 16 && vpt == 4 ? (const void*)&ce_fwd_stream<TT, SC, 4, 16> \
-                                                 : nullptr))
+    // two shapes: 8 consumer warps with 8 vectors a thread a slot (168
+    // registers), or 16 warps with 4 (96 registers, a few bytes spilled);
+    // both take 2048 vectors per slot
+#define GBCE_STREAM(TT, SC)                                                         \
+    (nw == 8 && vpt == 8                                                            \
+         ? (const void*)&ce_fwd_stream<TT, SC, 8, 8, false>                         \
+         : (nw == 16 && vpt == 4 ? (const void*)&ce_fwd_stream<TT, SC, 4, 16, false> \
+                                 : nullptr))
     if (dtype == 0) return softcap ? GBCE_STREAM(float, true) : GBCE_STREAM(float, false);
     if (dtype == 1)
         return softcap ? GBCE_STREAM(__nv_bfloat16, true) : GBCE_STREAM(__nv_bfloat16, false);

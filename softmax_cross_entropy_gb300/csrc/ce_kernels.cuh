@@ -300,6 +300,8 @@ const void* staged_kernel_f32_nocap_wsmooth(int cfg);
 const void* staged_kernel_f32_softcap_plain(int cfg);
 const void* staged_kernel_f32_softcap_wsmooth(int cfg);
 const void* stream_kernel(int dtype, bool softcap, int vpt, int nw);
+// class weights with label smoothing: 8 consumer warps, 8 vectors a thread
+const void* stream_kernel_ws(int dtype, bool softcap);
 constexpr int kStreamMaxSlots = 48;   // ring slots (all groups) of the streaming kernel
 constexpr int kStreamMaxGroups = 8;
 const void* generic_kernel(int dtype, bool softcap);

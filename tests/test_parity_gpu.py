@@ -360,13 +360,13 @@ def test_module_reduction_none_backward():
 KINDS = {"staged": "1", "stream": "2", "general": "3"}
 
 
-@pytest.mark.parametrize("kind", sorted(KINDS) + ["stream16"])
+@pytest.mark.parametrize("kind", sorted(KINDS) + ["stream8", "stream16"])
 @pytest.mark.parametrize("dtype,V,rows", [("bf16", 4096, 300), ("bf16", 32768, 90),
                                           ("f32", 8192, 77), ("bf16", 131072, 20),
                                           ("f32", 24, 33)])
 def test_kernel_kinds(monkeypatch, kind, dtype, V, rows):
-    if kind == "stream16":
-        monkeypatch.setenv("GBCE_STREAM_WARPS", "16")
+    if kind in ("stream8", "stream16"):
+        monkeypatch.setenv("GBCE_STREAM_WARPS", kind[6:])
         kind = "stream"
     monkeypatch.setenv("GBCE_KERNEL", KINDS[kind])
     for opts in (dict(), dict(label_smoothing=0.1, softcap=20.0, lse_square_scale=1e-3),
@@ -396,4 +396,27 @@ def test_stream_twice_from_l2(monkeypatch, dtype, V, warps):
     monkeypatch.setenv("GBCE_STREAM_WARPS", str(warps))
     for opts in (dict(), dict(label_smoothing=0.2, softcap=10.0)):
         case = workloads.random_case(80, 61, V, dtype=dtype, **opts)
+        check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+@pytest.mark.parametrize("dtype,V,rows,twice", [
+    ("bf16", 4096, 150, 0),    # rows resident in the ring
+    ("bf16", 32000, 70, 0),    # the weights leave room for three 32 KB slots
+    ("bf16", 32000, 70, 1),
+    ("f32", 8192, 40, 0),
+    ("f32", 20000, 33, 1),
+    ("bf16", 49152, 13, 0),    # 192 KB of weights: smaller slots
+    ("f32", 24, 33, 0),
+])
+def test_stream_weighted_smoothing(monkeypatch, dtype, V, rows, twice):
+    # class weights with label smoothing in the streaming kernel, the weights
+    # held in shared memory
+    monkeypatch.setenv("GBCE_KERNEL", "2")
+    if twice:
+        monkeypatch.setenv("GBCE_STREAM_TWICE", "1")
+    for opts in (dict(weight=True, label_smoothing=0.05),
+                 dict(weight=True, label_smoothing=0.1, softcap=15.0, lse_square_scale=1e-3,
+                      reduction="none"),
+                 dict(weight=True, label_smoothing=1.0, reduction="sum", ignore_frac=0.3)):
+        case = workloads.random_case(90 + rows, rows, V, dtype=dtype, **opts)
         check_full(case, want_z=True, want_acc=True, want_pred=True)
