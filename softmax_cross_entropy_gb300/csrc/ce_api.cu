@@ -216,13 +216,13 @@ bool try_stream(int dtype, int64_t V, bool softcap, bool ws, const DeviceInfo& d
     const int64_t vec_row = V * bytes / 16;
     const int force_ng = env_int("GBCE_STREAM_GROUPS", 0);
     const bool force_twice = env_int("GBCE_STREAM_TWICE", 0) != 0;
-    // 16 consumer warps hide the longer per-element latency of softcap and
-    // of fp32 logits, and the row-end latency of short rows, better; long
-    // plain bf16 rows stream fastest with 8 (and the class-weighted
-    // smoothing kernel exists with 8 only). GBCE_STREAM_WARPS (8 or 16)
-    // overrides.
+    // 16 consumer warps hide latency better than 8 (measured on GB300 at
+    // 4096 rows, bf16: 6045 against 5815 GB/s at V = 131072, 3877 against
+    // 3561 at V = 16384), except for plain rows of at most 8 KB. The
+    // class-weighted smoothing kernel exists with 8 only. GBCE_STREAM_WARPS
+    // (8 or 16) overrides.
     const int nw_env = env_int("GBCE_STREAM_WARPS", 0);
-    const int nw_auto = (softcap || dtype == CE_F32 || V * bytes <= 32768) ? 16 : 8;
+    const int nw_auto = (!softcap && V * bytes <= 8192) ? 8 : 16;
     const int nw = ws ? 8 : (nw_env == 8 || nw_env == 16 ? nw_env : nw_auto);
     const int vpt_res = nw == 8 ? 8 : 4;  // the two compiled shapes
     const size_t wbytes = ws ? static_cast<size_t>((V * 4 + 15) / 16 * 16) : 0;

@@ -328,64 +328,75 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
 
     if (warp == NW) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t pol_keep = l2_evict_last_policy();
-            const uint64_t pol_once = l2_evict_first_policy();
-            int pslot[kStreamMaxGroups];
-            uint32_t pphase[kStreamMaxGroups];
+        // The warp's lanes read the targets of the CTA's next 32 rows at once
+        // (which rows count); lane 0 then issues the copies of those rows.
+        const uint64_t pol_keep = l2_evict_last_policy();
+        const uint64_t pol_once = l2_evict_first_policy();
+        int pslot[kStreamMaxGroups];
+        uint32_t pphase[kStreamMaxGroups];
 #pragma unroll
-            for (int k = 0; k < kStreamMaxGroups; ++k) {
-                pslot[k] = 0;
-                pphase[k] = 0;
-            }
-            bool failed = false;
-            int g = 0;
-            for (int64_t r = cid; r < a.rows && !failed; r += ncta) {
-                const int gg = g;
-                g = (g + 1 == ng) ? 0 : g + 1;
-                if (!row_counts(a, load_target(a, r))) continue;
-                const int passes = a.resident ? 1 : 2;
-                for (int p = 0; p < passes && !failed; ++p) {
-                    for (int c = 0; c < nchunk; ++c) {
-                        int ls = 0;
-                        uint32_t ph = 0;
+        for (int k = 0; k < kStreamMaxGroups; ++k) {
+            pslot[k] = 0;
+            pphase[k] = 0;
+        }
+        int failed = 0;
+        int g = 0;
+        for (int64_t rb = cid; rb < a.rows && !failed; rb += 32 * ncta) {
+            const int64_t rl = rb + lane * ncta;
+            const bool lane_counts = rl < a.rows && row_counts(a, load_target(a, rl));
+            const uint32_t counted = __ballot_sync(0xffffffffu, lane_counts);
+            if (lane == 0) {
+                for (int j = 0; j < 32 && !failed; ++j) {
+                    const int64_t r = rb + j * ncta;
+                    if (r >= a.rows) break;
+                    const int gg = g;
+                    g = (g + 1 == ng) ? 0 : g + 1;
+                    if (!((counted >> j) & 1u)) continue;
+                    const int passes = a.resident ? 1 : 2;
+                    for (int p = 0; p < passes && !failed; ++p) {
+                        for (int c = 0; c < nchunk; ++c) {
+                            int ls = 0;
+                            uint32_t ph = 0;
 #pragma unroll
-                        for (int k = 0; k < kStreamMaxGroups; ++k) {
-                            if (k == gg) {
-                                ls = pslot[k];
-                                ph = pphase[k];
-                                if (++pslot[k] == sg) {
-                                    pslot[k] = 0;
-                                    pphase[k] ^= 1u;
+                            for (int k = 0; k < kStreamMaxGroups; ++k) {
+                                if (k == gg) {
+                                    ls = pslot[k];
+                                    ph = pphase[k];
+                                    if (++pslot[k] == sg) {
+                                        pslot[k] = 0;
+                                        pphase[k] ^= 1u;
+                                    }
                                 }
                             }
+                            const int slot = gg * sg + ls;
+                            if (!mbar_wait_bounded(smem_u32(&empty_bar[slot]), ph ^ 1u,
+                                                   a.timeout_ns)) {
+                                failed = 1;
+                                break;
+                            }
+                            const int64_t v0 = static_cast<int64_t>(c) * chunk_vec;
+                            const uint32_t bytes =
+                                static_cast<uint32_t>(imin64(chunk_vec, vec_row - v0)) * 16u;
+                            const uint32_t fb = smem_u32(&full_bar[slot]);
+                            mbar_arrive_expect_tx(fb, bytes);
+                            const char* src = reinterpret_cast<const char*>(a.x) +
+                                              (r * a.V + v0 * VE) * static_cast<int64_t>(sizeof(T));
+                            const uint32_t dst =
+                                smem_u32(ring + static_cast<size_t>(slot) * chunk_bytes);
+                            const uint64_t pol = (!a.resident && p == 0) ? pol_keep : pol_once;
+                            for (uint32_t off = 0; off < bytes; off += kStreamCopyChunk)
+                                bulk_g2s(dst + off, src + off, min(kStreamCopyChunk, bytes - off),
+                                         fb, pol);
+                            s_issued[slot] = 2u + ph;  // nonzero: used; low bit: phase of the last use
                         }
-                        const int slot = gg * sg + ls;
-                        if (!mbar_wait_bounded(smem_u32(&empty_bar[slot]), ph ^ 1u,
-                                               a.timeout_ns)) {
-                            failed = true;
-                            break;
-                        }
-                        const int64_t v0 = static_cast<int64_t>(c) * chunk_vec;
-                        const uint32_t bytes =
-                            static_cast<uint32_t>(imin64(chunk_vec, vec_row - v0)) * 16u;
-                        const uint32_t fb = smem_u32(&full_bar[slot]);
-                        mbar_arrive_expect_tx(fb, bytes);
-                        const char* src = reinterpret_cast<const char*>(a.x) +
-                                          (r * a.V + v0 * VE) * static_cast<int64_t>(sizeof(T));
-                        const uint32_t dst = smem_u32(ring + static_cast<size_t>(slot) * chunk_bytes);
-                        const uint64_t pol = (!a.resident && p == 0) ? pol_keep : pol_once;
-                        for (uint32_t off = 0; off < bytes; off += kStreamCopyChunk)
-                            bulk_g2s(dst + off, src + off, min(kStreamCopyChunk, bytes - off), fb,
-                                     pol);
-                        s_issued[slot] = 2u + ph;  // nonzero: used; low bit: phase of the last use
                     }
                 }
             }
-            if (failed) {
-                atomicOr(&a.scratch->status, kDevErrTimeout);
-                s_failed = 1;
-            }
+            failed = __shfl_sync(0xffffffffu, failed, 0);
+        }
+        if (failed && lane == 0) {
+            atomicOr(&a.scratch->status, kDevErrTimeout);
+            s_failed = 1;
         }
     } else {
         // ------------------------------------------------------------ consumers
@@ -458,9 +469,13 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
         // multiple of GT vectors)
         auto owner_of = [&](int v) { return v & (GT - 1); };
 
-        for (int64_t r = cid + static_cast<int64_t>(g) * ncta; r < a.rows;
-             r += static_cast<int64_t>(ng) * ncta) {
-            const int64_t t = load_target(a, r);
+        // the next row's target is read one row ahead
+        const int64_t rstep = static_cast<int64_t>(ng) * ncta;
+        const int64_t r_first = cid + static_cast<int64_t>(g) * ncta;
+        int64_t t_next = r_first < a.rows ? load_target(a, r_first) : 0;
+        for (int64_t r = r_first; r < a.rows; r += rstep) {
+            const int64_t t = t_next;
+            if (r + rstep < a.rows) t_next = load_target(a, r + rstep);
             const bool counts = row_counts(a, t);
             T* xrow = reinterpret_cast<T*>(a.x) + r * a.V;
             uint4* rowv = reinterpret_cast<uint4*>(xrow);
