@@ -7,8 +7,8 @@ the two share no code. The arithmetic lives in ``ce_oracle.c`` (plain C,
 double precision, single-threaded); this module compiles it with gcc and
 marshals numpy arrays in and out.
 
-Logit storage: ``"f64"``, ``"f32"``, or ``"bf16"`` given as the raw uint16
-bit patterns (the oracle decodes them exactly).
+Logit storage: ``"f64"``, ``"f32"``, or ``"bf16"`` / ``"f16"`` given as the
+raw uint16 bit patterns (the oracle decodes them exactly).
 """
 from __future__ import annotations
 
@@ -23,8 +23,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "ce_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libceoracle.so")
 
-_DTYPES = {"f64": 0, "f32": 1, "bf16": 2}
-_NP_STORAGE = {"f64": np.float64, "f32": np.float32, "bf16": np.uint16}
+_DTYPES = {"f64": 0, "f32": 1, "bf16": 2, "f16": 3}
+_NP_STORAGE = {"f64": np.float64, "f32": np.float32, "bf16": np.uint16, "f16": np.uint16}
 REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
 
 _lock = threading.Lock()
@@ -68,6 +68,8 @@ def _load():
             lib.orc_ce_backward.restype = None
             lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.orc_bf16_to_double.restype = d
+            lib.orc_f16_to_double.argtypes = [ctypes.c_uint16]
+            lib.orc_f16_to_double.restype = d
             _lib = lib
     return _lib
 
@@ -172,3 +174,7 @@ def backward(grad, grad_output):
 
 def bf16_to_double(bits: int) -> float:
     return _load().orc_bf16_to_double(int(bits) & 0xFFFF)
+
+
+def f16_to_double(bits: int) -> float:
+    return _load().orc_f16_to_double(int(bits) & 0xFFFF)

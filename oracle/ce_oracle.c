@@ -36,15 +36,15 @@
  * loss 0, gradient +0 and predicted token -1, and its logits are never
  * read; accuracy is n_correct / n_valid (a 0/1 value per row under "none").
  *
- * Arithmetic: every input element is converted exactly to double (bf16 and
- * fp32 embed exactly in binary64); sums use Neumaier's compensated
+ * Arithmetic: every input element is converted exactly to double (bf16,
+ * fp16 and fp32 embed exactly in binary64); sums use Neumaier's compensated
  * summation.
  */
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
 
-enum { ORC_F64 = 0, ORC_F32 = 1, ORC_BF16 = 2 };
+enum { ORC_F64 = 0, ORC_F32 = 1, ORC_BF16 = 2, ORC_F16 = 3 };
 enum { ORC_NONE = 0, ORC_SUM = 1, ORC_MEAN = 2 };
 enum { ORC_OK = 0, ORC_BAD_ARG = 1, ORC_TARGET_RANGE = 2 };
 
@@ -59,10 +59,28 @@ static double bf16_bits_to_double(uint16_t bits) {
     return (double)f;
 }
 
+/* IEEE 754 binary16: sign bit, 5 exponent bits with bias 15, 10 fraction
+ * bits. Exponent field 0 holds zero and the subnormals (fraction * 2^-24);
+ * 31 holds the infinities (fraction 0) and NaN; otherwise the value is
+ * (1024 + fraction) * 2^(exponent - 25). Every value is exact in double. */
+static double f16_bits_to_double(uint16_t bits) {
+    const int e = (bits >> 10) & 0x1F;
+    const int f = bits & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return (bits & 0x8000) ? -v : v;
+}
+
 static double logit(const void* x, int dtype, int64_t k) {
     switch (dtype) {
     case ORC_F64: return ((const double*)x)[k];
     case ORC_F32: return (double)((const float*)x)[k];
+    case ORC_F16: return f16_bits_to_double(((const uint16_t*)x)[k]);
     default: return bf16_bits_to_double(((const uint16_t*)x)[k]);
     }
 }
@@ -227,7 +245,8 @@ static int check_args(const void* x, int dtype, int64_t rows, int64_t V,
                       int reduction) {
     if (rows < 0 || V <= 0) return ORC_BAD_ARG;
     if (rows > 0 && (!x || !target)) return ORC_BAD_ARG;
-    if (dtype != ORC_F64 && dtype != ORC_F32 && dtype != ORC_BF16) return ORC_BAD_ARG;
+    if (dtype != ORC_F64 && dtype != ORC_F32 && dtype != ORC_BF16 && dtype != ORC_F16)
+        return ORC_BAD_ARG;
     if (!(eps >= 0.0 && eps <= 1.0)) return ORC_BAD_ARG;
     if (isnan(softcap) || isinf(softcap)) return ORC_BAD_ARG;
     if (reduction != ORC_NONE && reduction != ORC_SUM && reduction != ORC_MEAN)
@@ -347,3 +366,7 @@ void orc_ce_backward(double* grad, int64_t rows, int64_t V,
 /* Exposes the bf16 decoding so that a test can pin it to known bit
  * patterns. */
 double orc_bf16_to_double(uint16_t bits) { return bf16_bits_to_double(bits); }
+
+/* Exposes the fp16 decoding so that a test can pin it against every bit
+ * pattern. */
+double orc_f16_to_double(uint16_t bits) { return f16_bits_to_double(bits); }

@@ -130,6 +130,46 @@ def test_bf16_storage_matches_f64_storage(oracle_mod):
     assert np.array_equal(a["loss"], b["loss"]) and np.array_equal(a["grad"], b["grad"])
 
 
+def test_f16_decoding_matches_numpy_for_every_bit_pattern(oracle_mod):
+    # numpy's float16 -> float64 widening is exact (IEEE binary16): it pins
+    # the oracle's own decoder on all 65536 patterns, subnormals, signed
+    # zeros, infinities and NaNs included
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle_mod.f16_to_double(int(b)) for b in bits])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+    # a few values written out
+    pins = {0x3C00: 1.0, 0xC000: -2.0, 0x0001: 2.0 ** -24, 0x0400: 2.0 ** -14,
+            0x7BFF: 65504.0, 0x3555: 0.333251953125}
+    for b, v in pins.items():
+        assert oracle_mod.f16_to_double(b) == v, hex(b)
+
+
+def test_f16_storage_matches_f64_storage(oracle_mod):
+    rng = np.random.default_rng(5)
+    xf = rng.normal(0, 3, (4, 41)).astype(np.float32)
+    bits = workloads.f32_to_f16_bits(xf)
+    t = rng.integers(0, 41, 4)
+    opts = dict(reduction="none", label_smoothing=0.1, lse_square_scale=1e-3, softcap=9.0)
+    a = oracle_mod.forward(bits, t, dtype="f16", **opts)
+    b = oracle_mod.forward(bits.view(np.float16).astype(np.float64), t, dtype="f64", **opts)
+    assert np.array_equal(a["loss"], b["loss"]) and np.array_equal(a["grad"], b["grad"])
+
+
+def test_generator_f16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    vals = np.array([1.0, 1.0 + 2 ** -11, 1.0 + 3 * 2 ** -11, -2.5, 70000.0, 1e-8,
+                     3e-5, np.inf, -np.inf], np.float32)
+    rng = np.random.default_rng(6)
+    vals = np.concatenate([vals, rng.normal(0, 10, 1000).astype(np.float32)])
+    ours = workloads.f32_to_f16_bits(vals)
+    ref = torch.from_numpy(vals).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
 def test_generator_bf16_rounding_matches_torch():
     torch = pytest.importorskip("torch")
     vals = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 3.4e38, 1e-40,

@@ -54,8 +54,8 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 @dataclass
 class Case:
     name: str
-    x: np.ndarray             # float32 (rows, V), or uint16 bf16 bits (rows, V)
-    dtype: str                # "f32" | "bf16"
+    x: np.ndarray             # float32 (rows, V), or uint16 bf16 / fp16 bits (rows, V)
+    dtype: str                # "f32" | "bf16" | "f16"
     target: np.ndarray        # int32 (rows,)
     weight: np.ndarray | None = None   # float32 (V,)
     ignore_index: int = IGNORE_INDEX
@@ -88,14 +88,20 @@ class Case:
 _BLOCK_ELEMS = 1 << 22  # elements per independently seeded block
 
 
-def _blocked_normal(seed, rows, V, std, to_bf16):
+def f32_to_f16_bits(a: np.ndarray) -> np.ndarray:
+    """Rounds float32 values to IEEE binary16 (numpy's conversion: nearest,
+    ties to even; overflow to infinity) and returns the uint16 bit patterns."""
+    return np.ascontiguousarray(a, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def _blocked_normal(seed, rows, V, std, storage):
     """N(0, std^2) logits drawn in fixed row blocks, block b from child b of
     SeedSequence([seed, 0]); blocks run on a thread pool (numpy's generators
     and ufuncs release the GIL), so the values do not depend on the number
     of threads."""
     from concurrent.futures import ThreadPoolExecutor
     import os
-    out = np.empty((rows, V), np.uint16 if to_bf16 else np.float32)
+    out = np.empty((rows, V), np.float32 if storage == "f32" else np.uint16)
     if out.size == 0:
         return out
     brows = max(1, _BLOCK_ELEMS // max(V, 1))
@@ -107,7 +113,12 @@ def _blocked_normal(seed, rows, V, std, to_bf16):
         r1 = min(rows, r0 + brows)
         blk = np.random.default_rng(seeds[i]).standard_normal((r1 - r0, V), dtype=np.float32)
         blk *= np.float32(std)
-        out[r0:r1] = f32_to_bf16_bits(blk) if to_bf16 else blk
+        if storage == "bf16":
+            out[r0:r1] = f32_to_bf16_bits(blk)
+        elif storage == "f16":
+            out[r0:r1] = f32_to_f16_bits(blk)
+        else:
+            out[r0:r1] = blk
 
     if len(starts) == 1:
         fill(0)
@@ -118,11 +129,15 @@ def _blocked_normal(seed, rows, V, std, to_bf16):
 
 
 def _normal(seed, rows, V, std):
-    return _blocked_normal(seed, rows, V, std, to_bf16=False)
+    return _blocked_normal(seed, rows, V, std, "f32")
 
 
 def _bf16_normal(seed, rows, V, std):
-    return _blocked_normal(seed, rows, V, std, to_bf16=True)
+    return _blocked_normal(seed, rows, V, std, "bf16")
+
+
+def _f16_normal(seed, rows, V, std):
+    return _blocked_normal(seed, rows, V, std, "f16")
 
 
 def _aux_rng(seed):
@@ -193,7 +208,8 @@ def weighted(seed=0, rows=16384, V=32000, reduction="mean") -> Case:
 def random_case(seed, rows, V, dtype="f32", std=3.0, ignore_frac=0.1, **opts) -> Case:
     """Generic seeded case for parity sweeps over shapes and options."""
     rng = _aux_rng(seed)
-    x = _normal(seed, rows, V, std) if dtype == "f32" else _bf16_normal(seed, rows, V, std)
+    gen = {"f32": _normal, "bf16": _bf16_normal, "f16": _f16_normal}[dtype]
+    x = gen(seed, rows, V, std)
     t = targets(rng, rows, V, ignore_frac)
     w = opts.pop("weight", None)
     if w is True:
@@ -202,7 +218,9 @@ def random_case(seed, rows, V, dtype="f32", std=3.0, ignore_frac=0.1, **opts) ->
 
 
 def logits_f64(case: Case) -> np.ndarray:
-    """The logits as float64 values (exact for both storages)."""
+    """The logits as float64 values (exact for every storage)."""
     if case.dtype == "bf16":
         return bf16_bits_to_f32(case.x).astype(np.float64)
+    if case.dtype == "f16":
+        return np.ascontiguousarray(case.x, dtype=np.uint16).view(np.float16).astype(np.float64)
     return case.x.astype(np.float64)
