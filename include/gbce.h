@@ -45,8 +45,9 @@
  * and a 0/1 value per row for "none"; a row is correct when its argmax
  * (over the raw logits, lowest index on ties) equals its target.
  *
- * Arithmetic: fp32 in registers for every input dtype; gradients are
- * rounded to nearest-even into the logit dtype. Partial sums of the scalar
+ * Arithmetic: fp32 in registers for every input dtype (fp32, bf16, fp16);
+ * gradients are rounded to nearest-even into the logit dtype (fp16
+ * gradients below 2^-24 in magnitude round to zero or a subnormal). Partial sums of the scalar
  * outputs are combined in a fixed order, so results are run-to-run
  * deterministic.
  *
@@ -79,7 +80,7 @@ typedef enum {
     CE_ERR_TIMEOUT = 5        /* a bounded device wait gave up; that call's outputs are invalid */
 } ce_status;
 
-typedef enum { CE_F32 = 0, CE_BF16 = 1 } ce_dtype;
+typedef enum { CE_F32 = 0, CE_BF16 = 1, CE_F16 = 2 } ce_dtype;
 
 typedef enum { CE_RED_NONE = 0, CE_RED_SUM = 1, CE_RED_MEAN = 2 } ce_reduction;
 
@@ -94,7 +95,7 @@ enum {
 /*
  * ce_fwd - fused forward (and, with CE_FLAG_GRAD, the in-forward gradient).
  *
- * logits       [rows, V] row-major, dtype `dtype` (CE_F32 or CE_BF16). With
+ * logits       [rows, V] row-major, dtype `dtype` (CE_F32, CE_BF16 or CE_F16). With
  *              CE_FLAG_GRAD it is overwritten by dlogits (d loss / d logits
  *              of the reduced loss; for "none", of the sum of the row
  *              losses). The fast path needs a 16-byte aligned base and
@@ -160,6 +161,50 @@ ce_status ce_fwd_noalloc(void* logits, int dtype, int64_t rows, int64_t V,
                          float label_smoothing, float lse_square_scale, float softcap,
                          int reduction, uint32_t flags, float* loss, float* z_loss,
                          float* acc, int64_t* pred, ce_stream_t stream);
+
+/*
+ * ce_count - counts of one shard of rows, for a "mean" over a batch whose
+ * rows are split across calls or GPUs (the mean divides by D, the sum of
+ * w[t_i] over the rows that take part: "Kernel Profile: CrossEntropy",
+ * §Forward Pass, reductions; tt-mlir pull request #9324 review comments,
+ * total_weight).
+ *
+ * target, weight, rows, V, ignore_index, flags (only CE_FLAG_TARGET_I64)
+ *              as for ce_fwd; rows may be 0.
+ * counts       device pointer to two doubles, written: counts[0] = D of
+ *              these rows (the count when weight is NULL), counts[1] = the
+ *              number of rows that take part (target not ignore_index and in
+ *              [0, V); out-of-range targets are reported by ce_fwd).
+ * Asynchronous on `stream`; deterministic (fixed-order sums in double).
+ * Uses the library scratch of (device, stream), like ce_fwd.
+ */
+ce_status ce_count(const void* target, const float* weight, int64_t rows, int64_t V,
+                   int64_t ignore_index, uint32_t flags, double* counts, ce_stream_t stream);
+
+/*
+ * ce_fwd_shard - ce_fwd for one shard of a batch whose counts are known.
+ *
+ * The caller adds the ce_count outputs of every shard (an all-reduce sum
+ * across GPUs, one exchange before the forward) and passes the totals in
+ * batch_counts (device pointer to two doubles: D and the number of counted
+ * rows of the whole batch). Arguments and outputs are those of ce_fwd,
+ * except that the batch totals replace this call's own counts:
+ *  - "mean": loss = (sum of this shard's row losses) / D, likewise z_loss,
+ *    and the gradient is scaled by 1 / D, so adding the shards' losses gives
+ *    the whole batch's mean and every shard's gradient is already the
+ *    gradient of that mean;
+ *  - "sum" and "mean": acc = (this shard's correct rows) / (the batch's
+ *    counted rows), so the shards' values add up to the batch accuracy;
+ *  - "none" is unaffected.
+ * A shard with no rows writes 0 (not NaN) for loss, z_loss and acc when the
+ * batch has counted rows. batch_counts NULL is CE_ERR_INVALID_ARG.
+ */
+ce_status ce_fwd_shard(void* logits, int dtype, int64_t rows, int64_t V,
+                       const void* target, const float* weight, int64_t ignore_index,
+                       float label_smoothing, float lse_square_scale, float softcap,
+                       int reduction, uint32_t flags, float* loss, float* z_loss,
+                       float* acc, int64_t* pred, const double* batch_counts,
+                       ce_stream_t stream);
 
 /*
  * ce_bwd - backward (§Backward Pass: the stored gradient times

@@ -8,7 +8,8 @@
 
 The arguments and outputs are those of the Liger-Kernel cross-entropy kernel
 profile (§Forward Pass, §Module Parameters). ``logits`` is a 2-D (B*T, V)
-CUDA tensor in float32 or bfloat16; ``target`` holds int32 or int64 labels.
+CUDA tensor in float32, bfloat16 or float16; ``target`` holds int32 or int64
+labels.
 When ``logits.requires_grad`` the forward writes the gradient of the reduced
 loss over ``logits`` itself (§Backward Pass: the gradient-in-forward trick),
 so the logits' values are gone after the call and backward only scales that
@@ -22,17 +23,19 @@ from collections import namedtuple
 import torch
 
 from . import _lib
-from ._lib import CEError, ce_bwd, ce_device_status, ce_fwd, ce_last_error, ce_status_string
+from ._lib import (CEError, ce_bwd, ce_count, ce_device_status, ce_fwd, ce_fwd_shard,
+                   ce_last_error, ce_status_string)
 
 __all__ = ["cross_entropy", "CrossEntropyLoss", "CrossEntropyFunction", "CrossEntropyOutput",
-           "CEError", "device_status", "ce_fwd", "ce_bwd", "ce_device_status",
-           "ce_status_string", "ce_last_error"]
+           "CEError", "device_status", "shard_counts", "ce_fwd", "ce_fwd_shard", "ce_count",
+           "ce_bwd", "ce_device_status", "ce_status_string", "ce_last_error"]
 
 CrossEntropyOutput = namedtuple("CrossEntropyOutput",
                                 ["loss", "z_loss", "token_accuracy", "predicted_tokens"])
 
 _REDUCTIONS = {"none": _lib.CE_RED_NONE, "sum": _lib.CE_RED_SUM, "mean": _lib.CE_RED_MEAN}
-_DTYPES = {torch.float32: _lib.CE_F32, torch.bfloat16: _lib.CE_BF16}
+_DTYPES = {torch.float32: _lib.CE_F32, torch.bfloat16: _lib.CE_BF16,
+           torch.float16: _lib.CE_F16}
 
 
 def _ptr(t):
@@ -50,7 +53,8 @@ def _check_inputs(logits, target, weight):
     if not logits.is_cuda:
         raise ValueError("logits must be a CUDA tensor")
     if logits.dtype not in _DTYPES:
-        raise TypeError(f"logits dtype {logits.dtype} is not supported (float32, bfloat16)")
+        raise TypeError(f"logits dtype {logits.dtype} is not supported "
+                        "(float32, bfloat16, float16)")
     if target.dim() != 1 or target.shape[0] != logits.shape[0]:
         raise ValueError("target must be 1-D with one label per row of logits")
     if target.dtype not in (torch.int32, torch.int64):
@@ -65,9 +69,9 @@ def _check_inputs(logits, target, weight):
 
 
 def _forward(logits, target, weight, ignore_index, lse_square_scale, label_smoothing,
-             reduction, softcap, want_grad, want_z, want_acc, want_pred):
-    """Runs ce_fwd; returns (loss, z_loss, acc, pred). Writes dlogits over
-    logits when want_grad."""
+             reduction, softcap, want_grad, want_z, want_acc, want_pred, batch_counts=None):
+    """Runs ce_fwd (ce_fwd_shard with batch_counts); returns (loss, z_loss,
+    acc, pred). Writes dlogits over logits when want_grad."""
     rows, V = logits.shape
     dev = logits.device
     red = _REDUCTIONS[reduction]
@@ -81,14 +85,37 @@ def _forward(logits, target, weight, ignore_index, lse_square_scale, label_smoot
              (_lib.CE_FLAG_ACC if want_acc else 0) | (_lib.CE_FLAG_PRED if want_pred else 0) |
              (_lib.CE_FLAG_TARGET_I64 if target.dtype == torch.int64 else 0))
     w = None if weight is None else weight.to(torch.float32).contiguous()
+    args = (_ptr(logits), _DTYPES[logits.dtype], rows, V, _ptr(target), _ptr(w),
+            int(ignore_index), float(label_smoothing), float(lse_square_scale),
+            float(softcap) if softcap is not None else 0.0, red, flags, _ptr(loss),
+            _ptr(z_loss), _ptr(acc), _ptr(pred))
     with torch.cuda.device(dev):
-        rc = ce_fwd(_ptr(logits), _DTYPES[logits.dtype], rows, V, _ptr(target), _ptr(w),
-                    int(ignore_index), float(label_smoothing), float(lse_square_scale),
-                    float(softcap) if softcap is not None else 0.0, red, flags, _ptr(loss),
-                    _ptr(z_loss), _ptr(acc), _ptr(pred), _stream(dev))
+        if batch_counts is None:
+            rc, where = ce_fwd(*args, _stream(dev)), "ce_fwd"
+        else:
+            rc, where = ce_fwd_shard(*args, _ptr(batch_counts), _stream(dev)), "ce_fwd_shard"
     if rc != _lib.CE_OK:
-        raise CEError(rc, "ce_fwd")
+        raise CEError(rc, where)
     return loss, z_loss, acc, pred
+
+
+def shard_counts(target, V, weight=None, ignore_index=-100):
+    """(D, counted rows) of these rows as a float64 CUDA tensor of 2 (ce_count):
+    D = sum of weight[t] (the count without weights) over the rows whose
+    target is neither ignore_index nor out of [0, V)."""
+    if target.dim() != 1 or not target.is_cuda or target.dtype not in (torch.int32, torch.int64):
+        raise ValueError("target must be a 1-D int32 or int64 CUDA tensor")
+    target = target.contiguous()
+    dev = target.device
+    w = None if weight is None else weight.to(device=dev, dtype=torch.float32).contiguous()
+    counts = torch.empty(2, dtype=torch.float64, device=dev)
+    flags = _lib.CE_FLAG_TARGET_I64 if target.dtype == torch.int64 else 0
+    with torch.cuda.device(dev):
+        rc = ce_count(_ptr(target), _ptr(w), target.shape[0], int(V), int(ignore_index), flags,
+                      _ptr(counts), _stream(dev))
+    if rc != _lib.CE_OK:
+        raise CEError(rc, "ce_count")
+    return counts
 
 
 class CrossEntropyFunction(torch.autograd.Function):
@@ -97,12 +124,12 @@ class CrossEntropyFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, logits, target, weight, ignore_index, lse_square_scale, label_smoothing,
-                reduction, softcap, return_z_loss, return_acc, return_pred):
+                reduction, softcap, return_z_loss, return_acc, return_pred, batch_counts=None):
         want_grad = logits.requires_grad
         loss, z_loss, acc, pred = _forward(logits, target, weight, ignore_index,
                                            lse_square_scale, label_smoothing, reduction,
                                            softcap, want_grad, return_z_loss, return_acc,
-                                           return_pred)
+                                           return_pred, batch_counts)
         ctx.reduction = reduction
         if want_grad:
             ctx.save_for_backward(logits.detach())  # now holds dlogits
@@ -122,16 +149,28 @@ class CrossEntropyFunction(torch.autograd.Function):
                         _stream(dlogits.device))
         if rc != _lib.CE_OK:
             raise CEError(rc, "ce_bwd")
-        return dlogits, None, None, None, None, None, None, None, None, None, None
+        return dlogits, None, None, None, None, None, None, None, None, None, None, None
 
 
 def cross_entropy(logits, target, weight=None, ignore_index=-100, lse_square_scale=0.0,
                   label_smoothing=0.0, reduction="mean", softcap=None, return_z_loss=False,
-                  return_token_accuracy=False, return_predicted_tokens=False):
+                  return_token_accuracy=False, return_predicted_tokens=False,
+                  batch_counts=None):
     """Fused softmax cross-entropy. Returns the loss tensor, or a
     CrossEntropyOutput(loss, z_loss, token_accuracy, predicted_tokens) when
-    any return_* flag is set (unrequested fields are None)."""
+    any return_* flag is set (unrequested fields are None).
+
+    batch_counts: for one shard of a row-sharded batch, the float64 CUDA
+    tensor (D, counted rows) of the whole batch (the sum over shards of
+    shard_counts, e.g. after an all-reduce). The "mean" loss is then this
+    shard's share of the batch mean (the shards' values add up to it) and
+    the gradient is that of the batch mean; accuracy likewise."""
     _check_inputs(logits, target, weight)
+    if batch_counts is not None:
+        if (not isinstance(batch_counts, torch.Tensor) or batch_counts.dtype != torch.float64
+                or batch_counts.numel() != 2 or batch_counts.device != logits.device):
+            raise ValueError("batch_counts must be a float64 tensor of 2 on the logits' device")
+        batch_counts = batch_counts.contiguous()
     if reduction not in _REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(_REDUCTIONS)}")
     if not 0.0 <= label_smoothing <= 1.0:
@@ -143,7 +182,7 @@ def cross_entropy(logits, target, weight=None, ignore_index=-100, lse_square_sca
     target = target.contiguous()
     loss, z_loss, acc, pred = CrossEntropyFunction.apply(
         logits, target, weight, ignore_index, lse_square_scale, label_smoothing, reduction,
-        softcap, return_z_loss, return_token_accuracy, return_predicted_tokens)
+        softcap, return_z_loss, return_token_accuracy, return_predicted_tokens, batch_counts)
     if return_z_loss or return_token_accuracy or return_predicted_tokens:
         return CrossEntropyOutput(loss, z_loss, acc, pred)
     return loss

@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgbce.so"
 
 CE_OK, CE_ERR_INVALID_ARG, CE_ERR_UNSUPPORTED, CE_ERR_CUDA, CE_ERR_TARGET_RANGE, \
     CE_ERR_TIMEOUT = range(6)
-CE_F32, CE_BF16 = 0, 1
+CE_F32, CE_BF16, CE_F16 = 0, 1, 2
 CE_RED_NONE, CE_RED_SUM, CE_RED_MEAN = 0, 1, 2
 CE_FLAG_GRAD, CE_FLAG_Z_LOSS, CE_FLAG_ACC, CE_FLAG_PRED, CE_FLAG_TARGET_I64 = 1, 2, 4, 8, 16
 
@@ -24,6 +24,9 @@ SIGNATURES = {
     "ce_fwd": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P, _P, _P, _P]),
     "ce_fwd_noalloc": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P, _P, _P,
                             _P]),
+    "ce_fwd_shard": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P, _P, _P,
+                          _P, _P]),
+    "ce_count": (_I, [_P, _P, _I64, _I64, _I64, _U32, _P, _P]),
     "ce_bwd": (_I, [_P, _I, _P, _I, _I64, _I64, _P]),
     "ce_device_status": (_I, [_P]),
     "ce_status_string": (ctypes.c_char_p, [_I]),
@@ -73,6 +76,18 @@ def ce_fwd_noalloc(logits, dtype, rows, V, target, weight, ignore_index, label_s
     return load().ce_fwd_noalloc(logits, dtype, rows, V, target, weight, ignore_index,
                                  label_smoothing, lse_square_scale, softcap, reduction, flags,
                                  loss, z_loss, acc, pred, stream)
+
+
+def ce_fwd_shard(logits, dtype, rows, V, target, weight, ignore_index, label_smoothing,
+                 lse_square_scale, softcap, reduction, flags, loss, z_loss, acc, pred,
+                 batch_counts, stream):
+    return load().ce_fwd_shard(logits, dtype, rows, V, target, weight, ignore_index,
+                               label_smoothing, lse_square_scale, softcap, reduction, flags,
+                               loss, z_loss, acc, pred, batch_counts, stream)
+
+
+def ce_count(target, weight, rows, V, ignore_index, flags, counts, stream):
+    return load().ce_count(target, weight, rows, V, ignore_index, flags, counts, stream)
 
 
 def ce_bwd(grad_output, grad_per_row, dlogits, dtype, rows, V, stream):

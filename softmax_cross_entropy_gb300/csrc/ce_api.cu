@@ -102,6 +102,7 @@ ce_status scratch_for(int dev, cudaStream_t st, Scratch** out) {
 }
 
 const void* staged_fn(int dtype, int cfg, bool softcap, bool wsmooth) {
+    if (dtype == CE_F16) return nullptr;  // fp16 takes the streaming or the general kernel
     if (dtype == CE_BF16) {
         if (softcap)
             return wsmooth ? staged_kernel_bf16_softcap_wsmooth(cfg)
@@ -118,7 +119,7 @@ const void* staged_fn(int dtype, int cfg, bool softcap, bool wsmooth) {
 // the general path are tried); `occ` receives the CTAs per SM.
 bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, int cfg,
                 const DeviceInfo& dev, Plan* out, int* occ, ce_status* err) {
-    const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
+    const int64_t bytes = dtype == CE_F32 ? 4 : 2;
     const int64_t ve = 16 / bytes;
     const int64_t vec_row = V / ve;
     const int64_t per = (vec_row + C - 1) / C;
@@ -212,7 +213,7 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, int cfg
 // least two slots.
 bool try_stream(int dtype, int64_t V, bool softcap, bool ws, const DeviceInfo& dev, Plan* out,
                 ce_status* err) {
-    const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
+    const int64_t bytes = dtype == CE_F32 ? 4 : 2;
     const int64_t vec_row = V * bytes / 16;
     const int force_ng = env_int("GBCE_STREAM_GROUPS", 0);
     const bool force_twice = env_int("GBCE_STREAM_TWICE", 0) != 0;
@@ -330,7 +331,7 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     ce_status rc = device_info(devid, &dev);
     if (rc != CE_OK) return rc;
     Plan best;
-    const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
+    const int64_t bytes = dtype == CE_F32 ? 4 : 2;
     const bool fast_ok = aligned && (V * bytes) % 16 == 0 && forced_c >= 0 && forced_kind != 3;
     if (fast_ok && forced_kind != 1) {
         rc = CE_OK;
@@ -418,76 +419,83 @@ bool finite(float v) { return std::isfinite(v); }
 
 using namespace gbce;
 
-extern "C" ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V, const void* target,
-                            const float* weight, int64_t ignore_index, float label_smoothing,
-                            float lse_square_scale, float softcap, int reduction, uint32_t flags,
-                            float* loss, float* z_loss, float* acc, int64_t* pred,
-                            ce_stream_t stream) {
+namespace gbce {
+namespace {
+
+// Argument checks shared by the forward entry points (CE_OK: go on).
+ce_status check_fwd(const FwdCall& c) {
     const uint32_t known =
         CE_FLAG_GRAD | CE_FLAG_Z_LOSS | CE_FLAG_ACC | CE_FLAG_PRED | CE_FLAG_TARGET_I64;
-    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_INVALID_ARG;
-    if (rows < 0 || V <= 0) return CE_ERR_INVALID_ARG;
-    if (V > INT32_MAX - 16) return CE_ERR_UNSUPPORTED;
-    if (reduction != CE_RED_NONE && reduction != CE_RED_SUM && reduction != CE_RED_MEAN)
+    if (c.dtype != CE_F32 && c.dtype != CE_BF16 && c.dtype != CE_F16) return CE_ERR_INVALID_ARG;
+    if (c.rows < 0 || c.V <= 0) return CE_ERR_INVALID_ARG;
+    if (c.V > INT32_MAX - 16) return CE_ERR_UNSUPPORTED;
+    if (c.reduction != CE_RED_NONE && c.reduction != CE_RED_SUM && c.reduction != CE_RED_MEAN)
         return CE_ERR_INVALID_ARG;
-    if (flags & ~known) return CE_ERR_INVALID_ARG;
-    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return CE_ERR_INVALID_ARG;
-    if (!finite(lse_square_scale)) return CE_ERR_INVALID_ARG;
-    if (!finite(softcap) || softcap < 0.f) return CE_ERR_INVALID_ARG;
-    if (!loss) return CE_ERR_INVALID_ARG;
-    if ((flags & CE_FLAG_Z_LOSS) && !z_loss) return CE_ERR_INVALID_ARG;
-    if ((flags & CE_FLAG_ACC) && !acc) return CE_ERR_INVALID_ARG;
-    if ((flags & CE_FLAG_PRED) && !pred) return CE_ERR_INVALID_ARG;
-    if (rows > 0 && (!logits || !target)) return CE_ERR_INVALID_ARG;
-    if (rows > 0 && V > INT64_MAX / rows / 4) return CE_ERR_INVALID_ARG;
-    if (rows == 0 && reduction == CE_RED_NONE) return CE_OK;  // nothing to write
+    if (c.flags & ~known) return CE_ERR_INVALID_ARG;
+    if (!(c.label_smoothing >= 0.f && c.label_smoothing <= 1.f)) return CE_ERR_INVALID_ARG;
+    if (!finite(c.lse_square_scale)) return CE_ERR_INVALID_ARG;
+    if (!finite(c.softcap) || c.softcap < 0.f) return CE_ERR_INVALID_ARG;
+    if (!c.loss) return CE_ERR_INVALID_ARG;
+    if ((c.flags & CE_FLAG_Z_LOSS) && !c.z_loss) return CE_ERR_INVALID_ARG;
+    if ((c.flags & CE_FLAG_ACC) && !c.acc) return CE_ERR_INVALID_ARG;
+    if ((c.flags & CE_FLAG_PRED) && !c.pred) return CE_ERR_INVALID_ARG;
+    if (c.rows > 0 && (!c.logits || !c.target)) return CE_ERR_INVALID_ARG;
+    if (c.rows > 0 && c.V > INT64_MAX / c.rows / 4) return CE_ERR_INVALID_ARG;
+    return CE_OK;
+}
 
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    Scratch* scratch = nullptr;
-    ce_status rc = scratch_for(dev, st, &scratch);
-    if (rc != CE_OK) return rc;
-
+// Plans and launches one checked forward call with `scratch`, whose ticket
+// and status word are zero on entry or, with clear_header, cleared here.
+// A grid that would need more than max_slots partial-sum slots is refused.
+// Called with g_mu held.
+ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots,
+                  bool clear_header, cudaStream_t st) {
     FwdArgs a = {};
-    a.x = logits;
-    a.rows = rows;
-    a.V = V;
-    a.target = target;
-    a.tgt64 = (flags & CE_FLAG_TARGET_I64) ? 1 : 0;
-    a.weight = weight;
-    a.ignore_index = ignore_index;
-    a.eps = label_smoothing;
-    a.lam = lse_square_scale;
-    const bool sc = softcap > 0.f;
-    a.softcap = sc ? softcap : 0.f;
-    a.sc_k2 = sc ? 2.f * kLog2e / softcap : 0.f;
-    a.sc_slog2e = sc ? softcap * kLog2e : 0.f;
-    a.reduction = reduction;
-    a.grad = (flags & CE_FLAG_GRAD) ? 1 : 0;
-    a.want_z = (flags & CE_FLAG_Z_LOSS) ? 1 : 0;
-    a.want_acc = (flags & CE_FLAG_ACC) ? 1 : 0;
-    a.want_pred = (flags & CE_FLAG_PRED) ? 1 : 0;
-    a.loss = loss;
-    a.zloss = z_loss;
-    a.acc = acc;
-    a.pred = pred;
+    a.x = c.logits;
+    a.rows = c.rows;
+    a.V = c.V;
+    a.target = c.target;
+    a.tgt64 = (c.flags & CE_FLAG_TARGET_I64) ? 1 : 0;
+    a.weight = c.weight;
+    a.ignore_index = c.ignore_index;
+    a.eps = c.label_smoothing;
+    a.lam = c.lse_square_scale;
+    const bool sc = c.softcap > 0.f;
+    a.softcap = sc ? c.softcap : 0.f;
+    a.sc_k2 = sc ? 2.f * kLog2e / c.softcap : 0.f;
+    a.sc_slog2e = sc ? c.softcap * kLog2e : 0.f;
+    a.reduction = c.reduction;
+    a.grad = (c.flags & CE_FLAG_GRAD) ? 1 : 0;
+    a.want_z = (c.flags & CE_FLAG_Z_LOSS) ? 1 : 0;
+    a.want_acc = (c.flags & CE_FLAG_ACC) ? 1 : 0;
+    a.want_pred = (c.flags & CE_FLAG_PRED) ? 1 : 0;
+    a.loss = c.loss;
+    a.zloss = c.z_loss;
+    a.acc = c.acc;
+    a.pred = c.pred;
     a.timeout_ns = static_cast<uint64_t>(env_int("GBCE_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
     a.scratch = scratch;
+    a.batch_counts = c.batch_counts;
 
-    const bool wsmooth = weight != nullptr && label_smoothing > 0.f;
-    const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16) == 0;
+    const bool wsmooth = c.weight != nullptr && c.label_smoothing > 0.f;
+    const bool aligned = (reinterpret_cast<uintptr_t>(c.logits) % 16) == 0;
     Plan p;
-    rc = make_plan(dev, dtype, V, sc, wsmooth, aligned, &p);
+    ce_status rc = make_plan(dev, c.dtype, c.V, sc, wsmooth, aligned, &p);
     if (rc != CE_OK) return rc;
-    if (rows == 0) {
-        // empty batch: the general kernel with one CTA writes the scalars
-        const void* fn = generic_kernel(dtype, sc);
-        return launch(fn, 1, kGenericThreads, 0, 1, st, &a);
+    const int64_t units = c.rows == 0 ? 1 : std::min<int64_t>(c.rows, p.max_units);
+    if (units > max_slots) {
+        g_last_error = "this launch needs " + std::to_string(units) +
+                       " partial-sum slots; the scratch holds " + std::to_string(max_slots);
+        return CE_ERR_UNSUPPORTED;
     }
-    const int64_t units = std::min<int64_t>(rows, p.max_units);
+    if (clear_header) {
+        // the ticket and the status word must start at zero (partial slots
+        // are written before they are read)
+        const cudaError_t e = cudaMemsetAsync(scratch, 0, 2 * sizeof(unsigned), st);
+        if (e != cudaSuccess) return cuda_failure(e, "cudaMemsetAsync(scratch header)");
+    }
+    if (c.rows == 0)  // empty batch: the general kernel with one CTA writes the scalars
+        return launch(generic_kernel(c.dtype, sc), 1, kGenericThreads, 0, 1, st, &a);
     if (p.kind == Kind::Stream) {
         a.ng = p.ng;
         a.sg = p.sg;
@@ -504,9 +512,101 @@ extern "C" ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V, co
     return launch(p.fn, static_cast<int>(units), p.nt, 0, 1, st, &a);
 }
 
+// A forward call with the library's scratch for (current device, stream).
+ce_status fwd_library_scratch(const FwdCall& c, ce_stream_t stream) {
+    ce_status rc = check_fwd(c);
+    if (rc != CE_OK) return rc;
+    if (c.rows == 0 && c.reduction == CE_RED_NONE) return CE_OK;  // nothing to write
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Scratch* scratch = nullptr;
+    rc = scratch_for(dev, st, &scratch);
+    if (rc != CE_OK) return rc;
+    return run_fwd(dev, c, scratch, kMaxPartials, false, st);
+}
+
+}  // namespace
+
+// The forward call with scratch that the caller provides (the static-scratch
+// entry point in ce_noalloc.cu): same checks, plan and launch as ce_fwd, the
+// scratch header cleared first; allocates nothing.
+ce_status fwd_with_scratch(Scratch* scratch, int max_slots, const FwdCall& c, cudaStream_t st) {
+    if (!scratch || max_slots < 1) return CE_ERR_INVALID_ARG;
+    ce_status rc = check_fwd(c);
+    if (rc != CE_OK) return rc;
+    if (c.rows == 0 && c.reduction == CE_RED_NONE) return CE_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    return run_fwd(dev, c, scratch, max_slots, true, st);
+}
+
+// Records a CUDA error for ce_last_error (for the static-scratch entry point).
+ce_status record_cuda_failure(cudaError_t e, const char* what) { return cuda_failure(e, what); }
+
+}  // namespace gbce
+
+extern "C" ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V, const void* target,
+                            const float* weight, int64_t ignore_index, float label_smoothing,
+                            float lse_square_scale, float softcap, int reduction, uint32_t flags,
+                            float* loss, float* z_loss, float* acc, int64_t* pred,
+                            ce_stream_t stream) {
+    const FwdCall c{logits, dtype, rows, V, target, weight, ignore_index, label_smoothing,
+                    lse_square_scale, softcap, reduction, flags, loss, z_loss, acc, pred, nullptr};
+    return fwd_library_scratch(c, stream);
+}
+
+extern "C" ce_status ce_fwd_shard(void* logits, int dtype, int64_t rows, int64_t V,
+                                  const void* target, const float* weight, int64_t ignore_index,
+                                  float label_smoothing, float lse_square_scale, float softcap,
+                                  int reduction, uint32_t flags, float* loss, float* z_loss,
+                                  float* acc, int64_t* pred, const double* batch_counts,
+                                  ce_stream_t stream) {
+    if (!batch_counts) return CE_ERR_INVALID_ARG;
+    const FwdCall c{logits, dtype, rows, V, target, weight, ignore_index, label_smoothing,
+                    lse_square_scale, softcap, reduction, flags, loss, z_loss, acc, pred,
+                    batch_counts};
+    return fwd_library_scratch(c, stream);
+}
+
+extern "C" ce_status ce_count(const void* target, const float* weight, int64_t rows, int64_t V,
+                              int64_t ignore_index, uint32_t flags, double* counts,
+                              ce_stream_t stream) {
+    if (rows < 0 || V <= 0 || !counts) return CE_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(CE_FLAG_TARGET_I64)) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && !target) return CE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    DeviceInfo info;
+    ce_status rc = device_info(dev, &info);
+    if (rc != CE_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Scratch* scratch = nullptr;
+    rc = scratch_for(dev, st, &scratch);
+    if (rc != CE_OK) return rc;
+    CountArgs a = {};
+    a.target = target;
+    a.tgt64 = (flags & CE_FLAG_TARGET_I64) ? 1 : 0;
+    a.weight = weight;
+    a.rows = rows;
+    a.V = V;
+    a.ignore_index = ignore_index;
+    a.counts = counts;
+    a.scratch = scratch;
+    const int64_t want = (rows + kCountThreads * 16 - 1) / (kCountThreads * 16);
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, info.sm_count));
+    return launch(count_kernel(), static_cast<int>(grid), kCountThreads, 0, 1, st, &a);
+}
+
 extern "C" ce_status ce_bwd(const float* grad_output, int grad_per_row, void* dlogits, int dtype,
                             int64_t rows, int64_t V, ce_stream_t stream) {
-    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_INVALID_ARG;
+    if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_INVALID_ARG;
     if (rows < 0 || V <= 0) return CE_ERR_INVALID_ARG;
     if (rows > 0 && (!grad_output || !dlogits)) return CE_ERR_INVALID_ARG;
     if (rows > 0 && V > INT64_MAX / rows / 4) return CE_ERR_INVALID_ARG;
@@ -518,7 +618,7 @@ extern "C" ce_status ce_bwd(const float* grad_output, int grad_per_row, void* dl
     DeviceInfo info;
     ce_status rc = device_info(dev, &info);
     if (rc != CE_OK) return rc;
-    const int64_t bytes = dtype == CE_BF16 ? 2 : 4;
+    const int64_t bytes = dtype == CE_F32 ? 4 : 2;
     BwdArgs b = {};
     b.g = grad_output;
     b.per_row = grad_per_row ? 1 : 0;
@@ -564,102 +664,3 @@ extern "C" const char* ce_status_string(ce_status s) {
 }
 
 extern "C" const char* ce_last_error(void) { return g_last_error.c_str(); }
-
-namespace gbce {
-
-// The forward call with scratch that the caller provides (the static-scratch
-// entry point in ce_noalloc.cu). Same checks, plan and launch as ce_fwd; the
-// launch is refused when its grid would need more partial slots than the
-// scratch holds. Allocates nothing.
-ce_status fwd_with_scratch(Scratch* scratch, int max_slots, void* logits, int dtype, int64_t rows,
-                           int64_t V, const void* target, const float* weight,
-                           int64_t ignore_index, float label_smoothing, float lse_square_scale,
-                           float softcap, int reduction, uint32_t flags, float* loss,
-                           float* z_loss, float* acc, int64_t* pred, cudaStream_t st) {
-    const uint32_t known =
-        CE_FLAG_GRAD | CE_FLAG_Z_LOSS | CE_FLAG_ACC | CE_FLAG_PRED | CE_FLAG_TARGET_I64;
-    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_INVALID_ARG;
-    if (rows < 0 || V <= 0) return CE_ERR_INVALID_ARG;
-    if (V > INT32_MAX - 16) return CE_ERR_UNSUPPORTED;
-    if (reduction != CE_RED_NONE && reduction != CE_RED_SUM && reduction != CE_RED_MEAN)
-        return CE_ERR_INVALID_ARG;
-    if (flags & ~known) return CE_ERR_INVALID_ARG;
-    if (!(label_smoothing >= 0.f && label_smoothing <= 1.f)) return CE_ERR_INVALID_ARG;
-    if (!finite(lse_square_scale)) return CE_ERR_INVALID_ARG;
-    if (!finite(softcap) || softcap < 0.f) return CE_ERR_INVALID_ARG;
-    if (!loss) return CE_ERR_INVALID_ARG;
-    if ((flags & CE_FLAG_Z_LOSS) && !z_loss) return CE_ERR_INVALID_ARG;
-    if ((flags & CE_FLAG_ACC) && !acc) return CE_ERR_INVALID_ARG;
-    if ((flags & CE_FLAG_PRED) && !pred) return CE_ERR_INVALID_ARG;
-    if (rows > 0 && (!logits || !target)) return CE_ERR_INVALID_ARG;
-    if (rows > 0 && V > INT64_MAX / rows / 4) return CE_ERR_INVALID_ARG;
-    if (!scratch || max_slots < 1) return CE_ERR_INVALID_ARG;
-    if (rows == 0 && reduction == CE_RED_NONE) return CE_OK;
-
-    std::lock_guard<std::mutex> lock(g_mu);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
-
-    FwdArgs a = {};
-    a.x = logits;
-    a.rows = rows;
-    a.V = V;
-    a.target = target;
-    a.tgt64 = (flags & CE_FLAG_TARGET_I64) ? 1 : 0;
-    a.weight = weight;
-    a.ignore_index = ignore_index;
-    a.eps = label_smoothing;
-    a.lam = lse_square_scale;
-    const bool sc = softcap > 0.f;
-    a.softcap = sc ? softcap : 0.f;
-    a.sc_k2 = sc ? 2.f * kLog2e / softcap : 0.f;
-    a.sc_slog2e = sc ? softcap * kLog2e : 0.f;
-    a.reduction = reduction;
-    a.grad = (flags & CE_FLAG_GRAD) ? 1 : 0;
-    a.want_z = (flags & CE_FLAG_Z_LOSS) ? 1 : 0;
-    a.want_acc = (flags & CE_FLAG_ACC) ? 1 : 0;
-    a.want_pred = (flags & CE_FLAG_PRED) ? 1 : 0;
-    a.loss = loss;
-    a.zloss = z_loss;
-    a.acc = acc;
-    a.pred = pred;
-    a.timeout_ns = static_cast<uint64_t>(env_int("GBCE_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
-    a.scratch = scratch;
-
-    const bool wsmooth = weight != nullptr && label_smoothing > 0.f;
-    const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16) == 0;
-    Plan p;
-    ce_status rc = make_plan(dev, dtype, V, sc, wsmooth, aligned, &p);
-    if (rc != CE_OK) return rc;
-    const int64_t units = rows == 0 ? 1 : std::min<int64_t>(rows, p.max_units);
-    if (units > max_slots) {
-        g_last_error = "this launch needs " + std::to_string(units) +
-                       " partial-sum slots; the static scratch holds " + std::to_string(max_slots);
-        return CE_ERR_UNSUPPORTED;
-    }
-    // the scratch keeps the previous call's contents: the ticket and the
-    // status word must start at zero (partial slots are written before read)
-    e = cudaMemsetAsync(scratch, 0, 2 * sizeof(unsigned), st);
-    if (e != cudaSuccess) return cuda_failure(e, "cudaMemsetAsync(scratch header)");
-    if (rows == 0) return launch(generic_kernel(dtype, sc), 1, kGenericThreads, 0, 1, st, &a);
-    if (p.kind == Kind::Stream) {
-        a.ng = p.ng;
-        a.sg = p.sg;
-        a.chunk_vec = p.chunk_vec;
-        a.nchunk = p.nchunk;
-        a.resident = p.resident;
-        return launch(p.fn, static_cast<int>(units), p.nt, p.smem, 1, st, &a);
-    }
-    if (p.kind == Kind::Staged) {
-        a.slice_vec = p.slice_vec;
-        a.stages = p.stages;
-        return launch(p.fn, static_cast<int>(units * p.cluster), p.nt, p.smem, p.cluster, st, &a);
-    }
-    return launch(p.fn, static_cast<int>(units), p.nt, 0, 1, st, &a);
-}
-
-// Records a CUDA error for ce_last_error (for the static-scratch entry point).
-ce_status record_cuda_failure(cudaError_t e, const char* what) { return cuda_failure(e, what); }
-
-}  // namespace gbce

@@ -7,6 +7,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace gbce {
@@ -250,6 +251,57 @@ struct Vec<__nv_bfloat16> {
     }
     __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
         reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+    }
+};
+
+template <>
+struct Vec<__half> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[8]) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ __forceinline__ static float vmax(const uint4& v) {
+        const __half2 a = *reinterpret_cast<const __half2*>(&v.x);
+        const __half2 b = *reinterpret_cast<const __half2*>(&v.y);
+        const __half2 c = *reinterpret_cast<const __half2*>(&v.z);
+        const __half2 d = *reinterpret_cast<const __half2*>(&v.w);
+        const __half2 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+        return fmaxf(__low2float(m), __high2float(m));
+    }
+    using MaxAcc = __half2;
+    __device__ __forceinline__ static MaxAcc max_init() {
+        return __halves2half2(__ushort_as_half(0xFC00u), __ushort_as_half(0xFC00u));
+    }
+    __device__ __forceinline__ static MaxAcc max_fold(MaxAcc acc, const uint4& v) {
+        const __half2 a = *reinterpret_cast<const __half2*>(&v.x);
+        const __half2 b = *reinterpret_cast<const __half2*>(&v.y);
+        const __half2 c = *reinterpret_cast<const __half2*>(&v.z);
+        const __half2 d = *reinterpret_cast<const __half2*>(&v.w);
+        return __hmax2(__hmax2(acc, a), __hmax2(__hmax2(b, c), d));
+    }
+    __device__ __forceinline__ static float max_value(MaxAcc acc) {
+        return fmaxf(__low2float(acc), __high2float(acc));
+    }
+    __device__ __forceinline__ static float load1(const void* p, int64_t i) {
+        return __half2float(reinterpret_cast<const __half*>(p)[i]);
+    }
+    __device__ __forceinline__ static void store1(void* p, int64_t i, float v) {
+        reinterpret_cast<__half*>(p)[i] = __float2half_rn(v);
     }
 };
 

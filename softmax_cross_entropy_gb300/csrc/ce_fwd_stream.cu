@@ -17,6 +17,7 @@ const void* stream_kernel(int dtype, bool softcap, int vpt, int nw) {
     if (dtype == 1)
         return softcap ? GBCE_STREAM(__nv_bfloat16, true) : GBCE_STREAM(__nv_bfloat16, false);
 #undef GBCE_STREAM
+    if (dtype == 2) return stream_kernel_f16(softcap, vpt, nw);
     return nullptr;
 }
 

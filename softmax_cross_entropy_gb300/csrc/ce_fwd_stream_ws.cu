@@ -12,6 +12,9 @@ const void* stream_kernel_ws(int dtype, bool softcap) {
     if (dtype == 1)
         return softcap ? (const void*)&ce_fwd_stream<__nv_bfloat16, true, 8, 8, true>
                        : (const void*)&ce_fwd_stream<__nv_bfloat16, false, 8, 8, true>;
+    if (dtype == 2)
+        return softcap ? (const void*)&ce_fwd_stream<__half, true, 8, 8, true>
+                       : (const void*)&ce_fwd_stream<__half, false, 8, 8, true>;
     return nullptr;
 }
 

@@ -205,12 +205,16 @@ const void* generic_kernel(int dtype, bool softcap) {
     if (dtype == 1)
         return softcap ? (const void*)&ce_fwd_generic<__nv_bfloat16, true>
                        : (const void*)&ce_fwd_generic<__nv_bfloat16, false>;
+    if (dtype == 2)
+        return softcap ? (const void*)&ce_fwd_generic<__half, true>
+                       : (const void*)&ce_fwd_generic<__half, false>;
     return nullptr;
 }
 
 const void* bwd_kernel(int dtype) {
     if (dtype == 0) return (const void*)&ce_bwd_scale<float>;
     if (dtype == 1) return (const void*)&ce_bwd_scale<__nv_bfloat16>;
+    if (dtype == 2) return (const void*)&ce_bwd_scale<__half>;
     return nullptr;
 }
 

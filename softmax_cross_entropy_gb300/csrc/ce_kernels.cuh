@@ -62,6 +62,38 @@ struct FwdArgs {
     int resident;   // 1: a row stays in its slots for both passes
     uint64_t timeout_ns;
     Scratch* scratch;
+    // {D, n_valid} of the whole batch when this call is one shard of it
+    // (the mean scale and the accuracy use them instead of this call's own
+    // counts), or nullptr
+    const double* batch_counts;
+};
+
+// Arguments of one forward call as the C ABI receives them (host side).
+struct FwdCall {
+    void* logits;
+    int dtype;
+    int64_t rows, V;
+    const void* target;
+    const float* weight;
+    int64_t ignore_index;
+    float label_smoothing, lse_square_scale, softcap;
+    int reduction;
+    uint32_t flags;
+    float* loss;
+    float* z_loss;
+    float* acc;
+    int64_t* pred;
+    const double* batch_counts;
+};
+
+// Arguments of the shard-count kernel (ce_count).
+struct CountArgs {
+    const void* target;
+    int tgt64;
+    const float* weight;
+    int64_t rows, V, ignore_index;
+    double* counts;  // out: {sum of w[t] over counted rows, counted rows}
+    Scratch* scratch;
 };
 
 __device__ __forceinline__ int64_t load_target(const FwdArgs& a, int64_t r) {
@@ -107,6 +139,11 @@ struct NamedSync {
 template <int NT, typename Sync = CtaSync>
 __device__ __forceinline__ void denominators(const FwdArgs& a, float* sh, float& D, int& n_valid,
                                              Sync sync = Sync()) {
+    if (a.batch_counts) {  // one shard of a batch whose counts are given
+        D = static_cast<float>(a.batch_counts[0]);
+        n_valid = static_cast<int>(a.batch_counts[1]);
+        return;
+    }
     float d = 0.f;
     int n = 0;
 #pragma unroll 8
@@ -300,11 +337,14 @@ const void* staged_kernel_f32_nocap_wsmooth(int cfg);
 const void* staged_kernel_f32_softcap_plain(int cfg);
 const void* staged_kernel_f32_softcap_wsmooth(int cfg);
 const void* stream_kernel(int dtype, bool softcap, int vpt, int nw);
+const void* stream_kernel_f16(bool softcap, int vpt, int nw);
 // class weights with label smoothing: 8 consumer warps, 8 vectors a thread
 const void* stream_kernel_ws(int dtype, bool softcap);
 constexpr int kStreamMaxSlots = 48;   // ring slots (all groups) of the streaming kernel
 constexpr int kStreamMaxGroups = 8;
 const void* generic_kernel(int dtype, bool softcap);
+const void* count_kernel();
+constexpr int kCountThreads = 256;
 const void* bwd_kernel(int dtype);
 
 }  // namespace gbce

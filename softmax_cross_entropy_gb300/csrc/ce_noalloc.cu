@@ -13,11 +13,7 @@
 
 namespace gbce {
 
-ce_status fwd_with_scratch(Scratch* scratch, int max_slots, void* logits, int dtype, int64_t rows,
-                           int64_t V, const void* target, const float* weight,
-                           int64_t ignore_index, float label_smoothing, float lse_square_scale,
-                           float softcap, int reduction, uint32_t flags, float* loss,
-                           float* z_loss, float* acc, int64_t* pred, cudaStream_t st);
+ce_status fwd_with_scratch(Scratch* scratch, int max_slots, const FwdCall& c, cudaStream_t st);
 ce_status record_cuda_failure(cudaError_t e, const char* what);
 
 namespace {
@@ -68,7 +64,7 @@ extern "C" ce_status ce_fwd_noalloc(void* logits, int dtype, int64_t rows, int64
     ce_status rc = static_scratch(dev, &s);
     if (rc != CE_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return fwd_with_scratch(s, kStaticSlots, logits, dtype, rows, V, target, weight,
-                            ignore_index, label_smoothing, lse_square_scale, softcap, reduction,
-                            flags, loss, z_loss, acc, pred, st);
+    const FwdCall c{logits, dtype, rows, V, target, weight, ignore_index, label_smoothing,
+                    lse_square_scale, softcap, reduction, flags, loss, z_loss, acc, pred, nullptr};
+    return fwd_with_scratch(s, kStaticSlots, c, st);
 }

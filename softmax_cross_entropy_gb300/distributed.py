@@ -13,6 +13,12 @@ D = sum of w[t_i] over non-ignored rows:
   gradient by 1/D_local; calling ce_bwd with grad_output = D_local/D_global
   (times the upstream gradient) turns it into the global-mean gradient, so
   no collective is needed before the forward.
+
+Or, with one exchange before the forward (`batch_counts`): every rank
+counts its rows on the device (ce_count), one all-reduce of the two numbers
+gives the batch's D and counted rows, and each rank's forward
+(ce_fwd_shard) then scales its gradient by the batch's 1/D directly; the
+ranks' loss outputs add up to the batch mean.
 """
 from __future__ import annotations
 
@@ -68,3 +74,17 @@ def mean_grad_factor(D_local: float, D_global: float) -> float:
     if D_global == 0 or math.isnan(D_global):
         raise ValueError("global denominator is zero while a shard has counted rows")
     return D_local / D_global
+
+
+def batch_counts(target, V, weight=None, ignore_index=-100, group=None):
+    """(D, counted rows) of the whole row-sharded batch on this rank's
+    device: this rank's counts (ce_count) all-reduced over `group` (the
+    rank's own counts when torch.distributed is not initialised). Pass the
+    result to cross_entropy(..., batch_counts=...)."""
+    import torch.distributed as dist
+
+    from . import shard_counts
+    counts = shard_counts(target, V, weight, ignore_index)
+    if dist.is_available() and dist.is_initialized():
+        dist.all_reduce(counts, group=group)
+    return counts

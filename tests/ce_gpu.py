@@ -20,14 +20,20 @@ import workloads
 # nearest bf16 value itself can lie more than 4e-3 from the exact one
 # (half a unit in the last place is 2^-8 at magnitude 1, 2^-7 at 2), and
 # the one-ulp bound governs.
-LOSS_RTOL = {"f32": 1e-5, "bf16": 1e-4}
-GRAD_ATOL = {"f32": 1e-6, "bf16": 4e-3}
+# fp16 logits (no bound stated for them): the same fp32 arithmetic, so the
+# bf16 loss bound; gradients rounded once to fp16, so within one fp16 unit
+# in the last place (2^-10 relative) plus the smallest subnormal step 2^-24,
+# and 5e-4 absolute below 0.5 (half a unit at 0.5 is 2^-12, plus noise).
+LOSS_RTOL = {"f32": 1e-5, "bf16": 1e-4, "f16": 1e-4}
+GRAD_ATOL = {"f32": 1e-6, "bf16": 4e-3, "f16": 5e-4}
+CE_DTYPE = {"f32": 0, "bf16": 1, "f16": 2}  # ce_dtype of each storage
 
 
 def to_device(case, device="cuda"):
     import torch
-    if case.dtype == "bf16":
-        x = torch.from_numpy(np.ascontiguousarray(case.x).view(np.int16)).view(torch.bfloat16)
+    if case.dtype in ("bf16", "f16"):
+        x = torch.from_numpy(np.ascontiguousarray(case.x).view(np.int16)).view(
+            torch.bfloat16 if case.dtype == "bf16" else torch.float16)
     else:
         x = torch.from_numpy(np.ascontiguousarray(case.x))
     x = x.to(device)
@@ -59,7 +65,7 @@ def run_cuda(case, *, grad=True, want_z=False, want_acc=False, want_pred=False, 
              (_lib.CE_FLAG_ACC if want_acc else 0) | (_lib.CE_FLAG_PRED if want_pred else 0) |
              (_lib.CE_FLAG_TARGET_I64 if dev_t.dtype == torch.int64 else 0))
     st = stream if stream is not None else torch.cuda.current_stream().cuda_stream
-    rc = _lib.ce_fwd(dev_x.data_ptr(), _lib.CE_BF16 if case.dtype == "bf16" else _lib.CE_F32,
+    rc = _lib.ce_fwd(dev_x.data_ptr(), CE_DTYPE[case.dtype],
                      rows, V, dev_t.data_ptr(), None if dev_w is None else dev_w.data_ptr(),
                      case.ignore_index, case.label_smoothing, case.lse_square_scale,
                      case.softcap or 0.0, {"none": 0, "sum": 1, "mean": 2}[red], flags,
@@ -123,7 +129,7 @@ def assert_grad_close(got, want, dtype, what="dlogits"):
     want = np.asarray(want, np.float64)
     assert got.shape == want.shape
     err = np.abs(got - want)
-    small = np.abs(want) < 0.5 if dtype == "bf16" else np.ones(want.shape, bool)
+    small = np.abs(want) < 0.5 if dtype in ("bf16", "f16") else np.ones(want.shape, bool)
     emax = err[small].max(initial=0.0)
     assert emax <= GRAD_ATOL[dtype], f"{what}: max abs err {emax}"
     if dtype == "bf16":
@@ -131,6 +137,9 @@ def assert_grad_close(got, want, dtype, what="dlogits"):
         # edge), plus the fp32 compute noise near zero
         gmax = np.abs(want).max(initial=0.0)
         bound = np.abs(want) * 2.0 ** -7 + 1e-6 * gmax + 1e-30
+    elif dtype == "f16":
+        gmax = np.abs(want).max(initial=0.0)
+        bound = np.abs(want) * 2.0 ** -10 + 1e-6 * gmax + 2.0 ** -24
     else:
         gmax = np.abs(want).max(initial=0.0)
         bound = 1e-5 * np.abs(want) + 1e-6 * gmax + 1e-30

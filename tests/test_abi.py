@@ -94,6 +94,41 @@ def test_bwd_invalid_arguments(lib, over):
     assert _lib.ce_bwd(**a) == _lib.CE_ERR_INVALID_ARG
 
 
+def test_fp16_dtype_is_part_of_the_boundary(lib):
+    from softmax_cross_entropy_gb300 import _lib
+    assert _lib.CE_F16 == 2
+    # an fp16 call with an invalid argument fails on the argument, not on the dtype
+    assert _fwd(lib, dtype=_lib.CE_F16, rows=-1) == _lib.CE_ERR_INVALID_ARG
+    assert _fwd(lib, dtype=3) == _lib.CE_ERR_INVALID_ARG
+
+
+def _shard(lib, **over):
+    from softmax_cross_entropy_gb300 import _lib
+    a = dict(logits=16, dtype=_lib.CE_BF16, rows=4, V=8, target=32, weight=None,
+             ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0, softcap=0.0,
+             reduction=_lib.CE_RED_MEAN, flags=0, loss=48, z_loss=None, acc=None, pred=None,
+             batch_counts=64, stream=None)
+    a.update(over)
+    return _lib.ce_fwd_shard(**a)
+
+
+@pytest.mark.parametrize("over", [dict(batch_counts=None), dict(dtype=9), dict(rows=-1),
+                                  dict(loss=None), dict(flags=64), dict(softcap=-2.0)])
+def test_shard_invalid_arguments(lib, over):
+    from softmax_cross_entropy_gb300 import _lib
+    assert _shard(lib, **over) == _lib.CE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("over", [dict(counts=None), dict(rows=-1), dict(V=0),
+                                  dict(flags=1), dict(flags=32), dict(target=None)])
+def test_count_invalid_arguments(lib, over):
+    from softmax_cross_entropy_gb300 import _lib
+    a = dict(target=16, weight=None, rows=5, V=10, ignore_index=-100, flags=0, counts=32,
+             stream=None)
+    a.update(over)
+    assert _lib.ce_count(**a) == _lib.CE_ERR_INVALID_ARG
+
+
 def test_python_api_rejects_rank_1_and_nd_logits():
     torch = pytest.importorskip("torch")
     import softmax_cross_entropy_gb300 as ce

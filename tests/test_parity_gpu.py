@@ -13,8 +13,8 @@ import numpy as np
 import pytest
 
 import workloads
-from ce_gpu import (assert_grad_close, assert_loss_close, assert_rowloss_close, grad_rows_f64,
-                    oracle_full, oracle_rows, run_cuda, sample_rows, to_device)
+from ce_gpu import (CE_DTYPE, assert_grad_close, assert_loss_close, assert_rowloss_close,
+                    grad_rows_f64, oracle_full, oracle_rows, run_cuda, sample_rows, to_device)
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -75,7 +75,7 @@ def check_sampled(case, *, want_z=False, want_acc=False, want_pred=True, reducti
     ign = np.nonzero(case.target == case.ignore_index)[0]
     if ign.size:
         g = out["x"][torch.as_tensor(ign, device=out["x"].device)]
-        assert bool((g.view(torch.int16 if case.dtype == "bf16" else torch.int32) == 0).all())
+        assert bool((g.view(torch.int32 if case.dtype == "f32" else torch.int16) == 0).all())
     return out, ref
 
 
@@ -93,6 +93,13 @@ def test_vsweep_reduced_rows(V):
 @pytest.mark.parametrize("V", workloads.VSWEEP)
 def test_vsweep_full_size(V):
     check_sampled(workloads.vsweep(V=V), want_acc=True)
+
+
+@pytest.mark.parametrize("V", [32768, 131072])
+def test_f16_full_size(V):
+    # fp16 logits at the bench shape (4096 rows), sampled against the oracle
+    case = workloads.random_case(21, 4096, V, dtype="f16", std=3.0, ignore_frac=0.05)
+    check_sampled(case, want_acc=True)
 
 
 @pytest.mark.parametrize("reduction", ["mean", "sum"])
@@ -163,7 +170,7 @@ OPTION_SETS = [
 
 
 @pytest.mark.parametrize("rows,V", EDGE_SHAPES)
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("opt", range(len(OPTION_SETS)))
 def test_edge_shapes(rows, V, dtype, opt):
     if rows * V > 2_000_000 and opt > 1:
@@ -298,7 +305,8 @@ def test_deterministic():
 
 # ------------------------------------------------------------------ backward
 
-@pytest.mark.parametrize("dtype,V", [("bf16", 4096), ("f32", 1000), ("bf16", 131072)])
+@pytest.mark.parametrize("dtype,V", [("bf16", 4096), ("f32", 1000), ("bf16", 131072),
+                                     ("f16", 4096)])
 def test_backward_scales_stored_gradient(dtype, V):
     import oracle
     from softmax_cross_entropy_gb300 import _lib
@@ -307,7 +315,7 @@ def test_backward_scales_stored_gradient(dtype, V):
     out = run_cuda(case)
     g = out["x"]
     stored = grad_rows_f64(g)
-    dt = _lib.CE_BF16 if dtype == "bf16" else _lib.CE_F32
+    dt = CE_DTYPE[dtype]
     st = torch.cuda.current_stream().cuda_stream
     one = torch.ones(1, device="cuda")
     assert _lib.ce_bwd(one.data_ptr(), 0, g.data_ptr(), dt, rows, V, st) == 0
@@ -321,7 +329,13 @@ def test_backward_scales_stored_gradient(dtype, V):
     half = torch.full((1,), 0.5, device="cuda")
     before = grad_rows_f64(g)
     assert _lib.ce_bwd(half.data_ptr(), 0, g.data_ptr(), dt, rows, V, st) == 0
-    np.testing.assert_array_equal(grad_rows_f64(g), before * 0.5)
+    if dtype == "f16":
+        # halving an fp16 subnormal rounds: numpy's fp16 product rounds the
+        # same way (exact product, one rounding to nearest even)
+        want_half = (before.astype(np.float16) * np.float16(0.5)).astype(np.float64)
+    else:
+        want_half = before * 0.5
+    np.testing.assert_array_equal(grad_rows_f64(g), want_half)
 
 
 def test_autograd_api_matches_c_abi():
@@ -363,8 +377,11 @@ KINDS = {"staged": "1", "stream": "2", "general": "3"}
 @pytest.mark.parametrize("kind", sorted(KINDS) + ["stream8", "stream16"])
 @pytest.mark.parametrize("dtype,V,rows", [("bf16", 4096, 300), ("bf16", 32768, 90),
                                           ("f32", 8192, 77), ("bf16", 131072, 20),
-                                          ("f32", 24, 33)])
+                                          ("f32", 24, 33), ("f16", 8192, 50),
+                                          ("f16", 131072, 9)])
 def test_kernel_kinds(monkeypatch, kind, dtype, V, rows):
+    if dtype == "f16" and kind == "staged":
+        pytest.skip("the staged kernel has no fp16 variant")
     if kind in ("stream8", "stream16"):
         monkeypatch.setenv("GBCE_STREAM_WARPS", kind[6:])
         kind = "stream"
@@ -387,7 +404,8 @@ def test_stream_groups(monkeypatch, groups, warps):
 
 
 @pytest.mark.parametrize("warps", [8, 16])
-@pytest.mark.parametrize("dtype,V", [("bf16", 32768), ("f32", 20000), ("bf16", 8200)])
+@pytest.mark.parametrize("dtype,V", [("bf16", 32768), ("f32", 20000), ("bf16", 8200),
+                                     ("f16", 16384)])
 def test_stream_twice_from_l2(monkeypatch, dtype, V, warps):
     # rows streamed through the ring twice (the large-vocabulary mode), at
     # sizes the oracle checks whole
@@ -407,6 +425,7 @@ def test_stream_twice_from_l2(monkeypatch, dtype, V, warps):
     ("f32", 20000, 33, 1),
     ("bf16", 49152, 13, 0),    # 192 KB of weights: smaller slots
     ("f32", 24, 33, 0),
+    ("f16", 32000, 40, 0),
 ])
 def test_stream_weighted_smoothing(monkeypatch, dtype, V, rows, twice):
     # class weights with label smoothing in the streaming kernel, the weights
