@@ -150,35 +150,61 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ GPU arm
 
+_RED = {"none": 0, "sum": 1, "mean": 2}
+_CE_DTYPE = {"f32": 0, "bf16": 1, "f16": 2}
+
+
 class GpuRunner:
+    """One workload on the device: pinned host copy, pristine device copy, a
+    pool of input buffers, an L2 flush buffer and a stream; ce_fwd and ce_bwd
+    through the C ABI with the workload's options."""
+
     def __init__(self, case, device, torch):
         from softmax_cross_entropy_gb300 import _lib
         self.torch, self.lib, self.case, self.dev = torch, _lib, case, device
-        x16 = np.ascontiguousarray(case.x).view(np.int16)
-        self.host = torch.from_numpy(x16).view(torch.bfloat16).pin_memory()
+        if case.dtype == "f32":
+            host = torch.from_numpy(np.ascontiguousarray(case.x))
+            self.elem = 4
+        else:
+            tdt = torch.bfloat16 if case.dtype == "bf16" else torch.float16
+            host = torch.from_numpy(np.ascontiguousarray(case.x).view(np.int16)).view(tdt)
+            self.elem = 2
+        self.dtype = _CE_DTYPE[case.dtype]
+        self.host = host.pin_memory()
         self.host_t = torch.from_numpy(case.target).pin_memory()
         self.pristine = self.host.to(device)
         self.target = self.host_t.to(device)
-        self.nbytes = self.pristine.numel() * 2
+        self.weight = None if case.weight is None else torch.from_numpy(case.weight).to(device)
+        self.nbytes = self.pristine.numel() * self.elem
         self.pool = max(2, min(16, math.ceil(3 * L2_BYTES / self.nbytes) + 1))
         self.bufs = [torch.empty_like(self.pristine) for _ in range(self.pool)]
-        self.loss = torch.empty(1, dtype=torch.float32, device=device)
+        self.red = _RED[case.reduction]
+        n = case.rows if self.red == 0 else 1
+        self.loss = torch.empty(n, dtype=torch.float32, device=device)
+        self.zl = torch.empty(n, dtype=torch.float32, device=device) if case.return_z_loss \
+            else None
+        self.flags = _lib.CE_FLAG_GRAD | (_lib.CE_FLAG_Z_LOSS if case.return_z_loss else 0)
         self.one = torch.ones(1, dtype=torch.float32, device=device)
         self.half = torch.full((1,), 0.5, dtype=torch.float32, device=device)
         self.flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
         self.stream = torch.cuda.Stream(device)
 
+    def bytes_per_step(self):
+        return algorithmic_bytes(self.case.rows, self.case.V, self.elem)
+
     def fwd(self, x, st):
-        L = self.lib
-        rc = L.ce_fwd(x.data_ptr(), L.CE_BF16, self.case.rows, self.case.V,
-                      self.target.data_ptr(), None, self.case.ignore_index, 0.0, 0.0, 0.0,
-                      L.CE_RED_MEAN, L.CE_FLAG_GRAD, self.loss.data_ptr(), None, None, None, st)
+        L, c = self.lib, self.case
+        rc = L.ce_fwd(x.data_ptr(), self.dtype, c.rows, c.V, self.target.data_ptr(),
+                      None if self.weight is None else self.weight.data_ptr(), c.ignore_index,
+                      c.label_smoothing, c.lse_square_scale, c.softcap or 0.0, self.red,
+                      self.flags, self.loss.data_ptr(),
+                      None if self.zl is None else self.zl.data_ptr(), None, None, st)
         if rc != 0:
             raise RuntimeError(f"ce_fwd: {L.ce_status_string(rc)} {L.ce_last_error()}")
 
     def bwd(self, x, g, st):
         L = self.lib
-        rc = L.ce_bwd(g.data_ptr(), 0, x.data_ptr(), L.CE_BF16, self.case.rows, self.case.V, st)
+        rc = L.ce_bwd(g.data_ptr(), 0, x.data_ptr(), self.dtype, self.case.rows, self.case.V, st)
         if rc != 0:
             raise RuntimeError(f"ce_bwd: {L.ce_status_string(rc)} {L.ce_last_error()}")
 
@@ -247,7 +273,7 @@ class GpuRunner:
             e1.record(self.stream)
         torch.cuda.synchronize(self.dev)
         barrier()
-        h2d = self.host.numel() * 2 + self.host_t.numel() * 4
+        h2d = self.host.numel() * self.elem + self.host_t.numel() * 4
         return e0.elapsed_time(e1) / 1e3, h2d, 4
 
 
@@ -354,6 +380,26 @@ def run_gpu(args):
             torch.cuda.empty_cache()
         line["sweep"] = sweep
 
+    # ---- the other workloads of the profile (forward with gradient +
+    # backward with grad_output = 1, like the headline step)
+    if not args.no_configs:
+        configs = []
+        for name, make in extra_workloads(rank):
+            c = make()
+            r = GpuRunner(c, device, torch)
+            r.warmup(max(W, 3))
+            g1 = r.capture(K, lambda b, st: (r.fwd(b, st), r.bwd(b, r.one, st)))
+            t = max_over_ranks(r.time_graph(g1, barrier))
+            by = r.bytes_per_step()
+            configs.append({"workload": name, "rows": c.rows, "V": c.V, "dtype": c.dtype,
+                            "GB/s": round(by * K / t / 1e9, 1),
+                            "frac": round(by * K / t / 1e9 / peak, 4),
+                            "us_per_step": round(t / K * 1e6, 2),
+                            "rows_per_s": round(c.rows * K / t, 1)})
+            del g1, r, c
+            torch.cuda.empty_cache()
+        line["configs"] = configs
+
     if clocks:
         line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -362,6 +408,26 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def extra_workloads(seed):
+    """(name, case factory) for the profile's other configurations, each
+    timed like the headline step and reported in the line's `configs`."""
+    return [
+        ("softcap 30 + smoothing 0.1 + z-loss 1e-4, 4096 x 131072 bf16 N(0,8^2), mean",
+         lambda: workloads.softcap_z(seed=seed)),
+        ("class weights U[0.5,2] + smoothing 0.05, 16384 x 32000 bf16, mean",
+         lambda: workloads.weighted(reduction="mean", seed=seed)),
+        ("class weights U[0.5,2] + smoothing 0.05, 16384 x 32000 bf16, none",
+         lambda: workloads.weighted(reduction="none", seed=seed)),
+        ("1023 x 128256 fp32 N(0,4^2) + 1% outliers, 15% ignored, mean",
+         lambda: workloads.tt_fp32(seed=seed)),
+        ("4096 x 131072 fp16 N(0,3^2), 5% ignored, mean",
+         lambda: workloads.random_case(seed, 4096, 131072, dtype="f16", std=3.0,
+                                       ignore_frac=0.05)),
+        ("64 x 4096 fp32 N(0,2^2), 10% ignored, mean (launch-bound)",
+         lambda: workloads.small(seed=seed)),
+    ]
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -437,7 +503,12 @@ def run_profile_target(args):
     from softmax_cross_entropy_gb300 import build
     build.build()
     device = torch.device("cuda", 0)
-    case = workloads.vsweep(V=args.V, rows=args.rows)
+    if args.ncu_config >= 0:
+        name, make = extra_workloads(0)[args.ncu_config]
+        case = make()
+    else:
+        name = workload_desc(args.V)
+        case = workloads.vsweep(V=args.V, rows=args.rows)
     r = GpuRunner(case, device, torch)
     st = r.stream.cuda_stream
     with torch.cuda.stream(r.stream):
@@ -447,7 +518,7 @@ def run_profile_target(args):
             r.fwd(b, st)
             r.bwd(b, r.one, st)
     torch.cuda.synchronize(device)
-    print(json.dumps({"profile_target": workload_desc(args.V), "rows": args.rows,
+    print(json.dumps({"profile_target": name, "rows": case.rows, "V": case.V,
                       "steps": args.ncu_steps}))
 
 
@@ -458,6 +529,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the profile's other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ncu", action="store_true",
@@ -465,6 +538,8 @@ def main():
     ap.add_argument("--ncu-steps", type=int, default=3)
     ap.add_argument("--rows", type=int, default=ROWS, help="rows of the --ncu target")
     ap.add_argument("--V", type=int, default=V_MAIN, help="vocabulary of the --ncu target")
+    ap.add_argument("--ncu-config", type=int, default=-1,
+                    help="profile the i-th of the other workloads (see extra_workloads)")
     args = ap.parse_args()
     if args.ncu:
         run_profile_target(args)
