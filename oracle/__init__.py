@@ -20,7 +20,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "ce_oracle.c")
+_SRCS = [os.path.join(_HERE, "ce_oracle.c"), os.path.join(_HERE, "aten_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "libceoracle.so")
 
 _DTYPES = {"f64": 0, "f32": 1, "bf16": 2, "f16": 3}
@@ -36,14 +36,15 @@ class OracleError(RuntimeError):
 
 
 def build(force: bool = False) -> str:
-    """Compiles ce_oracle.c into a shared object next to it (no fast-math:
-    IEEE double semantics are part of the oracle's definition)."""
-    if force or not os.path.exists(_LIB_PATH) or (
-            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+    """Compiles ce_oracle.c and aten_oracle.c into a shared object next to
+    them (no fast-math: IEEE double semantics are part of the oracle's
+    definition)."""
+    if force or not os.path.exists(_LIB_PATH) or any(
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(src) for src in _SRCS):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.run(
             ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off",
-             "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"],
+             "-shared", "-fPIC", *_SRCS, "-o", tmp, "-lm"],
             check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -70,6 +71,14 @@ def _load():
             lib.orc_bf16_to_double.restype = d
             lib.orc_f16_to_double.argtypes = [ctypes.c_uint16]
             lib.orc_f16_to_double.restype = d
+            ci = ctypes.c_int
+            lib.ao_log_softmax.argtypes = [P, i64, i64, P]
+            lib.ao_nll_forward.argtypes = [P, P, P, i64, i64, i64, ci, P, P]
+            lib.ao_nll_backward.argtypes = [P, P, P, i64, i64, i64, ci, d, P]
+            lib.ao_log_softmax_backward.argtypes = [P, P, i64, i64, P]
+            for f in (lib.ao_log_softmax, lib.ao_nll_forward, lib.ao_nll_backward,
+                      lib.ao_log_softmax_backward):
+                f.restype = ci
             _lib = lib
     return _lib
 
@@ -178,3 +187,65 @@ def bf16_to_double(bits: int) -> float:
 
 def f16_to_double(bits: int) -> float:
     return _load().orc_f16_to_double(int(bits) & 0xFFFF)
+
+
+# ---------------------------------------------------------------- unfused (aten) ops
+
+def _f64_2d(a):
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    if a.ndim != 2:
+        raise ValueError("expected a 2-D (rows, C) array")
+    return a
+
+
+def _check_ao(rc, what):
+    if rc == 1:
+        raise OracleError(f"{what}: invalid arguments")
+    if rc == 2:
+        raise OracleError(f"{what}: target index out of range")
+
+
+def log_softmax(x):
+    """_log_softmax over the last dimension, float64."""
+    x = _f64_2d(x)
+    out = np.empty_like(x)
+    _check_ao(_load().ao_log_softmax(_ptr(x), x.shape[0], x.shape[1], _ptr(out)), "log_softmax")
+    return out
+
+
+def nll_forward(logp, target, weight=None, ignore_index=-100, reduction="mean"):
+    """nll_loss_forward: returns (output, total_weight); output has one value
+    per row for "none", else one."""
+    logp = _f64_2d(logp)
+    rows, C = logp.shape
+    target = np.ascontiguousarray(target, dtype=np.int64).reshape(-1)
+    w = None if weight is None else np.ascontiguousarray(weight, dtype=np.float64)
+    out = np.empty(max(rows, 1) if reduction == "none" else 1)
+    tw = np.zeros(1)
+    _check_ao(_load().ao_nll_forward(_ptr(logp), _ptr(target), _ptr(w), rows, C,
+                                     int(ignore_index), REDUCTIONS[reduction], _ptr(out),
+                                     _ptr(tw)), "nll_forward")
+    return (out[:rows] if reduction == "none" else float(out[0])), float(tw[0])
+
+
+def nll_backward(grad_output, target, C, weight=None, ignore_index=-100, reduction="mean",
+                 total_weight=1.0):
+    """nll_loss_backward: the (rows, C) gradient of the nll loss."""
+    target = np.ascontiguousarray(target, dtype=np.int64).reshape(-1)
+    rows = target.shape[0]
+    go = np.ascontiguousarray(np.atleast_1d(grad_output), dtype=np.float64)
+    w = None if weight is None else np.ascontiguousarray(weight, dtype=np.float64)
+    grad = np.empty((rows, C))
+    _check_ao(_load().ao_nll_backward(_ptr(go), _ptr(target), _ptr(w), rows, C,
+                                      int(ignore_index), REDUCTIONS[reduction],
+                                      float(total_weight), _ptr(grad)), "nll_backward")
+    return grad
+
+
+def log_softmax_backward(dy, y):
+    """_log_softmax_backward_data: dy - exp(y) * rowsum(dy)."""
+    dy, y = _f64_2d(dy), _f64_2d(y)
+    dx = np.empty_like(dy)
+    _check_ao(_load().ao_log_softmax_backward(_ptr(dy), _ptr(y), dy.shape[0], dy.shape[1],
+                                              _ptr(dx)), "log_softmax_backward")
+    return dx
