@@ -399,6 +399,12 @@ def run_gpu(args):
             del g1, r, c
             torch.cuda.empty_cache()
         line["configs"] = configs
+        # the decomposed (unfused) form on the decomposed graph's own shape;
+        # the fused step on the same workload is the configs entry above
+        line["unfused"] = {
+            "workload": "1023 x 128256 fp32 N(0,4^2) + 1% outliers, 15% ignored, mean",
+            "ops": measure_unfused(workloads.tt_fp32(seed=rank), device, torch, K, barrier,
+                                   max_over_ranks, peak)}
 
     if clocks:
         line["clocks"] = clocks
@@ -408,6 +414,81 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_unfused(case, device, torch, K, barrier, max_over_ranks, peak):
+    """Times the unfused (aten-shaped) ops on one workload, each in a CUDA
+    graph of K launches over two input buffers larger than L2 (fp32
+    1023 x 128256 is 525 MB), against its own algorithmic bytes:
+    _log_softmax R+W, nll_loss_forward the gathered elements, nll_loss_backward
+    W, _log_softmax_backward_data 2R+W; and the four chained."""
+    from softmax_cross_entropy_gb300 import _lib
+    rows, C = case.rows, case.V
+    b = 4 if case.dtype == "f32" else 2
+    dt = _CE_DTYPE[case.dtype]
+    r = GpuRunner(case, device, torch)
+    xs = [r.pristine.clone() for _ in range(2)]
+    ys = [torch.empty_like(r.pristine) for _ in range(2)]
+    dys = [torch.empty_like(r.pristine) for _ in range(2)]
+    f32 = dict(dtype=torch.float32, device=device)
+    out, tw, one = torch.empty(1, **f32), torch.empty(1, **f32), torch.ones(1, **f32)
+    red = _RED[case.reduction]
+    t = r.target.data_ptr()
+
+    def chk(rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what}: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
+
+    def lsm(k, st):
+        chk(_lib.ce_log_softmax(xs[k % 2].data_ptr(), ys[k % 2].data_ptr(), dt, rows, C, st),
+            "ce_log_softmax")
+
+    def nllf(k, st):
+        chk(_lib.ce_nll_loss_fwd(ys[k % 2].data_ptr(), dt, rows, C, t, None, case.ignore_index,
+                                 red, 0, out.data_ptr(), tw.data_ptr(), st), "ce_nll_loss_fwd")
+
+    def nllb(k, st):
+        chk(_lib.ce_nll_loss_bwd(one.data_ptr(), tw.data_ptr(), dys[k % 2].data_ptr(), dt, rows, C,
+                                 t, None, case.ignore_index, red, 0, st), "ce_nll_loss_bwd")
+
+    def lsmb(k, st):
+        chk(_lib.ce_log_softmax_bwd(dys[k % 2].data_ptr(), ys[k % 2].data_ptr(),
+                                    xs[k % 2].data_ptr(), dt, rows, C, st), "ce_log_softmax_bwd")
+
+    def chain(k, st):
+        lsm(k, st), nllf(k, st), nllb(k, st), lsmb(k, st)
+
+    n = rows * C
+    ops = [("_log_softmax", lsm, 2 * n * b), ("nll_loss_forward", nllf, rows * (b + 4)),
+           ("nll_loss_backward", nllb, n * b + rows * 4),
+           ("_log_softmax_backward_data", lsmb, 3 * n * b),
+           ("chain (all four)", chain, None)]
+    res = []
+    st = r.stream.cuda_stream
+    with torch.cuda.stream(r.stream):
+        for k in range(3):
+            chain(k, st)
+    torch.cuda.synchronize(device)
+    for name, fn, by in ops:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(r.stream):
+            with torch.cuda.graph(g, stream=r.stream):
+                for k in range(K):
+                    fn(k, st)
+        tsec = max_over_ranks(r.time_graph(g, barrier))
+        del g
+        ent = {"op": name, "us_per_launch": round(tsec / K * 1e6, 2)}
+        if by is not None:
+            ent["algorithmic_bytes"] = by
+            ent["GB/s"] = round(by * K / tsec / 1e9, 1)
+            ent["frac"] = round(by * K / tsec / 1e9 / peak, 4)
+        res.append(ent)
+    status = _lib.ce_device_status(st)
+    if status != 0:
+        raise RuntimeError(f"device status after the unfused ops: {_lib.ce_status_string(status)}")
+    del r, xs, ys, dys
+    torch.cuda.empty_cache()
+    return res
 
 
 def extra_workloads(seed):

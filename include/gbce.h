@@ -207,6 +207,54 @@ ce_status ce_fwd_shard(void* logits, int dtype, int64_t rows, int64_t V,
                        ce_stream_t stream);
 
 /*
+ * The unfused form: the four aten ops a decomposed F.cross_entropy graph
+ * runs (tt-mlir pull request #9324, the table of decomposed aten ops on
+ * [1023, 128256] f32 logits, and the #9339 description: max-shifted
+ * log-sum-exp, integer targets with ignore_index, mean/sum/none, zero
+ * gradients for an all-ignored batch). Class weights follow the aten
+ * operators' definitions. All tensors are [rows, C] row-major device
+ * arrays of `dtype` unless stated; fp32 arithmetic; results rounded to
+ * nearest-even into the dtype. CE_ERR_INVALID_ARG / CE_ERR_UNSUPPORTED
+ * mean nothing was enqueued; out-of-range targets are reported through
+ * ce_device_status (CE_ERR_TARGET_RANGE) and those rows are treated as
+ * ignored.
+ */
+
+/* _log_softmax over the last dimension: out[i, j] = x[i, j] - m_i - log S_i,
+ * m_i = max_j x[i, j], S_i = sum_j exp(x[i, j] - m_i). out may equal x. */
+ce_status ce_log_softmax(const void* x, void* out, int dtype, int64_t rows, int64_t C,
+                         ce_stream_t stream);
+
+/* nll_loss_forward: l_i = -w[t_i] * logp[i, t_i] for rows whose target is
+ * not ignore_index (0 otherwise). reduction CE_RED_NONE writes l_i to
+ * out[0 .. rows-1] and 0 to total_weight[0]; CE_RED_SUM writes sum l_i to
+ * out[0]; CE_RED_MEAN writes sum l_i / W (NaN when W is 0), W = sum of
+ * w[t_i] over those rows; both write W to total_weight[0]. out and
+ * total_weight are fp32 device pointers; flags may hold CE_FLAG_TARGET_I64.
+ * Deterministic (fixed-order double sums). */
+ce_status ce_nll_loss_fwd(const void* logp, int dtype, int64_t rows, int64_t C,
+                          const void* target, const float* weight, int64_t ignore_index,
+                          int reduction, uint32_t flags, float* out, float* total_weight,
+                          ce_stream_t stream);
+
+/* nll_loss_backward: writes every element of grad_input: 0, except
+ * grad_input[i, t_i] = -w[t_i] * g_i for rows whose target is not
+ * ignore_index, g_i = grad_output[i] (CE_RED_NONE), grad_output[0]
+ * (CE_RED_SUM) or grad_output[0] / total_weight[0] (CE_RED_MEAN; the
+ * forward's total_weight). grad_output and total_weight are fp32 device
+ * pointers (total_weight is read for CE_RED_MEAN only). */
+ce_status ce_nll_loss_bwd(const float* grad_output, const float* total_weight,
+                          void* grad_input, int dtype, int64_t rows, int64_t C,
+                          const void* target, const float* weight, int64_t ignore_index,
+                          int reduction, uint32_t flags, ce_stream_t stream);
+
+/* _log_softmax_backward_data: grad_input[i, j] = grad_output[i, j]
+ * - exp(output[i, j]) * sum_k grad_output[i, k], with output the
+ * log-softmax. grad_input may equal grad_output. */
+ce_status ce_log_softmax_bwd(const void* grad_output, const void* output, void* grad_input,
+                             int dtype, int64_t rows, int64_t C, ce_stream_t stream);
+
+/*
  * ce_bwd - backward (§Backward Pass: the stored gradient times
  * grad_output): dlogits *= grad_output, in place.
  *

@@ -28,6 +28,10 @@ SIGNATURES = {
                           _P, _P]),
     "ce_count": (_I, [_P, _P, _I64, _I64, _I64, _U32, _P, _P]),
     "ce_bwd": (_I, [_P, _I, _P, _I, _I64, _I64, _P]),
+    "ce_log_softmax": (_I, [_P, _P, _I, _I64, _I64, _P]),
+    "ce_nll_loss_fwd": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _I, _U32, _P, _P, _P]),
+    "ce_nll_loss_bwd": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _I64, _I, _U32, _P]),
+    "ce_log_softmax_bwd": (_I, [_P, _P, _P, _I, _I64, _I64, _P]),
     "ce_device_status": (_I, [_P]),
     "ce_status_string": (ctypes.c_char_p, [_I]),
     "ce_last_error": (ctypes.c_char_p, []),
@@ -92,6 +96,26 @@ def ce_count(target, weight, rows, V, ignore_index, flags, counts, stream):
 
 def ce_bwd(grad_output, grad_per_row, dlogits, dtype, rows, V, stream):
     return load().ce_bwd(grad_output, grad_per_row, dlogits, dtype, rows, V, stream)
+
+
+def ce_log_softmax(x, out, dtype, rows, C, stream):
+    return load().ce_log_softmax(x, out, dtype, rows, C, stream)
+
+
+def ce_nll_loss_fwd(logp, dtype, rows, C, target, weight, ignore_index, reduction, flags, out,
+                    total_weight, stream):
+    return load().ce_nll_loss_fwd(logp, dtype, rows, C, target, weight, ignore_index,
+                                  reduction, flags, out, total_weight, stream)
+
+
+def ce_nll_loss_bwd(grad_output, total_weight, grad_input, dtype, rows, C, target, weight,
+                    ignore_index, reduction, flags, stream):
+    return load().ce_nll_loss_bwd(grad_output, total_weight, grad_input, dtype, rows, C, target,
+                                  weight, ignore_index, reduction, flags, stream)
+
+
+def ce_log_softmax_bwd(grad_output, output, grad_input, dtype, rows, C, stream):
+    return load().ce_log_softmax_bwd(grad_output, output, grad_input, dtype, rows, C, stream)
 
 
 def ce_device_status(stream):

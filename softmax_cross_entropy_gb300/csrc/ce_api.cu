@@ -212,7 +212,7 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, int cfg
 // weights in shared memory after the ring, which must leave room for at
 // least two slots.
 bool try_stream(int dtype, int64_t V, bool softcap, bool ws, const DeviceInfo& dev, Plan* out,
-                ce_status* err) {
+                ce_status* err, bool lsm = false) {
     const int64_t bytes = dtype == CE_F32 ? 4 : 2;
     const int64_t vec_row = V * bytes / 16;
     const int force_ng = env_int("GBCE_STREAM_GROUPS", 0);
@@ -224,14 +224,17 @@ bool try_stream(int dtype, int64_t V, bool softcap, bool ws, const DeviceInfo& d
     // (8 or 16) overrides.
     const int nw_env = env_int("GBCE_STREAM_WARPS", 0);
     const int nw_auto = (!softcap && V * bytes <= 8192) ? 8 : 16;
-    const int nw = ws ? 8 : (nw_env == 8 || nw_env == 16 ? nw_env : nw_auto);
+    // (the log-softmax mode exists with 16 consumer warps only)
+    const int nw = lsm ? 16 : ws ? 8 : (nw_env == 8 || nw_env == 16 ? nw_env : nw_auto);
     const int vpt_res = nw == 8 ? 8 : 4;  // the two compiled shapes
     const size_t wbytes = ws ? static_cast<size_t>((V * 4 + 15) / 16 * 16) : 0;
     Plan p;
     const void* fn = nullptr;
     size_t ring_max = 0;
     auto prepare = [&](int vpt) -> bool {
-        fn = ws ? stream_kernel_ws(dtype, softcap) : stream_kernel(dtype, softcap, vpt, nw);
+        fn = lsm  ? stream_kernel_lsm(dtype)
+             : ws ? stream_kernel_ws(dtype, softcap)
+                  : stream_kernel(dtype, softcap, vpt, nw);
         if (!fn) return false;
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, fn);
@@ -602,6 +605,189 @@ extern "C" ce_status ce_count(const void* target, const float* weight, int64_t r
     const int64_t want = (rows + kCountThreads * 16 - 1) / (kCountThreads * 16);
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, info.sm_count));
     return launch(count_kernel(), static_cast<int>(grid), kCountThreads, 0, 1, st, &a);
+}
+
+// ---------------------------------------------------------------- unfused (aten-shaped) ops
+
+namespace gbce {
+namespace {
+
+bool dtype_ok(int dtype) { return dtype == CE_F32 || dtype == CE_BF16 || dtype == CE_F16; }
+int64_t dtype_bytes(int dtype) { return dtype == CE_F32 ? 4 : 2; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by the unfused entry points.
+ce_status check_rows_c(int dtype, int64_t rows, int64_t C) {
+    if (!dtype_ok(dtype) || rows < 0 || C <= 0) return CE_ERR_INVALID_ARG;
+    if (C > INT32_MAX - 16) return CE_ERR_UNSUPPORTED;
+    if (rows > 0 && C > INT64_MAX / rows / 4) return CE_ERR_INVALID_ARG;
+    return CE_OK;
+}
+
+// The current device, its properties and the (device, stream) scratch.
+// Called with g_mu held.
+ce_status device_and_scratch(cudaStream_t st, int* dev, DeviceInfo* info, Scratch** scratch) {
+    const cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    ce_status rc = device_info(*dev, info);
+    if (rc != CE_OK) return rc;
+    return scratch_for(*dev, st, scratch);
+}
+
+std::map<std::tuple<int, int, int64_t>, Plan> g_lsm_plans;
+
+}  // namespace
+}  // namespace gbce
+
+extern "C" ce_status ce_log_softmax(const void* x, void* out, int dtype, int64_t rows, int64_t C,
+                                    ce_stream_t stream) {
+    ce_status rc = check_rows_c(dtype, rows, C);
+    if (rc != CE_OK) return rc;
+    if (rows > 0 && (!x || !out)) return CE_ERR_INVALID_ARG;
+    if (rows == 0) return CE_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    DeviceInfo info;
+    Scratch* scratch = nullptr;
+    rc = device_and_scratch(st, &dev, &info, &scratch);
+    if (rc != CE_OK) return rc;
+    if (aligned16(x) && aligned16(out) && (C * dtype_bytes(dtype)) % 16 == 0) {
+        const auto key = std::make_tuple(dev, dtype, C);
+        auto it = g_lsm_plans.find(key);
+        if (it == g_lsm_plans.end()) {
+            Plan p;
+            rc = CE_OK;
+            if (!try_stream(dtype, C, false, false, info, &p, &rc, true)) {
+                if (rc != CE_OK) return rc;
+                p = Plan();  // no streaming plan: the general kernel below
+            }
+            it = g_lsm_plans.emplace(key, p).first;
+        }
+        const Plan& p = it->second;
+        if (p.kind == Kind::Stream) {
+            FwdArgs a = {};
+            a.x = const_cast<void*>(x);
+            a.out = out;
+            a.rows = rows;
+            a.V = C;
+            a.ignore_index = INT64_MIN;
+            a.reduction = CE_RED_NONE;
+            a.timeout_ns =
+                static_cast<uint64_t>(env_int("GBCE_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
+            a.scratch = scratch;
+            a.ng = p.ng;
+            a.sg = p.sg;
+            a.chunk_vec = p.chunk_vec;
+            a.nchunk = p.nchunk;
+            a.resident = p.resident;
+            const int64_t units = std::min<int64_t>(rows, p.max_units);
+            return launch(p.fn, static_cast<int>(units), p.nt, p.smem, 1, st, &a);
+        }
+    }
+    LsmArgs la = {x, out, rows, C};
+    const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(info.sm_count) * 4);
+    return launch(lsm_generic_kernel(dtype), static_cast<int>(grid), kLsmGenericThreads, 0, 1, st,
+                  &la);
+}
+
+extern "C" ce_status ce_nll_loss_fwd(const void* logp, int dtype, int64_t rows, int64_t C,
+                                     const void* target, const float* weight,
+                                     int64_t ignore_index, int reduction, uint32_t flags,
+                                     float* out, float* total_weight, ce_stream_t stream) {
+    ce_status rc = check_rows_c(dtype, rows, C);
+    if (rc != CE_OK) return rc;
+    if (reduction != CE_RED_NONE && reduction != CE_RED_SUM && reduction != CE_RED_MEAN)
+        return CE_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(CE_FLAG_TARGET_I64)) return CE_ERR_INVALID_ARG;
+    if (!out || !total_weight) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && (!logp || !target)) return CE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    DeviceInfo info;
+    Scratch* scratch = nullptr;
+    rc = device_and_scratch(st, &dev, &info, &scratch);
+    if (rc != CE_OK) return rc;
+    NllFwdArgs a = {};
+    a.logp = logp;
+    a.target = target;
+    a.tgt64 = (flags & CE_FLAG_TARGET_I64) ? 1 : 0;
+    a.weight = weight;
+    a.rows = rows;
+    a.C = C;
+    a.ignore_index = ignore_index;
+    a.reduction = reduction;
+    a.out = out;
+    a.total_weight = total_weight;
+    a.scratch = scratch;
+    const int64_t want = (rows + kNllThreads - 1) / kNllThreads;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, info.sm_count));
+    return launch(nll_fwd_kernel(dtype), static_cast<int>(grid), kNllThreads, 0, 1, st, &a);
+}
+
+extern "C" ce_status ce_nll_loss_bwd(const float* grad_output, const float* total_weight,
+                                     void* grad_input, int dtype, int64_t rows, int64_t C,
+                                     const void* target, const float* weight,
+                                     int64_t ignore_index, int reduction, uint32_t flags,
+                                     ce_stream_t stream) {
+    ce_status rc = check_rows_c(dtype, rows, C);
+    if (rc != CE_OK) return rc;
+    if (reduction != CE_RED_NONE && reduction != CE_RED_SUM && reduction != CE_RED_MEAN)
+        return CE_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(CE_FLAG_TARGET_I64)) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && (!grad_output || !grad_input || !target)) return CE_ERR_INVALID_ARG;
+    if (rows > 0 && reduction == CE_RED_MEAN && !total_weight) return CE_ERR_INVALID_ARG;
+    if (rows == 0) return CE_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    DeviceInfo info;
+    Scratch* scratch = nullptr;
+    rc = device_and_scratch(st, &dev, &info, &scratch);
+    if (rc != CE_OK) return rc;
+    NllBwdArgs a = {};
+    a.grad_output = grad_output;
+    a.total_weight = total_weight;
+    a.grad_input = grad_input;
+    a.target = target;
+    a.tgt64 = (flags & CE_FLAG_TARGET_I64) ? 1 : 0;
+    a.weight = weight;
+    a.rows = rows;
+    a.C = C;
+    a.ignore_index = ignore_index;
+    a.reduction = reduction;
+    a.vec_ok = (aligned16(grad_input) && (C * dtype_bytes(dtype)) % 16 == 0) ? 1 : 0;
+    a.scratch = scratch;
+    const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(info.sm_count) * 8);
+    return launch(nll_bwd_kernel(dtype), static_cast<int>(grid), kNllThreads, 0, 1, st, &a);
+}
+
+extern "C" ce_status ce_log_softmax_bwd(const void* grad_output, const void* output,
+                                        void* grad_input, int dtype, int64_t rows, int64_t C,
+                                        ce_stream_t stream) {
+    ce_status rc = check_rows_c(dtype, rows, C);
+    if (rc != CE_OK) return rc;
+    if (rows > 0 && (!grad_output || !output || !grad_input)) return CE_ERR_INVALID_ARG;
+    if (rows == 0) return CE_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    DeviceInfo info;
+    rc = device_info(dev, &info);
+    if (rc != CE_OK) return rc;
+    LsmBwdArgs a = {};
+    a.dy = grad_output;
+    a.y = output;
+    a.dx = grad_input;
+    a.rows = rows;
+    a.C = C;
+    a.vec_ok = (aligned16(grad_output) && aligned16(output) && aligned16(grad_input) &&
+                (C * dtype_bytes(dtype)) % 16 == 0) ? 1 : 0;
+    const int64_t grid = std::min<int64_t>(rows, info.sm_count);
+    return launch(lsm_bwd_kernel(dtype), static_cast<int>(grid), kLsmBwdThreads, 0, 1, st, &a);
 }
 
 extern "C" ce_status ce_bwd(const float* grad_output, int grad_per_row, void* dlogits, int dtype,

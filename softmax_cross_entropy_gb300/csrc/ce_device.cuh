@@ -105,6 +105,15 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     return pol;
 }
 
+// 16-byte global load with an L2 eviction-policy hint.
+__device__ __forceinline__ uint4 ld_v4_hint(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 // Global -> shared bulk copy that signals `bar` with the bytes it delivers.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,

@@ -258,6 +258,34 @@ __device__ __forceinline__ void grad_chunk(const uint4* ch, uint4* outv, int tg,
     }
 }
 
+// Log-softmax mode, pass 2 for the thread's VPT vectors of one slot:
+// out = (z - M) - log S, packed and stored.
+template <typename T, int VPT, bool FULL>
+__device__ __forceinline__ void lsm_chunk(const uint4* ch, uint4* outv, int tg, int nv, int GT,
+                                          float M, float logS) {
+    using VT = Vec<T>;
+    constexpr int VE = VT::N;
+    uint4 q[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+        if (FULL || tg + k * GT < nv) q[k] = ch[tg + k * GT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        if (FULL || tg + k * GT < nv) {
+            float f[VE];
+            VT::unpack(q[k], f);
+#pragma unroll
+            for (int j = 0; j < VE; j += 2) {
+                const float2 d = fadd2(fadd2(make_float2(f[j], f[j + 1]), make_float2(-M, -M)),
+                                       make_float2(-logS, -logS));
+                f[j] = d.x;
+                f[j + 1] = d.y;
+            }
+            outv[k * GT] = VT::pack(f);
+        }
+    }
+}
+
 // Ring position of a group: slot within the group's slots and the phase bit
 // of its current use, advanced without division.
 struct RingPos {
@@ -280,7 +308,11 @@ struct RingPos {
 // WS: class weights with label smoothing. The weights then sit in shared
 // memory after the ring (V floats, laid out for weights_of), loaded once per
 // CTA, and each CTA forms their total W in the same fixed order.
-template <typename T, bool SOFTCAP, int VPT, int NW, bool WS>
+//
+// LSM: the log-softmax of every row (the unfused _log_softmax), written to
+// a.out: no targets are read, no loss is formed, and pass 2 stores
+// (x - M) - log S instead of the gradient.
+template <typename T, bool SOFTCAP, int VPT, int NW, bool WS, bool LSM = false>
 __global__ void __launch_bounds__(32 * (NW + 1), 1)
 ce_fwd_stream(const __grid_constant__ FwdArgs a) {
     using VT = Vec<T>;
@@ -343,7 +375,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
         int g = 0;
         for (int64_t rb = cid; rb < a.rows && !failed; rb += 32 * ncta) {
             const int64_t rl = rb + lane * ncta;
-            const bool lane_counts = rl < a.rows && row_counts(a, load_target(a, rl));
+            const bool lane_counts = rl < a.rows && (LSM || row_counts(a, load_target(a, rl)));
             const uint32_t counted = __ballot_sync(0xffffffffu, lane_counts);
             if (lane == 0) {
                 for (int j = 0; j < 32 && !failed; ++j) {
@@ -472,14 +504,14 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
         // the next row's target is read one row ahead
         const int64_t rstep = static_cast<int64_t>(ng) * ncta;
         const int64_t r_first = cid + static_cast<int64_t>(g) * ncta;
-        int64_t t_next = r_first < a.rows ? load_target(a, r_first) : 0;
+        int64_t t_next = (!LSM && r_first < a.rows) ? load_target(a, r_first) : 0;
         for (int64_t r = r_first; r < a.rows; r += rstep) {
             const int64_t t = t_next;
-            if (r + rstep < a.rows) t_next = load_target(a, r + rstep);
-            const bool counts = row_counts(a, t);
+            if (!LSM && r + rstep < a.rows) t_next = load_target(a, r + rstep);
+            const bool counts = LSM || row_counts(a, t);
             T* xrow = reinterpret_cast<T*>(a.x) + r * a.V;
             uint4* rowv = reinterpret_cast<uint4*>(xrow);
-            if (gleader && t != a.ignore_index && !counts)
+            if (!LSM && gleader && t != a.ignore_index && !counts)
                 atomicOr(&a.scratch->status, kDevErrTarget);
             if (!counts) {
                 // Ignored row: exact +0 gradient, zero per-row outputs, pred -1.
@@ -496,10 +528,10 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                 continue;
             }
             const int tvec = static_cast<int>(t / VE);
-            const bool t_owner = tg == owner_of(tvec);
+            const bool t_owner = !LSM && tg == owner_of(tvec);
             float xt = 0.f;
-            if (gleader || t_owner) xt = VT::load1(xrow, t);  // before any store to this row
-            const float wt = a.weight ? __ldg(a.weight + t) : 1.f;
+            if (!LSM && (gleader || t_owner)) xt = VT::load1(xrow, t);  // before any store to this row
+            const float wt = (!LSM && a.weight) ? __ldg(a.weight + t) : 1.f;
 
             // ---- pass 1: thread statistics over the row's slots
             PassOne<T, SOFTCAP, VPT, WS> st;
@@ -550,7 +582,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
             const float M = tot.M;
             const float logS = logf(tot.S);
 
-            if (gleader) {
+            if (!LSM && gleader) {
                 const float zt = SOFTCAP ? a.softcap * tanh_from_scaled(xt * a.sc_k2) : xt;
                 float zl;
                 const float l = row_loss(a, M, logS, zt, wt, Wtot,
@@ -588,7 +620,16 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                 }
                 const uint4* ch = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * chunk_bytes);
                 const int nv = min(chunk_vec, vrow - v0);
-                if (a.grad && !failed) {
+                if (LSM) {
+                    uint4* ov = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.out) + r * a.V) +
+                                v0 + tg;
+                    if (!failed) {
+                        if (nv == VPT * GT)
+                            lsm_chunk<T, VPT, true>(ch, ov, tg, nv, GT, M, logS);
+                        else
+                            lsm_chunk<T, VPT, false>(ch, ov, tg, nv, GT, M, logS);
+                    }
+                } else if (a.grad && !failed) {
                     if (nv == VPT * GT)
                         grad_chunk<T, SOFTCAP, VPT, true, WS>(ch, rowv + v0 + tg, tg, nv, GT, M,
                                                               ML, As, Bc, a, w4, vrow_w, v0 + tg);

@@ -62,6 +62,7 @@ struct FwdArgs {
     int resident;   // 1: a row stays in its slots for both passes
     uint64_t timeout_ns;
     Scratch* scratch;
+    void* out;  // log-softmax mode: [rows, V] output (may equal x)
     // {D, n_valid} of the whole batch when this call is one shard of it
     // (the mean scale and the accuracy use them instead of this call's own
     // counts), or nullptr
@@ -84,6 +85,46 @@ struct FwdCall {
     float* acc;
     int64_t* pred;
     const double* batch_counts;
+};
+
+// Arguments of the unfused (aten-shaped) kernels.
+struct NllFwdArgs {  // nll_loss_forward
+    const void* logp;  // [rows, C]
+    const void* target;
+    int tgt64;
+    const float* weight;  // [C] or nullptr
+    int64_t rows, C, ignore_index;
+    int reduction;
+    float* out;           // [rows] ("none") or [1]
+    float* total_weight;  // [1]
+    Scratch* scratch;
+};
+
+struct NllBwdArgs {  // nll_loss_backward
+    const float* grad_output;  // [rows] ("none") or [1]
+    const float* total_weight;  // [1], read for "mean"
+    void* grad_input;           // [rows, C], written
+    const void* target;
+    int tgt64;
+    const float* weight;
+    int64_t rows, C, ignore_index;
+    int reduction;
+    int vec_ok;  // 16-byte rows
+    Scratch* scratch;
+};
+
+struct LsmBwdArgs {  // _log_softmax_backward_data
+    const void* dy;  // [rows, C] incoming gradient
+    const void* y;   // [rows, C] log-softmax output
+    void* dx;        // [rows, C] (may equal dy)
+    int64_t rows, C;
+    int vec_ok;
+};
+
+struct LsmArgs {  // _log_softmax, general kernel (any alignment)
+    const void* x;
+    void* out;
+    int64_t rows, C;
 };
 
 // Arguments of the shard-count kernel (ce_count).
@@ -299,6 +340,38 @@ __device__ __forceinline__ void finish_scalars(const FwdArgs& a, int64_t slot, i
     s->ticket = 0u;
 }
 
+// Adds two doubles over the CTAs of a grid in a fixed order (as
+// finish_scalars does): called by the 32 lanes of one warp of every CTA,
+// lane 0 holding its CTA's (u, v). Returns true in lane 0 of the last CTA
+// to arrive, with the grid's totals in u and v, and resets the ticket.
+__device__ __forceinline__ bool grid_sum2(Scratch* s, double& u, double& v) {
+    const int lane = threadIdx.x & 31;
+    int last = 0;
+    if (lane == 0) {
+        s->partials[blockIdx.x].loss = u;
+        s->partials[blockIdx.x].zloss = v;
+        __threadfence();
+        last = atomicAdd(&s->ticket, 1u) == gridDim.x - 1;
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return false;
+    __threadfence();
+    double U = 0.0, W = 0.0;
+    for (unsigned c = lane; c < gridDim.x; c += 32) {
+        U += __ldcg(&s->partials[c].loss);
+        W += __ldcg(&s->partials[c].zloss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        U += __shfl_xor_sync(0xffffffffu, U, o);
+        W += __shfl_xor_sync(0xffffffffu, W, o);
+    }
+    if (lane != 0) return false;
+    u = U;
+    v = W;
+    s->ticket = 0u;
+    return true;
+}
+
 // ---------------------------------------------------------------- variants
 
 // Staged-kernel shapes: threads per CTA and 16-byte vectors each thread
@@ -344,6 +417,15 @@ constexpr int kStreamMaxSlots = 48;   // ring slots (all groups) of the streamin
 constexpr int kStreamMaxGroups = 8;
 const void* generic_kernel(int dtype, bool softcap);
 const void* count_kernel();
+// unfused kernels (dtype 0 fp32, 1 bf16, 2 fp16)
+const void* stream_kernel_lsm(int dtype);
+const void* lsm_generic_kernel(int dtype);
+const void* nll_fwd_kernel(int dtype);
+const void* nll_bwd_kernel(int dtype);
+const void* lsm_bwd_kernel(int dtype);
+constexpr int kLsmGenericThreads = 512;
+constexpr int kNllThreads = 256;
+constexpr int kLsmBwdThreads = 1024;
 constexpr int kCountThreads = 256;
 const void* bwd_kernel(int dtype);
 
