@@ -140,6 +140,31 @@ def forward(x, target, *, dtype="f64", weight=None, ignore_index=-100,
     return {"loss": loss, "z_loss": zl, "acc": acc, "pred": pred, "grad": grad}
 
 
+def forward_nd(x, target, *, dtype="f64", **opts):
+    """Forward for N-D logits with the class dimension at axis 1, (N, C, d1,
+    ..., dk), and targets (N, d1, ..., dk): the cross-entropy of every
+    position's C logits, reduced over all positions. By definition this is
+    the 2-D computation on the logits with the class axis moved last and
+    the positions flattened into rows; the per-position outputs and the
+    gradient are reshaped back. Same keyword options as forward()."""
+    x = np.asarray(x)
+    if x.ndim < 2:
+        raise OracleError("N-D logits need at least (N, C)")
+    C = x.shape[1]
+    rows2d = np.ascontiguousarray(np.moveaxis(x, 1, -1)).reshape(-1, C)
+    t = np.asarray(target).reshape(-1)
+    r = forward(rows2d, t, dtype=dtype, **opts)
+    pos_shape = (x.shape[0],) + x.shape[2:]
+    out = dict(r)
+    if opts.get("reduction", "mean") == "none":
+        for k in ("loss", "z_loss", "acc"):
+            out[k] = r[k].reshape(pos_shape)
+    out["pred"] = r["pred"].reshape(pos_shape)
+    if r["grad"] is not None:
+        out["grad"] = np.moveaxis(r["grad"].reshape(pos_shape + (C,)), -1, 1)
+    return out
+
+
 def rows(x, target, row_idx, *, dtype="f64", weight=None, ignore_index=-100,
          label_smoothing=0.0, lse_square_scale=0.0, softcap=None,
          reduction="mean", want_grad=True):
