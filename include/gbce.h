@@ -207,6 +207,44 @@ ce_status ce_fwd_shard(void* logits, int dtype, int64_t rows, int64_t V,
                        ce_stream_t stream);
 
 /*
+ * ce_fwd_nd - ce_fwd for N-D logits with the class dimension at axis 1,
+ * [N, C, d1, ..., dk] (F.cross_entropy's N-D form; tt-mlir pull request
+ * #9324, review comments: the reductions run over every non-class
+ * dimension). Each position (n, d1..dk) is one row of the ce_fwd
+ * definition with V = C, so loss, z_loss, accuracy, predicted tokens and
+ * the in-place gradient are those of ce_fwd applied to the logits with the
+ * class axis moved last.
+ *
+ * logits       [N, C, inner] row-major, inner = d1 * ... * dk (inner >= 0;
+ *              inner == 1 is exactly ce_fwd with rows = N). Overwritten by
+ *              dlogits (same layout) with CE_FLAG_GRAD.
+ * target       [N, inner] (int32, or int64 with CE_FLAG_TARGET_I64).
+ * loss, z_loss, acc   [N, inner] fp32 for CE_RED_NONE, else [1].
+ * pred         [N, inner] int64.
+ * Other arguments, results and errors as for ce_fwd. N * inner must stay
+ * below 2^31 (CE_ERR_UNSUPPORTED otherwise). For "sum" and "mean" the call
+ * enqueues a count kernel before the forward (D and the counted positions
+ * land in the library scratch of (device, stream)). Vectorised loads need
+ * a 16-byte aligned base and inner a multiple of 16 / sizeof(dtype); other
+ * shapes take single-element loads with the same results.
+ */
+ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, int64_t inner,
+                    const void* target, const float* weight, int64_t ignore_index,
+                    float label_smoothing, float lse_square_scale, float softcap,
+                    int reduction, uint32_t flags, float* loss, float* z_loss,
+                    float* acc, int64_t* pred, ce_stream_t stream);
+
+/*
+ * ce_bwd_nd - backward of ce_fwd_nd ("Kernel Profile: CrossEntropy",
+ * §Backward Pass): dlogits *= grad_output in place, where grad_output is one
+ * fp32 value (grad_per_position == 0) or [N, inner] fp32 values, one per
+ * position, multiplying all C classes of that position (reduction "none").
+ * A scalar factor of exactly 1.0 leaves dlogits untouched.
+ */
+ce_status ce_bwd_nd(const float* grad_output, int grad_per_position, void* dlogits,
+                    int dtype, int64_t N, int64_t C, int64_t inner, ce_stream_t stream);
+
+/*
  * The unfused form: the four aten ops a decomposed F.cross_entropy graph
  * runs (tt-mlir pull request #9324, the table of decomposed aten ops on
  * [1023, 128256] f32 logits, and the #9339 description: max-shifted

@@ -8,8 +8,10 @@
 
 The arguments and outputs are those of the Liger-Kernel cross-entropy kernel
 profile (§Forward Pass, §Module Parameters). ``logits`` is a 2-D (B*T, V)
-CUDA tensor in float32, bfloat16 or float16; ``target`` holds int32 or int64
-labels.
+CUDA tensor in float32, bfloat16 or float16, or an N-D (N, C, d1, ..., dk)
+tensor with the class dimension at axis 1 (F.cross_entropy's N-D form; the
+reductions then run over every non-class dimension); ``target`` holds int32
+or int64 labels, shaped (B*T,) or (N, d1, ..., dk).
 When ``logits.requires_grad`` the forward writes the gradient of the reduced
 loss over ``logits`` itself (§Backward Pass: the gradient-in-forward trick),
 so the logits' values are gone after the call and backward only scales that
@@ -18,17 +20,19 @@ buffer by grad_output. Every step runs in the CUDA kernels of libgbce.so
 """
 from __future__ import annotations
 
+import math
 from collections import namedtuple
 
 import torch
 
 from . import _lib
-from ._lib import (CEError, ce_bwd, ce_count, ce_device_status, ce_fwd, ce_fwd_shard,
-                   ce_last_error, ce_status_string)
+from ._lib import (CEError, ce_bwd, ce_bwd_nd, ce_count, ce_device_status, ce_fwd,
+                   ce_fwd_nd, ce_fwd_shard, ce_last_error, ce_status_string)
 
 __all__ = ["cross_entropy", "CrossEntropyLoss", "CrossEntropyFunction", "CrossEntropyOutput",
            "CEError", "device_status", "shard_counts", "ce_fwd", "ce_fwd_shard", "ce_count",
-           "ce_bwd", "ce_device_status", "ce_status_string", "ce_last_error"]
+           "ce_bwd", "ce_fwd_nd", "ce_bwd_nd", "ce_device_status", "ce_status_string",
+           "ce_last_error"]
 
 CrossEntropyOutput = namedtuple("CrossEntropyOutput",
                                 ["loss", "z_loss", "token_accuracy", "predicted_tokens"])
@@ -47,16 +51,17 @@ def _stream(device):
 
 
 def _check_inputs(logits, target, weight):
-    if not isinstance(logits, torch.Tensor) or logits.dim() != 2:
-        raise ValueError("logits must be a 2-D (B*T, V) tensor; flatten the batch dimensions "
-                         "first (class dimension last)")
+    if not isinstance(logits, torch.Tensor) or logits.dim() < 2:
+        raise ValueError("logits must be 2-D (B*T, V) or N-D (N, C, d1, ..., dk) with the "
+                         "class dimension at axis 1")
     if not logits.is_cuda:
         raise ValueError("logits must be a CUDA tensor")
     if logits.dtype not in _DTYPES:
         raise TypeError(f"logits dtype {logits.dtype} is not supported "
                         "(float32, bfloat16, float16)")
-    if target.dim() != 1 or target.shape[0] != logits.shape[0]:
-        raise ValueError("target must be 1-D with one label per row of logits")
+    want = (logits.shape[0],) + tuple(logits.shape[2:])
+    if tuple(target.shape) != want:
+        raise ValueError(f"target must have shape {want}: one label per position of logits")
     if target.dtype not in (torch.int32, torch.int64):
         raise TypeError("target must be int32 or int64")
     if target.device != logits.device:
@@ -70,30 +75,42 @@ def _check_inputs(logits, target, weight):
 
 def _forward(logits, target, weight, ignore_index, lse_square_scale, label_smoothing,
              reduction, softcap, want_grad, want_z, want_acc, want_pred, batch_counts=None):
-    """Runs ce_fwd (ce_fwd_shard with batch_counts); returns (loss, z_loss,
-    acc, pred). Writes dlogits over logits when want_grad."""
-    rows, V = logits.shape
+    """Runs ce_fwd (ce_fwd_shard with batch_counts; ce_fwd_nd for N-D
+    logits); returns (loss, z_loss, acc, pred). Writes dlogits over logits
+    when want_grad."""
+    nd = logits.dim() > 2
     dev = logits.device
     red = _REDUCTIONS[reduction]
-    out_shape = (rows,) if red == _lib.CE_RED_NONE else ()
+    pos_shape = tuple(target.shape)  # (rows,) or (N, d1, ..., dk)
+    out_shape = pos_shape if red == _lib.CE_RED_NONE else ()
     f32 = dict(dtype=torch.float32, device=dev)
     loss = torch.empty(out_shape, **f32)
     z_loss = torch.empty(out_shape, **f32) if want_z else None
     acc = torch.empty(out_shape, **f32) if want_acc else None
-    pred = torch.empty((rows,), dtype=torch.int64, device=dev) if want_pred else None
+    pred = torch.empty(pos_shape, dtype=torch.int64, device=dev) if want_pred else None
     flags = ((_lib.CE_FLAG_GRAD if want_grad else 0) | (_lib.CE_FLAG_Z_LOSS if want_z else 0) |
              (_lib.CE_FLAG_ACC if want_acc else 0) | (_lib.CE_FLAG_PRED if want_pred else 0) |
              (_lib.CE_FLAG_TARGET_I64 if target.dtype == torch.int64 else 0))
     w = None if weight is None else weight.to(torch.float32).contiguous()
-    args = (_ptr(logits), _DTYPES[logits.dtype], rows, V, _ptr(target), _ptr(w),
-            int(ignore_index), float(label_smoothing), float(lse_square_scale),
-            float(softcap) if softcap is not None else 0.0, red, flags, _ptr(loss),
-            _ptr(z_loss), _ptr(acc), _ptr(pred))
+    opts = (_ptr(target), _ptr(w), int(ignore_index), float(label_smoothing),
+            float(lse_square_scale), float(softcap) if softcap is not None else 0.0, red, flags,
+            _ptr(loss), _ptr(z_loss), _ptr(acc), _ptr(pred))
     with torch.cuda.device(dev):
-        if batch_counts is None:
-            rc, where = ce_fwd(*args, _stream(dev)), "ce_fwd"
+        if nd:
+            if batch_counts is not None:
+                raise ValueError("batch_counts applies to 2-D logits only")
+            N, C = logits.shape[0], logits.shape[1]
+            inner = math.prod(logits.shape[2:])
+            rc, where = ce_fwd_nd(_ptr(logits), _DTYPES[logits.dtype], N, C, inner, *opts,
+                                  _stream(dev)), "ce_fwd_nd"
         else:
-            rc, where = ce_fwd_shard(*args, _ptr(batch_counts), _stream(dev)), "ce_fwd_shard"
+            rows, V = logits.shape
+            args = (_ptr(logits), _DTYPES[logits.dtype], rows, V, *opts)
+            if batch_counts is None:
+                rc, where = ce_fwd(*args, _stream(dev)), "ce_fwd"
+            else:
+                rc, where = (ce_fwd_shard(*args, _ptr(batch_counts), _stream(dev)),
+                             "ce_fwd_shard")
     if rc != _lib.CE_OK:
         raise CEError(rc, where)
     return loss, z_loss, acc, pred
@@ -141,14 +158,20 @@ class CrossEntropyFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad_loss, *unused):
         (dlogits,) = ctx.saved_tensors
-        rows, V = dlogits.shape
         g = grad_loss.to(torch.float32).contiguous()
         per_row = 1 if ctx.reduction == "none" else 0
         with torch.cuda.device(dlogits.device):
-            rc = ce_bwd(_ptr(g), per_row, _ptr(dlogits), _DTYPES[dlogits.dtype], rows, V,
-                        _stream(dlogits.device))
+            if dlogits.dim() > 2:
+                N, C = dlogits.shape[0], dlogits.shape[1]
+                rc, where = ce_bwd_nd(_ptr(g), per_row, _ptr(dlogits), _DTYPES[dlogits.dtype], N,
+                                      C, math.prod(dlogits.shape[2:]),
+                                      _stream(dlogits.device)), "ce_bwd_nd"
+            else:
+                rows, V = dlogits.shape
+                rc, where = ce_bwd(_ptr(g), per_row, _ptr(dlogits), _DTYPES[dlogits.dtype], rows,
+                                   V, _stream(dlogits.device)), "ce_bwd"
         if rc != _lib.CE_OK:
-            raise CEError(rc, "ce_bwd")
+            raise CEError(rc, where)
         return dlogits, None, None, None, None, None, None, None, None, None, None, None
 
 

@@ -27,6 +27,9 @@ SIGNATURES = {
     "ce_fwd_shard": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P, _P, _P,
                           _P, _P]),
     "ce_count": (_I, [_P, _P, _I64, _I64, _I64, _U32, _P, _P]),
+    "ce_fwd_nd": (_I, [_P, _I, _I64, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P, _P,
+                       _P, _P]),
+    "ce_bwd_nd": (_I, [_P, _I, _P, _I, _I64, _I64, _I64, _P]),
     "ce_bwd": (_I, [_P, _I, _P, _I, _I64, _I64, _P]),
     "ce_log_softmax": (_I, [_P, _P, _I, _I64, _I64, _P]),
     "ce_nll_loss_fwd": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _I, _U32, _P, _P, _P]),
@@ -92,6 +95,17 @@ def ce_fwd_shard(logits, dtype, rows, V, target, weight, ignore_index, label_smo
 
 def ce_count(target, weight, rows, V, ignore_index, flags, counts, stream):
     return load().ce_count(target, weight, rows, V, ignore_index, flags, counts, stream)
+
+
+def ce_fwd_nd(logits, dtype, N, C, inner, target, weight, ignore_index, label_smoothing,
+              lse_square_scale, softcap, reduction, flags, loss, z_loss, acc, pred, stream):
+    return load().ce_fwd_nd(logits, dtype, N, C, inner, target, weight, ignore_index,
+                            label_smoothing, lse_square_scale, softcap, reduction, flags,
+                            loss, z_loss, acc, pred, stream)
+
+
+def ce_bwd_nd(grad_output, grad_per_position, dlogits, dtype, N, C, inner, stream):
+    return load().ce_bwd_nd(grad_output, grad_per_position, dlogits, dtype, N, C, inner, stream)
 
 
 def ce_bwd(grad_output, grad_per_row, dlogits, dtype, rows, V, stream):

@@ -850,3 +850,208 @@ extern "C" const char* ce_status_string(ce_status s) {
 }
 
 extern "C" const char* ce_last_error(void) { return g_last_error.c_str(); }
+
+// ---------------------------------------------------------------- N-D logits (class dimension 1)
+
+namespace gbce {
+namespace {
+
+// Tile layout of the N-D forward: 16-byte vectors of positions or single
+// positions, the tile of 32 * VP positions x C classes in shared memory or
+// read again from global memory (L2) by phases B and C.
+struct NdPlan {
+    const void* fn = nullptr;
+    bool vec = false;
+    bool staged = false;
+    size_t smem = 0;
+    int64_t max_ctas = 0;
+};
+
+std::map<std::tuple<int, int, int64_t, bool, bool, bool, int>, NdPlan> g_nd_plans;
+
+// GBCE_ND_MODE forces a layout: 1 vector staged, 2 vector from global,
+// 3 scalar staged, 4 scalar from global (0: automatic). Automatic takes the
+// first that fits in this order: vector staged, scalar staged, scalar from
+// global; a staged tile may use up to half of an SM's shared memory less
+// the fixed part, so two CTAs fit on an SM.
+ce_status nd_plan(int dev, const DeviceInfo& info, int dtype, int64_t C, bool vec_ok, bool softcap,
+                  bool argmax, NdPlan* out) {
+    const int mode = env_int("GBCE_ND_MODE", 0);
+    const auto key = std::make_tuple(dev, dtype, C, vec_ok, softcap, argmax, mode);
+    auto it = g_nd_plans.find(key);
+    if (it != g_nd_plans.end()) {
+        *out = it->second;
+        return CE_OK;
+    }
+    const int64_t b = dtype == CE_F32 ? 4 : 2;
+    const size_t fixed_vec = nd_fixed_smem(32 * static_cast<int>(16 / b));
+    const size_t fixed_one = nd_fixed_smem(32);
+    const int64_t tile_vec = C * 32 * 16;
+    const int64_t tile_one = C * 32 * b;
+    const int64_t half_sm = info.smem_per_sm / 2 - 1024;  // the runtime reserves 1 KB a CTA
+    const int64_t cap = info.smem_optin;
+    bool vec = false, staged = false;
+    switch (mode) {
+    case 1: vec = true; staged = true; break;
+    case 2: vec = true; break;
+    case 3: staged = true; break;
+    case 4: break;
+    default:
+        if (vec_ok && static_cast<int64_t>(fixed_vec) + tile_vec <= half_sm) {
+            vec = true;
+            staged = true;
+        } else if (static_cast<int64_t>(fixed_one) + tile_one <= half_sm) {
+            staged = true;
+        }
+    }
+    NdPlan p;
+    p.vec = vec;
+    p.staged = staged;
+    p.smem = (vec ? fixed_vec : fixed_one) + (staged ? (vec ? tile_vec : tile_one) : 0);
+    if ((vec && !vec_ok) || static_cast<int64_t>(p.smem) > cap) {
+        g_last_error = "the N-D layout forced by GBCE_ND_MODE cannot run this shape";
+        return CE_ERR_UNSUPPORTED;
+    }
+    p.fn = nd_kernel(dtype, vec, softcap, argmax);
+    if (!p.fn) return CE_ERR_INVALID_ARG;
+    // the largest dynamic size the kernel can take, set once for every plan
+    // that uses it (a smaller value would refuse the larger plans' launches)
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, p.fn);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncGetAttributes");
+    const size_t max_dyn = static_cast<size_t>(cap) - fa.sharedSizeBytes;
+    if (p.smem > max_dyn) {
+        g_last_error = "the N-D tile does not fit in shared memory";
+        return CE_ERR_UNSUPPORTED;
+    }
+    e = cudaFuncSetAttribute(p.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(max_dyn));
+    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute");
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p.fn, kNdThreads, p.smem);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (occ < 1) {
+        g_last_error = "the N-D kernel does not fit on an SM";
+        return CE_ERR_UNSUPPORTED;
+    }
+    p.max_ctas = static_cast<int64_t>(occ) * info.sm_count;
+    g_nd_plans[key] = p;
+    *out = p;
+    return CE_OK;
+}
+
+}  // namespace
+}  // namespace gbce
+
+extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, int64_t inner,
+                               const void* target, const float* weight, int64_t ignore_index,
+                               float label_smoothing, float lse_square_scale, float softcap,
+                               int reduction, uint32_t flags, float* loss, float* z_loss,
+                               float* acc, int64_t* pred, ce_stream_t stream) {
+    if (N < 0 || C <= 0 || inner < 0) return CE_ERR_INVALID_ARG;
+    if (inner > 0 && N > INT64_MAX / inner) return CE_ERR_INVALID_ARG;
+    const int64_t rows = N * inner;
+    const FwdCall c{logits, dtype, rows, C, target, weight, ignore_index, label_smoothing,
+                    lse_square_scale, softcap, reduction, flags, loss, z_loss, acc, pred, nullptr};
+    ce_status rc = check_fwd(c);
+    if (rc != CE_OK) return rc;
+    // one class dimension with nothing after it is the 2-D layout; so is an
+    // empty batch (which writes only the reduced scalars)
+    if (inner == 1 || rows == 0) return fwd_library_scratch(c, stream);
+    if (rows > INT32_MAX) return CE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    DeviceInfo info;
+    Scratch* scratch = nullptr;
+    rc = device_and_scratch(st, &dev, &info, &scratch);
+    if (rc != CE_OK) return rc;
+    const int64_t b = dtype == CE_F32 ? 4 : 2;
+    const bool vec_ok = aligned16(logits) && inner % (16 / b) == 0;
+    const bool sc = softcap > 0.f;
+    const bool argmax = (flags & (CE_FLAG_ACC | CE_FLAG_PRED)) != 0;
+    NdPlan p;
+    rc = nd_plan(dev, info, dtype, C, vec_ok, sc, argmax, &p);
+    if (rc != CE_OK) return rc;
+    if (reduction != CE_RED_NONE) {
+        // D and the counted positions first: the gradient's mean scale needs
+        // them before any position is finished
+        CountArgs ca = {};
+        ca.target = target;
+        ca.tgt64 = (flags & CE_FLAG_TARGET_I64) ? 1 : 0;
+        ca.weight = weight;
+        ca.rows = rows;
+        ca.V = C;
+        ca.ignore_index = ignore_index;
+        ca.counts = scratch->counts;
+        ca.scratch = scratch;
+        const int64_t want = (rows + kCountThreads * 16 - 1) / (kCountThreads * 16);
+        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, info.sm_count));
+        rc = launch(count_kernel(), static_cast<int>(grid), kCountThreads, 0, 1, st, &ca);
+        if (rc != CE_OK) return rc;
+    }
+    FwdArgs a = {};
+    a.x = logits;
+    a.rows = rows;
+    a.V = C;
+    a.target = target;
+    a.tgt64 = (flags & CE_FLAG_TARGET_I64) ? 1 : 0;
+    a.weight = weight;
+    a.ignore_index = ignore_index;
+    a.eps = label_smoothing;
+    a.lam = lse_square_scale;
+    a.softcap = sc ? softcap : 0.f;
+    a.sc_k2 = sc ? 2.f * kLog2e / softcap : 0.f;
+    a.sc_slog2e = sc ? softcap * kLog2e : 0.f;
+    a.reduction = reduction;
+    a.grad = (flags & CE_FLAG_GRAD) ? 1 : 0;
+    a.want_z = (flags & CE_FLAG_Z_LOSS) ? 1 : 0;
+    a.want_acc = (flags & CE_FLAG_ACC) ? 1 : 0;
+    a.want_pred = (flags & CE_FLAG_PRED) ? 1 : 0;
+    a.loss = loss;
+    a.zloss = z_loss;
+    a.acc = acc;
+    a.pred = pred;
+    a.scratch = scratch;
+    a.batch_counts = reduction != CE_RED_NONE ? scratch->counts : nullptr;
+    a.inner = inner;
+    a.nd_staged = p.staged ? 1 : 0;
+    const int64_t P = p.vec ? 32 * (16 / b) : 32;
+    const int64_t tiles = (rows + P - 1) / P;
+    const int64_t grid = std::min<int64_t>(tiles, std::min<int64_t>(p.max_ctas, kMaxPartials));
+    return launch(p.fn, static_cast<int>(grid), kNdThreads, p.smem, 1, st, &a);
+}
+
+extern "C" ce_status ce_bwd_nd(const float* grad_output, int grad_per_position, void* dlogits,
+                               int dtype, int64_t N, int64_t C, int64_t inner,
+                               ce_stream_t stream) {
+    if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_INVALID_ARG;
+    if (N < 0 || C <= 0 || inner < 0) return CE_ERR_INVALID_ARG;
+    if (N > 0 && inner > 0 && (C > INT64_MAX / N / inner / 4)) return CE_ERR_INVALID_ARG;
+    if (N == 0 || inner == 0) return CE_OK;
+    if (!grad_output || !dlogits) return CE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    DeviceInfo info;
+    ce_status rc = device_info(dev, &info);
+    if (rc != CE_OK) return rc;
+    const int64_t b = dtype == CE_F32 ? 4 : 2;
+    NdBwdArgs a = {};
+    a.g = grad_output;
+    a.per_pos = grad_per_position ? 1 : 0;
+    a.x = dlogits;
+    a.N = N;
+    a.C = C;
+    a.inner = inner;
+    a.vec_ok = (aligned16(dlogits) && (inner * b) % 16 == 0) ? 1 : 0;
+    int64_t grid;
+    if (a.per_pos)
+        grid = std::min<int64_t>(N * C, static_cast<int64_t>(info.sm_count) * 8);
+    else
+        grid = std::max<int64_t>(1, std::min<int64_t>((N * C * inner + 2047) / 2048,
+                                                     static_cast<int64_t>(info.sm_count) * 8));
+    return launch(nd_bwd_kernel(dtype), static_cast<int>(grid), kBwdThreads, 0, 1,
+                  reinterpret_cast<cudaStream_t>(stream), &a);
+}

@@ -198,6 +198,75 @@ __global__ void __launch_bounds__(kBwdThreads) ce_bwd_scale(const __grid_constan
     }
 }
 
+// Backward of the N-D form [N, C, inner]: dlogits *= grad_output, one value
+// or one per position (n, s) for reduction "none". Each CTA walks the N * C
+// lines of `inner` elements; a line's factors are grad_output[n * inner +
+// s] for its n, so every position's factor multiplies its C classes.
+template <typename T>
+__global__ void __launch_bounds__(kBwdThreads) ce_bwd_nd_scale(const __grid_constant__ NdBwdArgs a) {
+    using VT = Vec<T>;
+    constexpr int VE = VT::N;
+    if (!a.per_pos) {
+        const float g = __ldg(a.g);
+        if (g == 1.f) return;  // multiplying by one changes nothing
+        const int64_t total = a.N * a.C * a.inner;
+        const int64_t stride = static_cast<int64_t>(gridDim.x) * kBwdThreads;
+        if (a.vec_ok) {
+            uint4* v = reinterpret_cast<uint4*>(a.x);
+#pragma unroll 4
+            for (int64_t i = static_cast<int64_t>(blockIdx.x) * kBwdThreads + threadIdx.x;
+                 i < total / VE; i += stride) {
+                float f[VE];
+                VT::unpack(v[i], f);
+#pragma unroll
+                for (int j = 0; j < VE; ++j) f[j] *= g;
+                v[i] = VT::pack(f);
+            }
+        } else {
+            for (int64_t i = static_cast<int64_t>(blockIdx.x) * kBwdThreads + threadIdx.x;
+                 i < total; i += stride)
+                VT::store1(a.x, i, VT::load1(a.x, i) * g);
+        }
+        return;
+    }
+    const int64_t lines = a.N * a.C;
+    for (int64_t l = blockIdx.x; l < lines; l += gridDim.x) {
+        const float* g = a.g + (l / a.C) * a.inner;
+        T* line = reinterpret_cast<T*>(a.x) + l * a.inner;
+        if (a.vec_ok) {
+            uint4* v = reinterpret_cast<uint4*>(line);
+            for (int64_t i = threadIdx.x; i < a.inner / VE; i += kBwdThreads) {
+                float f[VE];
+                VT::unpack(v[i], f);
+#pragma unroll
+                for (int j = 0; j < VE; ++j) f[j] *= __ldg(g + i * VE + j);
+                v[i] = VT::pack(f);
+            }
+        } else {
+            for (int64_t i = threadIdx.x; i < a.inner; i += kBwdThreads)
+                VT::store1(line, i, VT::load1(line, i) * __ldg(g + i));
+        }
+    }
+}
+
+const void* nd_bwd_kernel(int dtype) {
+    if (dtype == 0) return (const void*)&ce_bwd_nd_scale<float>;
+    if (dtype == 1) return (const void*)&ce_bwd_nd_scale<__nv_bfloat16>;
+    if (dtype == 2) return (const void*)&ce_bwd_nd_scale<__half>;
+    return nullptr;
+}
+
+const void* nd_kernel_f32(bool vec, bool softcap, bool argmax);
+const void* nd_kernel_bf16(bool vec, bool softcap, bool argmax);
+const void* nd_kernel_f16(bool vec, bool softcap, bool argmax);
+
+const void* nd_kernel(int dtype, bool vec, bool softcap, bool argmax) {
+    if (dtype == 0) return nd_kernel_f32(vec, softcap, argmax);
+    if (dtype == 1) return nd_kernel_bf16(vec, softcap, argmax);
+    if (dtype == 2) return nd_kernel_f16(vec, softcap, argmax);
+    return nullptr;
+}
+
 const void* generic_kernel(int dtype, bool softcap) {
     if (dtype == 0)
         return softcap ? (const void*)&ce_fwd_generic<float, true>

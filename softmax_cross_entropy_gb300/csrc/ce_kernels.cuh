@@ -22,13 +22,17 @@ struct alignas(32) Partial {
 };
 
 // Library-owned scratch: a self-resetting ticket for the last-CTA epilogue,
-// a sticky error word, and one Partial per cluster.
+// a sticky error word, the batch counts {D, counted rows} a count pre-pass
+// leaves for the N-D forward, and one Partial per cluster.
 struct Scratch {
     unsigned ticket;
     unsigned status;
-    unsigned pad[62];
+    unsigned pad0[2];
+    double counts[2];
+    unsigned pad[56];
     Partial partials[1];  // really kMaxPartials
 };
+static_assert(sizeof(Partial) == 32, "partial-sum slot layout");
 constexpr int kMaxPartials = 4096;
 constexpr size_t kScratchBytes = sizeof(Scratch) + (kMaxPartials - 1) * sizeof(Partial);
 
@@ -67,6 +71,11 @@ struct FwdArgs {
     // (the mean scale and the accuracy use them instead of this call's own
     // counts), or nullptr
     const double* batch_counts;
+    // N-D layout [N, C, inner] (class dimension 1): rows = N * inner
+    // positions, V = C classes; element (position r, class c) sits at
+    // (r / inner) * C * inner + c * inner + r % inner
+    int64_t inner;
+    int nd_staged;  // 1: the N-D kernel keeps its tile in shared memory
 };
 
 // Arguments of one forward call as the C ABI receives them (host side).
@@ -428,5 +437,28 @@ constexpr int kNllThreads = 256;
 constexpr int kLsmBwdThreads = 1024;
 constexpr int kCountThreads = 256;
 const void* bwd_kernel(int dtype);
+
+// N-D logits [N, C, inner] (class dimension 1). The forward kernel takes one
+// FwdArgs (rows = N * inner, V = C, inner, nd_staged); vec selects 16-byte
+// loads of consecutive positions (inner a multiple of 16 / sizeof(T), base
+// 16-byte aligned), argmax the first-argmax tracking (predicted tokens,
+// accuracy).
+constexpr int kNdThreads = 256;
+constexpr int kNdWarps = kNdThreads / 32;
+// shared memory of an N-D CTA besides its tile: per-warp partials and
+// per-position coefficients for `positions` positions
+constexpr size_t nd_fixed_smem(int positions) {
+    return static_cast<size_t>(2 * kNdWarps + 6) * positions * 4;
+}
+const void* nd_kernel(int dtype, bool vec, bool softcap, bool argmax);
+
+struct NdBwdArgs {
+    const float* g;  // one value, or one per position ([N, inner])
+    int per_pos;
+    void* x;         // [N, C, inner]
+    int64_t N, C, inner;
+    int vec_ok;      // inner * sizeof(T) % 16 == 0 and x 16-byte aligned
+};
+const void* nd_bwd_kernel(int dtype);
 
 }  // namespace gbce

@@ -217,6 +217,24 @@ def random_case(seed, rows, V, dtype="f32", std=3.0, ignore_frac=0.1, **opts) ->
     return Case(f"random_{rows}x{V}_{dtype}", x, dtype, t, weight=w, **opts)
 
 
+def nd_case(seed, shape, dtype="f32", std=3.0, ignore_frac=0.1, **opts) -> Case:
+    """Seeded case with N-D logits (N, C, d1, ..., dk), the class dimension at
+    axis 1, and targets (N, d1, ..., dk). The logits are the blocked normal
+    draws of an (N * C, d1 * ... * dk) matrix reshaped; the targets are
+    uniform in [0, C) with round(ignore_frac * positions) ignored."""
+    shape = tuple(int(d) for d in shape)
+    N, C = shape[0], shape[1]
+    inner = int(np.prod(shape[2:], dtype=np.int64))
+    rng = _aux_rng(seed)
+    gen = {"f32": _normal, "bf16": _bf16_normal, "f16": _f16_normal}[dtype]
+    x = gen(seed, N * C, inner, std).reshape(shape)
+    t = targets(rng, N * inner, C, ignore_frac).reshape((N,) + shape[2:])
+    w = opts.pop("weight", None)
+    if w is True:
+        w = rng.uniform(0.5, 2.0, size=C).astype(np.float32)
+    return Case(f"nd_{'x'.join(map(str, shape))}_{dtype}", x, dtype, t, weight=w, **opts)
+
+
 def logits_f64(case: Case) -> np.ndarray:
     """The logits as float64 values (exact for every storage)."""
     if case.dtype == "bf16":
