@@ -33,7 +33,7 @@ struct DeviceInfo {
 
 // A launch plan for one (device, dtype, V, variant): which kernel, how many
 // CTAs per row, ring depth, dynamic shared memory and the resident grid.
-enum class Kind { General, Staged, Stream };
+enum class Kind { General, Staged, Stream, Reg };
 
 struct Plan {
     const void* fn = nullptr;
@@ -47,6 +47,7 @@ struct Plan {
     int64_t max_units = 0;  // resident CTAs (cluster == 1) or clusters
     // streaming kernel layout
     int ng = 0, sg = 0, chunk_vec = 0, nchunk = 0, resident = 0;
+    int reg_wpr = 0;  // register-resident kernel: warps of a row team
 };
 
 using PlanKey = std::tuple<int, int, int64_t, bool, bool, int>;
@@ -189,7 +190,7 @@ bool try_staged(int dtype, int64_t V, bool softcap, bool wsmooth, int C, int cfg
         if (ncl < 1) return false;
         units = ncl;
     }
-    units = std::min<int64_t>(units, kMaxPartials);
+    units = std::min<int64_t>(units, kMaxUnits);
     out->fn = fn;
     out->staged = true;
     out->nt = nt;
@@ -306,25 +307,28 @@ bool try_stream(int dtype, int64_t V, bool softcap, bool ws, const DeviceInfo& d
         return false;
     }
     if (occ < 1) return false;
-    p.max_units = std::min<int64_t>(static_cast<int64_t>(occ) * dev.sm_count, kMaxPartials);
+    p.max_units = std::min<int64_t>(static_cast<int64_t>(occ) * dev.sm_count, kMaxUnits);
     *out = p;
     return true;
 }
 
 ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth, bool aligned,
-                    Plan* out) {
+                    bool w_aligned, Plan* out) {
     // Tuning overrides: GBCE_CLUSTER forces the CTAs per row (1, 2, 4, 8 or
     // 16; -1 forces the general path) and GBCE_CFG the CTA shape index.
     const int forced_c = env_int("GBCE_CLUSTER", 0);
     const int forced_cfg = env_int("GBCE_CFG", -1);
-    // GBCE_KERNEL: 1 staged, 2 streaming, 3 general (0: automatic)
+    // GBCE_KERNEL: 1 staged, 2 streaming, 3 general, 4 register-resident
+    // (0: automatic)
     const int forced_kind = env_int("GBCE_KERNEL", 0);
     const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth,
                       (forced_kind * 64 + forced_c) * 64 + forced_cfg +
                           1000000 * env_int("GBCE_STREAM_GROUPS", 0) +
                           100000000 * env_int("GBCE_STREAM_TWICE", 0) +
                           13 * env_int("GBCE_STREAM_SLOTS", 0) +
-                          17 * env_int("GBCE_STREAM_WARPS", 0));
+                          17 * env_int("GBCE_STREAM_WARPS", 0) +
+                          19 * (env_int("GBCE_REG_MAX_BYTES", 65536) + (w_aligned ? 0 : 1)) +
+                          7 * env_int("GBCE_REG_NVL", 16));
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
         *out = it->second;
@@ -336,7 +340,36 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     Plan best;
     const int64_t bytes = dtype == CE_F32 ? 4 : 2;
     const bool fast_ok = aligned && (V * bytes) % 16 == 0 && forced_c >= 0 && forced_kind != 3;
-    if (fast_ok && forced_kind != 1) {
+    // The register-resident kernel for rows of at most GBCE_REG_MAX_BYTES
+    // (default and limit 64 KB: 8 warps of 16 vectors a thread). A thread
+    // holds GBCE_REG_NVL (8 or 16, default 16) 16-byte vectors; a team of
+    // the fewest warps that hold a row owns it, and a CTA has as many teams
+    // as fit in 8 warps. Its class weights are read as 16-byte vectors.
+    const int64_t reg_max = env_int("GBCE_REG_MAX_BYTES", 65536);
+    const int nvl_env = env_int("GBCE_REG_NVL", 16);
+    const int nvl = (nvl_env == 8 || nvl_env == 16) ? nvl_env : 16;
+    const int64_t vrow = V * bytes / 16;
+    const int64_t wpr = (vrow + 32 * nvl - 1) / (32 * nvl);
+    if (fast_ok && (!wsmooth || w_aligned) && wpr <= kRegMaxWarps &&
+        (forced_kind == 4 || (forced_kind == 0 && V * bytes <= reg_max))) {
+        const void* fn = reg_kernel(dtype, softcap, wsmooth, nvl);
+        const int teams = kRegMaxWarps / static_cast<int>(wpr);
+        const int nt = 32 * static_cast<int>(wpr) * teams;
+        int occ = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, nt, 0);
+        if (e != cudaSuccess) return cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (occ >= 1) {
+            best.fn = fn;
+            best.kind = Kind::Reg;
+            best.nt = nt;
+            best.reg_wpr = static_cast<int>(wpr);
+            // at most 8 CTAs an SM: the partial-sum slots of a launch stay
+            // within 8 per SM, as for the other kernels
+            best.max_units = std::min<int64_t>(
+                static_cast<int64_t>(std::min(occ, 8)) * dev.sm_count, kMaxUnits);
+        }
+    }
+    if (fast_ok && forced_kind != 1 && best.kind == Kind::General) {
         rc = CE_OK;
         if (!try_stream(dtype, V, softcap, wsmooth, dev, &best, &rc) && rc != CE_OK) return rc;
     }
@@ -368,14 +401,15 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
         }
     }
     if ((forced_kind == 1 && best.kind != Kind::Staged) ||
-        (forced_kind == 2 && best.kind != Kind::Stream)) {
+        (forced_kind == 2 && best.kind != Kind::Stream) ||
+        (forced_kind == 4 && best.kind != Kind::Reg)) {
         g_last_error = "the kernel forced by GBCE_KERNEL cannot run this shape";
         return CE_ERR_UNSUPPORTED;
     }
     if (best.kind == Kind::General) {
         best.fn = generic_kernel(dtype, softcap);
         best.nt = kGenericThreads;
-        best.max_units = std::min<int64_t>(static_cast<int64_t>(dev.sm_count) * 8, kMaxPartials);
+        best.max_units = std::min<int64_t>(static_cast<int64_t>(dev.sm_count) * 8, kMaxUnits);
     }
     if (env_int("GBCE_VERBOSE", 0))
         std::fprintf(stderr,
@@ -383,8 +417,10 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
                      "stages=%d slice_vec=%d smem=%zu units=%lld ng=%d sg=%d chunk_vec=%d "
                      "nchunk=%d resident=%d\n",
                      dtype, static_cast<long long>(V), softcap ? 1 : 0, wsmooth ? 1 : 0,
-                     best.kind == Kind::Stream ? "stream"
-                                               : (best.kind == Kind::Staged ? "staged" : "general"),
+                     best.kind == Kind::Stream   ? "stream"
+                     : best.kind == Kind::Staged ? "staged"
+                     : best.kind == Kind::Reg    ? "reg"
+                                                 : "general",
                      best.nt, best.cluster, best.stages, best.slice_vec, best.smem,
                      static_cast<long long>(best.max_units), best.ng, best.sg, best.chunk_vec,
                      best.nchunk, best.resident);
@@ -393,21 +429,33 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     return CE_OK;
 }
 
+// pdl: the launch may begin before the previous launch on the stream has
+// finished (programmatic dependent launch); the kernel then waits for it
+// (griddepcontrol.wait) before reading what it produced.
 ce_status launch(const void* fn, int grid, int nt, size_t smem, int cluster, cudaStream_t st,
-                 void* arg) {
+                 void* arg, bool pdl = false) {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(static_cast<unsigned>(grid));
     lc.blockDim = dim3(static_cast<unsigned>(nt));
     lc.dynamicSmemBytes = smem;
     lc.stream = st;
-    cudaLaunchAttribute attr;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
     if (cluster > 1) {
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = static_cast<unsigned>(cluster);
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        lc.attrs = &attr;
-        lc.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (na) {
+        lc.attrs = attr;
+        lc.numAttrs = na;
     }
     void* args[] = {arg};
     cudaError_t e = cudaLaunchKernelExC(&lc, fn, args);
@@ -482,12 +530,13 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
 
     const bool wsmooth = c.weight != nullptr && c.label_smoothing > 0.f;
     const bool aligned = (reinterpret_cast<uintptr_t>(c.logits) % 16) == 0;
+    const bool w_aligned = (reinterpret_cast<uintptr_t>(c.weight) % 16) == 0;
     Plan p;
-    ce_status rc = make_plan(dev, c.dtype, c.V, sc, wsmooth, aligned, &p);
+    ce_status rc = make_plan(dev, c.dtype, c.V, sc, wsmooth, aligned, w_aligned, &p);
     if (rc != CE_OK) return rc;
     const int64_t units = c.rows == 0 ? 1 : std::min<int64_t>(c.rows, p.max_units);
-    if (units > max_slots) {
-        g_last_error = "this launch needs " + std::to_string(units) +
+    if (records_for(units) > max_slots) {
+        g_last_error = "this launch needs " + std::to_string(records_for(units)) +
                        " partial-sum slots; the scratch holds " + std::to_string(max_slots);
         return CE_ERR_UNSUPPORTED;
     }
@@ -506,6 +555,37 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
         a.nchunk = p.nchunk;
         a.resident = p.resident;
         return launch(p.fn, static_cast<int>(units), p.nt, p.smem, 1, st, &a);
+    }
+    if (p.kind == Kind::Reg) {
+        bool pdl = false;
+        // D is needed by "mean" (loss and gradient scale), the counted rows
+        // by the accuracy of "sum" and "mean"
+        const bool need = c.reduction == CE_RED_MEAN ||
+                          (c.reduction == CE_RED_SUM && (c.flags & CE_FLAG_ACC));
+        if (need && !c.batch_counts) {
+            // D and the counted rows by the count kernel, into the scratch
+            // header; the forward overlaps it and waits where it needs them
+            CountArgs ca = {};
+            ca.target = c.target;
+            ca.tgt64 = a.tgt64;
+            ca.weight = c.weight;
+            ca.rows = c.rows;
+            ca.V = c.V;
+            ca.ignore_index = c.ignore_index;
+            ca.counts = scratch->counts;
+            ca.scratch = scratch;
+            DeviceInfo info;
+            ce_status rc2 = device_info(dev, &info);
+            if (rc2 != CE_OK) return rc2;
+            const int64_t want = (c.rows + kCountThreads * 4 - 1) / (kCountThreads * 4);
+            const int64_t cgrid = std::max<int64_t>(1, std::min<int64_t>(want, info.sm_count));
+            rc2 = launch(count_kernel(), static_cast<int>(cgrid), kCountThreads, 0, 1, st, &ca);
+            if (rc2 != CE_OK) return rc2;
+            a.batch_counts = scratch->counts;
+            pdl = true;
+        }
+        a.reg_wpr = p.reg_wpr;
+        return launch(p.fn, static_cast<int>(units), p.nt, 0, 1, st, &a, pdl);
     }
     if (p.kind == Kind::Staged) {
         a.slice_vec = p.slice_vec;
@@ -1018,7 +1098,7 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     a.nd_staged = p.staged ? 1 : 0;
     const int64_t P = p.vec ? 32 * (16 / b) : 32;
     const int64_t tiles = (rows + P - 1) / P;
-    const int64_t grid = std::min<int64_t>(tiles, std::min<int64_t>(p.max_ctas, kMaxPartials));
+    const int64_t grid = std::min<int64_t>(tiles, std::min<int64_t>(p.max_ctas, kMaxUnits));
     return launch(p.fn, static_cast<int>(grid), kNdThreads, p.smem, 1, st, &a);
 }
 

@@ -14,6 +14,9 @@ namespace {
 // ticket) adds them in slot order with a fixed lane split and butterfly.
 __global__ void __launch_bounds__(kCountThreads) ce_count_kernel(const __grid_constant__ CountArgs a) {
     constexpr int NW = kCountThreads / 32;
+    // a forward launched after this one may start now; it waits for these
+    // counts where it first needs them
+    pdl_launch_dependents();
     __shared__ double s_d[NW];
     __shared__ long long s_n[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

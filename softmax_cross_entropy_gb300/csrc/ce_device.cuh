@@ -370,7 +370,9 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 }
 
 // Warp-wide maximum of a float and minimum of an int in one instruction
-// each (redux.sync on sm_100-class GPUs); every lane gets the result.
+// each (redux.sync on sm_100-class GPUs); every lane gets the result. The
+// whole warp must be converged at the call (__syncwarp() after a divergent
+// branch).
 __device__ __forceinline__ float warp_max_f32(float v) {
     float m;
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
@@ -378,9 +380,9 @@ __device__ __forceinline__ float warp_max_f32(float v) {
 }
 
 __device__ __forceinline__ int warp_min_s32(int v) {
-    int m;
-    asm volatile("redux.sync.min.s32 %0, %1, 0xffffffff;" : "=r"(m) : "r"(v));
-    return m;
+    // the compiler's own intrinsic for redux.sync.min.s32, which it keeps
+    // convergent (an asm statement may be duplicated into divergent paths)
+    return __reduce_min_sync(0xffffffffu, v);
 }
 
 }  // namespace gbce

@@ -372,7 +372,7 @@ ce_fwd_nd(const __grid_constant__ FwdArgs a) {
                 Z += red_d[NW + w];
                 Cn += red_n[w];
             }
-            finish_scalars(a, blockIdx.x, gridDim.x, L, Z, Cn, D, n_valid);
+            finish_scalars_2level(a, blockIdx.x, gridDim.x, L, Z, Cn, D, n_valid);
         }
     }
 }

@@ -1,0 +1,388 @@
+// Fused softmax cross-entropy forward with the in-forward gradient for rows
+// of at most 64 KB: the register-resident kernel.
+//
+// Method (Liger-Kernel cross-entropy kernel profile, §Forward Pass,
+// §Backward Pass, §Key Patterns): per row the max-shifted log-sum-exp, the
+// NLL with ignore_index, class weights, label smoothing, z-loss, softcap,
+// the argmax, and the gradient of the reduced loss written over the logits.
+//
+// GB300 design. A team of WPR warps owns one row at a time and each thread
+// holds NVL (8 or 16) 16-byte vectors of it in registers, so a row of up to
+// 512 B * NVL * WPR is read from HBM once, with 16-byte coalesced loads
+// issued all at once, and written once. Warp w of a team takes the row's
+// vectors [w * 32 * NVL, (w + 1) * 32 * NVL): lane l holds vectors
+// w * 32 * NVL + 32 k + l, so every load and store of a warp is 512
+// contiguous bytes and the offsets between a thread's vectors are
+// constants. A CTA holds several independent
+// teams (one warp each for a 4096-element bf16 row), so an SM has a dozen or
+// more rows in flight and their loads overlap one another's arithmetic,
+// which is what hides HBM latency here; no shared-memory staging or copy
+// engine is involved. Per row:
+//   1. raw maximum (packed 16-bit max for bf16/fp16), warp redux, one team
+//      barrier for the row's maximum; the first argmax only when asked for;
+//   2. S = sum exp(z - M) and the smoothing sum from the registers; a
+//      second team barrier merges them;
+//   3. the gradient As * exp(z - M) + Bc (times 1 - tanh^2 under softcap),
+//      the exponential formed again from the registers (the SFU has room
+//      for it, the register file has none for a copy of every e), stored
+//      with 16-byte stores; the owner of the target's vector adds the
+//      one-hot term and computes the row loss.
+// Only row-level sums cross threads, in a fixed order, so results are
+// deterministic. The mean denominator comes from the count kernel launched
+// just before (its completion is awaited only where the first gradient
+// needs it) or from the caller's batch counts.
+#pragma once
+
+#include <climits>
+
+#include "ce_kernels.cuh"
+
+namespace gbce {
+
+// Class weights of vector v (VE consecutive classes).
+template <int VE>
+__device__ __forceinline__ void reg_weights(const float* weight, int v, float (&w)[VE]) {
+    const float4* wv = reinterpret_cast<const float4*>(weight + v * VE);
+#pragma unroll
+    for (int h = 0; h < VE / 4; ++h) {
+        const float4 t4 = __ldg(wv + h);
+        w[4 * h] = t4.x;
+        w[4 * h + 1] = t4.y;
+        w[4 * h + 2] = t4.z;
+        w[4 * h + 3] = t4.w;
+    }
+}
+
+// z = softcap(x) and (under softcap) the tanh, for a pair of logits.
+template <bool SOFTCAP>
+__device__ __forceinline__ float2 reg_z2(float x0, float x1, const FwdArgs& a, float2& th) {
+    if constexpr (SOFTCAP) {
+        th = make_float2(tanh_from_scaled(x0 * a.sc_k2), tanh_from_scaled(x1 * a.sc_k2));
+        return make_float2(a.softcap * th.x, a.softcap * th.y);
+    } else {
+        return make_float2(x0, x1);
+    }
+}
+
+// exp2 arguments (z - M) * log2(e): one packed FFMA against the rounded
+// M * log2(e) for 16-bit logits, subtract first for fp32.
+template <typename T>
+__device__ __forceinline__ float2 reg_arg2(float2 z, float Ms, float ML) {
+    if constexpr (sizeof(T) == 2)
+        return ffma2(z, make_float2(kLog2e, kLog2e), make_float2(-ML, -ML));
+    else
+        return fmul2(fadd2(z, make_float2(-Ms, -Ms)), make_float2(kLog2e, kLog2e));
+}
+
+// 8 vectors a thread: three CTAs of 8 warps an SM (85 registers a thread);
+// 16 vectors: two (128 registers)
+template <typename T, bool SOFTCAP, bool WS, int NVL>
+__global__ void __launch_bounds__(32 * kRegMaxWarps, NVL == 8 ? 3 : 2)
+ce_fwd_reg(const __grid_constant__ FwdArgs a) {
+    using VT = Vec<T>;
+    constexpr int VE = VT::N;
+    constexpr int MW = kRegMaxWarps;
+    __shared__ float red_a[MW], red_b[MW], red_c[MW];
+    __shared__ int red_i[MW];
+    __shared__ double red_d[2][MW];
+    __shared__ long long red_n[MW];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int WPR = a.reg_wpr;           // warps of a team
+    const int team = warp / WPR;
+    const int wr = warp - team * WPR;    // warp within the team
+    const int w0 = team * WPR;           // the team's first warp
+    const int teams = (blockDim.x >> 5) / WPR;
+    const int vrow = static_cast<int>(a.V / VE);
+    const int vbase = wr * 32 * NVL + lane;  // this thread's first vector
+    const int vlim = vrow - vbase;           // its vector k exists when 32 k < vlim
+    const bool smooth = WS || a.eps > 0.f;
+    const bool want_arg = a.want_pred || a.want_acc;
+
+    // barrier over the team's warps (named barrier 1 + team; a lone warp
+    // needs only its own convergence)
+    auto team_sync = [&]() {
+        if (WPR == 1)
+            __syncwarp();
+        else
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * WPR) : "memory");
+    };
+    // lane-level fixed-order sum of the team's per-warp values: the same
+    // bits in every thread of the team
+    auto team_sum = [&](const float* red) {
+        float v = lane < WPR ? red[w0 + lane] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        return v;
+    };
+
+    // D = sum of w[t] over counted rows and the counted-row number come from
+    // a.batch_counts ("sum" and "mean"): the caller's batch totals, or the
+    // count kernel launched just before this one, which this launch
+    // overlaps (programmatic dependent launch) until it first needs them
+    float D = 0.f;
+    int n_valid = 0;
+    // "sum" without accuracy needs neither (and the host then launches no
+    // count kernel)
+    bool have_counts = a.reduction == kRedNone || (a.reduction == kRedSum && !a.want_acc);
+    auto need_counts = [&]() {
+        if (!have_counts) {
+            pdl_wait();
+            D = static_cast<float>(a.batch_counts[0]);
+            n_valid = static_cast<int>(a.batch_counts[1]);
+            have_counts = true;
+        }
+    };
+    const float inv_V = 1.f / static_cast<float>(a.V);
+    float Wtot = static_cast<float>(a.V);
+    if (WS) {
+        // W = sum of the class weights: every thread the same fixed order
+        float s = 0.f;
+        for (int c = tid; c < a.V; c += blockDim.x) s += __ldg(a.weight + c);
+        s = warp_sum(s);
+        if (lane == 0) red_a[warp] = s;
+        __syncthreads();
+        float v = lane < static_cast<int>(blockDim.x >> 5) ? red_a[lane] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        Wtot = v;
+        __syncthreads();
+    }
+    const float Wf = WS ? Wtot * inv_V : 1.f;
+
+    float accL = 0.f, accZ = 0.f;  // the rows whose target this thread owned
+    int accC = 0;
+    const int64_t nteams = static_cast<int64_t>(gridDim.x) * teams;
+    int64_t r = static_cast<int64_t>(blockIdx.x) * teams + team;
+    int64_t t_next = r < a.rows ? load_target(a, r) : 0;
+#pragma unroll 1
+    for (; r < a.rows; r += nteams) {
+        const int64_t t = t_next;
+        if (r + nteams < a.rows) t_next = load_target(a, r + nteams);
+        const bool counts = row_counts(a, t);
+        T* xrow = reinterpret_cast<T*>(a.x) + r * a.V;
+        uint4* rowv = reinterpret_cast<uint4*>(xrow);
+        if (!counts) {
+            // ignored row: exact +0 gradient without reading it
+            const bool lead = wr == 0 && lane == 0;
+            if (lead && t != a.ignore_index) atomicOr(&a.scratch->status, kDevErrTarget);
+            if (a.grad) {
+#pragma unroll
+                for (int k = 0; k < NVL; ++k)
+                    if (32 * k < vlim) rowv[vbase + 32 * k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (lead) {
+                if (a.reduction == kRedNone) {
+                    a.loss[r] = 0.f;
+                    if (a.want_z) a.zloss[r] = 0.f;
+                    if (a.want_acc) a.acc[r] = 0.f;
+                }
+                if (a.want_pred) a.pred[r] = -1;
+            }
+            continue;
+        }
+        // ---- the row into registers: vector vbase + 32 k
+        uint4 q[NVL];
+#pragma unroll
+        for (int k = 0; k < NVL; ++k)
+            q[k] = 32 * k < vlim ? rowv[vbase + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
+        const int tvec = static_cast<int>(t / VE);
+        const bool owner = lane == (tvec & 31) && wr == tvec / (32 * NVL);
+        const float xt = owner ? VT::load1(xrow, t) : 0.f;
+        const float wt = a.weight ? __ldg(a.weight + t) : 1.f;
+
+        // ---- 1. maximum of the raw logits
+        typename VT::MaxAcc macc = VT::max_init();
+#pragma unroll
+        for (int k = 0; k < NVL; ++k)
+            if (32 * k < vlim) macc = VT::max_fold(macc, q[k]);
+        const float lm = VT::max_value(macc);
+        __syncwarp();  // converged for the warp reductions
+        const float wm = warp_max_f32(lm);
+        float X = wm;
+        if (WPR > 1) {
+            if (lane == 0) red_a[warp] = wm;
+            team_sync();
+            X = warp_max_f32(lane < WPR ? red_a[w0 + lane] : -INFINITY);
+        }
+        int cand = INT_MAX;
+        if (want_arg) {
+            // first element of this thread equal to the row maximum (the
+            // thread's vectors come in increasing index order), by selects
+#pragma unroll
+            for (int k = NVL - 1; k >= 0; --k) {
+                float f[VE];
+                VT::unpack(q[k], f);
+#pragma unroll
+                for (int j = VE - 1; j >= 0; --j)
+                    cand = (32 * k < vlim && f[j] == X) ? (vbase + 32 * k) * VE + j : cand;
+            }
+        }
+        // softcap is monotone: the largest z is the cap of the largest x
+        const float M = SOFTCAP ? a.softcap * tanh_from_scaled(X * a.sc_k2) : X;
+        const float Ms = M == -INFINITY ? 0.f : M;
+        const float ML = Ms * kLog2e;
+
+        // ---- 2. S = sum exp(z - M), smoothing sum
+        float2 s2 = make_float2(0.f, 0.f), z2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NVL; ++k) {
+            if (32 * k < vlim) {
+                float f[VE], w[VE];
+                VT::unpack(q[k], f);
+                if (WS) reg_weights<VE>(a.weight, vbase + 32 * k, w);
+#pragma unroll
+                for (int j = 0; j < VE; j += 2) {
+                    float2 th;
+                    const float2 z = reg_z2<SOFTCAP>(f[j], f[j + 1], a, th);
+                    const float2 ar = reg_arg2<T>(z, Ms, ML);
+                    s2 = fadd2(s2, make_float2(ex2(ar.x), ex2(ar.y)));
+                    if (WS)
+                        z2 = ffma2(make_float2(w[j], w[j + 1]), z, z2);
+                    else if (smooth)
+                        z2 = fadd2(z2, z);
+                }
+            }
+        }
+        __syncwarp();  // the ragged tail diverges
+        float S = warp_sum(s2.x + s2.y);
+        float ZS = smooth ? warp_sum(z2.x + z2.y) : 0.f;
+        int I = cand;
+        if (want_arg) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) I = min(I, __shfl_xor_sync(0xffffffffu, I, o));
+        }
+        if (WPR > 1) {
+            if (lane == 0) {
+                red_b[warp] = S;
+                red_c[warp] = ZS;
+                red_i[warp] = I;
+            }
+            team_sync();
+            S = team_sum(red_b);
+            if (smooth) ZS = team_sum(red_c);
+            if (want_arg) {
+                I = lane < WPR ? red_i[w0 + lane] : INT_MAX;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) I = min(I, __shfl_xor_sync(0xffffffffu, I, o));
+            }
+        }
+        const float logS = logf(S);
+        const float lse = Ms + logS;
+        // the element count of the smoothing sum is V; with weights, the sum
+        // of w is W (sum (z - M) = sum z - V M, sum w (z - M) = sum wz - W M)
+        const float SZ = smooth ? fmaf(-Wtot, Ms, ZS) : 0.f;
+
+        // ---- row loss (the owner of the target's vector)
+        if (owner) {
+            const float zt = SOFTCAP ? a.softcap * tanh_from_scaled(xt * a.sc_k2) : xt;
+            float zl;
+            const float l = row_loss(a, Ms, logS, zt, wt, Wtot, SZ, zl);
+            const bool correct = static_cast<int64_t>(I) == t;
+            if (a.reduction == kRedNone) {
+                a.loss[r] = l;
+                if (a.want_z) a.zloss[r] = zl;
+                if (a.want_acc) a.acc[r] = correct ? 1.f : 0.f;
+            } else {
+                accL += l;
+                accZ += zl;
+                accC += correct ? 1 : 0;
+            }
+            if (a.want_pred) a.pred[r] = I;
+        }
+
+        // ---- 3. gradient in place
+        //   scale * [ (1-eps) w_t (p - onehot) + (eps/V)(W p - w) + 2 lam lse p ] * dz/dx
+        if (a.grad) {
+            need_counts();
+            const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;
+            const float As = scale * ((1.f - a.eps) * wt + a.eps * Wf + 2.f * a.lam * lse) / S;
+            const float Bc = -scale * a.eps * inv_V;
+#pragma unroll
+            for (int k = 0; k < NVL; ++k) {
+                if (32 * k < vlim) {
+                    float f[VE], g[VE], w[VE];
+                    VT::unpack(q[k], f);
+                    if (WS) reg_weights<VE>(a.weight, vbase + 32 * k, w);
+#pragma unroll
+                    for (int j = 0; j < VE; j += 2) {
+                        float2 th;
+                        const float2 z = reg_z2<SOFTCAP>(f[j], f[j + 1], a, th);
+                        const float2 ar = reg_arg2<T>(z, Ms, ML);
+                        const float2 bc = WS ? fmul2(make_float2(Bc, Bc), make_float2(w[j], w[j + 1]))
+                                             : make_float2(Bc, Bc);
+                        float2 gg = ffma2(make_float2(As, As), make_float2(ex2(ar.x), ex2(ar.y)), bc);
+                        if constexpr (SOFTCAP)
+                            gg = fmul2(gg, make_float2(fmaf(-th.x, th.x, 1.f), fmaf(-th.y, th.y, 1.f)));
+                        g[j] = gg.x;
+                        g[j + 1] = gg.y;
+                    }
+                    rowv[vbase + 32 * k] = VT::pack(g);
+                }
+            }
+            if (owner) {
+                // the one-hot term, over the element just stored
+                float et, fac = 1.f;
+                if (SOFTCAP) {
+                    const float tt = tanh_from_scaled(xt * a.sc_k2);
+                    fac = fmaf(-tt, tt, 1.f);
+                    et = ex2((a.softcap * tt - Ms) * kLog2e);
+                } else {
+                    et = ex2((xt - Ms) * kLog2e);
+                }
+                const float gt =
+                    (fmaf(As, et, WS ? Bc * wt : Bc) - scale * (1.f - a.eps) * wt) * fac;
+                VT::store1(xrow, t, gt);
+            }
+        }
+        // red_a is written again only after the next row's loads, by warps
+        // that passed this row's second team barrier, which every warp of
+        // the team reaches after reading red_a; red_b / red_c / red_i are
+        // read before the next row's first team barrier
+    }
+
+    if (a.reduction != kRedNone) {
+        need_counts();
+        // fixed-order CTA sum of the per-thread partials: a thread holds the
+        // rows whose target it owned, so the warp butterfly runs in fp32
+        // (the fp64 pipe is narrow on this GPU) and the warps' sums in fp64
+        float fl = accL, fz = accZ;
+        int ic = accC;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            fl += __shfl_xor_sync(0xffffffffu, fl, o);
+            fz += __shfl_xor_sync(0xffffffffu, fz, o);
+            ic += __shfl_xor_sync(0xffffffffu, ic, o);
+        }
+        __syncthreads();  // the row loop's last reads of the shared arrays
+        if (lane == 0) {
+            red_d[0][warp] = fl;
+            red_d[1][warp] = fz;
+            red_n[warp] = ic;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            double L = 0.0, Z = 0.0;
+            long long Cn = 0;
+            for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+                L += red_d[0][w];
+                Z += red_d[1][w];
+                Cn += red_n[w];
+            }
+            finish_scalars_2level(a, blockIdx.x, gridDim.x, L, Z, Cn, D, n_valid);
+        }
+    }
+}
+
+template <typename T, int NVL>
+const void* reg_kernel_of(bool softcap, bool ws) {
+    if (softcap)
+        return ws ? (const void*)&ce_fwd_reg<T, true, true, NVL>
+                  : (const void*)&ce_fwd_reg<T, true, false, NVL>;
+    return ws ? (const void*)&ce_fwd_reg<T, false, true, NVL>
+              : (const void*)&ce_fwd_reg<T, false, false, NVL>;
+}
+
+}  // namespace gbce

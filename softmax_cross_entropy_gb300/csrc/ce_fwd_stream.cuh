@@ -196,6 +196,7 @@ __device__ __forceinline__ float capped1(float x, const FwdArgs& a) {
 template <bool SOFTCAP>
 __device__ __forceinline__ RowSums warp_merge(float m, float S, float SZ, float n, float x, int i,
                                               bool smooth, const FwdArgs& a, int span = 32) {
+    __syncwarp();  // converged for the warp reductions
     const float X = warp_max_f32(x);
     const int I = warp_min_s32(x == X ? i : INT_MAX);
     const float M = capped1<SOFTCAP>(X, a);

@@ -169,7 +169,7 @@ ce_fwd_generic(const __grid_constant__ FwdArgs a) {
         // after its first barrier, which every thread reaches after reading
     }
     if (a.reduction != kRedNone && tid < 32)
-        finish_scalars(a, blockIdx.x, gridDim.x, accL, accZ, accC, D, n_valid);
+        finish_scalars_2level(a, blockIdx.x, gridDim.x, accL, accZ, accC, D, n_valid);
 }
 
 template <typename T>
@@ -253,6 +253,17 @@ const void* nd_bwd_kernel(int dtype) {
     if (dtype == 0) return (const void*)&ce_bwd_nd_scale<float>;
     if (dtype == 1) return (const void*)&ce_bwd_nd_scale<__nv_bfloat16>;
     if (dtype == 2) return (const void*)&ce_bwd_nd_scale<__half>;
+    return nullptr;
+}
+
+const void* reg_kernel_f32(bool softcap, bool ws, int nvl);
+const void* reg_kernel_bf16(bool softcap, bool ws, int nvl);
+const void* reg_kernel_f16(bool softcap, bool ws, int nvl);
+
+const void* reg_kernel(int dtype, bool softcap, bool ws, int nvl) {
+    if (dtype == 0) return reg_kernel_f32(softcap, ws, nvl);
+    if (dtype == 1) return reg_kernel_bf16(softcap, ws, nvl);
+    if (dtype == 2) return reg_kernel_f16(softcap, ws, nvl);
     return nullptr;
 }
 

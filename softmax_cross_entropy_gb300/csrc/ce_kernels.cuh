@@ -76,6 +76,7 @@ struct FwdArgs {
     // (r / inner) * C * inner + c * inner + r % inner
     int64_t inner;
     int nd_staged;  // 1: the N-D kernel keeps its tile in shared memory
+    int reg_wpr;    // register-resident kernel: warps a row team has
 };
 
 // Arguments of one forward call as the C ABI receives them (host side).
@@ -145,6 +146,16 @@ struct CountArgs {
     double* counts;  // out: {sum of w[t] over counted rows, counted rows}
     Scratch* scratch;
 };
+
+// Programmatic dependent launch: a kernel that produces what the next
+// launch on its stream needs lets that launch start early
+// (pdl_launch_dependents), and the next launch waits for the producer's
+// completion and memory (pdl_wait) only where it reads the result. Without
+// the launch attribute on the dependent launch both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ int64_t load_target(const FwdArgs& a, int64_t r) {
     return a.tgt64 ? reinterpret_cast<const int64_t*>(a.target)[r]
@@ -301,7 +312,10 @@ __device__ __forceinline__ float row_loss(const FwdArgs& a, float M, float logS,
     return (1.f - a.eps) * ce + a.eps * sm + zl;
 }
 
-// Epilogue for "sum" and "mean": each participating CTA publishes its
+// Epilogue for "sum" and "mean" for launches of a few hundred CTAs at most
+// (it keeps the hot loop's register allocation of the streaming and staged
+// kernels free of spills, which the two-level form below does not): each
+// participating CTA publishes its
 // partials; the last one to arrive (atomic ticket) adds them and writes the
 // scalar outputs, then resets the ticket for the next call. Called by all 32
 // lanes of one warp of each participating CTA; lane 0 holds the CTA's
@@ -348,6 +362,96 @@ __device__ __forceinline__ void finish_scalars(const FwdArgs& a, int64_t slot, i
     if (a.want_acc) a.acc[0] = static_cast<float>(static_cast<double>(C) / n_valid);
     s->ticket = 0u;
 }
+
+// Epilogue for "sum" and "mean" for launches of many CTAs, in two levels so
+// that no thread adds more than a few records one after another. Slots form groups of 32; each
+// participating CTA publishes its partials to its slot, and the last CTA of
+// a group to arrive (ticket in the group's record) adds the group's slots
+// (lane k: slot 32 g + k) with a fixed butterfly and publishes the total to
+// record nslots + g; the last group to finish (the scratch ticket) adds the
+// group totals (lane k: groups k, k + 32, ...) the same way and writes the
+// scalar outputs. Every sum has a fixed order, so the result does not
+// depend on which CTA finishes last. Uses nslots + ceil(nslots / 32)
+// records and resets every ticket it used. Called by all 32 lanes of one
+// warp of each participating CTA; lane 0 holds the CTA's partials.
+__device__ __forceinline__ void finish_scalars_2level(const FwdArgs& a, int64_t slot, int64_t nslots,
+                                               double l, double z, long long nc, float D,
+                                               int n_valid) {
+    Scratch* s = a.scratch;
+    const int lane = threadIdx.x & 31;
+    const int64_t ng = (nslots + 31) / 32;
+    const int64_t g = slot / 32;
+    const int gsize = static_cast<int>(nslots - g * 32 < 32 ? nslots - g * 32 : 32);
+    Partial* grec = &s->partials[nslots + g];
+    unsigned long long* gticket = reinterpret_cast<unsigned long long*>(&grec->pad);
+    int last = 0;
+    if (lane == 0) {
+        s->partials[slot].loss = l;
+        s->partials[slot].zloss = z;
+        s->partials[slot].n_correct = nc;
+        __threadfence();
+        last = atomicAdd(gticket, 1ull) == static_cast<unsigned long long>(gsize - 1);
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    double L = 0.0, Z = 0.0;
+    long long C = 0;
+    if (lane < gsize) {
+        const Partial* p = &s->partials[g * 32 + lane];
+        L = __ldcg(&p->loss);
+        Z = __ldcg(&p->zloss);
+        C = __ldcg(&p->n_correct);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        L += __shfl_xor_sync(0xffffffffu, L, o);
+        Z += __shfl_xor_sync(0xffffffffu, Z, o);
+        C += __shfl_xor_sync(0xffffffffu, C, o);
+    }
+    int glast = 0;
+    if (lane == 0) {
+        grec->loss = L;
+        grec->zloss = Z;
+        grec->n_correct = C;
+        *gticket = 0ull;
+        __threadfence();
+        glast = atomicAdd(&s->ticket, 1u) == static_cast<unsigned>(ng - 1);
+    }
+    if (!__shfl_sync(0xffffffffu, glast, 0)) return;
+    __threadfence();
+    L = 0.0;
+    Z = 0.0;
+    C = 0;
+    for (int64_t k = lane; k < ng; k += 32) {
+        const Partial* p = &s->partials[nslots + k];
+        L += __ldcg(&p->loss);
+        Z += __ldcg(&p->zloss);
+        C += __ldcg(&p->n_correct);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        L += __shfl_xor_sync(0xffffffffu, L, o);
+        Z += __shfl_xor_sync(0xffffffffu, Z, o);
+        C += __shfl_xor_sync(0xffffffffu, C, o);
+    }
+    if (lane != 0) return;
+    if (a.reduction == kRedMean) {
+        // no counted row: 0/0 = NaN, as the mean of an empty set
+        L = L / static_cast<double>(D);
+        Z = Z / static_cast<double>(D);
+    }
+    a.loss[0] = static_cast<float>(L);
+    if (a.want_z) a.zloss[0] = static_cast<float>(Z);
+    if (a.want_acc) a.acc[0] = static_cast<float>(static_cast<double>(C) / n_valid);
+    s->ticket = 0u;
+}
+
+// Partial-sum records a launch of `units` CTAs (or clusters) needs in the
+// scratch: one per CTA and one per group of 32 (finish_scalars).
+__host__ __device__ constexpr int64_t records_for(int64_t units) { return units + (units + 31) / 32; }
+// The most CTAs (or clusters) a launch with the library scratch may have.
+constexpr int64_t kMaxUnits = 3968;
+static_assert(records_for(kMaxUnits) <= kMaxPartials, "scratch records");
 
 // Adds two doubles over the CTAs of a grid in a fixed order (as
 // finish_scalars does): called by the 32 lanes of one warp of every CTA,
@@ -425,6 +529,11 @@ const void* stream_kernel_ws(int dtype, bool softcap);
 constexpr int kStreamMaxSlots = 48;   // ring slots (all groups) of the streaming kernel
 constexpr int kStreamMaxGroups = 8;
 const void* generic_kernel(int dtype, bool softcap);
+// register-resident kernel for rows of at most 64 KB: a team of WPR warps
+// owns a row, nvl (8 or 16) 16-byte vectors a thread; a CTA has one or more
+// teams, at most kRegMaxWarps warps
+const void* reg_kernel(int dtype, bool softcap, bool ws, int nvl);
+constexpr int kRegMaxWarps = 8;
 const void* count_kernel();
 // unfused kernels (dtype 0 fp32, 1 bf16, 2 fp16)
 const void* stream_kernel_lsm(int dtype);

@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(kLsmGenericThreads) ce_lsm_generic(const __gri
         const int64_t base = r * a.C;
         float m = -INFINITY;
         for (int64_t j = tid; j < a.C; j += NT) m = fmaxf(m, load_elem<T>(a.x, base + j));
+        __syncwarp();
         m = warp_max_f32(m);
         if ((tid & 31) == 0) sh[tid >> 5] = m;
         __syncthreads();

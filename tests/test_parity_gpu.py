@@ -371,7 +371,7 @@ def test_module_reduction_none_backward():
 
 # ------------------------------------------------------------------ kernel variants
 
-KINDS = {"staged": "1", "stream": "2", "general": "3"}
+KINDS = {"staged": "1", "stream": "2", "general": "3", "reg": "4"}
 
 
 @pytest.mark.parametrize("kind", sorted(KINDS) + ["stream8", "stream16"])
@@ -382,6 +382,8 @@ KINDS = {"staged": "1", "stream": "2", "general": "3"}
 def test_kernel_kinds(monkeypatch, kind, dtype, V, rows):
     if dtype == "f16" and kind == "staged":
         pytest.skip("the staged kernel has no fp16 variant")
+    if kind == "reg" and V * (4 if dtype == "f32" else 2) > 32768:
+        pytest.skip("the register-resident kernel takes rows of at most 32 KB")
     if kind in ("stream8", "stream16"):
         monkeypatch.setenv("GBCE_STREAM_WARPS", kind[6:])
         kind = "stream"
@@ -439,3 +441,65 @@ def test_stream_weighted_smoothing(monkeypatch, dtype, V, rows, twice):
                  dict(weight=True, label_smoothing=1.0, reduction="sum", ignore_frac=0.3)):
         case = workloads.random_case(90 + rows, rows, V, dtype=dtype, **opts)
         check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+@pytest.mark.parametrize("dtype,V,rows", [
+    ("bf16", 1024, 150),    # one warp a row
+    ("bf16", 4096, 300),    # the bench sweep's shortest row: 4 warps
+    ("bf16", 5000, 97),     # ragged: the last warp's vectors partly past the row
+    ("bf16", 16000, 40),    # 16 warps, the last vectors ragged
+    ("bf16", 16384, 33),    # 16 warps exactly
+    ("f32", 8192, 70),
+    ("f32", 6000, 21),
+    ("f32", 12, 33),        # three vectors: most threads hold nothing
+    ("f16", 8192, 50),
+])
+def test_register_kernel(monkeypatch, dtype, V, rows):
+    # the register-resident kernel (rows of at most 32 KB) forced, every
+    # option set, whole-batch comparison
+    monkeypatch.setenv("GBCE_KERNEL", "4")
+    for opts in (dict(),
+                 dict(label_smoothing=0.1, softcap=20.0, lse_square_scale=1e-3),
+                 dict(weight=True, reduction="none"),
+                 dict(weight=True, label_smoothing=0.05, reduction="sum"),
+                 dict(weight=True, label_smoothing=0.2, softcap=8.0, ignore_frac=0.3)):
+        case = workloads.random_case(110 + rows, rows, V, dtype=dtype, **opts)
+        check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+def test_register_kernel_ties_across_warps(monkeypatch):
+    # the row maximum repeated in several warps' vectors: the lowest index
+    # wins
+    monkeypatch.setenv("GBCE_KERNEL", "4")
+    case = workloads.random_case(5, 64, 16384, dtype="bf16")
+    x = case.x.copy()
+    top = workloads.f32_to_bf16_bits(np.array([60.0], np.float32))[0]
+    for r in range(case.rows):
+        cols = sorted({(r * 977) % 16384, (r * 977 + 4100) % 16384, (r * 977 + 9000) % 16384})
+        x[r, cols] = top
+    case = case.with_(x=x)
+    out, ref = check_full(case, want_acc=True, want_pred=True)
+    valid = case.target != case.ignore_index
+    firsts = np.array([min((r * 977) % 16384, (r * 977 + 4100) % 16384,
+                           (r * 977 + 9000) % 16384) for r in range(case.rows)])
+    assert np.array_equal(out["pred"][valid], firsts[valid])
+
+
+def test_register_kernel_unaligned_weights_fall_back(monkeypatch):
+    # class weights that do not start on a 16-byte boundary: the register
+    # kernel's vector weight loads are not used, the result is the same
+    case = workloads.random_case(7, 50, 4096, dtype="bf16", weight=True, label_smoothing=0.1)
+    import torch as _t
+    from softmax_cross_entropy_gb300 import _lib
+    x, t, w = to_device(case)
+    wbuf = _t.empty(case.V + 1, dtype=_t.float32, device="cuda")
+    wbuf[1:] = w
+    w_off = wbuf[1:]
+    loss = _t.empty(1, device="cuda")
+    rc = _lib.ce_fwd(x.data_ptr(), 1, case.rows, case.V, t.data_ptr(), w_off.data_ptr(), -100,
+                     0.1, 0.0, 0.0, 2, _lib.CE_FLAG_GRAD, loss.data_ptr(), None, None, None,
+                     _t.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    ref = oracle_full(case)
+    assert_loss_close(float(loss.item()), ref["loss"], "bf16")
+    assert_grad_close(grad_rows_f64(x), ref["grad"], "bf16")
