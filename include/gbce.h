@@ -142,11 +142,10 @@ ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V,
  * process exits) and allocates nothing.
  *
  * Arguments, outputs and results are those of ce_fwd. Differences:
- *  - The scratch holds 2048 partial-sum records: a launch uses one per CTA
- *    (or cluster) plus one per group of 32 of them; a launch that would
- *    need more returns CE_ERR_UNSUPPORTED and ce_last_error names the
- *    number. (On a GB300 no launch of this library has more than 8 CTAs
- *    per SM, 1216 in all, which need 1254 records.)
+ *  - The scratch holds 2048 partial-sum slots, one per CTA (or cluster) of
+ *    the launch; a launch that would need more returns CE_ERR_UNSUPPORTED
+ *    and ce_last_error names the number. (On a GB300 no launch of this
+ *    library uses more than 8 slots per SM, 1216 in all.)
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.

@@ -105,6 +105,7 @@ ce_fwd_nd(const __grid_constant__ FwdArgs a) {
     Raw* tile = reinterpret_cast<Raw*>(pos_pred + P);  // [C][32] when staged
     __shared__ double red_d[2 * NW];
     __shared__ long long red_n[NW];
+    __shared__ int s_flag;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -363,17 +364,18 @@ ce_fwd_nd(const __grid_constant__ FwdArgs a) {
             red_n[wy] = accC;
         }
         __syncthreads();
-        if (wy == 0) {
-            double L = 0.0, Z = 0.0;
-            long long Cn = 0;
+        double L = 0.0, Z = 0.0;
+        long long Cn = 0;
+        if (tid == 0) {
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
                 L += red_d[w];
                 Z += red_d[NW + w];
                 Cn += red_n[w];
             }
-            finish_scalars_2level(a, blockIdx.x, gridDim.x, L, Z, Cn, D, n_valid);
         }
+        __syncthreads();  // red_d is the epilogue's scratch next
+        finish_scalars_cta(a, L, Z, Cn, D, n_valid, &s_flag, red_d, red_d + NW, red_n);
     }
 }
 

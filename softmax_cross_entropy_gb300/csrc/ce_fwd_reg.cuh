@@ -86,6 +86,7 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     __shared__ int red_i[MW];
     __shared__ double red_d[2][MW];
     __shared__ long long red_n[MW];
+    __shared__ int s_flag;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -121,7 +122,9 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     // D = sum of w[t] over counted rows and the counted-row number come from
     // a.batch_counts ("sum" and "mean"): the caller's batch totals, or the
     // count kernel launched just before this one, which this launch
-    // overlaps (programmatic dependent launch) until it first needs them
+    // overlaps (programmatic dependent launch) until it first needs them.
+    // (Every CTA reading the batch's targets itself was slower: they all hit
+    // the same L2 lines at once.)
     float D = 0.f;
     int n_valid = 0;
     // "sum" without accuracy needs neither (and the host then launches no
@@ -363,16 +366,17 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             red_n[warp] = ic;
         }
         __syncthreads();
-        if (warp == 0) {
-            double L = 0.0, Z = 0.0;
-            long long Cn = 0;
+        double L = 0.0, Z = 0.0;
+        long long Cn = 0;
+        if (tid == 0) {
             for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
                 L += red_d[0][w];
                 Z += red_d[1][w];
                 Cn += red_n[w];
             }
-            finish_scalars_2level(a, blockIdx.x, gridDim.x, L, Z, Cn, D, n_valid);
         }
+        __syncthreads();  // red_d is the epilogue's scratch next
+        finish_scalars_cta(a, L, Z, Cn, D, n_valid, &s_flag, red_d[0], red_d[1], red_n);
     }
 }
 

@@ -168,8 +168,13 @@ ce_fwd_generic(const __grid_constant__ FwdArgs a) {
         // red_s, red_z, red_p are read above; the next row writes them only
         // after its first barrier, which every thread reaches after reading
     }
-    if (a.reduction != kRedNone && tid < 32)
-        finish_scalars_2level(a, blockIdx.x, gridDim.x, accL, accZ, accC, D, n_valid);
+    // thread 0 holds the CTA's sums (it formed every row's loss)
+    if (a.reduction != kRedNone) {
+        __shared__ double red_l[NW], red_zz[NW];
+        __shared__ long long red_cc[NW];
+        __shared__ int s_flag;
+        finish_scalars_cta(a, accL, accZ, accC, D, n_valid, &s_flag, red_l, red_zz, red_cc);
+    }
 }
 
 template <typename T>

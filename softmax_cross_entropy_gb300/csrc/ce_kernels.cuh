@@ -363,44 +363,42 @@ __device__ __forceinline__ void finish_scalars(const FwdArgs& a, int64_t slot, i
     s->ticket = 0u;
 }
 
-// Epilogue for "sum" and "mean" for launches of many CTAs, in two levels so
-// that no thread adds more than a few records one after another. Slots form groups of 32; each
-// participating CTA publishes its partials to its slot, and the last CTA of
-// a group to arrive (ticket in the group's record) adds the group's slots
-// (lane k: slot 32 g + k) with a fixed butterfly and publishes the total to
-// record nslots + g; the last group to finish (the scratch ticket) adds the
-// group totals (lane k: groups k, k + 32, ...) the same way and writes the
-// scalar outputs. Every sum has a fixed order, so the result does not
-// depend on which CTA finishes last. Uses nslots + ceil(nslots / 32)
-// records and resets every ticket it used. Called by all 32 lanes of one
-// warp of each participating CTA; lane 0 holds the CTA's partials.
-__device__ __forceinline__ void finish_scalars_2level(const FwdArgs& a, int64_t slot, int64_t nslots,
-                                               double l, double z, long long nc, float D,
-                                               int n_valid) {
+// Epilogue for "sum" and "mean" for launches of many CTAs, called by every
+// thread of every CTA (thread 0 holding the CTA's partials; `flag` a shared
+// int). Thread 0 publishes the partials to the CTA's slot and takes a ticket
+// with a release atomic; in the last CTA to arrive, thread t adds slots t,
+// t + nt, ... in order and a fixed warp butterfly and warp order combine the
+// threads, so the result does not depend on which CTA finishes last, and no
+// thread adds more than a few slots one after another.
+__device__ __forceinline__ void finish_scalars_cta(const FwdArgs& a, double l, double z,
+                                                   long long nc, float D, int n_valid,
+                                                   int* flag, double* red_l, double* red_z,
+                                                   long long* red_c) {
     Scratch* s = a.scratch;
-    const int lane = threadIdx.x & 31;
-    const int64_t ng = (nslots + 31) / 32;
-    const int64_t g = slot / 32;
-    const int gsize = static_cast<int>(nslots - g * 32 < 32 ? nslots - g * 32 : 32);
-    Partial* grec = &s->partials[nslots + g];
-    unsigned long long* gticket = reinterpret_cast<unsigned long long*>(&grec->pad);
-    int last = 0;
-    if (lane == 0) {
-        s->partials[slot].loss = l;
-        s->partials[slot].zloss = z;
-        s->partials[slot].n_correct = nc;
-        __threadfence();
-        last = atomicAdd(gticket, 1ull) == static_cast<unsigned long long>(gsize - 1);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = static_cast<int>(blockDim.x >> 5);
+    if (tid == 0) {
+        Partial* p = &s->partials[blockIdx.x];
+        p->loss = l;
+        p->zloss = z;
+        p->n_correct = nc;
+        unsigned t;
+        // release: the slot is visible before the ticket moves; acquire: the
+        // last CTA sees every slot
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;"
+                     : "=r"(t)
+                     : "l"(&s->ticket)
+                     : "memory");
+        *flag = t == gridDim.x - 1;
     }
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    __threadfence();
+    __syncthreads();
+    if (!*flag) return;
     double L = 0.0, Z = 0.0;
     long long C = 0;
-    if (lane < gsize) {
-        const Partial* p = &s->partials[g * 32 + lane];
-        L = __ldcg(&p->loss);
-        Z = __ldcg(&p->zloss);
-        C = __ldcg(&p->n_correct);
+    for (unsigned c = tid; c < gridDim.x; c += blockDim.x) {
+        L += __ldcg(&s->partials[c].loss);
+        Z += __ldcg(&s->partials[c].zloss);
+        C += __ldcg(&s->partials[c].n_correct);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -408,33 +406,21 @@ __device__ __forceinline__ void finish_scalars_2level(const FwdArgs& a, int64_t 
         Z += __shfl_xor_sync(0xffffffffu, Z, o);
         C += __shfl_xor_sync(0xffffffffu, C, o);
     }
-    int glast = 0;
     if (lane == 0) {
-        grec->loss = L;
-        grec->zloss = Z;
-        grec->n_correct = C;
-        *gticket = 0ull;
-        __threadfence();
-        glast = atomicAdd(&s->ticket, 1u) == static_cast<unsigned>(ng - 1);
+        red_l[warp] = L;
+        red_z[warp] = Z;
+        red_c[warp] = C;
     }
-    if (!__shfl_sync(0xffffffffu, glast, 0)) return;
-    __threadfence();
+    __syncthreads();
+    if (tid != 0) return;
     L = 0.0;
     Z = 0.0;
     C = 0;
-    for (int64_t k = lane; k < ng; k += 32) {
-        const Partial* p = &s->partials[nslots + k];
-        L += __ldcg(&p->loss);
-        Z += __ldcg(&p->zloss);
-        C += __ldcg(&p->n_correct);
+    for (int w = 0; w < nw; ++w) {
+        L += red_l[w];
+        Z += red_z[w];
+        C += red_c[w];
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        L += __shfl_xor_sync(0xffffffffu, L, o);
-        Z += __shfl_xor_sync(0xffffffffu, Z, o);
-        C += __shfl_xor_sync(0xffffffffu, C, o);
-    }
-    if (lane != 0) return;
     if (a.reduction == kRedMean) {
         // no counted row: 0/0 = NaN, as the mean of an empty set
         L = L / static_cast<double>(D);
@@ -447,11 +433,10 @@ __device__ __forceinline__ void finish_scalars_2level(const FwdArgs& a, int64_t 
 }
 
 // Partial-sum records a launch of `units` CTAs (or clusters) needs in the
-// scratch: one per CTA and one per group of 32 (finish_scalars).
-__host__ __device__ constexpr int64_t records_for(int64_t units) { return units + (units + 31) / 32; }
+// scratch: one per CTA (or cluster).
+__host__ __device__ constexpr int64_t records_for(int64_t units) { return units; }
 // The most CTAs (or clusters) a launch with the library scratch may have.
-constexpr int64_t kMaxUnits = 3968;
-static_assert(records_for(kMaxUnits) <= kMaxPartials, "scratch records");
+constexpr int64_t kMaxUnits = kMaxPartials;
 
 // Adds two doubles over the CTAs of a grid in a fixed order (as
 // finish_scalars does): called by the 32 lanes of one warp of every CTA,
