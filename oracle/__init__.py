@@ -71,6 +71,8 @@ def _load():
             lib.orc_bf16_to_double.restype = d
             lib.orc_f16_to_double.argtypes = [ctypes.c_uint16]
             lib.orc_f16_to_double.restype = d
+            lib.orc_decode.argtypes = [P, ctypes.c_int, i64, P]
+            lib.orc_decode.restype = None
             ci = ctypes.c_int
             lib.ao_log_softmax.argtypes = [P, i64, i64, P]
             lib.ao_nll_forward.argtypes = [P, P, P, i64, i64, i64, ci, P, P]
@@ -204,6 +206,53 @@ def backward(grad, grad_output):
     per_row = 1 if go.shape[0] == grad.shape[0] and go.shape[0] != 1 else 0
     lib.orc_ce_backward(_ptr(grad), grad.shape[0], grad.shape[1], _ptr(go), per_row)
     return grad
+
+
+def decode(x, dtype):
+    """The stored values of an array (``"f64"``, ``"f32"``, or bf16 / fp16 bit
+    patterns) as float64, exactly."""
+    if dtype not in _DTYPES:
+        raise ValueError(f"unknown storage {dtype!r}")
+    x = np.ascontiguousarray(x, dtype=_NP_STORAGE[dtype])
+    out = np.empty(x.shape, np.float64)
+    _load().orc_decode(_ptr(x), _DTYPES[dtype], x.size, _ptr(out))
+    return out
+
+
+def flce_forward(hidden, lm_weight, target, *, dtype="f64", bias=None, weight=None,
+                 ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0, softcap=None,
+                 reduction="mean", want_grad=True):
+    """Fused linear cross-entropy ("Kernel Profile: CrossEntropy",
+    closest_existing_kernel: fused_linear_cross_entropy, the cross-entropy
+    kernel with the linear layer fused in): the cross-entropy of the logits
+    hidden @ lm_weight^T (+ bias), by definition. hidden [rows, H] and
+    lm_weight [V, H] in storage ``dtype`` (decoded exactly), bias [V] float
+    or None; ``weight`` is the class weight of the cross-entropy. The logits
+    are formed in float64 and handed to forward(); with want_grad the chain
+    rule gives grad_hidden = G @ lm_weight, grad_weight = G^T @ hidden and
+    grad_bias = the column sums of G, G the gradient forward() returns
+    (that of the reduced loss; for "none", of the sum of the row losses)."""
+    h = decode(hidden, dtype)
+    w = decode(lm_weight, dtype)
+    if h.ndim != 2 or w.ndim != 2 or h.shape[1] != w.shape[1]:
+        raise OracleError("hidden [rows, H] and lm_weight [V, H] expected")
+    logits = h @ w.T
+    if bias is not None:
+        b = np.ascontiguousarray(bias, dtype=np.float64).reshape(-1)
+        if b.shape[0] != w.shape[0]:
+            raise OracleError("bias must have V entries")
+        logits = logits + b[None, :]
+    r = forward(logits, target, dtype="f64", weight=weight, ignore_index=ignore_index,
+                label_smoothing=label_smoothing, lse_square_scale=lse_square_scale,
+                softcap=softcap, reduction=reduction, want_grad=want_grad)
+    out = dict(r)
+    out["logits"] = logits
+    if want_grad:
+        g = r["grad"]
+        out["grad_hidden"] = g @ w
+        out["grad_weight"] = g.T @ h
+        out["grad_bias"] = g.sum(axis=0)
+    return out
 
 
 def bf16_to_double(bits: int) -> float:

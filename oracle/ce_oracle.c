@@ -370,3 +370,8 @@ double orc_bf16_to_double(uint16_t bits) { return bf16_bits_to_double(bits); }
 /* Exposes the fp16 decoding so that a test can pin it against every bit
  * pattern. */
 double orc_f16_to_double(uint16_t bits) { return f16_bits_to_double(bits); }
+
+/* Decodes n stored values (dtype as for the logits) into doubles, exactly. */
+void orc_decode(const void* x, int dtype, int64_t n, double* out) {
+    for (int64_t k = 0; k < n; ++k) out[k] = logit(x, dtype, k);
+}
