@@ -406,6 +406,8 @@ def run_gpu(args):
             "ops": measure_unfused(workloads.tt_fp32(seed=rank), device, torch, K, barrier,
                                    max_over_ranks, peak)}
 
+        line["flce"] = measure_flce(device, torch, barrier, max_over_ranks, rank)
+
     if clocks:
         line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -414,6 +416,72 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s of this GPU (sustained: a step of milliseconds)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1700.0, "fallback"
+
+
+def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5):
+    """Fused linear cross-entropy (ce_flce) forward + gradients on
+    rows = 4096 (B=8, T=512), H = 4096, V = 128256 bf16, mean: time per step
+    (CUDA events, eager: a step is milliseconds) and tensor throughput over
+    the three GEMMs' 6 rows V H flops, against the measured bf16 peak."""
+    from softmax_cross_entropy_gb300 import _lib
+    rows, H, V = 4096, 4096, 128256
+    g = torch.Generator(device="cpu").manual_seed(1000 + rank)
+    hidden = torch.randn(rows, H, generator=g).to(device=device, dtype=torch.bfloat16)
+    lm_w = (torch.randn(V, H, generator=g) * (3.0 / H ** 0.5)).to(device=device,
+                                                                  dtype=torch.bfloat16)
+    target = torch.randint(0, V, (rows,), generator=g, dtype=torch.int32)
+    target[torch.randperm(rows, generator=g)[: rows // 20]] = -100
+    target = target.to(device)
+    loss = torch.empty(1, dtype=torch.float32, device=device)
+    gh = torch.empty_like(hidden)
+    gw = torch.empty(V, H, dtype=torch.float32, device=device)
+    nbytes = _lib.ce_flce_workspace_bytes(_lib.CE_BF16, rows, V, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    st = torch.cuda.current_stream(device).cuda_stream
+
+    def step():
+        rc = _lib.ce_flce(hidden.data_ptr(), lm_w.data_ptr(), None, _lib.CE_BF16, rows, H, V,
+                          target.data_ptr(), None, -100, 0.0, 0.0, 0.0, _lib.CE_RED_MEAN,
+                          _lib.CE_FLAG_GRAD, loss.data_ptr(), None, None, None, gh.data_ptr(),
+                          gw.data_ptr(), None, 0, ws.data_ptr(), nbytes, st)
+        if rc != 0:
+            raise RuntimeError(f"ce_flce: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(device)
+    barrier()
+    t = max_over_ranks(e0.elapsed_time(e1) / 1e3) / steps
+    flops = 6.0 * rows * V * H
+    peak_t, kind = measured_tensor_peak()
+    out = {"workload": f"rows={rows} (B=8, T=512), H={H}, V={V} bf16 hidden and lm_weight, "
+                       f"5% ignored, mean; logits, grad_hidden and grad_weight (fp32)",
+           "ms_per_step": round(t * 1e3, 3), "TFLOP/s": round(flops / t / 1e12, 1),
+           "frac": round(flops / t / 1e12 / peak_t, 4), "peak_TFLOP/s": peak_t,
+           "peak_kind": kind + " (bf16, sustained)",
+           "chunk_rows": max(1, (1 << 29) // (V * 4)),
+           "gemms": "cuBLAS (bf16 in, fp32 accumulate)"}
+    del hidden, lm_w, gh, gw, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_unfused(case, device, torch, K, barrier, max_over_ranks, peak):

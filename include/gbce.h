@@ -62,6 +62,7 @@
 #ifndef GBCE_H
 #define GBCE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -243,6 +244,59 @@ ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, int64_t inner
  */
 ce_status ce_bwd_nd(const float* grad_output, int grad_per_position, void* dlogits,
                     int dtype, int64_t N, int64_t C, int64_t inner, ce_stream_t stream);
+
+/*
+ * ce_flce - fused linear cross-entropy: the cross-entropy (as ce_fwd
+ * defines it) of the logits hidden @ lm_weight^T + bias, with the gradients
+ * of hidden, lm_weight and bias, without materialising more than one chunk
+ * of rows of logits ("Kernel Profile: CrossEntropy", closest_existing_kernel:
+ * fused_linear_cross_entropy, the cross-entropy kernel extended with the
+ * linear layer).
+ *
+ * hidden       [rows, H] row-major, dtype CE_BF16, CE_F16 or CE_F32.
+ * lm_weight    [V, H] row-major, same dtype.
+ * bias         [V] fp32, or NULL.
+ * target, class_weight, ignore_index, label_smoothing, lse_square_scale,
+ * softcap, reduction, flags, loss, z_loss, acc, pred
+ *              as for ce_fwd over the [rows, V] logits. With CE_FLAG_GRAD the
+ *              gradients of the reduced loss (for "none", of the sum of the
+ *              row losses) are written to the non-NULL ones of:
+ * grad_hidden  [rows, H] in dtype;
+ * grad_weight  [V, H] fp32 (overwritten, not accumulated into);
+ * grad_bias    [V] fp32.
+ * chunk_rows   rows per chunk (<= 0: about 512 MB of fp32 logits a chunk).
+ * workspace    device memory of at least ce_flce_workspace_bytes(dtype,
+ *              rows, V, chunk_rows) bytes, 256-byte aligned, owned by the
+ *              caller; it holds one chunk of fp32 logits (and of the gradient
+ *              in dtype) and the chunks' partial sums.
+ * Per chunk: logits by a tensor-core GEMM (cuBLAS; inputs in dtype, fp32
+ * accumulation and output), the fused forward of this library in place
+ * over them (one shard of the batch, D from ce_count), the gradient rounded
+ * to dtype, then grad_hidden = G @ lm_weight and grad_weight += G^T @ hidden
+ * (cuBLAS, fp32 accumulation) and grad_bias += column sums. Scalars are
+ * added in chunk order: deterministic. Asynchronous on `stream`; uses the
+ * library scratch of (device, stream) and a cuBLAS handle per device.
+ * Errors as for ce_fwd; CE_ERR_INVALID_ARG also for a missing or too small
+ * workspace.
+ */
+size_t ce_flce_workspace_bytes(int dtype, int64_t rows, int64_t V, int64_t chunk_rows);
+
+ce_status ce_flce(const void* hidden, const void* lm_weight, const float* bias, int dtype,
+                  int64_t rows, int64_t H, int64_t V, const void* target,
+                  const float* class_weight, int64_t ignore_index, float label_smoothing,
+                  float lse_square_scale, float softcap, int reduction, uint32_t flags,
+                  float* loss, float* z_loss, float* acc, int64_t* pred, void* grad_hidden,
+                  float* grad_weight, float* grad_bias, int64_t chunk_rows, void* workspace,
+                  size_t workspace_bytes, ce_stream_t stream);
+
+/*
+ * ce_scale_round - out[i] = in[i] * grad_output[0], rounded to nearest-even
+ * into dtype (the backward of ce_flce's fp32 weight gradient for a weight
+ * stored in dtype). in [n] fp32, grad_output one fp32 value, out [n] dtype;
+ * device pointers; out may equal in only for CE_F32.
+ */
+ce_status ce_scale_round(const float* in, const float* grad_output, void* out, int dtype,
+                         int64_t n, ce_stream_t stream);
 
 /*
  * The unfused form: the four aten ops a decomposed F.cross_entropy graph

@@ -26,13 +26,15 @@ from collections import namedtuple
 import torch
 
 from . import _lib
-from ._lib import (CEError, ce_bwd, ce_bwd_nd, ce_count, ce_device_status, ce_fwd,
-                   ce_fwd_nd, ce_fwd_shard, ce_last_error, ce_status_string)
+from ._lib import (CEError, ce_bwd, ce_bwd_nd, ce_count, ce_device_status, ce_flce,
+                   ce_flce_workspace_bytes, ce_fwd, ce_fwd_nd, ce_fwd_shard, ce_last_error,
+                   ce_scale_round, ce_status_string)
 
 __all__ = ["cross_entropy", "CrossEntropyLoss", "CrossEntropyFunction", "CrossEntropyOutput",
            "CEError", "device_status", "shard_counts", "ce_fwd", "ce_fwd_shard", "ce_count",
-           "ce_bwd", "ce_fwd_nd", "ce_bwd_nd", "ce_device_status", "ce_status_string",
-           "ce_last_error"]
+           "ce_bwd", "ce_fwd_nd", "ce_bwd_nd", "ce_flce", "ce_flce_workspace_bytes",
+           "ce_scale_round", "ce_device_status", "ce_status_string", "ce_last_error",
+           "fused_linear_cross_entropy", "FusedLinearCrossEntropyFunction"]
 
 CrossEntropyOutput = namedtuple("CrossEntropyOutput",
                                 ["loss", "z_loss", "token_accuracy", "predicted_tokens"])
@@ -206,6 +208,137 @@ def cross_entropy(logits, target, weight=None, ignore_index=-100, lse_square_sca
     loss, z_loss, acc, pred = CrossEntropyFunction.apply(
         logits, target, weight, ignore_index, lse_square_scale, label_smoothing, reduction,
         softcap, return_z_loss, return_token_accuracy, return_predicted_tokens, batch_counts)
+    if return_z_loss or return_token_accuracy or return_predicted_tokens:
+        return CrossEntropyOutput(loss, z_loss, acc, pred)
+    return loss
+
+
+def _flce_call(hidden, lm_weight, target, bias, weight, ignore_index, lse_square_scale,
+               label_smoothing, reduction, softcap, want_z, want_acc, want_pred, want_grad,
+               chunk_rows):
+    """Runs ce_flce; returns (loss, z_loss, acc, pred, grad_hidden, grad_weight (fp32),
+    grad_bias (fp32)), the gradients None unless want_grad."""
+    dev = hidden.device
+    dt = _DTYPES[hidden.dtype]
+    rows, H = hidden.shape
+    V = lm_weight.shape[0]
+    red = _REDUCTIONS[reduction]
+    out_shape = (rows,) if red == _lib.CE_RED_NONE else ()
+    f32 = dict(dtype=torch.float32, device=dev)
+    loss = torch.empty(out_shape, **f32)
+    z_loss = torch.empty(out_shape, **f32) if want_z else None
+    acc = torch.empty(out_shape, **f32) if want_acc else None
+    pred = torch.empty((rows,), dtype=torch.int64, device=dev) if want_pred else None
+    gh = torch.empty_like(hidden) if want_grad else None
+    gw = torch.empty((V, H), **f32) if want_grad else None
+    gb = torch.empty((V,), **f32) if (want_grad and bias is not None) else None
+    nbytes = ce_flce_workspace_bytes(dt, rows, V, int(chunk_rows))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)  # 256-byte aligned by the allocator
+    flags = ((_lib.CE_FLAG_GRAD if want_grad else 0) | (_lib.CE_FLAG_Z_LOSS if want_z else 0) |
+             (_lib.CE_FLAG_ACC if want_acc else 0) | (_lib.CE_FLAG_PRED if want_pred else 0) |
+             (_lib.CE_FLAG_TARGET_I64 if target.dtype == torch.int64 else 0))
+    b = None if bias is None else bias.to(torch.float32).contiguous()
+    w = None if weight is None else weight.to(torch.float32).contiguous()
+    with torch.cuda.device(dev):
+        rc = ce_flce(_ptr(hidden), _ptr(lm_weight), _ptr(b), dt, rows, H, V, _ptr(target),
+                     _ptr(w), int(ignore_index), float(label_smoothing), float(lse_square_scale),
+                     float(softcap) if softcap is not None else 0.0, red, flags, _ptr(loss),
+                     _ptr(z_loss), _ptr(acc), _ptr(pred), _ptr(gh), _ptr(gw), _ptr(gb),
+                     int(chunk_rows), _ptr(ws), nbytes, _stream(dev))
+    if rc != _lib.CE_OK:
+        raise CEError(rc, "ce_flce")
+    return loss, z_loss, acc, pred, gh, gw, gb
+
+
+class FusedLinearCrossEntropyFunction(torch.autograd.Function):
+    """Autograd wrapper of ce_flce: the forward computes the gradients of the
+    reduced loss along with it (one chunk of logits at a time); backward
+    scales them by the scalar grad_output in the library's kernels."""
+
+    @staticmethod
+    def forward(ctx, hidden, lm_weight, target, bias, weight, ignore_index, lse_square_scale,
+                label_smoothing, reduction, softcap, return_z_loss, return_acc, return_pred,
+                chunk_rows):
+        want_grad = hidden.requires_grad or lm_weight.requires_grad or (
+            bias is not None and bias.requires_grad)
+        if want_grad and reduction == "none":
+            raise ValueError("fused_linear_cross_entropy differentiates a scalar loss: use "
+                             "reduction 'mean' or 'sum' (or no gradient)")
+        loss, z_loss, acc, pred, gh, gw, gb = _flce_call(
+            hidden, lm_weight, target, bias, weight, ignore_index, lse_square_scale,
+            label_smoothing, reduction, softcap, return_z_loss, return_acc, return_pred,
+            want_grad, chunk_rows)
+        ctx.w_dtype = lm_weight.dtype
+        ctx.has_bias = bias is not None
+        if want_grad:
+            ctx.save_for_backward(gh, gw, gb if gb is not None else torch.empty(0))
+        extras = [t for t in (z_loss, acc, pred) if t is not None]
+        if extras:
+            ctx.mark_non_differentiable(*extras)
+        return loss, z_loss, acc, pred
+
+    @staticmethod
+    def backward(ctx, grad_loss, *unused):
+        gh, gw, gb = ctx.saved_tensors
+        g = grad_loss.to(torch.float32).reshape(1).contiguous()
+        dev = gh.device
+        with torch.cuda.device(dev):
+            st = _stream(dev)
+            rows, H = gh.shape
+            rc = ce_bwd(_ptr(g), 0, _ptr(gh), _DTYPES[gh.dtype], rows, H, st)
+            if rc != _lib.CE_OK:
+                raise CEError(rc, "ce_bwd")
+            gw_out = torch.empty(gw.shape, dtype=ctx.w_dtype, device=dev)
+            rc = ce_scale_round(_ptr(gw), _ptr(g), _ptr(gw_out), _DTYPES[ctx.w_dtype],
+                                gw.numel(), st)
+            if rc != _lib.CE_OK:
+                raise CEError(rc, "ce_scale_round")
+            gb_out = None
+            if ctx.has_bias:
+                rc = ce_bwd(_ptr(g), 0, _ptr(gb), _lib.CE_F32, 1, gb.numel(), st)
+                if rc != _lib.CE_OK:
+                    raise CEError(rc, "ce_bwd")
+                gb_out = gb
+        return (gh, gw_out, None, gb_out, None, None, None, None, None, None, None, None, None,
+                None)
+
+
+def fused_linear_cross_entropy(hidden, lm_weight, target, bias=None, weight=None,
+                               ignore_index=-100, lse_square_scale=0.0, label_smoothing=0.0,
+                               reduction="mean", softcap=None, return_z_loss=False,
+                               return_token_accuracy=False, return_predicted_tokens=False,
+                               chunk_rows=0):
+    """Cross-entropy of the logits hidden @ lm_weight^T + bias (the profile's
+    closest_existing_kernel, fused_linear_cross_entropy) without forming all
+    logits: ce_flce, one chunk of rows at a time. hidden [rows, H] and
+    lm_weight [V, H] in float32, bfloat16 or float16; bias [V] or None;
+    the other arguments as for cross_entropy. Returns the loss, or a
+    CrossEntropyOutput when a return_* flag is set."""
+    if not (isinstance(hidden, torch.Tensor) and isinstance(lm_weight, torch.Tensor)):
+        raise TypeError("hidden and lm_weight must be tensors")
+    if hidden.dim() != 2 or lm_weight.dim() != 2 or hidden.shape[1] != lm_weight.shape[1]:
+        raise ValueError("hidden must be [rows, H] and lm_weight [V, H]")
+    if not hidden.is_cuda or lm_weight.device != hidden.device:
+        raise ValueError("hidden and lm_weight must be on one CUDA device")
+    if hidden.dtype not in _DTYPES or lm_weight.dtype != hidden.dtype:
+        raise TypeError("hidden and lm_weight must share one of float32, bfloat16, float16")
+    if target.dim() != 1 or target.shape[0] != hidden.shape[0]:
+        raise ValueError("target must be 1-D with one label per row of hidden")
+    if target.dtype not in (torch.int32, torch.int64) or target.device != hidden.device:
+        raise TypeError("target must be an int32 or int64 tensor on the hidden's device")
+    if reduction not in _REDUCTIONS:
+        raise ValueError(f"reduction must be one of {sorted(_REDUCTIONS)}")
+    if not 0.0 <= label_smoothing <= 1.0:
+        raise ValueError("label_smoothing must lie in [0, 1]")
+    if softcap is not None and not softcap > 0:
+        raise ValueError("softcap must be positive or None")
+    hidden = hidden.contiguous()
+    lm_weight = lm_weight.contiguous()
+    target = target.contiguous()
+    loss, z_loss, acc, pred = FusedLinearCrossEntropyFunction.apply(
+        hidden, lm_weight, target, bias, weight, ignore_index, lse_square_scale,
+        label_smoothing, reduction, softcap, return_z_loss, return_token_accuracy,
+        return_predicted_tokens, chunk_rows)
     if return_z_loss or return_token_accuracy or return_predicted_tokens:
         return CrossEntropyOutput(loss, z_loss, acc, pred)
     return loss

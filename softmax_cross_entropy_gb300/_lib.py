@@ -30,6 +30,10 @@ SIGNATURES = {
     "ce_fwd_nd": (_I, [_P, _I, _I64, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P, _P,
                        _P, _P]),
     "ce_bwd_nd": (_I, [_P, _I, _P, _I, _I64, _I64, _I64, _P]),
+    "ce_flce_workspace_bytes": (ctypes.c_size_t, [_I, _I64, _I64, _I64]),
+    "ce_scale_round": (_I, [_P, _P, _P, _I, _I64, _P]),
+    "ce_flce": (_I, [_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P,
+                     _P, _P, _P, _P, _P, _I64, _P, ctypes.c_size_t, _P]),
     "ce_bwd": (_I, [_P, _I, _P, _I, _I64, _I64, _P]),
     "ce_log_softmax": (_I, [_P, _P, _I, _I64, _I64, _P]),
     "ce_nll_loss_fwd": (_I, [_P, _I, _I64, _I64, _P, _P, _I64, _I, _U32, _P, _P, _P]),
@@ -106,6 +110,24 @@ def ce_fwd_nd(logits, dtype, N, C, inner, target, weight, ignore_index, label_sm
 
 def ce_bwd_nd(grad_output, grad_per_position, dlogits, dtype, N, C, inner, stream):
     return load().ce_bwd_nd(grad_output, grad_per_position, dlogits, dtype, N, C, inner, stream)
+
+
+def ce_flce_workspace_bytes(dtype, rows, V, chunk_rows):
+    return load().ce_flce_workspace_bytes(dtype, rows, V, chunk_rows)
+
+
+def ce_flce(hidden, lm_weight, bias, dtype, rows, H, V, target, class_weight, ignore_index,
+            label_smoothing, lse_square_scale, softcap, reduction, flags, loss, z_loss, acc,
+            pred, grad_hidden, grad_weight, grad_bias, chunk_rows, workspace, workspace_bytes,
+            stream):
+    return load().ce_flce(hidden, lm_weight, bias, dtype, rows, H, V, target, class_weight,
+                          ignore_index, label_smoothing, lse_square_scale, softcap, reduction,
+                          flags, loss, z_loss, acc, pred, grad_hidden, grad_weight, grad_bias,
+                          chunk_rows, workspace, workspace_bytes, stream)
+
+
+def ce_scale_round(inp, grad_output, out, dtype, n, stream):
+    return load().ce_scale_round(inp, grad_output, out, dtype, n, stream)
 
 
 def ce_bwd(grad_output, grad_per_row, dlogits, dtype, rows, V, stream):

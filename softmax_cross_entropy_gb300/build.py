@@ -4,7 +4,8 @@
 
 Each .cu file under csrc/ is compiled by its own nvcc process, in parallel,
 then linked into softmax_cross_entropy_gb300/libgbce.so. The CUDA runtime is
-linked statically, so the library needs only the NVIDIA driver at run time.
+linked statically; cuBLAS (the plain GEMMs of the fused linear
+cross-entropy) dynamically, from the toolkit's lib64 (recorded as rpath).
 """
 from __future__ import annotations
 
@@ -76,7 +77,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if err.strip():
                 print(f"== {os.path.basename(obj)}\n{err}", file=sys.stderr)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static"]
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static",
+           "-L" + cuda_lib, "-lcublas", "-Xlinker", "-rpath=" + cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")

@@ -631,6 +631,9 @@ ce_status fwd_with_scratch(Scratch* scratch, int max_slots, const FwdCall& c, cu
 // Records a CUDA error for ce_last_error (for the static-scratch entry point).
 ce_status record_cuda_failure(cudaError_t e, const char* what) { return cuda_failure(e, what); }
 
+// Records a message for ce_last_error.
+void record_message(const std::string& msg) { g_last_error = msg; }
+
 }  // namespace gbce
 
 extern "C" ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V, const void* target,
