@@ -71,10 +71,16 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources the headline workload's forward kernel is built from: a change
+# to any of them voids the DRAM traffic recorded for it
+HEADLINE_KERNEL_SOURCES = ("ce_fwd_stream.cuh", "ce_fwd_stream.cu", "ce_kernels.cuh",
+                           "ce_device.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "softmax_cross_entropy_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in HEADLINE_KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
