@@ -463,19 +463,28 @@ def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5):
         if rc != 0:
             raise RuntimeError(f"ce_flce: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize(device)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize(device)
-    barrier()
-    t = max_over_ranks(e0.elapsed_time(e1) / 1e3) / steps
+    def timed():
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(device)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize(device)
+        barrier()
+        return max_over_ranks(e0.elapsed_time(e1) / 1e3) / steps
+
+    t = timed()
+    # the same step with the logits GEMM on this library's tcgen05 kernel
+    os.environ["GBCE_FLCE_GEMM"] = "tcgen05"
+    try:
+        t_tc = timed()
+    finally:
+        os.environ.pop("GBCE_FLCE_GEMM", None)
     flops = 6.0 * rows * V * H
     peak_t, kind = measured_tensor_peak()
     out = {"workload": f"rows={rows} (B=8, T=512), H={H}, V={V} bf16 hidden and lm_weight, "
@@ -484,7 +493,11 @@ def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5):
            "frac": round(flops / t / 1e12 / peak_t, 4), "peak_TFLOP/s": peak_t,
            "peak_kind": kind + " (bf16, sustained)",
            "chunk_rows": max(1, (1 << 29) // (V * 4)),
-           "gemms": "cuBLAS (bf16 in, fp32 accumulate)"}
+           "gemms": "cuBLAS (bf16 in, fp32 accumulate)",
+           "tcgen05_logits": {"ms_per_step": round(t_tc * 1e3, 3),
+                              "TFLOP/s": round(flops / t_tc / 1e12, 1),
+                              "gemms": "logits GEMM on ce_gemm_abt (tcgen05), the two "
+                                       "gradient GEMMs on cuBLAS"}}
     del hidden, lm_w, gh, gw, ws
     torch.cuda.empty_cache()
     return out

@@ -290,6 +290,19 @@ ce_status ce_flce(const void* hidden, const void* lm_weight, const float* bias, 
                   size_t workspace_bytes, ce_stream_t stream);
 
 /*
+ * ce_gemm_abt - C = A @ B^T (+ bias), the logits GEMM of ce_flce, on the
+ * tensor cores (tcgen05, operands staged by TMA, fp32 accumulator in tensor
+ * memory). A [M, K] and B [N, K] row-major in CE_BF16 or CE_F16 with
+ * 16-byte aligned bases and K a multiple of 8 (else CE_ERR_UNSUPPORTED);
+ * C [M, N] fp32 row-major, written; bias [N] fp32 or NULL. The method has
+ * no counterpart: it is the linear layer the fused linear cross-entropy
+ * folds in. A bounded wait that gives up records CE_ERR_TIMEOUT for
+ * ce_device_status (that call's C is then invalid).
+ */
+ce_status ce_gemm_abt(const void* A, const void* B, int dtype, int64_t M, int64_t N,
+                      int64_t K, float* C, const float* bias, ce_stream_t stream);
+
+/*
  * ce_scale_round - out[i] = in[i] * grad_output[0], rounded to nearest-even
  * into dtype (the backward of ce_flce's fp32 weight gradient for a weight
  * stored in dtype). in [n] fp32, grad_output one fp32 value, out [n] dtype;

@@ -219,6 +219,23 @@ def decode(x, dtype):
     return out
 
 
+def linear(hidden, lm_weight, *, dtype="f64", bias=None):
+    """The logits of the fused linear cross-entropy: hidden [rows, H] @
+    lm_weight[V, H]^T (+ bias [V]), in float64 from the exactly decoded
+    stored values."""
+    h = decode(hidden, dtype)
+    w = decode(lm_weight, dtype)
+    if h.ndim != 2 or w.ndim != 2 or h.shape[1] != w.shape[1]:
+        raise OracleError("hidden [rows, H] and lm_weight [V, H] expected")
+    logits = h @ w.T
+    if bias is not None:
+        b = np.ascontiguousarray(bias, dtype=np.float64).reshape(-1)
+        if b.shape[0] != w.shape[0]:
+            raise OracleError("bias must have V entries")
+        logits = logits + b[None, :]
+    return logits
+
+
 def flce_forward(hidden, lm_weight, target, *, dtype="f64", bias=None, weight=None,
                  ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0, softcap=None,
                  reduction="mean", want_grad=True):
@@ -234,14 +251,7 @@ def flce_forward(hidden, lm_weight, target, *, dtype="f64", bias=None, weight=No
     (that of the reduced loss; for "none", of the sum of the row losses)."""
     h = decode(hidden, dtype)
     w = decode(lm_weight, dtype)
-    if h.ndim != 2 or w.ndim != 2 or h.shape[1] != w.shape[1]:
-        raise OracleError("hidden [rows, H] and lm_weight [V, H] expected")
-    logits = h @ w.T
-    if bias is not None:
-        b = np.ascontiguousarray(bias, dtype=np.float64).reshape(-1)
-        if b.shape[0] != w.shape[0]:
-            raise OracleError("bias must have V entries")
-        logits = logits + b[None, :]
+    logits = linear(hidden, lm_weight, dtype=dtype, bias=bias)
     r = forward(logits, target, dtype="f64", weight=weight, ignore_index=ignore_index,
                 label_smoothing=label_smoothing, lse_square_scale=lse_square_scale,
                 softcap=softcap, reduction=reduction, want_grad=want_grad)

@@ -32,6 +32,7 @@ SIGNATURES = {
     "ce_bwd_nd": (_I, [_P, _I, _P, _I, _I64, _I64, _I64, _P]),
     "ce_flce_workspace_bytes": (ctypes.c_size_t, [_I, _I64, _I64, _I64]),
     "ce_scale_round": (_I, [_P, _P, _P, _I, _I64, _P]),
+    "ce_gemm_abt": (_I, [_P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
     "ce_flce": (_I, [_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P,
                      _P, _P, _P, _P, _P, _I64, _P, ctypes.c_size_t, _P]),
     "ce_bwd": (_I, [_P, _I, _P, _I, _I64, _I64, _P]),
@@ -124,6 +125,10 @@ def ce_flce(hidden, lm_weight, bias, dtype, rows, H, V, target, class_weight, ig
                           ignore_index, label_smoothing, lse_square_scale, softcap, reduction,
                           flags, loss, z_loss, acc, pred, grad_hidden, grad_weight, grad_bias,
                           chunk_rows, workspace, workspace_bytes, stream)
+
+
+def ce_gemm_abt(A, B, dtype, M, N, K, C, bias, stream):
+    return load().ce_gemm_abt(A, B, dtype, M, N, K, C, bias, stream)
 
 
 def ce_scale_round(inp, grad_output, out, dtype, n, stream):

@@ -634,6 +634,20 @@ ce_status record_cuda_failure(cudaError_t e, const char* what) { return cuda_fai
 // Records a message for ce_last_error.
 void record_message(const std::string& msg) { g_last_error = msg; }
 
+// The device status word of the library scratch of (current device, stream)
+// (allocated on first use, like every other call's scratch).
+ce_status library_status_word(cudaStream_t st, unsigned** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaGetDevice");
+    Scratch* scratch = nullptr;
+    const ce_status rc = scratch_for(dev, st, &scratch);
+    if (rc != CE_OK) return rc;
+    *out = &scratch->status;
+    return CE_OK;
+}
+
 }  // namespace gbce
 
 extern "C" ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V, const void* target,

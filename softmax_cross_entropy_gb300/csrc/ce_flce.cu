@@ -6,7 +6,8 @@
 //
 // Per chunk of c rows, on the caller's stream:
 //   1. logits [c, V] fp32 = hidden_c @ W^T (+ bias): tensor-core GEMM
-//      (cuBLAS, inputs in the storage type, fp32 accumulation);
+//      (cuBLAS, or this library's tcgen05 kernel with GBCE_FLCE_GEMM=tcgen05;
+//      inputs in the storage type, fp32 accumulation);
 //   2. the fused forward of this library over the chunk, as one shard of
 //      the batch (the batch's D and counted rows from ce_count), writing
 //      the gradient of the batch's reduced loss in place over the logits;
@@ -17,6 +18,8 @@
 // results are deterministic.
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <string>
@@ -29,6 +32,11 @@
 namespace gbce {
 ce_status record_cuda_failure(cudaError_t e, const char* what);
 void record_message(const std::string& msg);
+ce_status library_status_word(cudaStream_t st, unsigned** out);
+bool tc_gemm_supported(const void* A, const void* B, int dtype, int64_t K);
+ce_status tc_gemm_abt_launch(const void* A, const void* B, int dtype, int64_t M, int64_t N,
+                             int64_t K, float* C, const float* bias, unsigned* status,
+                             unsigned* abort, cudaStream_t st);
 
 namespace {
 
@@ -222,25 +230,42 @@ extern "C" ce_status ce_flce(const void* hidden, const void* lm_weight, const fl
         e = cudaGetLastError();
         if (e != cudaSuccess) return record_cuda_failure(e, "fill");
     }
+    // The logits GEMM: cuBLAS, or with GBCE_FLCE_GEMM=tcgen05 this
+    // library's tensor-core kernel (ce_gemm_abt; bias added in its epilogue)
+    const char* genv = std::getenv("GBCE_FLCE_GEMM");
+    const bool use_tc = genv && std::strcmp(genv, "tcgen05") == 0 &&
+                        tc_gemm_supported(hidden, lm_weight, dtype, H);
+    unsigned* status = nullptr;
+    if (use_tc) {
+        rc = library_status_word(st, &status);
+        if (rc != CE_OK) return rc;
+    }
     const float one = 1.f, zero = 0.f;
     for (int64_t k = 0; k < L.nchunks; ++k) {
         const int64_t r0 = k * L.chunk;
         const int64_t c = std::min<int64_t>(L.chunk, rows - r0);
         const char* hc = static_cast<const char*>(hidden) + r0 * H * b;
         // 1. logits = hidden_c @ W^T (+ bias), column-major [V, c]
-        if (bias) {
-            flce_bias_rows<<<static_cast<int>(std::min<int64_t>((c * V + 255) / 256, 8L * sms)),
-                             kFlceThreads, 0, st>>>(logits, bias, c, V);
-            e = cudaGetLastError();
-            if (e != cudaSuccess) return record_cuda_failure(e, "bias");
+        if (use_tc) {
+            rc = tc_gemm_abt_launch(hc, lm_weight, dtype, c, V, H, logits, bias, status,
+                                    status + 1, st);
+            if (rc != CE_OK) return rc;
+        } else {
+            if (bias) {
+                flce_bias_rows<<<static_cast<int>(std::min<int64_t>((c * V + 255) / 256, 8L * sms)),
+                                 kFlceThreads, 0, st>>>(logits, bias, c, V);
+                e = cudaGetLastError();
+                if (e != cudaSuccess) return record_cuda_failure(e, "bias");
+            }
+            rc = blas_check(cublasGemmEx(blas, CUBLAS_OP_T, CUBLAS_OP_N, static_cast<int>(V),
+                                         static_cast<int>(c), static_cast<int>(H), &one, lm_weight,
+                                         dt, static_cast<int>(H), hc, dt, static_cast<int>(H),
+                                         bias ? &one : &zero, logits, CUDA_R_32F,
+                                         static_cast<int>(V), CUBLAS_COMPUTE_32F,
+                                         CUBLAS_GEMM_DEFAULT),
+                            "logits GEMM");
+            if (rc != CE_OK) return rc;
         }
-        rc = blas_check(cublasGemmEx(blas, CUBLAS_OP_T, CUBLAS_OP_N, static_cast<int>(V),
-                                     static_cast<int>(c), static_cast<int>(H), &one, lm_weight, dt,
-                                     static_cast<int>(H), hc, dt, static_cast<int>(H),
-                                     bias ? &one : &zero, logits, CUDA_R_32F, static_cast<int>(V),
-                                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT),
-                        "logits GEMM");
-        if (rc != CE_OK) return rc;
         // 2. the fused forward over the chunk (one shard of the batch)
         const bool none = reduction == CE_RED_NONE;
         rc = ce_fwd_shard(logits, CE_F32, c, V, static_cast<const char*>(target) + r0 * tbytes,

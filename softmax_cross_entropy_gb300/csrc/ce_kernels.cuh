@@ -27,7 +27,7 @@ struct alignas(32) Partial {
 struct Scratch {
     unsigned ticket;
     unsigned status;
-    unsigned pad0[2];
+    unsigned pad0[2];  // pad0[0]: abort flag of the tensor-core GEMM launch
     double counts[2];
     unsigned pad[56];
     Partial partials[1];  // really kMaxPartials

@@ -238,3 +238,12 @@ def test_flce_rejects_small_workspace():
                       -100, 0.0, 0.0, 0.0, 2, 0, loss.data_ptr(), None, None, None, None, None,
                       None, 0, ws.data_ptr(), nbytes - 256, torch.cuda.current_stream().cuda_stream)
     assert rc == _lib.CE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_flce_with_tensor_core_logits(monkeypatch, dtype, reduction):
+    # the logits GEMM on this library's tcgen05 kernel (bias in its epilogue)
+    monkeypatch.setenv("GBCE_FLCE_GEMM", "tcgen05")
+    h, w, t, b, cw = make_case(21, 300, 136, 5000, dtype, with_bias=True, class_weight=True)
+    check(h, w, t, b, cw, dtype, reduction, 64, OPTS["smooth_z"])

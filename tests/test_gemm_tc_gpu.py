@@ -1,0 +1,78 @@
+"""GPU parity of the tensor-core GEMM of the fused linear cross-entropy
+(ce_gemm_abt: C = A @ B^T + bias on tcgen05, operands staged by TMA) against
+the oracle's float64 logits (oracle.linear) on seeded inputs. C is an fp32
+sum of exact bf16 / fp16 products, so each entry is within
+K * 2^-23 * sum_k |a_ik b_jk| of the exact value (fp32 accumulation,
+rounding or truncation in the adds), plus one fp32 rounding of the bias
+sum."""
+import math
+
+import numpy as np
+import pytest
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+CE_DT = {"bf16": 1, "f16": 2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from softmax_cross_entropy_gb300 import build, _lib
+    build.build()
+    _lib.load()
+
+
+def dev16(a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+        torch.bfloat16 if dtype == "bf16" else torch.float16).cuda()
+
+
+def run(M, N, K, dtype, with_bias, seed):
+    import oracle
+    from softmax_cross_entropy_gb300 import _lib
+    a = workloads.random_case(seed, M, K, dtype=dtype, std=1.0, ignore_frac=0.0).x
+    b = workloads.random_case(seed + 1, N, K, dtype=dtype, std=1.0 / math.sqrt(K),
+                              ignore_frac=0.0).x
+    bias = np.random.default_rng(seed).normal(0, 1, N).astype(np.float32) if with_bias else None
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    db = None if bias is None else torch.from_numpy(bias).cuda()
+    st = torch.cuda.current_stream().cuda_stream
+    da, dbm = dev16(a, dtype), dev16(b, dtype)  # held until the kernel has run
+    rc = _lib.ce_gemm_abt(da.data_ptr(), dbm.data_ptr(), CE_DT[dtype], M, N, K, C.data_ptr(),
+                          None if db is None else db.data_ptr(), st)
+    assert rc == _lib.CE_OK, (_lib.ce_status_string(rc), _lib.ce_last_error())
+    assert _lib.ce_device_status(st) == 0
+    got = C.double().cpu().numpy()
+    want = oracle.linear(a, b, dtype=dtype, bias=bias)
+    bound = K * 2.0 ** -23 * (np.abs(oracle.decode(a, dtype)) @ np.abs(oracle.decode(b, dtype)).T)
+    bound += 2.0 ** -23 * np.abs(want) + 1e-30
+    err = np.abs(got - want)
+    assert np.all(np.isfinite(got))
+    bad = err > bound
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} out of bound; first at "
+                           f"{tuple(np.argwhere(bad)[0])}: got {got[bad][0]} want {want[bad][0]}")
+
+
+def test_one_tile():
+    run(128, 256, 64, "bf16", False, 1)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 1000, 136), (1, 17, 8), (129, 257, 520),
+                                   (1046, 2048, 1024)])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_gemm_parity(dtype, M, N, K, with_bias):
+    run(M, N, K, dtype, with_bias, M + N + K)
+
+
+def test_unsupported_k():
+    from softmax_cross_entropy_gb300 import _lib
+    a = torch.zeros(4, 12, dtype=torch.bfloat16, device="cuda")
+    C = torch.empty(4, 4, device="cuda")
+    rc = _lib.ce_gemm_abt(a.data_ptr(), a.data_ptr(), 1, 4, 4, 12, C.data_ptr(), None,
+                          torch.cuda.current_stream().cuda_stream)
+    assert rc == _lib.CE_ERR_UNSUPPORTED
