@@ -674,6 +674,10 @@ def run_profile_target(args):
     if args.ncu_config >= 0:
         name, make = extra_workloads(0)[args.ncu_config]
         case = make()
+        if args.rows != ROWS and args.rows < case.rows:
+            # a smaller case of the same workload: its first rows
+            case = case.with_(x=case.x[: args.rows], target=case.target[: args.rows])
+            name += f" (first {args.rows} rows)"
     else:
         name = workload_desc(args.V)
         case = workloads.vsweep(V=args.V, rows=args.rows)

@@ -48,6 +48,7 @@ struct Plan {
     // streaming kernel layout
     int ng = 0, sg = 0, chunk_vec = 0, nchunk = 0, resident = 0;
     int reg_wpr = 0;  // register-resident kernel: warps of a row team
+    uint32_t reg_buf_stride = 0;  // register-resident kernel: bytes of a team's row buffer
 };
 
 using PlanKey = std::tuple<int, int, int64_t, bool, bool, int>;
@@ -328,7 +329,7 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
                           13 * env_int("GBCE_STREAM_SLOTS", 0) +
                           17 * env_int("GBCE_STREAM_WARPS", 0) +
                           19 * (env_int("GBCE_REG_MAX_BYTES", 65536) + (w_aligned ? 0 : 1)) +
-                          7 * env_int("GBCE_REG_NVL", 16));
+                          7 * env_int("GBCE_REG_NVL", 0));
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
         *out = it->second;
@@ -342,26 +343,44 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     const bool fast_ok = aligned && (V * bytes) % 16 == 0 && forced_c >= 0 && forced_kind != 3;
     // The register-resident kernel for rows of at most GBCE_REG_MAX_BYTES
     // (default and limit 64 KB: 8 warps of 16 vectors a thread). A thread
-    // holds GBCE_REG_NVL (8 or 16, default 16) 16-byte vectors; a team of
+    // holds 8 or 16 16-byte vectors (GBCE_REG_NVL forces one); a team of
     // the fewest warps that hold a row owns it, and a CTA has as many teams
     // as fit in 8 warps. Its class weights are read as 16-byte vectors.
     const int64_t reg_max = env_int("GBCE_REG_MAX_BYTES", 65536);
-    const int nvl_env = env_int("GBCE_REG_NVL", 16);
-    const int nvl = (nvl_env == 8 || nvl_env == 16) ? nvl_env : 16;
     const int64_t vrow = V * bytes / 16;
+    // 8 vectors a thread while a row fits 8 warps (more rows in flight an
+    // SM; measured 2-4% faster at 8-32 KB rows), else 16
+    const int nvl_env = env_int("GBCE_REG_NVL", 0);
+    const int nvl = (nvl_env == 8 || nvl_env == 16) ? nvl_env
+                    : (vrow <= 32 * 8 * kRegMaxWarps ? 8 : 16);
     const int64_t wpr = (vrow + 32 * nvl - 1) / (32 * nvl);
     if (fast_ok && (!wsmooth || w_aligned) && wpr <= kRegMaxWarps &&
         (forced_kind == 4 || (forced_kind == 0 && V * bytes <= reg_max))) {
         const void* fn = reg_kernel(dtype, softcap, wsmooth, nvl);
         const int teams = kRegMaxWarps / static_cast<int>(wpr);
         const int nt = 32 * static_cast<int>(wpr) * teams;
+        // one row buffer a team (the next row's bulk copy)
+        const uint32_t stride = static_cast<uint32_t>((V * bytes + 127) / 128 * 128);
+        const size_t smem = static_cast<size_t>(teams) * stride;
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+        const size_t dyn_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(dyn_max));
+        if (e != cudaSuccess) return cuda_failure(e, "register kernel attributes");
         int occ = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, nt, 0);
-        if (e != cudaSuccess) return cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (smem <= dyn_max) {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, nt, smem);
+            if (e != cudaSuccess)
+                return cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        }
         if (occ >= 1) {
             best.fn = fn;
             best.kind = Kind::Reg;
             best.nt = nt;
+            best.smem = smem;
+            best.reg_buf_stride = stride;
             best.reg_wpr = static_cast<int>(wpr);
             // at most 8 CTAs an SM: the partial-sum slots of a launch stay
             // within 8 per SM, as for the other kernels
@@ -585,7 +604,8 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
             pdl = true;
         }
         a.reg_wpr = p.reg_wpr;
-        return launch(p.fn, static_cast<int>(units), p.nt, 0, 1, st, &a, pdl);
+        a.reg_buf_stride = p.reg_buf_stride;
+        return launch(p.fn, static_cast<int>(units), p.nt, p.smem, 1, st, &a, pdl);
     }
     if (p.kind == Kind::Staged) {
         a.slice_vec = p.slice_vec;

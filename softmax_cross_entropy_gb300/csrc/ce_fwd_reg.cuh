@@ -8,16 +8,16 @@
 //
 // GB300 design. A team of WPR warps owns one row at a time and each thread
 // holds NVL (8 or 16) 16-byte vectors of it in registers, so a row of up to
-// 512 B * NVL * WPR is read from HBM once, with 16-byte coalesced loads
-// issued all at once, and written once. Warp w of a team takes the row's
-// vectors [w * 32 * NVL, (w + 1) * 32 * NVL): lane l holds vectors
-// w * 32 * NVL + 32 k + l, so every load and store of a warp is 512
+// 512 B * NVL * WPR is read from HBM once and written once. Warp w of a
+// team takes the row's vectors [w * 32 * NVL, (w + 1) * 32 * NVL): lane l
+// holds vectors w * 32 * NVL + 32 k + l, so every access of a warp is 512
 // contiguous bytes and the offsets between a thread's vectors are
-// constants. A CTA holds several independent
-// teams (one warp each for a 4096-element bf16 row), so an SM has a dozen or
-// more rows in flight and their loads overlap one another's arithmetic,
-// which is what hides HBM latency here; no shared-memory staging or copy
-// engine is involved. Per row:
+// constants. A CTA holds several independent teams (one warp each for a
+// 4096-element bf16 row), so an SM has a dozen or more rows in flight, and
+// each team's leader copies the team's next row into a shared-memory buffer
+// with a 1-D bulk async copy while the team computes the current one: the
+// HBM latency of the next row hides behind this row's arithmetic, and the
+// current row moves from the buffer into registers once. Per row:
 //   1. raw maximum (packed 16-bit max for bf16/fp16), warp redux, one team
 //      barrier for the row's maximum; the first argmax only when asked for;
 //   2. S = sum exp(z - M) and the smoothing sum from the registers; a
@@ -38,6 +38,16 @@
 #include "ce_kernels.cuh"
 
 namespace gbce {
+
+// 16-byte global load that does not allocate in L1 (data read once per
+// pass; keeps L1 for data that is reused, such as class weights).
+__device__ __forceinline__ uint4 ld_v4_no_l1(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
 
 // Class weights of vector v (VE consecutive classes).
 template <int VE>
@@ -87,6 +97,8 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     __shared__ double red_d[2][MW];
     __shared__ long long red_n[MW];
     __shared__ int s_flag;
+    __shared__ __align__(8) uint64_t pf_bar[MW];  // one per team
+    extern __shared__ __align__(128) unsigned char reg_smem[];  // teams x reg_buf_stride
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -158,18 +170,48 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     float accL = 0.f, accZ = 0.f;  // the rows whose target this thread owned
     int accC = 0;
     const int64_t nteams = static_cast<int64_t>(gridDim.x) * teams;
+    // Each team owns a shared-memory buffer of one row; its leader copies the
+    // team's next counted row into it (1-D bulk async copy, mbarrier
+    // completion) while the team computes the current row from registers,
+    // so the HBM latency of the next row overlaps this row's arithmetic.
+    const uint32_t row_bytes = static_cast<uint32_t>(vrow) * 16u;
+    const uint32_t buf = smem_u32(reg_smem) + static_cast<uint32_t>(team) * a.reg_buf_stride;
+    const uint32_t bar = smem_u32(&pf_bar[team]);
+    const bool lead = wr == 0 && lane == 0;
+    const uint64_t pol = l2_evict_first_policy();
+    uint32_t pf_phase = 0;
+    bool pf_pending = false;  // leader: a copy into the buffer is outstanding
+    bool failed = false;
+    auto prefetch = [&](int64_t row) {  // leader only, buffer free
+        const char* src = reinterpret_cast<const char*>(a.x) + row * a.V * static_cast<int64_t>(sizeof(T));
+        mbar_arrive_expect_tx(bar, row_bytes);
+        for (uint32_t off = 0; off < row_bytes; off += 32768u)
+            bulk_g2s(buf + off, src + off, min(32768u, row_bytes - off), bar, pol);
+        pf_pending = true;
+    };
+    if (tid == 0) {
+        for (int tm = 0; tm < teams; ++tm) mbar_init(smem_u32(&pf_bar[tm]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
     int64_t r = static_cast<int64_t>(blockIdx.x) * teams + team;
-    int64_t t_next = r < a.rows ? load_target(a, r) : 0;
+    int64_t t_cur = r < a.rows ? load_target(a, r) : 0;                // row r
+    int64_t t_nxt = r + nteams < a.rows ? load_target(a, r + nteams) : 0;  // row r + nteams
+    if (lead && r < a.rows && row_counts(a, t_cur)) prefetch(r);
 #pragma unroll 1
     for (; r < a.rows; r += nteams) {
-        const int64_t t = t_next;
-        if (r + nteams < a.rows) t_next = load_target(a, r + nteams);
+        const int64_t t = t_cur;
+        const int64_t rn = r + nteams;
+        const bool next_counts = rn < a.rows && row_counts(a, t_nxt);
+        t_cur = t_nxt;
+        t_nxt = rn + nteams < a.rows ? load_target(a, rn + nteams) : 0;
         const bool counts = row_counts(a, t);
         T* xrow = reinterpret_cast<T*>(a.x) + r * a.V;
         uint4* rowv = reinterpret_cast<uint4*>(xrow);
         if (!counts) {
-            // ignored row: exact +0 gradient without reading it
-            const bool lead = wr == 0 && lane == 0;
+            // ignored row: exact +0 gradient without reading it; nothing was
+            // copied for it, so the buffer takes the next row now
+            if (lead && next_counts && !failed) prefetch(rn);
             if (lead && t != a.ignore_index) atomicOr(&a.scratch->status, kDevErrTarget);
             if (a.grad) {
 #pragma unroll
@@ -186,11 +228,18 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             }
             continue;
         }
-        // ---- the row into registers: vector vbase + 32 k
+        // ---- the row into registers from the buffer: vector vbase + 32 k
+        if (!failed && !mbar_wait_bounded(bar, pf_phase, a.timeout_ns)) {
+            failed = true;
+            if (lead) atomicOr(&a.scratch->status, kDevErrTimeout);
+        }
+        pf_phase ^= 1u;
+        if (lead) pf_pending = false;
         uint4 q[NVL];
+        const uint4* sb = reinterpret_cast<const uint4*>(reg_smem + static_cast<size_t>(team) * a.reg_buf_stride);
 #pragma unroll
         for (int k = 0; k < NVL; ++k)
-            q[k] = 32 * k < vlim ? rowv[vbase + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
+            q[k] = 32 * k < vlim ? sb[vbase + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
         const int tvec = static_cast<int>(t / VE);
         const bool owner = lane == (tvec & 31) && wr == tvec / (32 * NVL);
         const float xt = owner ? VT::load1(xrow, t) : 0.f;
@@ -210,6 +259,10 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             team_sync();
             X = warp_max_f32(lane < WPR ? red_a[w0 + lane] : -INFINITY);
         }
+        // every thread of the team holds its vectors (the warp reduction
+        // above, or the team barrier, follows every thread's buffer reads):
+        // the buffer takes the team's next counted row
+        if (lead && next_counts && !failed) prefetch(rn);
         int cand = INT_MAX;
         if (want_arg) {
             // first element of this thread equal to the row maximum (the
@@ -346,6 +399,8 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
         // read before the next row's first team barrier
     }
 
+    // a copy still in flight (after a timeout) lands before the CTA exits
+    if (lead && pf_pending) (void)mbar_wait_bounded(bar, pf_phase, a.timeout_ns);
     if (a.reduction != kRedNone) {
         need_counts();
         // fixed-order CTA sum of the per-thread partials: a thread holds the

@@ -447,17 +447,22 @@ def test_stream_weighted_smoothing(monkeypatch, dtype, V, rows, twice):
     ("bf16", 1024, 150),    # one warp a row
     ("bf16", 4096, 300),    # the bench sweep's shortest row: 4 warps
     ("bf16", 5000, 97),     # ragged: the last warp's vectors partly past the row
-    ("bf16", 16000, 40),    # 16 warps, the last vectors ragged
-    ("bf16", 16384, 33),    # 16 warps exactly
+    ("bf16", 16000, 40),    # 8 warps of 8 vectors, the last vectors ragged
+    ("bf16", 16384, 33),    # 8 warps of 8 vectors exactly
+    ("bf16", 32000, 20),    # 16 vectors a thread only (8 warps)
     ("f32", 8192, 70),
     ("f32", 6000, 21),
     ("f32", 12, 33),        # three vectors: most threads hold nothing
     ("f16", 8192, 50),
 ])
-def test_register_kernel(monkeypatch, dtype, V, rows):
-    # the register-resident kernel (rows of at most 32 KB) forced, every
+@pytest.mark.parametrize("nvl", ["8", "16"])
+def test_register_kernel(monkeypatch, dtype, V, rows, nvl):
+    # the register-resident kernel forced, 8 or 16 vectors a thread, every
     # option set, whole-batch comparison
+    if nvl == "8" and V * (4 if dtype == "f32" else 2) > 32768:
+        pytest.skip("8 vectors a thread hold rows of at most 32 KB")
     monkeypatch.setenv("GBCE_KERNEL", "4")
+    monkeypatch.setenv("GBCE_REG_NVL", nvl)
     for opts in (dict(),
                  dict(label_smoothing=0.1, softcap=20.0, lse_square_scale=1e-3),
                  dict(weight=True, reduction="none"),
