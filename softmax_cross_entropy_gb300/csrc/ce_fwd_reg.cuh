@@ -39,16 +39,6 @@
 
 namespace gbce {
 
-// 16-byte global load that does not allocate in L1 (data read once per
-// pass; keeps L1 for data that is reused, such as class weights).
-__device__ __forceinline__ uint4 ld_v4_no_l1(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 // Class weights of vector v (VE consecutive classes).
 template <int VE>
 __device__ __forceinline__ void reg_weights(const float* weight, int v, float (&w)[VE]) {
