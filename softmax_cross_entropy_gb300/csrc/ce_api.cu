@@ -319,8 +319,8 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     // 16; -1 forces the general path) and GBCE_CFG the CTA shape index.
     const int forced_c = env_int("GBCE_CLUSTER", 0);
     const int forced_cfg = env_int("GBCE_CFG", -1);
-    // GBCE_KERNEL: 1 staged, 2 streaming, 3 general, 4 register-resident
-    // (0: automatic)
+    // GBCE_KERNEL: 1 staged, 2 streaming, 3 general, 4 register-resident,
+    // 5 register-resident with a cluster of CTAs a row (0: automatic)
     const int forced_kind = env_int("GBCE_KERNEL", 0);
     const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth,
                       (forced_kind * 64 + forced_c) * 64 + forced_cfg +
@@ -329,7 +329,7 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
                           13 * env_int("GBCE_STREAM_SLOTS", 0) +
                           17 * env_int("GBCE_STREAM_WARPS", 0) +
                           19 * (env_int("GBCE_REG_MAX_BYTES", 65536) + (w_aligned ? 0 : 1)) +
-                          7 * env_int("GBCE_REG_NVL", 0));
+                          7 * env_int("GBCE_REG_NVL", 0) + 3 * env_int("GBCE_REG_CLUSTER", 0));
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
         *out = it->second;
@@ -388,6 +388,57 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
                 static_cast<int64_t>(std::min(occ, 8)) * dev.sm_count, kMaxUnits);
         }
     }
+    // Rows longer than one CTA of the register-resident kernel holds: a
+    // cluster of C CTAs owns a row, each one 8-warp team holding a slice of
+    // 32 * 8 * nvl vectors (C <= 8, the portable cluster size).
+    const int64_t cl_nvl = nvl_env == 8 ? 8 : 16;
+    const int64_t cl_vpc = 32 * kRegMaxWarps * cl_nvl;
+    const int64_t cl_C = (vrow + cl_vpc - 1) / cl_vpc;
+    if (fast_ok && (!wsmooth || w_aligned) && best.kind == Kind::General && cl_C >= 2 &&
+        cl_C <= 8 && (forced_kind == 5 || (forced_kind == 0 && env_int("GBCE_REG_CLUSTER", 0)))) {
+        const void* fn = reg_kernel(dtype, softcap, wsmooth, static_cast<int>(cl_nvl));
+        const int nt = 32 * kRegMaxWarps;
+        const uint32_t stride = static_cast<uint32_t>(cl_vpc * 16);
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+        const size_t dyn_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(dyn_max));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        if (e != cudaSuccess) return cuda_failure(e, "register kernel attributes");
+        int ncl = 0;
+        if (stride <= dyn_max) {
+            cudaLaunchConfig_t lc = {};
+            lc.gridDim = dim3(static_cast<unsigned>(cl_C * dev.sm_count));
+            lc.blockDim = dim3(static_cast<unsigned>(nt));
+            lc.dynamicSmemBytes = stride;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = static_cast<unsigned>(cl_C);
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            lc.attrs = &attr;
+            lc.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&ncl, fn, &lc);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                ncl = 0;
+            }
+        }
+        if (ncl >= 1) {
+            best.fn = fn;
+            best.kind = Kind::Reg;
+            best.nt = nt;
+            best.smem = stride;
+            best.reg_buf_stride = stride;
+            best.reg_wpr = kRegMaxWarps;
+            best.cluster = static_cast<int>(cl_C);
+            // clusters; a launch's CTAs stay within the partial-sum slots
+            best.max_units = std::min<int64_t>(ncl, kMaxUnits / cl_C);
+        }
+    }
     if (fast_ok && forced_kind != 1 && best.kind == Kind::General) {
         rc = CE_OK;
         if (!try_stream(dtype, V, softcap, wsmooth, dev, &best, &rc) && rc != CE_OK) return rc;
@@ -421,7 +472,8 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     }
     if ((forced_kind == 1 && best.kind != Kind::Staged) ||
         (forced_kind == 2 && best.kind != Kind::Stream) ||
-        (forced_kind == 4 && best.kind != Kind::Reg)) {
+        (forced_kind == 4 && best.kind != Kind::Reg) ||
+        (forced_kind == 5 && (best.kind != Kind::Reg || best.cluster < 2))) {
         g_last_error = "the kernel forced by GBCE_KERNEL cannot run this shape";
         return CE_ERR_UNSUPPORTED;
     }
@@ -554,8 +606,11 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
     ce_status rc = make_plan(dev, c.dtype, c.V, sc, wsmooth, aligned, w_aligned, &p);
     if (rc != CE_OK) return rc;
     const int64_t units = c.rows == 0 ? 1 : std::min<int64_t>(c.rows, p.max_units);
-    if (records_for(units) > max_slots) {
-        g_last_error = "this launch needs " + std::to_string(records_for(units)) +
+    // the register kernel's clusters: a partial-sum slot for each CTA
+    const int64_t slots =
+        records_for(p.kind == Kind::Reg && c.rows > 0 ? units * p.cluster : units);
+    if (slots > max_slots) {
+        g_last_error = "this launch needs " + std::to_string(slots) +
                        " partial-sum slots; the scratch holds " + std::to_string(max_slots);
         return CE_ERR_UNSUPPORTED;
     }
@@ -605,7 +660,9 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
         }
         a.reg_wpr = p.reg_wpr;
         a.reg_buf_stride = p.reg_buf_stride;
-        return launch(p.fn, static_cast<int>(units), p.nt, p.smem, 1, st, &a, pdl);
+        a.reg_cluster = p.cluster;
+        return launch(p.fn, static_cast<int>(units * p.cluster), p.nt, p.smem, p.cluster, st, &a,
+                      pdl);
     }
     if (p.kind == Kind::Staged) {
         a.slice_vec = p.slice_vec;

@@ -39,6 +39,14 @@
 
 namespace gbce {
 
+// One fp32 from the shared memory of a CTA of the cluster (address from
+// map_to_rank).
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Class weights of vector v (VE consecutive classes).
 template <int VE>
 __device__ __forceinline__ void reg_weights(const float* weight, int v, float (&w)[VE]) {
@@ -88,6 +96,7 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     __shared__ long long red_n[MW];
     __shared__ int s_flag;
     __shared__ __align__(8) uint64_t pf_bar[MW];  // one per team
+    __shared__ __align__(16) float cl_red[4];  // cluster mode: this CTA's max, S, SZ, argmax
     extern __shared__ __align__(128) unsigned char reg_smem[];  // teams x reg_buf_stride
 
     const int tid = threadIdx.x;
@@ -99,7 +108,15 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     const int w0 = team * WPR;           // the team's first warp
     const int teams = (blockDim.x >> 5) / WPR;
     const int vrow = static_cast<int>(a.V / VE);
-    const int vbase = wr * 32 * NVL + lane;  // this thread's first vector
+    // Rows longer than one CTA holds: a cluster of CL CTAs (one team of 8
+    // warps each) owns a row, CTA c the slice of vectors [c * VPC, (c + 1) *
+    // VPC); the row's maximum and sums merge across the cluster through
+    // distributed shared memory.
+    const int CL = a.reg_cluster;
+    constexpr int VPC = kRegMaxWarps * 32 * NVL;  // vectors of a CTA's slice (cluster mode)
+    const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int cta_vec0 = crank * VPC;              // first vector of this CTA's slice
+    const int vbase = cta_vec0 + wr * 32 * NVL + lane;  // this thread's first vector
     const int vlim = vrow - vbase;           // its vector k exists when 32 k < vlim
     const bool smooth = WS || a.eps > 0.f;
     const bool want_arg = a.want_pred || a.want_acc;
@@ -159,12 +176,15 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
 
     float accL = 0.f, accZ = 0.f;  // the rows whose target this thread owned
     int accC = 0;
-    const int64_t nteams = static_cast<int64_t>(gridDim.x) * teams;
+    const int64_t nteams = CL > 1 ? static_cast<int64_t>(ncluster_x())
+                                  : static_cast<int64_t>(gridDim.x) * teams;
     // Each team owns a shared-memory buffer of one row; its leader copies the
     // team's next counted row into it (1-D bulk async copy, mbarrier
     // completion) while the team computes the current row from registers,
     // so the HBM latency of the next row overlaps this row's arithmetic.
-    const uint32_t row_bytes = static_cast<uint32_t>(vrow) * 16u;
+    // bytes of the row this CTA's team copies (its slice in cluster mode)
+    const uint32_t row_bytes =
+        static_cast<uint32_t>(max(0, min(vrow - cta_vec0, CL > 1 ? VPC : vrow))) * 16u;
     const uint32_t buf = smem_u32(reg_smem) + static_cast<uint32_t>(team) * a.reg_buf_stride;
     const uint32_t bar = smem_u32(&pf_bar[team]);
     const bool lead = wr == 0 && lane == 0;
@@ -173,7 +193,9 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     bool pf_pending = false;  // leader: a copy into the buffer is outstanding
     bool failed = false;
     auto prefetch = [&](int64_t row) {  // leader only, buffer free
-        const char* src = reinterpret_cast<const char*>(a.x) + row * a.V * static_cast<int64_t>(sizeof(T));
+        const char* src = reinterpret_cast<const char*>(a.x) +
+                          row * a.V * static_cast<int64_t>(sizeof(T)) +
+                          static_cast<int64_t>(cta_vec0) * 16;
         mbar_arrive_expect_tx(bar, row_bytes);
         for (uint32_t off = 0; off < row_bytes; off += 32768u)
             bulk_g2s(buf + off, src + off, min(32768u, row_bytes - off), bar, pol);
@@ -184,10 +206,13 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
         fence_mbar_init();
     }
     __syncthreads();
-    int64_t r = static_cast<int64_t>(blockIdx.x) * teams + team;
+    int64_t r = CL > 1 ? static_cast<int64_t>(cluster_id_x())
+                       : static_cast<int64_t>(blockIdx.x) * teams + team;
     int64_t t_cur = r < a.rows ? load_target(a, r) : 0;                // row r
     int64_t t_nxt = r + nteams < a.rows ? load_target(a, r + nteams) : 0;  // row r + nteams
-    if (lead && r < a.rows && row_counts(a, t_cur)) prefetch(r);
+    // (a CTA whose slice is empty copies and waits for nothing)
+    const bool has_slice = row_bytes > 0;
+    if (lead && has_slice && r < a.rows && row_counts(a, t_cur)) prefetch(r);
 #pragma unroll 1
     for (; r < a.rows; r += nteams) {
         const int64_t t = t_cur;
@@ -201,14 +226,14 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
         if (!counts) {
             // ignored row: exact +0 gradient without reading it; nothing was
             // copied for it, so the buffer takes the next row now
-            if (lead && next_counts && !failed) prefetch(rn);
-            if (lead && t != a.ignore_index) atomicOr(&a.scratch->status, kDevErrTarget);
+            if (lead && has_slice && next_counts && !failed) prefetch(rn);
+            if (lead && crank == 0 && t != a.ignore_index) atomicOr(&a.scratch->status, kDevErrTarget);
             if (a.grad) {
 #pragma unroll
                 for (int k = 0; k < NVL; ++k)
                     if (32 * k < vlim) rowv[vbase + 32 * k] = make_uint4(0u, 0u, 0u, 0u);
             }
-            if (lead) {
+            if (lead && crank == 0) {
                 if (a.reduction == kRedNone) {
                     a.loss[r] = 0.f;
                     if (a.want_z) a.zloss[r] = 0.f;
@@ -219,19 +244,21 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             continue;
         }
         // ---- the row into registers from the buffer: vector vbase + 32 k
-        if (!failed && !mbar_wait_bounded(bar, pf_phase, a.timeout_ns)) {
-            failed = true;
-            if (lead) atomicOr(&a.scratch->status, kDevErrTimeout);
+        if (has_slice) {
+            if (!failed && !mbar_wait_bounded(bar, pf_phase, a.timeout_ns)) {
+                failed = true;
+                if (lead) atomicOr(&a.scratch->status, kDevErrTimeout);
+            }
+            pf_phase ^= 1u;
+            if (lead) pf_pending = false;
         }
-        pf_phase ^= 1u;
-        if (lead) pf_pending = false;
         uint4 q[NVL];
         const uint4* sb = reinterpret_cast<const uint4*>(reg_smem + static_cast<size_t>(team) * a.reg_buf_stride);
 #pragma unroll
         for (int k = 0; k < NVL; ++k)
-            q[k] = 32 * k < vlim ? sb[vbase + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
-        const int tvec = static_cast<int>(t / VE);
-        const bool owner = lane == (tvec & 31) && wr == tvec / (32 * NVL);
+            q[k] = 32 * k < vlim ? sb[vbase - cta_vec0 + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
+        const int tvec = static_cast<int>(t / VE) - cta_vec0;  // in this CTA's slice
+        const bool owner = tvec >= 0 && lane == (tvec & 31) && wr == tvec / (32 * NVL);
         const float xt = owner ? VT::load1(xrow, t) : 0.f;
         const float wt = a.weight ? __ldg(a.weight + t) : 1.f;
 
@@ -252,7 +279,17 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
         // every thread of the team holds its vectors (the warp reduction
         // above, or the team barrier, follows every thread's buffer reads):
         // the buffer takes the team's next counted row
-        if (lead && next_counts && !failed) prefetch(rn);
+        if (lead && has_slice && next_counts && !failed) prefetch(rn);
+        if (CL > 1) {
+            // the row's maximum over the cluster: lane i reads CTA i's
+            if (tid == 0) cl_red[0] = X;
+            __syncwarp();
+            cluster_sync();
+            float o = -INFINITY;
+            if (lane < CL) o = ld_dsmem_f32(map_to_rank(smem_u32(&cl_red[0]), lane));
+            __syncwarp();
+            X = warp_max_f32(o);
+        }
         int cand = INT_MAX;
         if (want_arg) {
             // first element of this thread equal to the row maximum (the
@@ -314,6 +351,34 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) I = min(I, __shfl_xor_sync(0xffffffffu, I, o));
             }
+        }
+        if (CL > 1) {
+            // the row's sums over the cluster, added in rank order by a
+            // fixed butterfly (the same bits in every thread)
+            if (tid == 0) {
+                cl_red[1] = S;
+                cl_red[2] = ZS;
+                cl_red[3] = __int_as_float(I);
+            }
+            __syncwarp();
+            cluster_sync();
+            float s_ = 0.f, z_ = 0.f;
+            int i_ = INT_MAX;
+            if (lane < CL) {
+                const uint32_t rb = map_to_rank(smem_u32(&cl_red[0]), lane);
+                s_ = ld_dsmem_f32(rb + 4);
+                z_ = ld_dsmem_f32(rb + 8);
+                i_ = __float_as_int(ld_dsmem_f32(rb + 12));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                s_ += __shfl_xor_sync(0xffffffffu, s_, o);
+                z_ += __shfl_xor_sync(0xffffffffu, z_, o);
+                i_ = min(i_, __shfl_xor_sync(0xffffffffu, i_, o));
+            }
+            S = s_;
+            ZS = z_;
+            I = i_;
         }
         const float logS = logf(S);
         const float lse = Ms + logS;
@@ -422,6 +487,12 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
         }
         __syncthreads();  // red_d is the epilogue's scratch next
         finish_scalars_cta(a, L, Z, Cn, D, n_valid, &s_flag, red_d[0], red_d[1], red_n);
+    }
+    // no CTA of a cluster leaves while another may still read its shared
+    // memory
+    if (CL > 1) {
+        __syncwarp();
+        cluster_sync();
     }
 }
 

@@ -78,6 +78,7 @@ struct FwdArgs {
     int nd_staged;  // 1: the N-D kernel keeps its tile in shared memory
     int reg_wpr;    // register-resident kernel: warps a row team has
     uint32_t reg_buf_stride;  // register-resident kernel: bytes of a team's row buffer
+    int reg_cluster;  // register-resident kernel: CTAs of the cluster that owns a row (0, 1: one CTA)
 };
 
 // Arguments of one forward call as the C ABI receives them (host side).

@@ -472,6 +472,50 @@ def test_register_kernel(monkeypatch, dtype, V, rows, nvl):
         check_full(case, want_z=True, want_acc=True, want_pred=True)
 
 
+@pytest.mark.parametrize("dtype,V,rows", [
+    ("bf16", 65536, 24),    # 2 CTAs of 64 KB
+    ("bf16", 131072, 20),   # 4 CTAs
+    ("bf16", 98312, 17),    # 4 CTAs, the last holds one vector
+    ("bf16", 40000, 30),    # 2 CTAs, the second ragged
+    ("f32", 128256, 9),     # 8 CTAs of 16 vectors a thread
+    ("f16", 50264, 19),
+])
+@pytest.mark.parametrize("nvl", ["8", "16"])
+def test_register_cluster_kernel(monkeypatch, dtype, V, rows, nvl):
+    # a cluster of CTAs a row (row maximum and sums merged through
+    # distributed shared memory), every option set, whole-batch comparison
+    vrow = V * (4 if dtype == "f32" else 2) // 16
+    if -(-vrow // (256 * int(nvl))) > 8:
+        pytest.skip("more than 8 CTAs a row")
+    monkeypatch.setenv("GBCE_KERNEL", "5")
+    monkeypatch.setenv("GBCE_REG_NVL", nvl)
+    for opts in (dict(),
+                 dict(label_smoothing=0.1, softcap=20.0, lse_square_scale=1e-3),
+                 dict(weight=True, reduction="none"),
+                 dict(weight=True, label_smoothing=0.05, reduction="sum"),
+                 dict(weight=True, label_smoothing=0.2, softcap=8.0, ignore_frac=0.3)):
+        case = workloads.random_case(130 + rows, rows, V, dtype=dtype, **opts)
+        check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+def test_register_cluster_ties_across_ctas(monkeypatch):
+    # the row maximum repeated in several CTAs' slices: the lowest index wins
+    monkeypatch.setenv("GBCE_KERNEL", "5")
+    V = 131072
+    case = workloads.random_case(6, 40, V, dtype="bf16")
+    x = case.x.copy()
+    top = workloads.f32_to_bf16_bits(np.array([60.0], np.float32))[0]
+    firsts = []
+    for r in range(case.rows):
+        cols = sorted({(r * 7919) % V, (r * 7919 + 40000) % V, (r * 7919 + 90001) % V})
+        x[r, cols] = top
+        firsts.append(cols[0])
+    case = case.with_(x=x)
+    out, ref = check_full(case, want_acc=True, want_pred=True)
+    valid = case.target != case.ignore_index
+    assert np.array_equal(out["pred"][valid], np.array(firsts)[valid])
+
+
 def test_register_kernel_ties_across_warps(monkeypatch):
     # the row maximum repeated in several warps' vectors: the lowest index
     # wins
