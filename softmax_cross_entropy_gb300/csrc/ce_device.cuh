@@ -205,6 +205,18 @@ __device__ __forceinline__ float tanh_from_scaled(float two_y_log2e) {
     return fmaf(-2.0f, rcp_approx(u + 1.0f), 1.0f);
 }
 
+// Softcap z = s tanh(x/s) through r = 1 / (1 + exp(2x/s)), for a pair of
+// logits (k2 = 2 log2(e) / s). With it z = s (1 - 2r) and dz/dx =
+// 1 - tanh^2 = 4 r (1 - r), so the exp2 argument (z - m) log2(e) is one FFMA
+// of r, c1 r + c0 with c1 = -2 s log2(e) and c0 = (s - m) log2(e), and the
+// gradient's factor is one FFMA, r - r^2, the 4 going into the gradient's
+// constants. r = 0 for x = +inf, 1 for x = -inf; NaN stays NaN.
+__device__ __forceinline__ float2 softcap_r2(float x0, float x1, float k2) {
+    const float2 v = fmul2(make_float2(x0, x1), make_float2(k2, k2));
+    const float2 u = fadd2(make_float2(ex2(v.x), ex2(v.y)), make_float2(1.f, 1.f));
+    return make_float2(rcp_approx(u.x), rcp_approx(u.y));
+}
+
 // ---------------------------------------------------------------- storage
 
 template <typename T>

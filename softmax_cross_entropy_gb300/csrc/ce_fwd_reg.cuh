@@ -61,17 +61,6 @@ __device__ __forceinline__ void reg_weights(const float* weight, int v, float (&
     }
 }
 
-// z = softcap(x) and (under softcap) the tanh, for a pair of logits.
-template <bool SOFTCAP>
-__device__ __forceinline__ float2 reg_z2(float x0, float x1, const FwdArgs& a, float2& th) {
-    if constexpr (SOFTCAP) {
-        th = make_float2(tanh_from_scaled(x0 * a.sc_k2), tanh_from_scaled(x1 * a.sc_k2));
-        return make_float2(a.softcap * th.x, a.softcap * th.y);
-    } else {
-        return make_float2(x0, x1);
-    }
-}
-
 // exp2 arguments (z - M) * log2(e): one packed FFMA against the rounded
 // M * log2(e) for 16-bit logits, subtract first for fp32.
 template <typename T>
@@ -309,6 +298,9 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
         const float ML = Ms * kLog2e;
 
         // ---- 2. S = sum exp(z - M), smoothing sum
+        // (softcap: exp2 argument c1 r + c0 and z = s - 2 s r, softcap_r2)
+        const float sc_c1 = -2.f * a.sc_slog2e;
+        const float sc_c0 = fmaf(-Ms, kLog2e, a.sc_slog2e);
         float2 s2 = make_float2(0.f, 0.f), z2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < NVL; ++k) {
@@ -318,10 +310,20 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
                 if (WS) reg_weights<VE>(a.weight, vbase + 32 * k, w);
 #pragma unroll
                 for (int j = 0; j < VE; j += 2) {
-                    float2 th;
-                    const float2 z = reg_z2<SOFTCAP>(f[j], f[j + 1], a, th);
-                    const float2 ar = reg_arg2<T>(z, Ms, ML);
-                    s2 = fadd2(s2, make_float2(ex2(ar.x), ex2(ar.y)));
+                    float2 z;
+                    if constexpr (SOFTCAP) {
+                        const float2 r = softcap_r2(f[j], f[j + 1], a.sc_k2);
+                        const float2 ar = ffma2(r, make_float2(sc_c1, sc_c1),
+                                                make_float2(sc_c0, sc_c0));
+                        s2 = fadd2(s2, make_float2(ex2(ar.x), ex2(ar.y)));
+                        if (smooth)
+                            z = ffma2(r, make_float2(-2.f * a.softcap, -2.f * a.softcap),
+                                      make_float2(a.softcap, a.softcap));
+                    } else {
+                        z = make_float2(f[j], f[j + 1]);
+                        const float2 ar = reg_arg2<T>(z, Ms, ML);
+                        s2 = fadd2(s2, make_float2(ex2(ar.x), ex2(ar.y)));
+                    }
                     if (WS)
                         z2 = ffma2(make_float2(w[j], w[j + 1]), z, z2);
                     else if (smooth)
@@ -411,6 +413,7 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;
             const float As = scale * ((1.f - a.eps) * wt + a.eps * Wf + 2.f * a.lam * lse) / S;
             const float Bc = -scale * a.eps * inv_V;
+            const float As4 = 4.f * As, Bc4 = 4.f * Bc;  // softcap: times r - r^2
 #pragma unroll
             for (int k = 0; k < NVL; ++k) {
                 if (32 * k < vlim) {
@@ -419,14 +422,22 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
                     if (WS) reg_weights<VE>(a.weight, vbase + 32 * k, w);
 #pragma unroll
                     for (int j = 0; j < VE; j += 2) {
-                        float2 th;
-                        const float2 z = reg_z2<SOFTCAP>(f[j], f[j + 1], a, th);
-                        const float2 ar = reg_arg2<T>(z, Ms, ML);
-                        const float2 bc = WS ? fmul2(make_float2(Bc, Bc), make_float2(w[j], w[j + 1]))
-                                             : make_float2(Bc, Bc);
-                        float2 gg = ffma2(make_float2(As, As), make_float2(ex2(ar.x), ex2(ar.y)), bc);
-                        if constexpr (SOFTCAP)
-                            gg = fmul2(gg, make_float2(fmaf(-th.x, th.x, 1.f), fmaf(-th.y, th.y, 1.f)));
+                        float2 gg;
+                        if constexpr (SOFTCAP) {
+                            // (As e + Bc) (1 - tanh^2) = (4 As e + 4 Bc) (r - r^2)
+                            const float2 r = softcap_r2(f[j], f[j + 1], a.sc_k2);
+                            const float2 ar = ffma2(r, make_float2(sc_c1, sc_c1),
+                                                    make_float2(sc_c0, sc_c0));
+                            const float2 bc = WS ? fmul2(make_float2(Bc4, Bc4), make_float2(w[j], w[j + 1]))
+                                                 : make_float2(Bc4, Bc4);
+                            gg = ffma2(make_float2(As4, As4), make_float2(ex2(ar.x), ex2(ar.y)), bc);
+                            gg = fmul2(gg, ffma2(make_float2(-r.x, -r.y), r, r));
+                        } else {
+                            const float2 ar = reg_arg2<T>(make_float2(f[j], f[j + 1]), Ms, ML);
+                            const float2 bc = WS ? fmul2(make_float2(Bc, Bc), make_float2(w[j], w[j + 1]))
+                                                 : make_float2(Bc, Bc);
+                            gg = ffma2(make_float2(As, As), make_float2(ex2(ar.x), ex2(ar.y)), bc);
+                        }
                         g[j] = gg.x;
                         g[j + 1] = gg.y;
                     }

@@ -42,14 +42,6 @@ constexpr uint32_t kStreamCopyChunk = 32768;
 
 __device__ __forceinline__ int64_t imin64(int64_t x, int64_t y) { return x < y ? x : y; }
 
-// z = softcap(x) for a pair of logits.
-template <bool SOFTCAP>
-__device__ __forceinline__ float2 capped2(float x0, float x1, const FwdArgs& a) {
-    if (!SOFTCAP) return make_float2(x0, x1);
-    return make_float2(a.softcap * tanh_from_scaled(x0 * a.sc_k2),
-                       a.softcap * tanh_from_scaled(x1 * a.sc_k2));
-}
-
 // exp2 arguments (z - m) * log2(e) for a pair. bf16 logits use one packed
 // FFMA against the rounded m*log2(e) (that rounding is common to a thread's
 // terms); fp32 logits subtract first.
@@ -141,6 +133,9 @@ struct PassOne {
         S *= ex2((m - mn) * kLog2e);
         m = mn;
         mL = fmaxf(mn, -1.0e30f) * kLog2e;
+        // softcap: the exp2 argument c1 r + c0 and z = s - 2 s r (softcap_r2)
+        const float sc_c1 = -2.f * a.sc_slog2e;
+        const float sc_c0 = fmaf(-mn, kLog2e, a.sc_slog2e);
         float2 sk[VPT], zk[VPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -152,9 +147,20 @@ struct PassOne {
                 if (WS) weights_of<VE>(w4, vidx0 + k * stride, vrow, w);
 #pragma unroll
                 for (int j = 0; j < VE; j += 2) {
-                    const float2 z = capped2<SOFTCAP>(f[j], f[j + 1], a);
-                    const float2 ar = exp_arg2<T>(z, m, mL);
-                    sk[k] = fadd2(sk[k], make_float2(ex2(ar.x), ex2(ar.y)));
+                    float2 z;
+                    if constexpr (SOFTCAP) {
+                        const float2 r = softcap_r2(f[j], f[j + 1], a.sc_k2);
+                        const float2 ar = ffma2(r, make_float2(sc_c1, sc_c1),
+                                                make_float2(sc_c0, sc_c0));
+                        sk[k] = fadd2(sk[k], make_float2(ex2(ar.x), ex2(ar.y)));
+                        if (WS || smooth)
+                            z = ffma2(r, make_float2(-2.f * a.softcap, -2.f * a.softcap),
+                                      make_float2(a.softcap, a.softcap));
+                    } else {
+                        z = make_float2(f[j], f[j + 1]);
+                        const float2 ar = exp_arg2<T>(z, m, mL);
+                        sk[k] = fadd2(sk[k], make_float2(ex2(ar.x), ex2(ar.y)));
+                    }
                     if (WS)
                         zk[k] = ffma2(make_float2(w[j], w[j + 1]), z, zk[k]);
                     else if (smooth)
@@ -226,6 +232,10 @@ __device__ __forceinline__ void grad_chunk(const uint4* ch, uint4* outv, int tg,
                                            int vg0) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;
+    // softcap (softcap_r2): exp2 argument c1 r + c0, constants times 4
+    const float sc_c1 = -2.f * a.sc_slog2e;
+    const float sc_c0 = fmaf(-M, kLog2e, a.sc_slog2e);
+    const float As4 = 4.f * As, Bc4 = 4.f * Bc;
     uint4 q[VPT];
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
@@ -238,19 +248,21 @@ __device__ __forceinline__ void grad_chunk(const uint4* ch, uint4* outv, int tg,
             if (WS) weights_of<VE>(w4, vg0 + k * GT, vrow, w);
 #pragma unroll
             for (int j = 0; j < VE; j += 2) {
-                float2 fac = make_float2(1.f, 1.f);
-                float2 z = make_float2(f[j], f[j + 1]);
-                if (SOFTCAP) {
-                    const float t0 = tanh_from_scaled(f[j] * a.sc_k2);
-                    const float t1 = tanh_from_scaled(f[j + 1] * a.sc_k2);
-                    fac = make_float2(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
-                    z = make_float2(a.softcap * t0, a.softcap * t1);
+                float2 g;
+                if constexpr (SOFTCAP) {
+                    // (As e + Bc) (1 - tanh^2) = (4 As e + 4 Bc) (r - r^2)
+                    const float2 r = softcap_r2(f[j], f[j + 1], a.sc_k2);
+                    const float2 ar = ffma2(r, make_float2(sc_c1, sc_c1), make_float2(sc_c0, sc_c0));
+                    const float2 bc = WS ? fmul2(make_float2(Bc4, Bc4), make_float2(w[j], w[j + 1]))
+                                         : make_float2(Bc4, Bc4);
+                    g = ffma2(make_float2(As4, As4), make_float2(ex2(ar.x), ex2(ar.y)), bc);
+                    g = fmul2(g, ffma2(make_float2(-r.x, -r.y), r, r));
+                } else {
+                    const float2 ar = exp_arg2<T>(make_float2(f[j], f[j + 1]), M, ML);
+                    const float2 bc = WS ? fmul2(make_float2(Bc, Bc), make_float2(w[j], w[j + 1]))
+                                         : make_float2(Bc, Bc);
+                    g = ffma2(make_float2(As, As), make_float2(ex2(ar.x), ex2(ar.y)), bc);
                 }
-                const float2 ar = exp_arg2<T>(z, M, ML);
-                const float2 bc = WS ? fmul2(make_float2(Bc, Bc), make_float2(w[j], w[j + 1]))
-                                     : make_float2(Bc, Bc);
-                float2 g = ffma2(make_float2(As, As), make_float2(ex2(ar.x), ex2(ar.y)), bc);
-                if (SOFTCAP) g = fmul2(g, fac);
                 gr[j] = g.x;
                 gr[j + 1] = g.y;
             }
