@@ -516,6 +516,49 @@ def test_register_cluster_ties_across_ctas(monkeypatch):
     assert np.array_equal(out["pred"][valid], np.array(firsts)[valid])
 
 
+def test_register_kernel_counts_back_to_back(monkeypatch):
+    # The register kernel forms the batch's D and counted rows in its
+    # leading CTA: launches queued back to back on one stream, with
+    # different D each (weights, ignore fractions, a batch with every row
+    # ignored, a single row), each against the oracle.
+    from softmax_cross_entropy_gb300 import _lib
+    monkeypatch.setenv("GBCE_KERNEL", "4")
+    cases = [workloads.random_case(61, 300, 4096, dtype="bf16", weight=True, ignore_frac=0.2),
+             workloads.random_case(62, 300, 4096, dtype="bf16", ignore_frac=1.0),
+             workloads.random_case(63, 1, 4096, dtype="bf16", weight=True),
+             workloads.random_case(64, 977, 2048, dtype="f32", ignore_frac=0.5),
+             workloads.random_case(65, 300, 4096, dtype="bf16", weight=True, ignore_frac=0.05)]
+    st = torch.cuda.current_stream().cuda_stream
+    runs = []
+    for case in cases:
+        x, t, w = to_device(case)
+        loss = torch.full((1,), float("nan"), device="cuda")
+        acc = torch.full((1,), float("nan"), device="cuda")
+        rc = _lib.ce_fwd(x.data_ptr(), CE_DTYPE[case.dtype], case.rows, case.V, t.data_ptr(),
+                         None if w is None else w.data_ptr(), case.ignore_index, 0.0, 0.0, 0.0,
+                         2, _lib.CE_FLAG_GRAD | _lib.CE_FLAG_ACC, loss.data_ptr(), None,
+                         acc.data_ptr(), None, st)
+        assert rc == 0
+        runs.append((case, x, t, w, loss, acc))
+    assert _lib.ce_device_status(st) == 0
+    for case, x, t, w, loss, acc in runs:
+        ref = oracle_full(case.with_(label_smoothing=0.0), reduction="mean")
+        if math.isnan(ref["loss"]):
+            assert math.isnan(float(loss.item())) and math.isnan(float(acc.item()))
+        else:
+            assert_loss_close(float(loss.item()), ref["loss"], case.dtype)
+            assert np.float32(acc.item()) == np.float32(ref["acc"])
+        assert_grad_close(grad_rows_f64(x), ref["grad"], case.dtype)
+
+
+def test_register_kernel_counts_many_rows(monkeypatch):
+    # more rows than the leading CTA counts by itself: the count kernel
+    # runs first, as for the other kernels
+    monkeypatch.setenv("GBCE_KERNEL", "4")
+    case = workloads.random_case(66, 40000, 256, dtype="bf16", weight=True, ignore_frac=0.3)
+    check_full(case, want_acc=True)
+
+
 def test_register_kernel_ties_across_warps(monkeypatch):
     # the row maximum repeated in several warps' vectors: the lowest index
     # wins
