@@ -500,10 +500,6 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     return CE_OK;
 }
 
-// The most rows whose targets the register kernel's leading CTA counts by
-// itself (a few microseconds for one CTA); more rows go to the count kernel.
-constexpr int64_t kSelfCountRows = 32768;
-
 // pdl: the launch may begin before the previous launch on the stream has
 // finished (programmatic dependent launch); the kernel then waits for it
 // (griddepcontrol.wait) before reading what it produced.
@@ -640,11 +636,7 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
         // by the accuracy of "sum" and "mean"
         const bool need = c.reduction == CE_RED_MEAN ||
                           (c.reduction == CE_RED_SUM && (c.flags & CE_FLAG_ACC));
-        if (need && !c.batch_counts && p.cluster <= 1 && c.rows <= kSelfCountRows) {
-            // the kernel's first CTA forms D and the counted rows itself
-            // (one launch); the others wait for them where they need them
-            a.self_count = 1;
-        } else if (need && !c.batch_counts) {
+        if (need && !c.batch_counts) {
             // D and the counted rows by the count kernel, into the scratch
             // header; the forward overlaps it and waits where it needs them
             CountArgs ca = {};

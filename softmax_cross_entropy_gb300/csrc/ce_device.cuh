@@ -76,58 +76,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ unsigned atom_add_acq_rel_gpu_u32(unsigned* p, unsigned v) {
-    unsigned old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
-                 : "=r"(old)
-                 : "l"(p), "r"(v)
-                 : "memory");
-    return old;
-}
-
-__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Waits until both words carry `tag` in their high 32 bits (each word is
-// written whole, so its low half is then the value published with the tag),
-// for at most timeout_ns nanoseconds of wall time, sleeping between reads.
-// The two reads of a round are independent (one load latency). Returns
-// false on timeout; lo0 / lo1 receive the low halves.
-__device__ __forceinline__ bool wait_tagged_pair(const unsigned long long* p, unsigned tag,
-                                                 uint64_t timeout_ns, unsigned& lo0,
-                                                 unsigned& lo1) {
-    uint64_t t0 = 0;
-#pragma unroll 1
-    for (int it = 0;; ++it) {
-        const unsigned long long v0 = ld_relaxed_gpu_u64(p);
-        const unsigned long long v1 = ld_relaxed_gpu_u64(p + 1);
-        if (static_cast<unsigned>(v0 >> 32) == tag && static_cast<unsigned>(v1 >> 32) == tag) {
-            lo0 = static_cast<unsigned>(v0);
-            lo1 = static_cast<unsigned>(v1);
-            return true;
-        }
-        if (it == 0) {
-            t0 = global_timer_ns();
-        } else if (global_timer_ns() - t0 > timeout_ns) {
-            return false;
-        }
-        __nanosleep(64);
-    }
-}
-
 // Waits for the phase of `bar` with the given parity to complete, for at
 // most timeout_ns nanoseconds of wall time. Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,

@@ -138,23 +138,11 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     // "sum" without accuracy needs neither (and the host then launches no
     // count kernel)
     bool have_counts = a.reduction == kRedNone || (a.reduction == kRedSum && !a.want_acc);
-    unsigned gen = 0;  // self_count: this launch's generation
-    auto need_counts = [&]() {  // by whole warps
+    auto need_counts = [&]() {
         if (!have_counts) {
-            if (a.self_count) {
-                // lane 0 waits (bounded) for the leading CTA's totals, which
-                // carry this launch's tag
-                unsigned dbits = 0x7fc00000u, nv = 0u;  // NaN, 0 after a timeout
-                if (lane == 0 &&
-                    !wait_tagged_pair(a.scratch->d_pub, gen + 1u, a.timeout_ns, dbits, nv))
-                    atomicOr(&a.scratch->status, kDevErrTimeout);
-                D = __uint_as_float(__shfl_sync(0xffffffffu, dbits, 0));
-                n_valid = static_cast<int>(__shfl_sync(0xffffffffu, nv, 0));
-            } else {
-                pdl_wait();
-                D = static_cast<float>(a.batch_counts[0]);
-                n_valid = static_cast<int>(a.batch_counts[1]);
-            }
+            pdl_wait();
+            D = static_cast<float>(a.batch_counts[0]);
+            n_valid = static_cast<int>(a.batch_counts[1]);
             have_counts = true;
         }
     };
@@ -202,8 +190,6 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             bulk_g2s(buf + off, src + off, min(32768u, row_bytes - off), bar, pol);
         pf_pending = true;
     };
-    __shared__ unsigned s_gen;
-    __shared__ int s_lead;
     if (tid == 0) {
         for (int tm = 0; tm < teams; ++tm) mbar_init(smem_u32(&pf_bar[tm]), 1);
         fence_mbar_init();
@@ -216,89 +202,6 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     // (a CTA whose slice is empty copies and waits for nothing)
     const bool has_slice = row_bytes > 0;
     if (lead && has_slice && r < a.rows && row_counts(a, t_cur)) prefetch(r);
-    if (a.self_count) {
-        // (with the first rows' copies in flight) The generation is read
-        // before arriving (the arrival is a release), and only the last CTA
-        // to arrive advances it, after its own arrival (an acquire): every
-        // CTA reads the same value. The first CTA to arrive leads.
-        if (tid == 0) {
-            const unsigned g = ld_acquire_gpu_u32(&a.scratch->d_gen);
-            const unsigned t = atom_add_acq_rel_gpu_u32(&a.scratch->d_arrive, 1u);
-            if (t == gridDim.x - 1) {
-                a.scratch->d_arrive = 0u;
-                a.scratch->d_gen = g + 1u;
-            }
-            s_gen = g;
-            s_lead = t == 0;
-        }
-        __syncthreads();
-        gen = s_gen;
-    }
-    if (a.self_count && s_lead) {
-        // the leading CTA (running, whatever else is resident) forms D =
-        // sum of w[t] over the batch's counted rows and their number, in a
-        // fixed order (thread-strided rows, warp butterfly, warps in
-        // order), while its first rows' copies are in flight
-        double d = 0.0;
-        long long n = 0;
-        auto count1 = [&](int64_t ti) {
-            if (row_counts(a, ti)) {
-                d += a.weight ? static_cast<double>(__ldg(a.weight + ti)) : 1.0;
-                ++n;
-            }
-        };
-        const int nthr = static_cast<int>(blockDim.x);
-        int64_t done = 0;  // rows counted by the vector loads
-        if (!a.tgt64 && (reinterpret_cast<uintptr_t>(a.target) & 15) == 0) {
-            // int32 targets four at a time, eight 16-byte loads a thread in
-            // flight at once (one round of load latency for 8192 rows)
-            const int4* t4 = reinterpret_cast<const int4*>(a.target);
-            const int64_t n4 = a.rows / 4;
-#pragma unroll 1
-            for (int64_t base = tid; base < n4; base += 8 * nthr) {
-                int4 v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (base + u * nthr < n4) v[u] = __ldg(t4 + base + u * nthr);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (base + u * nthr < n4) {
-                        count1(v[u].x);
-                        count1(v[u].y);
-                        count1(v[u].z);
-                        count1(v[u].w);
-                    }
-                }
-            }
-            done = n4 * 4;
-        }
-#pragma unroll 4
-        for (int64_t i = done + tid; i < a.rows; i += nthr) count1(load_target(a, i));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            d += __shfl_xor_sync(0xffffffffu, d, o);
-            n += __shfl_xor_sync(0xffffffffu, n, o);
-        }
-        if (lane == 0) {
-            red_d[0][warp] = d;
-            red_n[warp] = n;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            double dt = 0.0;
-            long long nt = 0;
-            for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
-                dt += red_d[0][w];
-                nt += red_n[w];
-            }
-            // D as the kernels use it (fp32) and the counted rows, each
-            // word tagged with this launch's generation + 1
-            const unsigned long long tag = static_cast<unsigned long long>(gen + 1u) << 32;
-            st_relaxed_gpu_u64(&a.scratch->d_pub[0], tag | __float_as_uint(static_cast<float>(dt)));
-            st_relaxed_gpu_u64(&a.scratch->d_pub[1], tag | static_cast<unsigned>(nt));
-        }
-        __syncthreads();
-    }
 #pragma unroll 1
     for (; r < a.rows; r += nteams) {
         const int64_t t = t_cur;

@@ -27,18 +27,9 @@ struct alignas(32) Partial {
 struct Scratch {
     unsigned ticket;
     unsigned status;
-    unsigned gemm_abort;  // abort flag of the tensor-core GEMM launch
-    // Register kernel counting its own batch (FwdArgs::self_count): CTAs
-    // that arrived this launch (reset by the last), the launch generation
-    // (advanced by the last), and the totals as {generation + 1 (high 32
-    // bits), fp32 bits of D / counted rows (low 32 bits)}, each word valid
-    // on its own
-    unsigned d_arrive;
+    unsigned pad0[2];  // pad0[0]: abort flag of the tensor-core GEMM launch
     double counts[2];
-    unsigned d_gen;
-    unsigned pad1;
-    unsigned long long d_pub[2];
-    unsigned pad[50];
+    unsigned pad[56];
     Partial partials[1];  // really kMaxPartials
 };
 static_assert(sizeof(Partial) == 32, "partial-sum slot layout");
@@ -88,10 +79,6 @@ struct FwdArgs {
     int reg_wpr;    // register-resident kernel: warps a row team has
     uint32_t reg_buf_stride;  // register-resident kernel: bytes of a team's row buffer
     int reg_cluster;  // register-resident kernel: CTAs of the cluster that owns a row (0, 1: one CTA)
-    // register-resident kernel, "sum" / "mean" without batch_counts: the
-    // first CTA to start forms D and the counted rows of the whole batch
-    // and publishes them through the scratch (no count kernel)
-    int self_count;
 };
 
 // Arguments of one forward call as the C ABI receives them (host side).

@@ -517,10 +517,10 @@ def test_register_cluster_ties_across_ctas(monkeypatch):
 
 
 def test_register_kernel_counts_back_to_back(monkeypatch):
-    # The register kernel forms the batch's D and counted rows in its
-    # leading CTA: launches queued back to back on one stream, with
-    # different D each (weights, ignore fractions, a batch with every row
-    # ignored, a single row), each against the oracle.
+    # Launches of the register kernel (and its count kernel) queued back to
+    # back on one stream, with a different D each (weights, ignore
+    # fractions, a batch with every row ignored, a single row), each against
+    # the oracle.
     from softmax_cross_entropy_gb300 import _lib
     monkeypatch.setenv("GBCE_KERNEL", "4")
     cases = [workloads.random_case(61, 300, 4096, dtype="bf16", weight=True, ignore_frac=0.2),
@@ -552,8 +552,7 @@ def test_register_kernel_counts_back_to_back(monkeypatch):
 
 
 def test_register_kernel_counts_many_rows(monkeypatch):
-    # more rows than the leading CTA counts by itself: the count kernel
-    # runs first, as for the other kernels
+    # many rows and a short row: many count-kernel CTAs
     monkeypatch.setenv("GBCE_KERNEL", "4")
     case = workloads.random_case(66, 40000, 256, dtype="bf16", weight=True, ignore_frac=0.3)
     check_full(case, want_acc=True)
