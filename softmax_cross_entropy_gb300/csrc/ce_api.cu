@@ -390,13 +390,12 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     }
     // Rows longer than one CTA of the register-resident kernel holds: a
     // cluster of C CTAs owns a row, each one 8-warp team holding a slice of
-    // 32 * 8 * nvl vectors (C <= 8, the portable cluster size).
-    const int64_t cl_nvl = nvl_env == 8 ? 8 : 16;
-    const int64_t cl_vpc = 32 * kRegMaxWarps * cl_nvl;
+    // 32 * 8 * 16 vectors (C <= 8, the portable cluster size).
+    const int64_t cl_vpc = 32 * kRegMaxWarps * 16;
     const int64_t cl_C = (vrow + cl_vpc - 1) / cl_vpc;
     if (fast_ok && (!wsmooth || w_aligned) && best.kind == Kind::General && cl_C >= 2 &&
         cl_C <= 8 && (forced_kind == 5 || (forced_kind == 0 && env_int("GBCE_REG_CLUSTER", 0)))) {
-        const void* fn = reg_kernel(dtype, softcap, wsmooth, static_cast<int>(cl_nvl));
+        const void* fn = reg_cluster_kernel(dtype, softcap, wsmooth);
         const int nt = 32 * kRegMaxWarps;
         const uint32_t stride = static_cast<uint32_t>(cl_vpc * 16);
         cudaFuncAttributes fa;

@@ -73,7 +73,9 @@ __device__ __forceinline__ float2 reg_arg2(float2 z, float Ms, float ML) {
 
 // 8 vectors a thread: three CTAs of 8 warps an SM (85 registers a thread);
 // 16 vectors: two (128 registers)
-template <typename T, bool SOFTCAP, bool WS, int NVL>
+// CLU: the cluster variant (a.reg_cluster CTAs a row); otherwise one CTA
+// holds whole rows and the cluster code folds away.
+template <typename T, bool SOFTCAP, bool WS, int NVL, bool CLU>
 __global__ void __launch_bounds__(32 * kRegMaxWarps, NVL == 8 ? 3 : 2)
 ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     using VT = Vec<T>;
@@ -101,7 +103,7 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     // warps each) owns a row, CTA c the slice of vectors [c * VPC, (c + 1) *
     // VPC); the row's maximum and sums merge across the cluster through
     // distributed shared memory.
-    const int CL = a.reg_cluster;
+    const int CL = CLU ? a.reg_cluster : 1;
     constexpr int VPC = kRegMaxWarps * 32 * NVL;  // vectors of a CTA's slice (cluster mode)
     const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     const int cta_vec0 = crank * VPC;              // first vector of this CTA's slice
@@ -507,13 +509,13 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     }
 }
 
-template <typename T, int NVL>
+template <typename T, int NVL, bool CLU = false>
 const void* reg_kernel_of(bool softcap, bool ws) {
     if (softcap)
-        return ws ? (const void*)&ce_fwd_reg<T, true, true, NVL>
-                  : (const void*)&ce_fwd_reg<T, true, false, NVL>;
-    return ws ? (const void*)&ce_fwd_reg<T, false, true, NVL>
-              : (const void*)&ce_fwd_reg<T, false, false, NVL>;
+        return ws ? (const void*)&ce_fwd_reg<T, true, true, NVL, CLU>
+                  : (const void*)&ce_fwd_reg<T, true, false, NVL, CLU>;
+    return ws ? (const void*)&ce_fwd_reg<T, false, true, NVL, CLU>
+              : (const void*)&ce_fwd_reg<T, false, false, NVL, CLU>;
 }
 
 }  // namespace gbce

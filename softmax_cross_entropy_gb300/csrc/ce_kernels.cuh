@@ -520,6 +520,8 @@ const void* generic_kernel(int dtype, bool softcap);
 // owns a row, nvl (8 or 16) 16-byte vectors a thread; a CTA has one or more
 // teams, at most kRegMaxWarps warps
 const void* reg_kernel(int dtype, bool softcap, bool ws, int nvl);
+// The register-resident kernel's cluster variant (16 vectors a thread).
+const void* reg_cluster_kernel(int dtype, bool softcap, bool ws);
 constexpr int kRegMaxWarps = 8;
 const void* count_kernel();
 // unfused kernels (dtype 0 fp32, 1 bf16, 2 fp16)
