@@ -21,6 +21,7 @@ buffer by grad_output. Every step runs in the CUDA kernels of libgbce.so
 from __future__ import annotations
 
 import math
+import os
 from collections import namedtuple
 
 import torch
@@ -42,6 +43,27 @@ CrossEntropyOutput = namedtuple("CrossEntropyOutput",
 _REDUCTIONS = {"none": _lib.CE_RED_NONE, "sum": _lib.CE_RED_SUM, "mean": _lib.CE_RED_MEAN}
 _DTYPES = {torch.float32: _lib.CE_F32, torch.bfloat16: _lib.CE_BF16,
            torch.float16: _lib.CE_F16}
+
+
+# NVTX ranges around the library's calls (forward, backward) for profiler
+# timelines, when GBCE_NVTX=1 at import; otherwise the ranges cost nothing.
+_NVTX = os.environ.get("GBCE_NVTX", "") not in ("", "0")
+
+
+class _Range:
+    __slots__ = ("name",)
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        if _NVTX:
+            torch.cuda.nvtx.range_push(self.name)
+
+    def __exit__(self, *exc):
+        if _NVTX:
+            torch.cuda.nvtx.range_pop()
+        return False
 
 
 def _ptr(t):
@@ -145,10 +167,11 @@ class CrossEntropyFunction(torch.autograd.Function):
     def forward(ctx, logits, target, weight, ignore_index, lse_square_scale, label_smoothing,
                 reduction, softcap, return_z_loss, return_acc, return_pred, batch_counts=None):
         want_grad = logits.requires_grad
-        loss, z_loss, acc, pred = _forward(logits, target, weight, ignore_index,
-                                           lse_square_scale, label_smoothing, reduction,
-                                           softcap, want_grad, return_z_loss, return_acc,
-                                           return_pred, batch_counts)
+        with _Range("gbce.cross_entropy.forward"):
+            loss, z_loss, acc, pred = _forward(logits, target, weight, ignore_index,
+                                               lse_square_scale, label_smoothing, reduction,
+                                               softcap, want_grad, return_z_loss, return_acc,
+                                               return_pred, batch_counts)
         ctx.reduction = reduction
         if want_grad:
             ctx.save_for_backward(logits.detach())  # now holds dlogits
@@ -162,7 +185,7 @@ class CrossEntropyFunction(torch.autograd.Function):
         (dlogits,) = ctx.saved_tensors
         g = grad_loss.to(torch.float32).contiguous()
         per_row = 1 if ctx.reduction == "none" else 0
-        with torch.cuda.device(dlogits.device):
+        with torch.cuda.device(dlogits.device), _Range("gbce.cross_entropy.backward"):
             if dlogits.dim() > 2:
                 N, C = dlogits.shape[0], dlogits.shape[1]
                 rc, where = ce_bwd_nd(_ptr(g), per_row, _ptr(dlogits), _DTYPES[dlogits.dtype], N,
@@ -264,10 +287,11 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
         if want_grad and reduction == "none":
             raise ValueError("fused_linear_cross_entropy differentiates a scalar loss: use "
                              "reduction 'mean' or 'sum' (or no gradient)")
-        loss, z_loss, acc, pred, gh, gw, gb = _flce_call(
-            hidden, lm_weight, target, bias, weight, ignore_index, lse_square_scale,
-            label_smoothing, reduction, softcap, return_z_loss, return_acc, return_pred,
-            want_grad, chunk_rows)
+        with _Range("gbce.fused_linear_cross_entropy.forward"):
+            loss, z_loss, acc, pred, gh, gw, gb = _flce_call(
+                hidden, lm_weight, target, bias, weight, ignore_index, lse_square_scale,
+                label_smoothing, reduction, softcap, return_z_loss, return_acc, return_pred,
+                want_grad, chunk_rows)
         ctx.w_dtype = lm_weight.dtype
         ctx.has_bias = bias is not None
         if want_grad:
@@ -282,7 +306,7 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
         gh, gw, gb = ctx.saved_tensors
         g = grad_loss.to(torch.float32).reshape(1).contiguous()
         dev = gh.device
-        with torch.cuda.device(dev):
+        with torch.cuda.device(dev), _Range("gbce.fused_linear_cross_entropy.backward"):
             st = _stream(dev)
             rows, H = gh.shape
             rc = ce_bwd(_ptr(g), 0, _ptr(gh), _DTYPES[gh.dtype], rows, H, st)

@@ -597,6 +597,9 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
     a.timeout_ns = static_cast<uint64_t>(env_int("GBCE_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
     a.scratch = scratch;
     a.batch_counts = c.batch_counts;
+    // test hook: the streaming and register kernels leave one copy out, so
+    // one bounded wait runs out (GBCE_TEST_STALL_COPY=1)
+    a.test_stall = env_int("GBCE_TEST_STALL_COPY", 0) != 0 ? 1 : 0;
 
     const bool wsmooth = c.weight != nullptr && c.label_smoothing > 0.f;
     const bool aligned = (reinterpret_cast<uintptr_t>(c.logits) % 16) == 0;

@@ -183,7 +183,14 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     uint32_t pf_phase = 0;
     bool pf_pending = false;  // leader: a copy into the buffer is outstanding
     bool failed = false;
+    // test hook (FwdArgs::test_stall): the first copy of CTA 0's first team
+    // is left out, so the team's wait for it runs out
+    bool stall = a.test_stall && blockIdx.x == 0 && team == 0;
     auto prefetch = [&](int64_t row) {  // leader only, buffer free
+        if (stall) {
+            stall = false;
+            return;
+        }
         const char* src = reinterpret_cast<const char*>(a.x) +
                           row * a.V * static_cast<int64_t>(sizeof(T)) +
                           static_cast<int64_t>(cta_vec0) * 16;

@@ -386,6 +386,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
         }
         int failed = 0;
         int g = 0;
+        bool stall = a.test_stall && cid == 0;  // test hook (FwdArgs::test_stall)
         for (int64_t rb = cid; rb < a.rows && !failed; rb += 32 * ncta) {
             const int64_t rl = rb + lane * ncta;
             const bool lane_counts = rl < a.rows && (LSM || row_counts(a, load_target(a, rl)));
@@ -423,6 +424,10 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                             const uint32_t bytes =
                                 static_cast<uint32_t>(imin64(chunk_vec, vec_row - v0)) * 16u;
                             const uint32_t fb = smem_u32(&full_bar[slot]);
+                            if (stall) {
+                                stall = false;
+                                continue;
+                            }
                             mbar_arrive_expect_tx(fb, bytes);
                             const char* src = reinterpret_cast<const char*>(a.x) +
                                               (r * a.V + v0 * VE) * static_cast<int64_t>(sizeof(T));

@@ -79,6 +79,9 @@ struct FwdArgs {
     int reg_wpr;    // register-resident kernel: warps a row team has
     uint32_t reg_buf_stride;  // register-resident kernel: bytes of a team's row buffer
     int reg_cluster;  // register-resident kernel: CTAs of the cluster that owns a row (0, 1: one CTA)
+    // test hook: CTA 0 does not issue its first bulk copy, so the wait for
+    // it runs out (status CE_ERR_TIMEOUT, outputs invalid, nothing faults)
+    int test_stall;
 };
 
 // Arguments of one forward call as the C ABI receives them (host side).

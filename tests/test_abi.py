@@ -139,3 +139,24 @@ def test_python_api_rejects_rank_1_and_nd_logits():
         ce.cross_entropy(torch.zeros(2, 4, 5), t)    # class dimension not last / N-D
     with pytest.raises(ValueError):
         ce.cross_entropy(torch.zeros(4, 5), t)       # not on a CUDA device
+
+
+def test_nvtx_ranges_only_when_asked(monkeypatch):
+    # the wrapper's NVTX ranges push and pop in pairs when enabled, and call
+    # nothing when not
+    import torch
+    import softmax_cross_entropy_gb300 as gbce
+    calls = []
+    monkeypatch.setattr(torch.cuda.nvtx, "range_push", lambda n: calls.append(("push", n)))
+    monkeypatch.setattr(torch.cuda.nvtx, "range_pop", lambda: calls.append(("pop",)))
+    monkeypatch.setattr(gbce, "_NVTX", False)
+    with gbce._Range("gbce.x"):
+        pass
+    assert calls == []
+    monkeypatch.setattr(gbce, "_NVTX", True)
+    try:
+        with gbce._Range("gbce.y"):
+            raise KeyError("inside")
+    except KeyError:
+        pass
+    assert calls == [("push", "gbce.y"), ("pop",)]
