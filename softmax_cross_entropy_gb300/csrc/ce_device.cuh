@@ -114,6 +114,13 @@ __device__ __forceinline__ uint4 ld_v4_hint(const void* p, uint64_t pol) {
     return v;
 }
 
+// 16-byte global store with an L2 eviction-policy hint.
+__device__ __forceinline__ void st_v4_hint(void* p, const uint4& v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
 // Global -> shared bulk copy that signals `bar` with the bytes it delivers.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
