@@ -229,7 +229,7 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             if (a.grad) {
 #pragma unroll
                 for (int k = 0; k < NVL; ++k)
-                    if (32 * k < vlim) rowv[vbase + 32 * k] = make_uint4(0u, 0u, 0u, 0u);
+                    if (32 * k < vlim) st_v4_hint(rowv + vbase + 32 * k, make_uint4(0u, 0u, 0u, 0u), pol);
             }
             if (lead && crank == 0) {
                 if (a.reduction == kRedNone) {
@@ -450,7 +450,13 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
                         g[j] = gg.x;
                         g[j + 1] = gg.y;
                     }
-                    rowv[vbase + 32 * k] = VT::pack(g);
+                    // (evict-first stores: measured 2% faster for short rows;
+                    // the weighted-smoothing kernel keeps plain stores, which
+                    // measured 1% faster there)
+                    if constexpr (WS)
+                        rowv[vbase + 32 * k] = VT::pack(g);
+                    else
+                        st_v4_hint(rowv + vbase + 32 * k, VT::pack(g), pol);
                 }
             }
             if (owner) {
