@@ -86,6 +86,21 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def provenance():
+    """What produced the line: the git commit when the tree is a checkout
+    (None otherwise, e.g. on a copy without .git) and the hash of the headline
+    kernel's sources, which is always known."""
+    sha = None
+    try:
+        r = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True,
+                           text=True, timeout=10)
+        if r.returncode == 0:
+            sha = r.stdout.strip() or None
+    except Exception:
+        sha = None
+    return {"git_sha": sha, "headline_kernel_sources": kernel_source_hash()}
+
+
 def recorded_traffic(workload_key):
     """DRAM bytes per launch of the forward kernel from the committed ncu
     summary, or None if absent or taken on other kernel sources."""
@@ -416,6 +431,7 @@ def run_gpu(args):
 
     if clocks:
         line["clocks"] = clocks
+    line["source"] = provenance()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
     if rank == 0:

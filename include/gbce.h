@@ -376,6 +376,13 @@ ce_status ce_bwd(const float* grad_output, int grad_per_row, void* dlogits,
  * ce_device_status - synchronizes `stream`, then reads and clears the
  * device-side error word of that stream's scratch area. Returns CE_OK,
  * CE_ERR_TARGET_RANGE, CE_ERR_TIMEOUT or CE_ERR_CUDA.
+ *
+ * Environment read at each call: GBCE_WAIT_TIMEOUT_MS (default 2000) bounds
+ * every device wait of a launch in wall time; GBCE_TEST_STALL_COPY=1 is a
+ * test hook that makes CTA 0 of the streaming or register-resident forward
+ * kernel leave its first bulk copy out, so that one wait runs out and the
+ * call records CE_ERR_TIMEOUT (its outputs are then invalid; nothing
+ * faults).
  */
 ce_status ce_device_status(ce_stream_t stream);
 

@@ -160,3 +160,13 @@ def test_nvtx_ranges_only_when_asked(monkeypatch):
     except KeyError:
         pass
     assert calls == [("push", "gbce.y"), ("pop",)]
+
+
+def test_bench_provenance_names_the_sources():
+    # the bench line records what produced it: the headline kernel's source
+    # hash always, the git commit when the tree is a checkout
+    import bench
+    p = bench.provenance()
+    assert p["headline_kernel_sources"] == bench.kernel_source_hash()
+    assert len(p["headline_kernel_sources"]) == 16
+    assert p["git_sha"] is None or len(p["git_sha"]) == 40
