@@ -51,7 +51,9 @@ struct Plan {
     uint32_t reg_buf_stride = 0;  // register-resident kernel: bytes of a team's row buffer
 };
 
-using PlanKey = std::tuple<int, int, int64_t, bool, bool, int>;
+// (device, dtype, V (negative when the logits are not 16-byte aligned),
+// softcap, weighted smoothing, weights 16-byte aligned, tuning signature)
+using PlanKey = std::tuple<int, int, int64_t, bool, bool, bool, std::string>;
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
@@ -61,6 +63,23 @@ std::map<PlanKey, Plan> g_plans;
 int env_int(const char* name, int fallback) {
     const char* v = std::getenv(name);
     return (v && *v) ? std::atoi(v) : fallback;
+}
+
+// Every tuning override that the kernel plans read, as one string: part of
+// each plan cache key, so that a plan made under one setting never serves
+// another.
+std::string tuning_signature() {
+    static const char* const kVars[] = {
+        "GBCE_KERNEL",        "GBCE_CLUSTER",      "GBCE_CFG",          "GBCE_MAX_STAGES",
+        "GBCE_STREAM_GROUPS", "GBCE_STREAM_TWICE", "GBCE_STREAM_SLOTS", "GBCE_STREAM_WARPS",
+        "GBCE_REG_MAX_BYTES", "GBCE_REG_NVL",      "GBCE_REG_CLUSTER"};
+    std::string sig;
+    for (const char* name : kVars) {
+        const char* v = std::getenv(name);
+        if (v) sig += v;
+        sig += '|';
+    }
+    return sig;
 }
 
 ce_status device_info(int dev, DeviceInfo* out) {
@@ -322,14 +341,8 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     // GBCE_KERNEL: 1 staged, 2 streaming, 3 general, 4 register-resident,
     // 5 register-resident with a cluster of CTAs a row (0: automatic)
     const int forced_kind = env_int("GBCE_KERNEL", 0);
-    const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth,
-                      (forced_kind * 64 + forced_c) * 64 + forced_cfg +
-                          1000000 * env_int("GBCE_STREAM_GROUPS", 0) +
-                          100000000 * env_int("GBCE_STREAM_TWICE", 0) +
-                          13 * env_int("GBCE_STREAM_SLOTS", 0) +
-                          17 * env_int("GBCE_STREAM_WARPS", 0) +
-                          19 * (env_int("GBCE_REG_MAX_BYTES", 65536) + (w_aligned ? 0 : 1)) +
-                          7 * env_int("GBCE_REG_NVL", 0) + 3 * env_int("GBCE_REG_CLUSTER", 0));
+    const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth, w_aligned,
+                      tuning_signature());
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
         *out = it->second;
@@ -810,7 +823,7 @@ ce_status device_and_scratch(cudaStream_t st, int* dev, DeviceInfo* info, Scratc
     return scratch_for(*dev, st, scratch);
 }
 
-std::map<std::tuple<int, int, int64_t>, Plan> g_lsm_plans;
+std::map<std::tuple<int, int, int64_t, std::string>, Plan> g_lsm_plans;
 
 }  // namespace
 }  // namespace gbce
@@ -829,7 +842,7 @@ extern "C" ce_status ce_log_softmax(const void* x, void* out, int dtype, int64_t
     rc = device_and_scratch(st, &dev, &info, &scratch);
     if (rc != CE_OK) return rc;
     if (aligned16(x) && aligned16(out) && (C * dtype_bytes(dtype)) % 16 == 0) {
-        const auto key = std::make_tuple(dev, dtype, C);
+        const auto key = std::make_tuple(dev, dtype, C, tuning_signature());
         auto it = g_lsm_plans.find(key);
         if (it == g_lsm_plans.end()) {
             Plan p;
