@@ -136,7 +136,7 @@ def test_python_api_rejects_rank_1_and_nd_logits():
     with pytest.raises(ValueError):
         ce.cross_entropy(torch.zeros(4), t)          # rank 1
     with pytest.raises(ValueError):
-        ce.cross_entropy(torch.zeros(2, 4, 5), t)    # class dimension not last / N-D
+        ce.cross_entropy(torch.zeros(2, 4, 5), t)    # N-D logits on the CPU
     with pytest.raises(ValueError):
         ce.cross_entropy(torch.zeros(4, 5), t)       # not on a CUDA device
 

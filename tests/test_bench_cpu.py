@@ -25,3 +25,15 @@ def test_reference_arm_prints_one_json_line():
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["rows"] == 4096 and d["config"]["V"] == 131072
+
+
+def test_cpu_baseline_single_and_row_partitioned():
+    # the oracle timed single-threaded and over every host core, on a small
+    # bf16 case of the headline's kind
+    import bench
+    import workloads
+    case = workloads.vsweep(V=4096, rows=96)
+    b = bench.cpu_baseline(case, 0.5, partitioned_seconds=1.0)
+    assert b["kind"] == "oracle" and b["cores"] == 1 and b["value"] > 0
+    p = b["row_partitioned"]
+    assert p["cores"] == bench.host_cores() >= 1 and p["value"] > 0 and p["unit"] == "GB/s"
