@@ -12,14 +12,19 @@ throughput over the algorithmic bytes (one read and one write of the logits
 plus the targets) and rows/s; the V sweep of the same profile is reported
 beside it.
 
-Timing: W eager warm-up steps, then exactly K steps replayed from a captured
-CUDA graph, bracketed by a barrier and device synchronisation and timed with
+Timing: W eager warm-up steps, then exactly K steps replayed from captured
+CUDA graphs, bracketed by a barrier and device synchronisation and timed with
 CUDA events on the launching stream; the maximum over ranks is reported.
-Steps cycle over a pool of device input buffers; each buffer is larger than
-L2 or the pool is deep enough that a buffer is evicted before its reuse, and
-L2 is flushed before the timed region. The pool is filled with the seeded
-logits before the timed region; the in-place gradient of a step becomes the
-next input of that buffer (the work per step does not depend on the values).
+Every timed step runs on its own device buffer holding the seeded logits:
+the pool has one buffer per step (as many as fit in 60% of free device
+memory; beyond that the K steps run as several graph replays, each timed
+alone and summed, with the pool refilled and L2 flushed outside the timed
+regions). The pool is refilled and L2 flushed (a write of twice its size)
+before every timed region.
+
+--gpus N: one process per GPU. When the launcher has not set WORLD_SIZE,
+bench.py starts the N ranks itself (torch.distributed.run on 127.0.0.1);
+every rank times its own batch (weak scaling, no data-path collective).
 
 --impl reference times the CPU float64 oracle on the host cores, on a
 bounded sample of the same workload, and prints the same JSON line.
@@ -180,7 +185,7 @@ class GpuRunner:
     pool of input buffers, an L2 flush buffer and a stream; ce_fwd and ce_bwd
     through the C ABI with the workload's options."""
 
-    def __init__(self, case, device, torch):
+    def __init__(self, case, device, torch, steps=2):
         from softmax_cross_entropy_gb300 import _lib
         self.torch, self.lib, self.case, self.dev = torch, _lib, case, device
         if case.dtype == "f32":
@@ -197,7 +202,10 @@ class GpuRunner:
         self.target = self.host_t.to(device)
         self.weight = None if case.weight is None else torch.from_numpy(case.weight).to(device)
         self.nbytes = self.pristine.numel() * self.elem
-        self.pool = max(2, min(16, math.ceil(3 * L2_BYTES / self.nbytes) + 1))
+        # one buffer per timed step, within 60% of the free device memory
+        free = torch.cuda.mem_get_info(device)[0]
+        fit = int(0.6 * free // max(self.nbytes, 1))
+        self.pool = max(2, min(max(steps, 2), fit))
         self.bufs = [torch.empty_like(self.pristine) for _ in range(self.pool)]
         self.red = _RED[case.reduction]
         n = case.rows if self.red == 0 else 1
@@ -259,6 +267,23 @@ class GpuRunner:
         barrier()
         return e0.elapsed_time(e1) / 1e3
 
+    def time_steps(self, steps, body, barrier):
+        """Times `steps` steps, each on a fresh pool buffer: graphs of at
+        most `pool` steps, each replay timed alone (pool refilled and L2
+        flushed before it) and the times summed. Returns seconds."""
+        full, rem = divmod(steps, self.pool)
+        total = 0.0
+        if full:
+            g = self.capture(self.pool, body)
+            for _ in range(full):
+                total += self.time_graph(g, barrier)
+            del g
+        if rem:
+            g = self.capture(rem, body)
+            total += self.time_graph(g, barrier)
+            del g
+        return total
+
     def warmup(self, steps):
         st = self.stream.cuda_stream
         with self.torch.cuda.stream(self.stream):
@@ -272,11 +297,14 @@ class GpuRunner:
         if s != 0:
             raise RuntimeError(f"device status after warm-up: {self.lib.ce_status_string(s)}")
 
-    def e2e(self, steps, barrier):
+    def e2e(self, steps, barrier, read_grad=True):
         """Through the C ABI from pinned host memory: per step, copy the
-        logits and targets in, run forward + backward, read the loss back."""
+        logits and targets in, run forward + backward, read the loss back
+        and (read_grad) the gradient, which overwrote the logits, into a
+        pinned host buffer."""
         torch = self.torch
         out = torch.empty(1, dtype=torch.float32).pin_memory()
+        host_grad = torch.empty_like(self.host).pin_memory() if read_grad else None
         x = self.bufs[0]
         st = self.stream.cuda_stream
         torch.cuda.synchronize(self.dev)
@@ -291,11 +319,14 @@ class GpuRunner:
                 self.fwd(x, st)
                 self.bwd(x, self.one, st)
                 out.copy_(self.loss, non_blocking=True)
+                if read_grad:
+                    host_grad.copy_(x, non_blocking=True)
             e1.record(self.stream)
         torch.cuda.synchronize(self.dev)
         barrier()
         h2d = self.host.numel() * self.elem + self.host_t.numel() * 4
-        return e0.elapsed_time(e1) / 1e3, h2d, 4
+        d2h = 4 + (self.host.numel() * self.elem if read_grad else 0)
+        return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
 def run_gpu(args):
@@ -303,6 +334,8 @@ def run_gpu(args):
     import torch.distributed as dist
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE is {world}")
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     device = torch.device("cuda", local)
@@ -333,22 +366,27 @@ def run_gpu(args):
 
     # ---- headline workload
     case = workloads.vsweep(V=V_MAIN, rows=ROWS, seed=rank)
-    runner = GpuRunner(case, device, torch)
+    runner = GpuRunner(case, device, torch, steps=K)
     if sampler:
         sampler.start()
     runner.warmup(W)
-    g_step = runner.capture(K, lambda b, st: (runner.fwd(b, st), runner.bwd(b, runner.one, st)))
-    g_fwd = runner.capture(K, lambda b, st: runner.fwd(b, st))
-    t_step = max_over_ranks(runner.time_graph(g_step, barrier))
-    t_fwd = max_over_ranks(runner.time_graph(g_fwd, barrier))
+    t_step = max_over_ranks(runner.time_steps(
+        K, lambda b, st: (runner.fwd(b, st), runner.bwd(b, runner.one, st)), barrier))
+    t_fwd = max_over_ranks(runner.time_steps(K, lambda b, st: runner.fwd(b, st), barrier))
     clocks = sampler.stop() if sampler else None
-    g_bwd = runner.capture(K, lambda b, st: runner.bwd(b, runner.half, st))
-    t_bwd = max_over_ranks(runner.time_graph(g_bwd, barrier))
+    t_bwd = max_over_ranks(runner.time_steps(
+        K, lambda b, st: runner.bwd(b, runner.half, st), barrier))
+    # forward only (loss and metrics, no gradient): one read of the logits
+    runner.flags &= ~runner.lib.CE_FLAG_GRAD
+    t_fo = max_over_ranks(runner.time_steps(K, lambda b, st: runner.fwd(b, st), barrier))
+    runner.flags |= runner.lib.CE_FLAG_GRAD
     t_e2e, h2d, d2h = runner.e2e(K, barrier)
     t_e2e = max_over_ranks(t_e2e)
-    del g_step, g_fwd, g_bwd
+    t_e2e_loss, h2d_l, d2h_l = runner.e2e(K, barrier, read_grad=False)
+    t_e2e_loss = max_over_ranks(t_e2e_loss)
 
     bytes_step = algorithmic_bytes(case.rows, case.V, 2)
+    fo_bytes = case.rows * (case.V * 2 + 4)
     value = world * bytes_step * K / t_step / 1e9
     achieved = bytes_step / (t_fwd / K) / 1e9
     traffic = recorded_traffic(f"vsweep_V{V_MAIN}")
@@ -359,10 +397,12 @@ def run_gpu(args):
         "data": "synthetic (seeded N(0,3^2) bf16 logits, uniform targets, 5% ignored)",
         "config": {"workload": workload_desc(V_MAIN), "rows": ROWS, "V": V_MAIN,
                    "parallelism": f"dp{world} (independent row shards, no collective)",
-                   "l2": f"inputs larger than L2 (pool of {runner.pool} x "
-                         f"{runner.nbytes / 2**30:.2f} GiB buffers), L2 flushed before the "
-                         f"timed region",
-                   "timing": "CUDA graph of K steps, CUDA events on the launching stream"},
+                   "l2": f"inputs larger than L2: every timed step on its own buffer of "
+                         f"seeded logits (pool of {runner.pool} x "
+                         f"{runner.nbytes / 2**30:.2f} GiB), L2 flushed before each timed "
+                         f"region",
+                   "timing": "CUDA graphs of up to K steps (one buffer a step), CUDA events "
+                             "on the launching stream"},
         "rows_per_s": round(world * case.rows * K / t_step, 1),
         "elements_per_s": round(world * case.rows * case.V * K / t_step, 1),
         "frac_of_peak": round(value / world / peak, 4),
@@ -374,8 +414,21 @@ def run_gpu(args):
                      "avg_launch_us": round(t_fwd / K * 1e6, 2)},
         "e2e": {"value": round(world * bytes_step * K / t_e2e / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(t_e2e / K * 1e3, 4)},
+                "ms_per_step": round(t_e2e / K * 1e3, 4),
+                "what": "per step: logits and targets copied in from pinned host memory, "
+                        "ce_fwd + ce_bwd through the C ABI, loss and the whole gradient "
+                        "copied back to pinned host memory"},
+        "e2e_loss_only": {"value": round(world * bytes_step * K / t_e2e_loss / 1e9, 1),
+                          "unit": "GB/s", "h2d_bytes_per_step": h2d_l,
+                          "d2h_bytes_per_step": d2h_l,
+                          "ms_per_step": round(t_e2e_loss / K * 1e3, 4)},
         "gpu_launches": 2 * K,
+        "forward_only": {
+            "value": round(fo_bytes * K / t_fo / 1e9, 1), "unit": "GB/s",
+            "frac": round(fo_bytes * K / t_fo / 1e9 / peak, 4),
+            "us_per_launch": round(t_fo / K * 1e6, 2), "bytes_per_launch": fo_bytes,
+            "what": "ce_fwd without CE_FLAG_GRAD (loss and metrics only): one read of the "
+                    "logits plus the targets"},
         "bwd_scale_g_ne_1": {"value": round(bytes_step * K / t_bwd / 1e9, 1), "unit": "GB/s",
                              "us_per_launch": round(t_bwd / K * 1e6, 2)},
     }
@@ -387,17 +440,17 @@ def run_gpu(args):
         sweep = []
         for V in workloads.VSWEEP:
             c = workloads.vsweep(V=V, rows=ROWS, seed=rank)
-            r = GpuRunner(c, device, torch)
+            r = GpuRunner(c, device, torch, steps=K)
             r.warmup(max(W, 3))
             ks = K
-            g1 = r.capture(ks, lambda b, st: (r.fwd(b, st), r.bwd(b, r.one, st)))
-            t = max_over_ranks(r.time_graph(g1, barrier))
+            t = max_over_ranks(r.time_steps(
+                ks, lambda b, st: (r.fwd(b, st), r.bwd(b, r.one, st)), barrier))
             by = algorithmic_bytes(c.rows, c.V, 2)
             sweep.append({"V": V, "GB/s": round(by * ks / t / 1e9, 1),
                           "frac": round(by * ks / t / 1e9 / peak, 4),
                           "us_per_step": round(t / ks * 1e6, 2),
                           "rows_per_s": round(c.rows * ks / t, 1)})
-            del g1, r
+            del r
             torch.cuda.empty_cache()
         line["sweep"] = sweep
 
@@ -407,17 +460,17 @@ def run_gpu(args):
         configs = []
         for name, make in extra_workloads(rank):
             c = make()
-            r = GpuRunner(c, device, torch)
+            r = GpuRunner(c, device, torch, steps=K)
             r.warmup(max(W, 3))
-            g1 = r.capture(K, lambda b, st: (r.fwd(b, st), r.bwd(b, r.one, st)))
-            t = max_over_ranks(r.time_graph(g1, barrier))
+            t = max_over_ranks(r.time_steps(
+                K, lambda b, st: (r.fwd(b, st), r.bwd(b, r.one, st)), barrier))
             by = r.bytes_per_step()
             configs.append({"workload": name, "rows": c.rows, "V": c.V, "dtype": c.dtype,
                             "GB/s": round(by * K / t / 1e9, 1),
                             "frac": round(by * K / t / 1e9 / peak, 4),
                             "us_per_step": round(t / K * 1e6, 2),
                             "rows_per_s": round(c.rows * K / t, 1)})
-            del g1, r, c
+            del r, c
             torch.cuda.empty_cache()
         line["configs"] = configs
         # the decomposed (unfused) form on the decomposed graph's own shape;
@@ -757,6 +810,19 @@ def run_profile_target(args):
                       "steps": args.ncu_steps}))
 
 
+def launch_ranks(n):
+    """Starts n ranks of this same command line (one process per GPU,
+    torch.distributed.run on 127.0.0.1) and returns their exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -781,6 +847,10 @@ def main():
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(args.gpus))
     if args.impl == "reference":
         run_reference(args)
     else:

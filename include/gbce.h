@@ -145,23 +145,43 @@ ce_status ce_fwd(void* logits, int dtype, int64_t rows, int64_t V,
  * Arguments, outputs and results are those of ce_fwd. Differences:
  *  - The scratch holds 2048 partial-sum slots, one per CTA (or cluster) of
  *    the launch; a launch that would need more returns CE_ERR_UNSUPPORTED
- *    and ce_last_error names the number. (On a GB300 no launch of this
- *    library uses more than 8 slots per SM, 1216 in all.)
+ *    with nothing enqueued, and ce_last_error names the number. (Every
+ *    launch plan of this library is capped at 8 slots per SM, 1216 on a
+ *    GB300's 152 SMs, so this happens only on a GPU with more than 256
+ *    SMs.)
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.
  *  - Every call, on every stream, shares the same array. Each call clears
- *    the part that must start at zero, but calls that overlap on the GPU
- *    (different streams, or concurrent host threads) race on it; order
- *    them on one stream or synchronise between them.
- *  - Its device-side status word is cleared at the start of each call and
- *    is not reported by ce_device_status.
+ *    the part that must start at zero (the epilogue's ticket), but calls
+ *    that overlap on the GPU (different streams, or concurrent host
+ *    threads) race on it; order them on one stream or synchronise between
+ *    them.
+ *  - Device-detected errors (a target outside [0, V), a bounded wait that
+ *    ran out) go to the array's own sticky status word, which
+ *    ce_noalloc_status reads and clears; ce_device_status does not see it.
+ *  - Test hook, read at each call: GBCE_TEST_NOALLOC_SLOTS=n (1 <= n <
+ *    2048) lowers the usable slots to n, so that the refusal above can be
+ *    exercised on any GPU.
  */
 ce_status ce_fwd_noalloc(void* logits, int dtype, int64_t rows, int64_t V,
                          const void* target, const float* weight, int64_t ignore_index,
                          float label_smoothing, float lse_square_scale, float softcap,
                          int reduction, uint32_t flags, float* loss, float* z_loss,
                          float* acc, int64_t* pred, ce_stream_t stream);
+
+/*
+ * ce_noalloc_status - the device-detected errors of ce_fwd_noalloc calls.
+ *
+ * Like ce_device_status, but for the fixed array ce_fwd_noalloc uses (the
+ * method has no counterpart for it either). Synchronises `stream`, copies
+ * the array's status word of the current device into a host variable,
+ * clears it, and returns CE_ERR_TIMEOUT or CE_ERR_TARGET_RANGE if any
+ * ce_fwd_noalloc call since the last read recorded one (the word is shared
+ * by every stream), else CE_OK. Allocates nothing; CE_ERR_CUDA if a copy
+ * or the synchronisation fails.
+ */
+ce_status ce_noalloc_status(ce_stream_t stream);
 
 /*
  * ce_count - counts of one shard of rows, for a "mean" over a batch whose
@@ -391,6 +411,15 @@ const char* ce_status_string(ce_status status);
 
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */
 const char* ce_last_error(void);
+
+/*
+ * ce_scratch_areas - how many (device, stream) scratch areas ce_fwd and the
+ * other allocating calls have made so far in this process (each about
+ * 128 KB of device memory, kept until exit). ce_fwd_noalloc and
+ * ce_noalloc_status never add one. Not part of the method; a query for
+ * callers that budget device memory.
+ */
+int64_t ce_scratch_areas(void);
 
 #ifdef __cplusplus
 }

@@ -41,6 +41,8 @@ SIGNATURES = {
     "ce_nll_loss_bwd": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _I64, _I, _U32, _P]),
     "ce_log_softmax_bwd": (_I, [_P, _P, _P, _I, _I64, _I64, _P]),
     "ce_device_status": (_I, [_P]),
+    "ce_noalloc_status": (_I, [_P]),
+    "ce_scratch_areas": (_I64, []),
     "ce_status_string": (ctypes.c_char_p, [_I]),
     "ce_last_error": (ctypes.c_char_p, []),
 }
@@ -161,6 +163,14 @@ def ce_log_softmax_bwd(grad_output, output, grad_input, dtype, rows, C, stream):
 
 def ce_device_status(stream):
     return load().ce_device_status(stream)
+
+
+def ce_noalloc_status(stream):
+    return load().ce_noalloc_status(stream)
+
+
+def ce_scratch_areas():
+    return load().ce_scratch_areas()
 
 
 def ce_status_string(status):

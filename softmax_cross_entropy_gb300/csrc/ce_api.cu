@@ -494,6 +494,15 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
         best.nt = kGenericThreads;
         best.max_units = std::min<int64_t>(static_cast<int64_t>(dev.sm_count) * 8, kMaxUnits);
     }
+    // At most 8 partial-sum slots an SM for every plan (a launch takes one
+    // slot per CTA of the register kernel, else one per CTA or cluster), so
+    // that a launch on a GB300 needs at most 8 * 152 = 1216 slots, whatever
+    // the occupancy calculator allows.
+    {
+        const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
+        const int64_t per_unit = best.kind == Kind::Reg ? best.cluster : 1;
+        best.max_units = std::max<int64_t>(1, std::min(best.max_units, cap / per_unit));
+    }
     if (env_int("GBCE_VERBOSE", 0))
         std::fprintf(stderr,
                      "gbce plan: dtype=%d V=%lld softcap=%d wsmooth=%d -> %s nt=%d C=%d "
@@ -579,7 +588,7 @@ ce_status check_fwd(const FwdCall& c) {
 }
 
 // Plans and launches one checked forward call with `scratch`, whose ticket
-// and status word are zero on entry or, with clear_header, cleared here.
+// is zero on entry or, with clear_header, cleared here.
 // A grid that would need more than max_slots partial-sum slots is refused.
 // Called with g_mu held.
 ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots,
@@ -630,10 +639,10 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
         return CE_ERR_UNSUPPORTED;
     }
     if (clear_header) {
-        // the ticket and the status word must start at zero (partial slots
-        // are written before they are read)
-        const cudaError_t e = cudaMemsetAsync(scratch, 0, 2 * sizeof(unsigned), st);
-        if (e != cudaSuccess) return cuda_failure(e, "cudaMemsetAsync(scratch header)");
+        // the ticket must start at zero (partial slots are written before
+        // they are read); the status word stays sticky until it is read
+        const cudaError_t e = cudaMemsetAsync(&scratch->ticket, 0, sizeof(unsigned), st);
+        if (e != cudaSuccess) return cuda_failure(e, "cudaMemsetAsync(scratch ticket)");
     }
     if (c.rows == 0)  // empty batch: the general kernel with one CTA writes the scalars
         return launch(generic_kernel(c.dtype, sc), 1, kGenericThreads, 0, 1, st, &a);
@@ -1039,6 +1048,11 @@ extern "C" const char* ce_status_string(ce_status s) {
 }
 
 extern "C" const char* ce_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int64_t ce_scratch_areas(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    return static_cast<int64_t>(g_scratch.size());
+}
 
 // ---------------------------------------------------------------- N-D logits (class dimension 1)
 

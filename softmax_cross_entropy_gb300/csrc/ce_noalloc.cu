@@ -5,6 +5,7 @@
 // one partial-sum slot per participating CTA) lives in a fixed file-scope
 // device array instead of memory from cudaMalloc.
 #include <cstdint>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 
@@ -51,6 +52,21 @@ ce_status static_scratch(int dev, Scratch** out) {
 
 using namespace gbce;
 
+namespace gbce {
+namespace {
+
+// The number of partial-sum slots a call may use: the array's, or fewer
+// when GBCE_TEST_NOALLOC_SLOTS lowers it (a test hook, so that the refusal
+// of an oversized launch can be exercised on any GPU).
+int usable_slots() {
+    const char* v = std::getenv("GBCE_TEST_NOALLOC_SLOTS");
+    const int lim = (v && *v) ? std::atoi(v) : 0;
+    return lim > 0 && lim < kStaticSlots ? lim : kStaticSlots;
+}
+
+}  // namespace
+}  // namespace gbce
+
 extern "C" ce_status ce_fwd_noalloc(void* logits, int dtype, int64_t rows, int64_t V,
                                     const void* target, const float* weight,
                                     int64_t ignore_index, float label_smoothing,
@@ -66,5 +82,27 @@ extern "C" ce_status ce_fwd_noalloc(void* logits, int dtype, int64_t rows, int64
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const FwdCall c{logits, dtype, rows, V, target, weight, ignore_index, label_smoothing,
                     lse_square_scale, softcap, reduction, flags, loss, z_loss, acc, pred, nullptr};
-    return fwd_with_scratch(s, kStaticSlots, c, st);
+    return fwd_with_scratch(s, usable_slots(), c, st);
+}
+
+extern "C" ce_status ce_noalloc_status(ce_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return record_cuda_failure(e, "cudaStreamSynchronize");
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record_cuda_failure(e, "cudaGetDevice");
+    Scratch* s = nullptr;
+    const ce_status rc = static_scratch(dev, &s);
+    if (rc != CE_OK) return rc;
+    // read the sticky word into a host variable, then clear it, in stream
+    // order; nothing is allocated
+    unsigned status = 0;
+    e = cudaMemcpyAsync(&status, &s->status, sizeof status, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&s->status, 0, sizeof status, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return record_cuda_failure(e, "reading the static scratch status");
+    if (status & kDevErrTimeout) return CE_ERR_TIMEOUT;
+    if (status & kDevErrTarget) return CE_ERR_TARGET_RANGE;
+    return CE_OK;
 }

@@ -86,5 +86,11 @@ def batch_counts(target, V, weight=None, ignore_index=-100, group=None):
     from . import shard_counts
     counts = shard_counts(target, V, weight, ignore_index)
     if dist.is_available() and dist.is_initialized():
-        dist.all_reduce(counts, group=group)
+        if dist.get_backend(group) == "gloo":
+            # a host-side exchange: the two doubles go through host memory
+            host = counts.cpu()
+            dist.all_reduce(host, group=group)
+            counts.copy_(host)
+        else:
+            dist.all_reduce(counts, group=group)
     return counts

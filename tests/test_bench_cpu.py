@@ -37,3 +37,25 @@ def test_cpu_baseline_single_and_row_partitioned():
     assert b["kind"] == "oracle" and b["cores"] == 1 and b["value"] > 0
     p = b["row_partitioned"]
     assert p["cores"] == bench.host_cores() >= 1 and p["value"] > 0 and p["unit"] == "GB/s"
+
+
+def test_gpus_flag_launches_the_ranks_itself():
+    # --gpus 2 without a launcher: bench.py starts two ranks itself
+    # (torch.distributed.run on 127.0.0.1); the reference arm runs on rank 0
+    # only and prints the one line
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "3"], capture_output=True,
+                       text=True, timeout=600, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1 and json.loads(lines[0])["impl"] == "reference"
+
+
+def test_gpus_flag_must_match_the_launcher_world_size():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT, env=env)
+    assert r.returncode != 0 and "WORLD_SIZE is 1" in r.stderr
