@@ -49,6 +49,7 @@ struct Plan {
     int ng = 0, sg = 0, chunk_vec = 0, nchunk = 0, resident = 0;
     int reg_wpr = 0;  // register-resident kernel: warps of a row team
     uint32_t reg_buf_stride = 0;  // register-resident kernel: bytes of a team's row buffer
+    int reg_nbuf = 1;             // register-resident kernel: row buffers a team
 };
 
 // (device, dtype, V (negative when the logits are not 16-byte aligned),
@@ -72,7 +73,8 @@ std::string tuning_signature() {
     static const char* const kVars[] = {
         "GBCE_KERNEL",        "GBCE_CLUSTER",      "GBCE_CFG",          "GBCE_MAX_STAGES",
         "GBCE_STREAM_GROUPS", "GBCE_STREAM_TWICE", "GBCE_STREAM_SLOTS", "GBCE_STREAM_WARPS",
-        "GBCE_REG_MAX_BYTES", "GBCE_REG_NVL",      "GBCE_REG_CLUSTER"};
+        "GBCE_REG_MAX_BYTES", "GBCE_REG_NVL",      "GBCE_REG_CLUSTER",  "GBCE_REG_SW",
+        "GBCE_REG_NBUF"};
     std::string sig;
     for (const char* name : kVars) {
         const char* v = std::getenv(name);
@@ -332,6 +334,36 @@ bool try_stream(int dtype, int64_t V, bool softcap, bool ws, const DeviceInfo& d
     return true;
 }
 
+// Row buffers of the register-resident kernel `fn` (nt threads, `teams`
+// teams, buffers of `stride` bytes, `extra` bytes of shared memory after
+// them): one a team. GBCE_REG_NBUF=2 gives each team two (two rows in
+// flight a team); that measured slower at every row length on GB300
+// (4096 rows bf16, forward alone: V = 4096 27.9 against 26.3 us, 8192 39.2
+// against 37.0, 16384 61.9 against 57.9). Sets the kernel's shared-memory
+// limit; occ = 0 when nothing fits.
+ce_status reg_buffers(const DeviceInfo& dev, const void* fn, int nt, int teams,
+                      uint32_t stride, size_t extra, int* nbuf, size_t* smem, int* occ) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    const size_t dyn_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(dyn_max));
+    if (e != cudaSuccess) return cuda_failure(e, "register kernel attributes");
+    int o[3] = {0, 0, 0};
+    for (int nb = 1; nb <= 2; ++nb) {
+        const size_t sm = static_cast<size_t>(teams) * nb * stride + extra;
+        if (sm > dyn_max) continue;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o[nb], fn, nt, sm);
+        if (e != cudaSuccess) return cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    }
+    const int nb = env_int("GBCE_REG_NBUF", 1) == 2 && o[2] >= 1 ? 2 : 1;
+    *nbuf = nb;
+    *occ = o[nb];
+    *smem = static_cast<size_t>(teams) * nb * stride + extra;
+    return CE_OK;
+}
+
 ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth, bool aligned,
                     bool w_aligned, Plan* out) {
     // Tuning overrides: GBCE_CLUSTER forces the CTAs per row (1, 2, 4, 8 or
@@ -367,33 +399,52 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     const int nvl = (nvl_env == 8 || nvl_env == 16) ? nvl_env
                     : (vrow <= 32 * 8 * kRegMaxWarps ? 8 : 16);
     const int64_t wpr = (vrow + 32 * nvl - 1) / (32 * nvl);
-    if (fast_ok && (!wsmooth || w_aligned) && wpr <= kRegMaxWarps &&
+    // Class-weighted smoothing: the weights in shared memory (one CTA of 16
+    // warps an SM, 8 vectors a thread, teams of up to 16 warps) when they
+    // fit beside the row buffers; the weights are then read once per CTA
+    // instead of twice per element from L1/L2 (GBCE_REG_SW=0 turns it off)
+    const int64_t wpr_sw = (vrow + 32 * 8 - 1) / (32 * 8);
+    if (fast_ok && wsmooth && w_aligned && wpr_sw <= kRegSwWarps && env_int("GBCE_REG_SW", 1) &&
         (forced_kind == 4 || (forced_kind == 0 && V * bytes <= reg_max))) {
-        const void* fn = reg_kernel(dtype, softcap, wsmooth, nvl);
-        const int teams = kRegMaxWarps / static_cast<int>(wpr);
-        const int nt = 32 * static_cast<int>(wpr) * teams;
-        // one row buffer a team (the next row's bulk copy)
+        const void* fn = reg_kernel_sw(dtype, softcap);
+        const int teams = kRegSwWarps / static_cast<int>(wpr_sw);
+        const int nt = 32 * static_cast<int>(wpr_sw) * teams;
         const uint32_t stride = static_cast<uint32_t>((V * bytes + 127) / 128 * 128);
-        const size_t smem = static_cast<size_t>(teams) * stride;
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
-        const size_t dyn_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(dyn_max));
-        if (e != cudaSuccess) return cuda_failure(e, "register kernel attributes");
-        int occ = 0;
-        if (smem <= dyn_max) {
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, nt, smem);
-            if (e != cudaSuccess)
-                return cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-        }
+        int nbuf = 1, occ = 0;
+        size_t smem = 0;
+        rc = reg_buffers(dev, fn, nt, teams, stride, static_cast<size_t>(V) * 4, &nbuf, &smem, &occ);
+        if (rc != CE_OK) return rc;
         if (occ >= 1) {
             best.fn = fn;
             best.kind = Kind::Reg;
             best.nt = nt;
             best.smem = smem;
             best.reg_buf_stride = stride;
+            best.reg_nbuf = nbuf;
+            best.reg_wpr = static_cast<int>(wpr_sw);
+            best.max_units = std::min<int64_t>(
+                static_cast<int64_t>(std::min(occ, 8)) * dev.sm_count, kMaxUnits);
+        }
+    }
+    if (best.kind == Kind::General && fast_ok && (!wsmooth || w_aligned) &&
+        wpr <= kRegMaxWarps &&
+        (forced_kind == 4 || (forced_kind == 0 && V * bytes <= reg_max))) {
+        const void* fn = reg_kernel(dtype, softcap, wsmooth, nvl);
+        const int teams = kRegMaxWarps / static_cast<int>(wpr);
+        const int nt = 32 * static_cast<int>(wpr) * teams;
+        // one or two row buffers a team (the next rows' bulk copies)
+        const uint32_t stride = static_cast<uint32_t>((V * bytes + 127) / 128 * 128);
+        int nbuf = 1, occ = 0;
+        size_t smem = 0;
+        rc = reg_buffers(dev, fn, nt, teams, stride, 0, &nbuf, &smem, &occ);
+        if (rc != CE_OK) return rc;
+        if (occ >= 1) {
+            best.fn = fn;
+            best.kind = Kind::Reg;
+            best.nt = nt;
+            best.smem = smem;
+            best.reg_buf_stride = stride;
+            best.reg_nbuf = nbuf;
             best.reg_wpr = static_cast<int>(wpr);
             // at most 8 CTAs an SM: the partial-sum slots of a launch stay
             // within 8 per SM, as for the other kernels
@@ -684,6 +735,7 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
         }
         a.reg_wpr = p.reg_wpr;
         a.reg_buf_stride = p.reg_buf_stride;
+        a.reg_nbuf = p.reg_nbuf;
         a.reg_cluster = p.cluster;
         return launch(p.fn, static_cast<int>(units * p.cluster), p.nt, p.smem, p.cluster, st, &a,
                       pdl);
@@ -1012,7 +1064,7 @@ extern "C" ce_status ce_bwd(const float* grad_output, int grad_per_row, void* dl
     b.vec_ok = ((V * bytes) % 16 == 0 && reinterpret_cast<uintptr_t>(dlogits) % 16 == 0) ? 1 : 0;
     const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(info.sm_count) * 8);
     return launch(bwd_kernel(dtype), static_cast<int>(grid), kBwdThreads, 0, 1,
-                  reinterpret_cast<cudaStream_t>(stream), &b);
+                  reinterpret_cast<cudaStream_t>(stream), &b, true);
 }
 
 extern "C" ce_status ce_device_status(ce_stream_t stream) {
@@ -1256,5 +1308,5 @@ extern "C" ce_status ce_bwd_nd(const float* grad_output, int grad_per_position, 
         grid = std::max<int64_t>(1, std::min<int64_t>((N * C * inner + 2047) / 2048,
                                                      static_cast<int64_t>(info.sm_count) * 8));
     return launch(nd_bwd_kernel(dtype), static_cast<int>(grid), kBwdThreads, 0, 1,
-                  reinterpret_cast<cudaStream_t>(stream), &a);
+                  reinterpret_cast<cudaStream_t>(stream), &a, true);
 }

@@ -71,24 +71,56 @@ __device__ __forceinline__ float2 reg_arg2(float2 z, float Ms, float ML) {
         return fmul2(fadd2(z, make_float2(-Ms, -Ms)), make_float2(kLog2e, kLog2e));
 }
 
+// Class weights of vector v from shared memory, where the 4-weight quarter
+// h of vector v sits at float4 h * vrow + v: the lanes of a warp hold
+// consecutive vectors and read consecutive 16-byte words.
+template <int VE>
+__device__ __forceinline__ void reg_weights_smem(const float4* w4, int v, int vrow,
+                                                 float (&w)[VE]) {
+#pragma unroll
+    for (int h = 0; h < VE / 4; ++h) {
+        const float4 t4 = w4[h * vrow + v];
+        w[4 * h] = t4.x;
+        w[4 * h + 1] = t4.y;
+        w[4 * h + 2] = t4.z;
+        w[4 * h + 3] = t4.w;
+    }
+}
+
 // 8 vectors a thread: three CTAs of 8 warps an SM (85 registers a thread);
 // 16 vectors: two (128 registers)
 // CLU: the cluster variant (a.reg_cluster CTAs a row); otherwise one CTA
 // holds whole rows and the cluster code folds away.
-template <typename T, bool SOFTCAP, bool WS, int NVL, bool CLU>
-__global__ void __launch_bounds__(32 * kRegMaxWarps, NVL == 8 ? 3 : 2)
+// MW: warps of a CTA. SW (class-weighted smoothing only): the V class
+// weights sit in shared memory after the row buffers, loaded once per CTA,
+// instead of being read from L1/L2 in both passes; one CTA of 16 warps an
+// SM then holds one or two teams.
+template <typename T, bool SOFTCAP, bool WS, int NVL, bool CLU, int MW = kRegMaxWarps,
+          bool SW = false>
+__global__ void __launch_bounds__(32 * MW, MW == 16 ? 1 : (NVL == 8 ? 3 : 2))
 ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;
-    constexpr int MW = kRegMaxWarps;
+    static_assert(!SW || (WS && !CLU), "shared-memory weights: class-weighted smoothing only");
     __shared__ float red_a[MW], red_b[MW], red_c[MW];
     __shared__ int red_i[MW];
     __shared__ double red_d[2][MW];
     __shared__ long long red_n[MW];
     __shared__ int s_flag;
-    __shared__ __align__(8) uint64_t pf_bar[MW];  // one per team
+    __shared__ __align__(8) uint64_t pf_bar[2 * MW];  // one per row buffer
+    // each team leader's copy queue, kept in shared memory so that it takes
+    // no registers in the other threads: the first of the team's rows not
+    // yet looked at, the buffer the next copy goes to, and bit masks (bit k
+    // for buffer k) of the unconsumed copies, of their completion parities
+    // and of the parity the next copy into each buffer completes
+    struct PfQueue {
+        long long next;
+        int k;
+        uint32_t pend, pend_par, ph;
+    };
+    __shared__ PfQueue pfq[MW];
     __shared__ __align__(16) float cl_red[4];  // cluster mode: this CTA's max, S, SZ, argmax
-    extern __shared__ __align__(128) unsigned char reg_smem[];  // teams x reg_buf_stride
+    extern __shared__ __align__(128) unsigned char reg_smem[];  // teams x nbuf x reg_buf_stride
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -104,7 +136,7 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     // VPC); the row's maximum and sums merge across the cluster through
     // distributed shared memory.
     const int CL = CLU ? a.reg_cluster : 1;
-    constexpr int VPC = kRegMaxWarps * 32 * NVL;  // vectors of a CTA's slice (cluster mode)
+    constexpr int VPC = MW * 32 * NVL;  // vectors of a CTA's slice (cluster mode)
     const int crank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     const int cta_vec0 = crank * VPC;              // first vector of this CTA's slice
     const int vbase = cta_vec0 + wr * 32 * NVL + lane;  // this thread's first vector
@@ -150,6 +182,17 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     };
     const float inv_V = 1.f / static_cast<float>(a.V);
     float Wtot = static_cast<float>(a.V);
+    // SW: the weights' place in shared memory, after the teams' row buffers
+    float4* w4s = reinterpret_cast<float4*>(
+        reg_smem + static_cast<size_t>(teams) * a.reg_nbuf * a.reg_buf_stride);
+    if (SW) {
+        float* wsm = reinterpret_cast<float*>(w4s);
+        for (int c = tid; c < a.V; c += blockDim.x) {
+            const int v = c / VE, e = c % VE;
+            wsm[((e >> 2) * vrow + v) * 4 + (e & 3)] = __ldg(a.weight + c);
+        }
+        // (visible to the CTA after the barriers of the sum below)
+    }
     if (WS) {
         // W = sum of the class weights: every thread the same fixed order
         float s = 0.f;
@@ -169,62 +212,83 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     int accC = 0;
     const int64_t nteams = CL > 1 ? static_cast<int64_t>(ncluster_x())
                                   : static_cast<int64_t>(gridDim.x) * teams;
-    // Each team owns a shared-memory buffer of one row; its leader copies the
-    // team's next counted row into it (1-D bulk async copy, mbarrier
-    // completion) while the team computes the current row from registers,
-    // so the HBM latency of the next row overlaps this row's arithmetic.
+    // Each team owns NB (a.reg_nbuf: 1 or 2) shared-memory buffers of one
+    // row; its leader copies the team's next counted rows into them (1-D
+    // bulk async copies, mbarrier completion), the counted rows taking the
+    // buffers in turn, while the team computes the current row from
+    // registers: the HBM latency of the next NB rows overlaps this row's
+    // arithmetic.
     // bytes of the row this CTA's team copies (its slice in cluster mode)
     const uint32_t row_bytes =
         static_cast<uint32_t>(max(0, min(vrow - cta_vec0, CL > 1 ? VPC : vrow))) * 16u;
-    const uint32_t buf = smem_u32(reg_smem) + static_cast<uint32_t>(team) * a.reg_buf_stride;
-    const uint32_t bar = smem_u32(&pf_bar[team]);
+    const int NB = a.reg_nbuf;
+    const uint32_t buf0 =
+        smem_u32(reg_smem) + static_cast<uint32_t>(team * NB) * a.reg_buf_stride;
+    const uint32_t bar0 = smem_u32(&pf_bar[team * NB]);
     const bool lead = wr == 0 && lane == 0;
     const uint64_t pol = l2_evict_first_policy();
-    uint32_t pf_phase = 0;
-    bool pf_pending = false;  // leader: a copy into the buffer is outstanding
+    uint32_t cons_phase = 0;  // bit k: parity of buffer k's next completion
+    int cons_k = 0;           // buffer of the team's next counted row
     bool failed = false;
     // test hook (FwdArgs::test_stall): the first copy of CTA 0's first team
     // is left out, so the team's wait for it runs out
     bool stall = a.test_stall && blockIdx.x == 0 && team == 0;
-    auto prefetch = [&](int64_t row) {  // leader only, buffer free
+    int64_t r = CL > 1 ? static_cast<int64_t>(cluster_id_x())
+                       : static_cast<int64_t>(blockIdx.x) * teams + team;
+    PfQueue& Q = pfq[team];
+    // leader only: copy the team's next counted row into buffer Q.k (its
+    // previous row has been read by every thread of the team)
+    auto prefetch_next = [&]() {
+        int64_t row = Q.next;
+        while (row < a.rows && !row_counts(a, load_target(a, row))) row += nteams;
+        if (row >= a.rows) {
+            Q.next = row;
+            return;
+        }
+        Q.next = row + nteams;
+        const int k = Q.k;
+        Q.k = (k + 1 == NB) ? 0 : k + 1;
+        const uint32_t par = (Q.ph >> k) & 1u;
+        Q.ph ^= 1u << k;
         if (stall) {
             stall = false;
             return;
         }
+        const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(k);
+        const uint32_t buf = buf0 + static_cast<uint32_t>(k) * a.reg_buf_stride;
         const char* src = reinterpret_cast<const char*>(a.x) +
                           row * a.V * static_cast<int64_t>(sizeof(T)) +
                           static_cast<int64_t>(cta_vec0) * 16;
         mbar_arrive_expect_tx(bar, row_bytes);
         for (uint32_t off = 0; off < row_bytes; off += 32768u)
             bulk_g2s(buf + off, src + off, min(32768u, row_bytes - off), bar, pol);
-        pf_pending = true;
+        Q.pend |= 1u << k;
+        Q.pend_par = (Q.pend_par & ~(1u << k)) | (par << k);
     };
     if (tid == 0) {
-        for (int tm = 0; tm < teams; ++tm) mbar_init(smem_u32(&pf_bar[tm]), 1);
+        for (int i = 0; i < teams * NB; ++i) mbar_init(smem_u32(&pf_bar[i]), 1);
         fence_mbar_init();
     }
+    if (lead) Q = PfQueue{r, 0, 0u, 0u, 0u};
     __syncthreads();
-    int64_t r = CL > 1 ? static_cast<int64_t>(cluster_id_x())
-                       : static_cast<int64_t>(blockIdx.x) * teams + team;
     int64_t t_cur = r < a.rows ? load_target(a, r) : 0;                // row r
     int64_t t_nxt = r + nteams < a.rows ? load_target(a, r + nteams) : 0;  // row r + nteams
     // (a CTA whose slice is empty copies and waits for nothing)
     const bool has_slice = row_bytes > 0;
-    if (lead && has_slice && r < a.rows && row_counts(a, t_cur)) prefetch(r);
+    if (lead && has_slice)
+        for (int k = 0; k < NB; ++k) prefetch_next();
 #pragma unroll 1
     for (; r < a.rows; r += nteams) {
         const int64_t t = t_cur;
         const int64_t rn = r + nteams;
-        const bool next_counts = rn < a.rows && row_counts(a, t_nxt);
         t_cur = t_nxt;
         t_nxt = rn + nteams < a.rows ? load_target(a, rn + nteams) : 0;
         const bool counts = row_counts(a, t);
         T* xrow = reinterpret_cast<T*>(a.x) + r * a.V;
         uint4* rowv = reinterpret_cast<uint4*>(xrow);
         if (!counts) {
-            // ignored row: exact +0 gradient without reading it; nothing was
-            // copied for it, so the buffer takes the next row now
-            if (lead && has_slice && next_counts && !failed) prefetch(rn);
+            // ignored row: exact +0 gradient without reading it (no buffer
+            // holds it)
             if (lead && crank == 0 && t != a.ignore_index) atomicOr(&a.scratch->status, kDevErrTarget);
             if (a.grad) {
 #pragma unroll
@@ -241,17 +305,24 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             }
             continue;
         }
-        // ---- the row into registers from the buffer: vector vbase + 32 k
+        // ---- the row into registers from its buffer: vector vbase + 32 k
+        const int kb = cons_k;
         if (has_slice) {
-            if (!failed && !mbar_wait_bounded(bar, pf_phase, a.timeout_ns)) {
-                failed = true;
-                if (lead) atomicOr(&a.scratch->status, kDevErrTimeout);
+            const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(kb);
+            if (!failed) {
+                if (mbar_wait_bounded(bar, (cons_phase >> kb) & 1u, a.timeout_ns)) {
+                    if (lead) Q.pend &= ~(1u << kb);
+                } else {
+                    failed = true;
+                    if (lead) atomicOr(&a.scratch->status, kDevErrTimeout);
+                }
             }
-            pf_phase ^= 1u;
-            if (lead) pf_pending = false;
+            cons_phase ^= 1u << kb;
+            cons_k = (cons_k + 1 == NB) ? 0 : cons_k + 1;
         }
         uint4 q[NVL];
-        const uint4* sb = reinterpret_cast<const uint4*>(reg_smem + static_cast<size_t>(team) * a.reg_buf_stride);
+        const uint4* sb = reinterpret_cast<const uint4*>(
+            reg_smem + static_cast<size_t>(team * NB + kb) * a.reg_buf_stride);
 #pragma unroll
         for (int k = 0; k < NVL; ++k)
             q[k] = 32 * k < vlim ? sb[vbase - cta_vec0 + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
@@ -277,7 +348,7 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
         // every thread of the team holds its vectors (the warp reduction
         // above, or the team barrier, follows every thread's buffer reads):
         // the buffer takes the team's next counted row
-        if (lead && has_slice && next_counts && !failed) prefetch(rn);
+        if (lead && has_slice && !failed) prefetch_next();
         if (CL > 1) {
             // the row's maximum over the cluster: lane i reads CTA i's
             if (tid == 0) cl_red[0] = X;
@@ -316,7 +387,12 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             if (32 * k < vlim) {
                 float f[VE], w[VE];
                 VT::unpack(q[k], f);
-                if (WS) reg_weights<VE>(a.weight, vbase + 32 * k, w);
+                if (WS) {
+                    if (SW)
+                        reg_weights_smem<VE>(w4s, vbase + 32 * k, vrow, w);
+                    else
+                        reg_weights<VE>(a.weight, vbase + 32 * k, w);
+                }
 #pragma unroll
                 for (int j = 0; j < VE; j += 2) {
                     float2 z;
@@ -428,7 +504,12 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
                 if (32 * k < vlim) {
                     float f[VE], g[VE], w[VE];
                     VT::unpack(q[k], f);
-                    if (WS) reg_weights<VE>(a.weight, vbase + 32 * k, w);
+                    if (WS) {
+                    if (SW)
+                        reg_weights_smem<VE>(w4s, vbase + 32 * k, vrow, w);
+                    else
+                        reg_weights<VE>(a.weight, vbase + 32 * k, w);
+                }
 #pragma unroll
                     for (int j = 0; j < VE; j += 2) {
                         float2 gg;
@@ -480,8 +561,13 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
         // read before the next row's first team barrier
     }
 
-    // a copy still in flight (after a timeout) lands before the CTA exits
-    if (lead && pf_pending) (void)mbar_wait_bounded(bar, pf_phase, a.timeout_ns);
+    // copies still in flight (after a timeout) land before the CTA exits
+    if (lead) {
+        for (int k = 0; k < NB; ++k)
+            if ((Q.pend >> k) & 1u)
+                (void)mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(k),
+                                        (Q.pend_par >> k) & 1u, a.timeout_ns);
+    }
     if (a.reduction != kRedNone) {
         need_counts();
         // fixed-order CTA sum of the per-thread partials: a thread holds the

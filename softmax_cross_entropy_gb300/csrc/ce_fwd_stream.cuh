@@ -92,7 +92,7 @@ struct PassOne {
     template <bool FULL>
     __device__ __forceinline__ void add_chunk(const uint4 (&q)[VPT], int vidx0, int vend,
                                               int stride, const FwdArgs& a, bool smooth_rt,
-                                              const float4* w4, int vrow) {
+                                              const float4* w4, int vrow, bool want_arg) {
         const bool smooth = WS || smooth_rt;
         typename VT::MaxAcc macc = VT::max_init();
         int nk = 0;
@@ -104,8 +104,12 @@ struct PassOne {
             }
         }
         const float cm = VT::max_value(macc);
-        const bool better = cm > xmax;
-        if (__any_sync(0xffffffffu, better)) {
+        if (!want_arg) {
+            // no argmax asked for: only the largest raw logit (the softcap
+            // of it is the row's largest z)
+            xmax = fmaxf(xmax, cm);
+        } else if (__any_sync(0xffffffffu, cm > xmax)) {
+            const bool better = cm > xmax;
             // a new thread maximum (frequent at a row's start, rare later):
             // find the first vector and element that hold it
             if (better) {
@@ -359,6 +363,9 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
     const int64_t vec_row = a.V / VE;
     const int64_t cid = blockIdx.x;
     const int64_t ncta = gridDim.x;
+    // a second pass over the row (the gradient, or the log-softmax output);
+    // without it (loss and metrics only) every row is streamed once
+    const bool two_pass = LSM || a.grad;
 
     if (tid == 0) {
         for (int i = 0; i < ng * sg; ++i) {
@@ -399,7 +406,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                     const int gg = g;
                     g = (g + 1 == ng) ? 0 : g + 1;
                     if (!((counted >> j) & 1u)) continue;
-                    const int passes = a.resident ? 1 : 2;
+                    const int passes = (a.resident || !two_pass) ? 1 : 2;
                     for (int p = 0; p < passes && !failed; ++p) {
                         for (int c = 0; c < nchunk; ++c) {
                             int ls = 0;
@@ -434,7 +441,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                                               (r * a.V + v0 * VE) * static_cast<int64_t>(sizeof(T));
                             const uint32_t dst =
                                 smem_u32(ring + static_cast<size_t>(slot) * chunk_bytes);
-                            const uint64_t pol = (!a.resident && p == 0) ? pol_keep : pol_once;
+                            const uint64_t pol = passes == 2 && p == 0 ? pol_keep : pol_once;
                             for (uint32_t off = 0; off < bytes; off += kStreamCopyChunk)
                                 bulk_g2s(dst + off, src + off, min(kStreamCopyChunk, bytes - off),
                                          fb, pol);
@@ -462,6 +469,7 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
         const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;  // unused when D == 0
         const float inv_V = 1.f / static_cast<float>(a.V);
         const bool smooth = WS || a.eps != 0.f;
+        const bool want_arg = a.want_pred || a.want_acc;
         const int vrow_w = static_cast<int>(vec_row);
         float4* w4 = reinterpret_cast<float4*>(ring + static_cast<size_t>(ng) * sg * chunk_bytes);
         float Wtot = static_cast<float>(a.V);
@@ -576,15 +584,15 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
 #pragma unroll
                     for (int k = 0; k < VPT; ++k) q[k] = ch[tg + k * GT];
                     st.template add_chunk<true>(q, v0 + tg, v0 + nv, GT, a, smooth, w4,
-                                                vrow_w);
+                                                vrow_w, want_arg);
                 } else {
 #pragma unroll
                     for (int k = 0; k < VPT; ++k)
                         if (tg + k * GT < nv) q[k] = ch[tg + k * GT];
                     st.template add_chunk<false>(q, v0 + tg, v0 + nv, GT, a, smooth, w4,
-                                                 vrow_w);
+                                                 vrow_w, want_arg);
                 }
-                if (!a.resident) {
+                if (!a.resident || !two_pass) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
                 }
@@ -635,8 +643,8 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                 tot.S;
             const float Bc = -scale * a.eps * inv_V;
             const float ML = M * kLog2e;
-            if (a.resident) pos = pos0;
-            for (int c = 0, v0 = 0; c < nchunk; ++c, v0 += chunk_vec) {
+            if (a.resident && two_pass) pos = pos0;
+            for (int c = 0, v0 = 0; two_pass && c < nchunk; ++c, v0 += chunk_vec) {
                 const int slot = g * sg + pos.slot;
                 if (!a.resident && !failed &&
                     !mbar_wait_bounded(smem_u32(&full_bar[slot]), pos.phase, a.timeout_ns)) {

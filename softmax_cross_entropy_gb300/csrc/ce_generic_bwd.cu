@@ -181,6 +181,10 @@ template <typename T>
 __global__ void __launch_bounds__(kBwdThreads) ce_bwd_scale(const __grid_constant__ BwdArgs a) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;
+    // launched as a programmatic dependent of the previous kernel on the
+    // stream (the forward that stored the gradient): the launch overlaps
+    // that kernel's end, and nothing is read before it has completed
+    pdl_wait();
     if (!a.per_row && __ldg(a.g) == 1.f) return;  // multiplying by one changes nothing
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
         const float g = a.per_row ? __ldg(a.g + r) : __ldg(a.g);
@@ -211,6 +215,7 @@ template <typename T>
 __global__ void __launch_bounds__(kBwdThreads) ce_bwd_nd_scale(const __grid_constant__ NdBwdArgs a) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;
+    pdl_wait();  // as in ce_bwd_scale
     if (!a.per_pos) {
         const float g = __ldg(a.g);
         if (g == 1.f) return;  // multiplying by one changes nothing

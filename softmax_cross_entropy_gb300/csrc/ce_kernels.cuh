@@ -78,6 +78,7 @@ struct FwdArgs {
     int nd_staged;  // 1: the N-D kernel keeps its tile in shared memory
     int reg_wpr;    // register-resident kernel: warps a row team has
     uint32_t reg_buf_stride;  // register-resident kernel: bytes of a team's row buffer
+    int reg_nbuf;             // register-resident kernel: row buffers a team (1 or 2)
     int reg_cluster;  // register-resident kernel: CTAs of the cluster that owns a row (0, 1: one CTA)
     // test hook: CTA 0 does not issue its first bulk copy, so the wait for
     // it runs out (status CE_ERR_TIMEOUT, outputs invalid, nothing faults)
@@ -523,6 +524,10 @@ const void* generic_kernel(int dtype, bool softcap);
 // owns a row, nvl (8 or 16) 16-byte vectors a thread; a CTA has one or more
 // teams, at most kRegMaxWarps warps
 const void* reg_kernel(int dtype, bool softcap, bool ws, int nvl);
+// Its class-weighted smoothing variant with the weights in shared memory:
+// 16 warps a CTA, 8 vectors a thread.
+const void* reg_kernel_sw(int dtype, bool softcap);
+constexpr int kRegSwWarps = 16;
 // The register-resident kernel's cluster variant (16 vectors a thread).
 const void* reg_cluster_kernel(int dtype, bool softcap, bool ws);
 constexpr int kRegMaxWarps = 8;

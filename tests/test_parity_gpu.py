@@ -297,6 +297,35 @@ def test_forward_only_leaves_logits_untouched():
     assert np.array_equal(out["pred"], ref["pred"])
 
 
+@pytest.mark.parametrize("make", [
+    lambda: workloads.vsweep(V=131072, rows=300),
+    lambda: workloads.softcap_z(rows=200),
+    lambda: workloads.tt_fp32(rows=200, reduction="sum"),
+    lambda: workloads.weighted(rows=300, reduction="none"),
+], ids=["bf16-131072", "softcap-131072", "fp32-128256-sum", "weighted-32000-none"])
+def test_forward_only_streams_once_and_matches(make):
+    # without CE_FLAG_GRAD the long-row kernel reads each row once; loss,
+    # z-loss, accuracy and predictions must still be the oracle's and the
+    # logits must be left as they were
+    case = make()
+    x, _, _ = to_device(case)
+    before = x.clone()
+    red = case.reduction
+    out = run_cuda(case, x=x, grad=False, want_z=True, want_acc=True, want_pred=True)
+    assert out["status"] == 0
+    assert torch.equal(x, before)
+    ref = oracle_full(case, want_grad=False)
+    if red == "none":
+        assert_rowloss_close(out["loss"], ref["loss"], case.dtype)
+        assert_rowloss_close(out["z_loss"], ref["z_loss"], case.dtype, "z_loss")
+        assert np.array_equal(out["acc"], ref["acc"])
+    else:
+        assert_loss_close(out["loss"], ref["loss"], case.dtype)
+        assert_loss_close(out["z_loss"], ref["z_loss"], case.dtype, "z_loss")
+        assert np.float32(out["acc"]) == np.float32(ref["acc"])
+    assert np.array_equal(out["pred"], ref["pred"])
+
+
 def test_deterministic():
     case = workloads.softcap_z(rows=300)
     a = run_cuda(case, want_z=True)
@@ -471,6 +500,23 @@ def test_register_kernel(monkeypatch, dtype, V, rows, nvl):
                  dict(weight=True, label_smoothing=0.05, reduction="sum"),
                  dict(weight=True, label_smoothing=0.2, softcap=8.0, ignore_frac=0.3)):
         case = workloads.random_case(110 + rows, rows, V, dtype=dtype, **opts)
+        check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+@pytest.mark.parametrize("sw,nbuf", [("0", "1"), ("1", "2"), ("0", "2")])
+@pytest.mark.parametrize("dtype,V,rows", [("bf16", 32000, 37), ("bf16", 4096, 301),
+                                          ("f32", 5000, 45), ("f16", 16384, 29)])
+def test_register_kernel_weight_and_buffer_options(monkeypatch, sw, nbuf, dtype, V, rows):
+    # class weights from L1/L2 (GBCE_REG_SW=0) or shared memory (the
+    # default), one or two row buffers a team (GBCE_REG_NBUF), whole batch
+    monkeypatch.setenv("GBCE_KERNEL", "4")
+    monkeypatch.setenv("GBCE_REG_SW", sw)
+    monkeypatch.setenv("GBCE_REG_NBUF", nbuf)
+    for opts in (dict(weight=True, label_smoothing=0.05, reduction="mean", ignore_frac=0.2),
+                 dict(weight=True, label_smoothing=0.1, softcap=12.0, lse_square_scale=1e-3,
+                      reduction="none"),
+                 dict(label_smoothing=0.1, reduction="sum")):
+        case = workloads.random_case(150 + rows, rows, V, dtype=dtype, **opts)
         check_full(case, want_z=True, want_acc=True, want_pred=True)
 
 
