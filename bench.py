@@ -797,16 +797,93 @@ def run_profile_target(args):
     else:
         name = workload_desc(args.V)
         case = workloads.vsweep(V=args.V, rows=args.rows)
+    if args.ncu_op == "nd":
+        profile_nd(args, device, torch)
+        return
+    if args.ncu_op == "gemm":
+        profile_gemm(args, device, torch)
+        return
     r = GpuRunner(case, device, torch)
     st = r.stream.cuda_stream
     with torch.cuda.stream(r.stream):
         for k in range(args.ncu_steps):
             b = r.bufs[k % r.pool]
             b.copy_(r.pristine)
-            r.fwd(b, st)
-            r.bwd(b, r.one, st)
+            if args.ncu_op == "fwd":
+                r.fwd(b, st)
+                r.bwd(b, r.one, st)
+            elif args.ncu_op == "bwd":  # the backward with grad_output 0.5 (a read and a write)
+                r.bwd(b, r.half, st)
+            else:  # the four unfused ops, each once
+                profile_unfused(r, b, st)
     torch.cuda.synchronize(device)
-    print(json.dumps({"profile_target": name, "rows": case.rows, "V": case.V,
+    print(json.dumps({"profile_target": name, "op": args.ncu_op, "rows": case.rows, "V": case.V,
+                      "steps": args.ncu_steps}))
+
+
+def profile_unfused(r, x, st):
+    """_log_softmax, nll_loss_forward, nll_loss_backward and
+    _log_softmax_backward_data once each over the runner's workload."""
+    from softmax_cross_entropy_gb300 import _lib
+    torch, c = r.torch, r.case
+    y, dy = torch.empty_like(x), torch.empty_like(x)
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out, tw, one = torch.empty(1, **f32), torch.empty(1, **f32), torch.ones(1, **f32)
+    red, t = _RED[c.reduction], r.target.data_ptr()
+    for rc in (_lib.ce_log_softmax(x.data_ptr(), y.data_ptr(), r.dtype, c.rows, c.V, st),
+               _lib.ce_nll_loss_fwd(y.data_ptr(), r.dtype, c.rows, c.V, t, None, c.ignore_index,
+                                    red, 0, out.data_ptr(), tw.data_ptr(), st),
+               _lib.ce_nll_loss_bwd(one.data_ptr(), tw.data_ptr(), dy.data_ptr(), r.dtype, c.rows,
+                                    c.V, t, None, c.ignore_index, red, 0, st),
+               _lib.ce_log_softmax_bwd(dy.data_ptr(), y.data_ptr(), x.data_ptr(), r.dtype, c.rows,
+                                       c.V, st)):
+        if rc != 0:
+            raise RuntimeError(f"unfused op: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
+
+
+def profile_nd(args, device, torch):
+    """ce_fwd_nd (with gradient, mean) `--ncu-steps` times on N-D bf16 logits
+    of shape --nd-shape (N, C, d1, ...)."""
+    from softmax_cross_entropy_gb300 import _lib
+    shape = tuple(int(v) for v in args.nd_shape.split(","))
+    case = workloads.nd_case(0, shape, "bf16", std=3.0)
+    x0 = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).to(device)
+    t = torch.from_numpy(case.target).to(device)
+    loss = torch.empty(1, dtype=torch.float32, device=device)
+    N, C = shape[0], shape[1]
+    inner = int(np.prod(shape[2:])) if len(shape) > 2 else 1
+    st = torch.cuda.current_stream(device).cuda_stream
+    for _ in range(args.ncu_steps):
+        x = x0.clone()
+        rc = _lib.ce_fwd_nd(x.data_ptr(), _lib.CE_BF16, N, C, inner, t.data_ptr(), None, -100,
+                            0.0, 0.0, 0.0, _lib.CE_RED_MEAN,
+                            _lib.CE_FLAG_GRAD | (_lib.CE_FLAG_TARGET_I64 if t.dtype == torch.int64
+                                                 else 0),
+                            loss.data_ptr(), None, None, None, st)
+        if rc != 0:
+            raise RuntimeError(f"ce_fwd_nd: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
+    torch.cuda.synchronize(device)
+    print(json.dumps({"profile_target": f"N-D bf16 logits {shape}", "op": "nd",
+                      "steps": args.ncu_steps}))
+
+
+def profile_gemm(args, device, torch):
+    """ce_gemm_abt (tcgen05, bf16 in, fp32 out) `--ncu-steps` times on
+    M = --rows, N = --V, K = --gemm-k."""
+    from softmax_cross_entropy_gb300 import _lib
+    M, N, K = args.rows, args.V, args.gemm_k
+    g = torch.Generator(device="cpu").manual_seed(0)
+    A = torch.randn(M, K, generator=g).to(device=device, dtype=torch.bfloat16)
+    B = torch.randn(N, K, generator=g).to(device=device, dtype=torch.bfloat16)
+    C = torch.empty(M, N, dtype=torch.float32, device=device)
+    st = torch.cuda.current_stream(device).cuda_stream
+    for _ in range(args.ncu_steps):
+        rc = _lib.ce_gemm_abt(A.data_ptr(), B.data_ptr(), _lib.CE_BF16, M, N, K, C.data_ptr(),
+                              None, st)
+        if rc != 0:
+            raise RuntimeError(f"ce_gemm_abt: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
+    torch.cuda.synchronize(device)
+    print(json.dumps({"profile_target": f"A[{M},{K}] B[{N},{K}] bf16 -> fp32", "op": "gemm",
                       "steps": args.ncu_steps}))
 
 
@@ -841,6 +918,12 @@ def main():
     ap.add_argument("--V", type=int, default=V_MAIN, help="vocabulary of the --ncu target")
     ap.add_argument("--ncu-config", type=int, default=-1,
                     help="profile the i-th of the other workloads (see extra_workloads)")
+    ap.add_argument("--ncu-op", choices=["fwd", "bwd", "unfused", "nd", "gemm"], default="fwd",
+                    help="what the --ncu target runs: forward + backward (default), the "
+                         "backward with grad_output 0.5, the four unfused ops, the N-D forward, "
+                         "or the tensor-core GEMM")
+    ap.add_argument("--nd-shape", default="8,32000,512", help="N-D logits shape for --ncu-op nd")
+    ap.add_argument("--gemm-k", type=int, default=4096, help="K of --ncu-op gemm")
     args = ap.parse_args()
     if args.ncu:
         run_profile_target(args)

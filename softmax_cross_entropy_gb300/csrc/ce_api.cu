@@ -33,7 +33,7 @@ struct DeviceInfo {
 
 // A launch plan for one (device, dtype, V, variant): which kernel, how many
 // CTAs per row, ring depth, dynamic shared memory and the resident grid.
-enum class Kind { General, Staged, Stream, Reg };
+enum class Kind { General, Staged, Stream, Reg, Tmem };
 
 struct Plan {
     const void* fn = nullptr;
@@ -50,11 +50,17 @@ struct Plan {
     int reg_wpr = 0;  // register-resident kernel: warps of a row team
     uint32_t reg_buf_stride = 0;  // register-resident kernel: bytes of a team's row buffer
     int reg_nbuf = 1;             // register-resident kernel: row buffers a team
+    int tm_slice_vec = 0, tm_slots = 0;  // tensor-memory kernel: slice of a CTA, ring slots
 };
 
 // (device, dtype, V (negative when the logits are not 16-byte aligned),
-// softcap, weighted smoothing, weights 16-byte aligned, tuning signature)
-using PlanKey = std::tuple<int, int, int64_t, bool, bool, bool, std::string>;
+// softcap (0 off, 1 on, 2 on and at most kTmMaxSoftcap), weighted
+// smoothing, weights 16-byte aligned, tuning signature)
+using PlanKey = std::tuple<int, int, int64_t, int, bool, bool, std::string>;
+
+// The tensor-memory kernel shifts exp(z) by the softcap s itself; exp(-2 s)
+// must stay a normal fp32
+constexpr float kTmMaxSoftcap = 40.f;
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
@@ -74,7 +80,7 @@ std::string tuning_signature() {
         "GBCE_KERNEL",        "GBCE_CLUSTER",      "GBCE_CFG",          "GBCE_MAX_STAGES",
         "GBCE_STREAM_GROUPS", "GBCE_STREAM_TWICE", "GBCE_STREAM_SLOTS", "GBCE_STREAM_WARPS",
         "GBCE_REG_MAX_BYTES", "GBCE_REG_NVL",      "GBCE_REG_CLUSTER",  "GBCE_REG_SW",
-        "GBCE_REG_NBUF"};
+        "GBCE_REG_NBUF",      "GBCE_TMEM"};
     std::string sig;
     for (const char* name : kVars) {
         const char* v = std::getenv(name);
@@ -364,8 +370,67 @@ ce_status reg_buffers(const DeviceInfo& dev, const void* fn, int nt, int teams,
     return CE_OK;
 }
 
-ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth, bool aligned,
-                    bool w_aligned, Plan* out) {
+// The tensor-memory kernel's plan for rows of vrow 16-byte vectors: a
+// cluster of C CTAs a row, CTA c the slice of slice vectors from c * slice,
+// each slice's r values within the 128 TMEM columns a consumer thread has;
+// a ring of 32 KB slots in the rest of shared memory; as many clusters as
+// fit. Leaves `best` alone when the row does not fit a cluster of 8.
+ce_status plan_tmem(const DeviceInfo& dev, int dtype, int64_t vrow, Plan* best) {
+    const int VE = dtype == CE_F32 ? 4 : 8;
+    const int64_t chunk = 32 * kTmWarps * kTmVecPerThread;
+    const int64_t max_vec_cta = 32 * kTmWarps * (128 / VE);  // 128 columns a thread
+    const int64_t C = (vrow + max_vec_cta - 1) / max_vec_cta;
+    const int64_t slice = ((vrow + C - 1) / C + chunk - 1) / chunk * chunk;
+    if (C > kTmMaxCluster || slice > max_vec_cta) return CE_OK;
+    const void* fn = tmem_kernel(dtype);
+    const int nt = 32 * (kTmWarps + 1);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    const size_t dyn_max = static_cast<size_t>(dev.smem_optin) - fa.sharedSizeBytes;
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(dyn_max));
+    if (e != cudaSuccess) return cuda_failure(e, "tensor-memory kernel attributes");
+    const int slots = static_cast<int>(
+        std::min<size_t>(kTmMaxSlots, dyn_max / (static_cast<size_t>(chunk) * 16)));
+    const size_t smem = static_cast<size_t>(slots) * chunk * 16;
+    // one CTA an SM: each allocates all 512 TMEM columns, and two CTAs of
+    // one cluster on one SM would wait on each other. (Two CTAs of 8
+    // consumer warps an SM, each with 256 columns, measured slower: 753
+    // against 536 us at 4096 x 131072 bf16, softcap 30.)
+    if (slots < 2 || 2 * (smem + fa.sharedSizeBytes) <= static_cast<size_t>(dev.smem_per_sm))
+        return CE_OK;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(C * dev.sm_count));
+    lc.blockDim = dim3(static_cast<unsigned>(nt));
+    lc.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(C);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    lc.attrs = &attr;
+    lc.numAttrs = 1;
+    int ncl = 0;
+    e = cudaOccupancyMaxActiveClusters(&ncl, fn, &lc);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CE_OK;  // not schedulable here: not a candidate
+    }
+    if (ncl < 1) return CE_OK;
+    best->fn = fn;
+    best->kind = Kind::Tmem;
+    best->nt = nt;
+    best->smem = smem;
+    best->cluster = static_cast<int>(C);
+    best->tm_slice_vec = static_cast<int>(slice);
+    best->tm_slots = slots;
+    best->max_units = ncl;
+    return CE_OK;
+}
+
+ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool sc_small, bool wsmooth,
+                    bool aligned, bool w_aligned, Plan* out) {
     // Tuning overrides: GBCE_CLUSTER forces the CTAs per row (1, 2, 4, 8 or
     // 16; -1 forces the general path) and GBCE_CFG the CTA shape index.
     const int forced_c = env_int("GBCE_CLUSTER", 0);
@@ -373,8 +438,8 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     // GBCE_KERNEL: 1 staged, 2 streaming, 3 general, 4 register-resident,
     // 5 register-resident with a cluster of CTAs a row (0: automatic)
     const int forced_kind = env_int("GBCE_KERNEL", 0);
-    const PlanKey key(devid, dtype, aligned ? V : -V, softcap, wsmooth, w_aligned,
-                      tuning_signature());
+    const PlanKey key(devid, dtype, aligned ? V : -V, softcap ? (sc_small ? 2 : 1) : 0, wsmooth,
+                      w_aligned, tuning_signature());
     auto it = g_plans.find(key);
     if (it != g_plans.end()) {
         *out = it->second;
@@ -502,6 +567,16 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
             best.max_units = std::min<int64_t>(ncl, kMaxUnits / cl_C);
         }
     }
+    // Softcapped rows longer than the register kernel takes: the
+    // tensor-memory kernel (tanh formed once an element and kept in TMEM, a
+    // cluster of C CTAs a row), for softcaps up to kTmMaxSoftcap
+    // (GBCE_TMEM=0 turns it off; GBCE_KERNEL=6 forces it)
+    if (fast_ok && softcap && sc_small && !wsmooth && best.kind == Kind::General &&
+        (forced_kind == 6 ||
+         (forced_kind == 0 && V * bytes > reg_max && env_int("GBCE_TMEM", 1)))) {
+        rc = plan_tmem(dev, dtype, vrow, &best);
+        if (rc != CE_OK) return rc;
+    }
     if (fast_ok && forced_kind != 1 && best.kind == Kind::General) {
         rc = CE_OK;
         if (!try_stream(dtype, V, softcap, wsmooth, dev, &best, &rc) && rc != CE_OK) return rc;
@@ -536,7 +611,8 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     if ((forced_kind == 1 && best.kind != Kind::Staged) ||
         (forced_kind == 2 && best.kind != Kind::Stream) ||
         (forced_kind == 4 && best.kind != Kind::Reg) ||
-        (forced_kind == 5 && (best.kind != Kind::Reg || best.cluster < 2))) {
+        (forced_kind == 5 && (best.kind != Kind::Reg || best.cluster < 2)) ||
+        (forced_kind == 6 && best.kind != Kind::Tmem)) {
         g_last_error = "the kernel forced by GBCE_KERNEL cannot run this shape";
         return CE_ERR_UNSUPPORTED;
     }
@@ -551,7 +627,8 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
     // the occupancy calculator allows.
     {
         const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
-        const int64_t per_unit = best.kind == Kind::Reg ? best.cluster : 1;
+        const int64_t per_unit =
+            (best.kind == Kind::Reg || best.kind == Kind::Tmem) ? best.cluster : 1;
         best.max_units = std::max<int64_t>(1, std::min(best.max_units, cap / per_unit));
     }
     if (env_int("GBCE_VERBOSE", 0))
@@ -563,6 +640,7 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool wsmooth,
                      best.kind == Kind::Stream   ? "stream"
                      : best.kind == Kind::Staged ? "staged"
                      : best.kind == Kind::Reg    ? "reg"
+                     : best.kind == Kind::Tmem   ? "tmem"
                                                  : "general",
                      best.nt, best.cluster, best.stages, best.slice_vec, best.smem,
                      static_cast<long long>(best.max_units), best.ng, best.sg, best.chunk_vec,
@@ -678,12 +756,16 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
     const bool aligned = (reinterpret_cast<uintptr_t>(c.logits) % 16) == 0;
     const bool w_aligned = (reinterpret_cast<uintptr_t>(c.weight) % 16) == 0;
     Plan p;
-    ce_status rc = make_plan(dev, c.dtype, c.V, sc, wsmooth, aligned, w_aligned, &p);
+    ce_status rc =
+        make_plan(dev, c.dtype, c.V, sc, sc && c.softcap <= kTmMaxSoftcap, wsmooth, aligned,
+                  w_aligned, &p);
     if (rc != CE_OK) return rc;
     const int64_t units = c.rows == 0 ? 1 : std::min<int64_t>(c.rows, p.max_units);
     // the register kernel's clusters: a partial-sum slot for each CTA
     const int64_t slots =
-        records_for(p.kind == Kind::Reg && c.rows > 0 ? units * p.cluster : units);
+        records_for((p.kind == Kind::Reg || p.kind == Kind::Tmem) && c.rows > 0
+                        ? units * p.cluster
+                        : units);
     if (slots > max_slots) {
         g_last_error = "this launch needs " + std::to_string(slots) +
                        " partial-sum slots; the scratch holds " + std::to_string(max_slots);
@@ -739,6 +821,11 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
         a.reg_cluster = p.cluster;
         return launch(p.fn, static_cast<int>(units * p.cluster), p.nt, p.smem, p.cluster, st, &a,
                       pdl);
+    }
+    if (p.kind == Kind::Tmem) {
+        a.tm_slice_vec = p.tm_slice_vec;
+        a.tm_slots = p.tm_slots;
+        return launch(p.fn, static_cast<int>(units * p.cluster), p.nt, p.smem, p.cluster, st, &a);
     }
     if (p.kind == Kind::Staged) {
         a.slice_vec = p.slice_vec;

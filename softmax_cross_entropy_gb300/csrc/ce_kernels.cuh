@@ -79,6 +79,8 @@ struct FwdArgs {
     int reg_wpr;    // register-resident kernel: warps a row team has
     uint32_t reg_buf_stride;  // register-resident kernel: bytes of a team's row buffer
     int reg_nbuf;             // register-resident kernel: row buffers a team (1 or 2)
+    int tm_slice_vec;         // tensor-memory kernel: 16-byte vectors of a CTA's slice of a row
+    int tm_slots;             // tensor-memory kernel: ring slots
     int reg_cluster;  // register-resident kernel: CTAs of the cluster that owns a row (0, 1: one CTA)
     // test hook: CTA 0 does not issue its first bulk copy, so the wait for
     // it runs out (status CE_ERR_TIMEOUT, outputs invalid, nothing faults)
@@ -527,6 +529,16 @@ const void* reg_kernel(int dtype, bool softcap, bool ws, int nvl);
 // Its class-weighted smoothing variant with the weights in shared memory:
 // 16 warps a CTA, 8 vectors a thread.
 const void* reg_kernel_sw(int dtype, bool softcap);
+// The softcap kernel that keeps tanh's intermediate in tensor memory
+// (ce_fwd_tmem.cuh): kTmWarps consumer warps and a producer warp, one CTA
+// an SM with all of the SM's TMEM (kTmCols columns), clusters of up to
+// kTmMaxCluster CTAs a row.
+const void* tmem_kernel(int dtype);
+constexpr int kTmWarps = 16;
+constexpr int kTmCols = 32 * kTmWarps;  // TMEM columns a CTA allocates
+constexpr int kTmVecPerThread = 4;  // 16-byte vectors a consumer thread takes from a slot
+constexpr int kTmMaxSlots = 8;
+constexpr int kTmMaxCluster = 8;
 constexpr int kRegSwWarps = 16;
 // The register-resident kernel's cluster variant (16 vectors a thread).
 const void* reg_cluster_kernel(int dtype, bool softcap, bool ws);

@@ -503,6 +503,58 @@ def test_register_kernel(monkeypatch, dtype, V, rows, nvl):
         check_full(case, want_z=True, want_acc=True, want_pred=True)
 
 
+@pytest.mark.parametrize("dtype,V,rows", [
+    ("bf16", 24576, 41),    # one CTA a row, two slots
+    ("bf16", 40000, 37),    # one CTA a row, the last slot ragged
+    ("bf16", 65536, 21),    # one CTA a row, every TMEM column
+    ("bf16", 65544, 19),    # two CTAs, the second holds one vector
+    ("bf16", 131072, 23),   # the softcap bench shape: two CTAs of 64K elements
+    ("f32", 128256, 11),    # two CTAs of 16384 vectors, the second ragged
+    ("f16", 100000, 13),
+    ("bf16", 200000, 5),    # four CTAs (clusters up to eight)
+])
+def test_tensor_memory_kernel(monkeypatch, dtype, V, rows):
+    # the softcap kernel that keeps tanh's intermediate in TMEM, forced,
+    # whole-batch comparison for every option it takes (softcap <= 40, no
+    # class-weighted smoothing)
+    monkeypatch.setenv("GBCE_KERNEL", "6")
+    for opts in (dict(softcap=30.0, std=8.0),
+                 dict(softcap=30.0, std=8.0, label_smoothing=0.1, lse_square_scale=1e-4),
+                 dict(softcap=5.0, std=20.0, label_smoothing=0.05, reduction="none"),
+                 dict(softcap=40.0, std=3.0, weight=True, lse_square_scale=1e-3, reduction="sum",
+                      ignore_frac=0.3),
+                 dict(softcap=1.0, std=3.0, ignore_frac=1.0)):
+        case = workloads.random_case(170 + rows, rows, V, dtype=dtype, **opts)
+        check_full(case, want_z=True, want_acc=True, want_pred=True)
+
+
+def test_tensor_memory_kernel_ties_and_forward_only(monkeypatch):
+    monkeypatch.setenv("GBCE_KERNEL", "6")
+    case = workloads.random_case(191, 9, 131072, dtype="bf16", std=2.0, softcap=20.0,
+                                 label_smoothing=0.1, ignore_frac=0.0)
+    # the row maximum twice, once in each CTA's slice, and twice in one vector
+    case.x[0, 70000] = case.x[0, 5] = workloads.f32_to_bf16_bits(np.array([40.0], np.float32))[0]
+    case.x[1, 9] = case.x[1, 10] = workloads.f32_to_bf16_bits(np.array([40.0], np.float32))[0]
+    check_full(case, want_z=True, want_acc=True, want_pred=True)
+    x, _, _ = to_device(case)
+    before = x.clone()
+    out = run_cuda(case, x=x, grad=False, want_pred=True)
+    assert torch.equal(x, before)
+    assert out["pred"][0] == 5 and out["pred"][1] == 9
+
+
+def test_tensor_memory_kernel_refuses_large_softcaps(monkeypatch):
+    from softmax_cross_entropy_gb300 import _lib
+    monkeypatch.setenv("GBCE_KERNEL", "6")
+    case = workloads.random_case(192, 4, 131072, dtype="bf16", softcap=50.0)
+    x, t, _ = to_device(case)
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    rc = _lib.ce_fwd(x.data_ptr(), 1, case.rows, case.V, t.data_ptr(), None, -100, 0.0, 0.0,
+                     50.0, 2, _lib.CE_FLAG_GRAD, loss.data_ptr(), None, None, None,
+                     torch.cuda.current_stream().cuda_stream)
+    assert rc == _lib.CE_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("sw,nbuf", [("0", "1"), ("1", "2"), ("0", "2")])
 @pytest.mark.parametrize("dtype,V,rows", [("bf16", 32000, 37), ("bf16", 4096, 301),
                                           ("f32", 5000, 45), ("f16", 16384, 29)])

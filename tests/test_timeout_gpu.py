@@ -24,7 +24,7 @@ def _library():
     _lib.load()
 
 
-@pytest.mark.parametrize("kernel,V", [("4", 4096), ("4", 32000), ("2", 65536)])
+@pytest.mark.parametrize("kernel,V", [("4", 4096), ("4", 32000), ("2", 65536), ("6", 131072)])
 @pytest.mark.parametrize("reduction", ["mean", "none"])
 def test_wait_runs_out_then_context_usable(monkeypatch, kernel, V, reduction):
     from softmax_cross_entropy_gb300 import _lib
@@ -33,7 +33,8 @@ def test_wait_runs_out_then_context_usable(monkeypatch, kernel, V, reduction):
     monkeypatch.setenv("GBCE_WAIT_TIMEOUT_MS", "20")
     # no ignored rows: CTA 0 owns row 0 (48 rows, one or a few a CTA), and an
     # ignored row would leave it no copy to leave out
-    case = workloads.random_case(17, 48, V, dtype="bf16", ignore_frac=0.0, reduction=reduction)
+    case = workloads.random_case(17, 48, V, dtype="bf16", ignore_frac=0.0, reduction=reduction,
+                                 softcap=30.0 if kernel == "6" else None)
     monkeypatch.setenv("GBCE_TEST_STALL_COPY", "1")
     out = run_cuda(case)
     assert out["status"] == _lib.CE_ERR_TIMEOUT
