@@ -289,13 +289,16 @@ ce_status ce_bwd_nd(const float* grad_output, int grad_per_position, void* dlogi
  *              rows, V, chunk_rows) bytes, 256-byte aligned, owned by the
  *              caller; it holds one chunk of fp32 logits (and of the gradient
  *              in dtype) and the chunks' partial sums.
- * Per chunk: logits by a tensor-core GEMM (cuBLAS; inputs in dtype, fp32
- * accumulation and output), the fused forward of this library in place
+ * Per chunk: logits by this library's tensor-core GEMM (ce_gemm; inputs in
+ * dtype, fp32 accumulation), the fused forward of this library in place
  * over them (one shard of the batch, D from ce_count), the gradient rounded
  * to dtype, then grad_hidden = G @ lm_weight and grad_weight += G^T @ hidden
- * (cuBLAS, fp32 accumulation) and grad_bias += column sums. Scalars are
- * added in chunk order: deterministic. Asynchronous on `stream`; uses the
- * library scratch of (device, stream) and a cuBLAS handle per device.
+ * (ce_gemm again, fp32 accumulation) and grad_bias += column sums. fp32
+ * inputs, and 16-bit ones with H or V not a multiple of 8 or unaligned
+ * bases, take cuBLAS for the three GEMMs (GBCE_FLCE_GEMM=cublas forces it).
+ * Scalars are added in chunk order: deterministic. Asynchronous on
+ * `stream`; uses the library scratch of (device, stream) (and a cuBLAS
+ * handle per device on the cuBLAS path).
  * Errors as for ce_fwd; CE_ERR_INVALID_ARG also for a missing or too small
  * workspace.
  */
@@ -321,6 +324,36 @@ ce_status ce_flce(const void* hidden, const void* lm_weight, const float* bias, 
  */
 ce_status ce_gemm_abt(const void* A, const void* B, int dtype, int64_t M, int64_t N,
                       int64_t K, float* C, const float* bias, ce_stream_t stream);
+
+/* What ce_gemm does with the product. */
+enum { CE_GEMM_F32 = 0, CE_GEMM_F32_ADD = 1, CE_GEMM_16BIT = 2 };
+
+/*
+ * ce_gemm - C = A @ B on the tensor cores, for the three GEMMs of the fused
+ * linear cross-entropy (logits = hidden @ lm_weight^T, grad_hidden = G @
+ * lm_weight, grad_weight += G^T @ hidden). The method has no counterpart:
+ * these are the linear layer the fused linear cross-entropy folds in.
+ *
+ * A            [M, K] as the math has it, stored K-major (a_mn = 0: row-major
+ *              [M, K], K contiguous) or MN-major (a_mn = 1: row-major [K, M],
+ *              M contiguous, i.e. the storage of A^T).
+ * B            [K, N], stored K-major (b_mn = 0: row-major [N, K]) or MN-major
+ *              (b_mn = 1: row-major [K, N]).
+ * dtype        CE_BF16 or CE_F16 for both operands; bases 16-byte aligned and
+ *              the contiguous dimension a multiple of 8 (K, M or N), else
+ *              CE_ERR_UNSUPPORTED.
+ * C            [M, N] row-major: fp32 written (c_mode CE_GEMM_F32, plus
+ *              bias [N] fp32 when bias is not NULL), fp32 added to
+ *              (CE_GEMM_F32_ADD), or rounded to nearest even into dtype
+ *              (CE_GEMM_16BIT). bias only with CE_GEMM_F32 (else
+ *              CE_ERR_INVALID_ARG).
+ * Accumulation in fp32 in tensor memory; K > 0. Asynchronous on `stream`;
+ * a bounded wait that gives up records CE_ERR_TIMEOUT for ce_device_status
+ * (that call's C is then invalid).
+ */
+ce_status ce_gemm(const void* A, int a_mn, const void* B, int b_mn, int dtype, int64_t M,
+                  int64_t N, int64_t K, void* C, int c_mode, const float* bias,
+                  ce_stream_t stream);
 
 /*
  * ce_scale_round - out[i] = in[i] * grad_output[0], rounded to nearest-even

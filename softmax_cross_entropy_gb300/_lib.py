@@ -33,6 +33,7 @@ SIGNATURES = {
     "ce_flce_workspace_bytes": (ctypes.c_size_t, [_I, _I64, _I64, _I64]),
     "ce_scale_round": (_I, [_P, _P, _P, _I, _I64, _P]),
     "ce_gemm_abt": (_I, [_P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
+    "ce_gemm": (_I, [_P, _I, _P, _I, _I, _I64, _I64, _I64, _P, _I, _P, _P]),
     "ce_flce": (_I, [_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _I64, _F, _F, _F, _I, _U32, _P, _P,
                      _P, _P, _P, _P, _P, _I64, _P, ctypes.c_size_t, _P]),
     "ce_bwd": (_I, [_P, _I, _P, _I, _I64, _I64, _P]),
@@ -131,6 +132,13 @@ def ce_flce(hidden, lm_weight, bias, dtype, rows, H, V, target, class_weight, ig
 
 def ce_gemm_abt(A, B, dtype, M, N, K, C, bias, stream):
     return load().ce_gemm_abt(A, B, dtype, M, N, K, C, bias, stream)
+
+
+CE_GEMM_F32, CE_GEMM_F32_ADD, CE_GEMM_16BIT = 0, 1, 2
+
+
+def ce_gemm(A, a_mn, B, b_mn, dtype, M, N, K, C, c_mode, bias, stream):
+    return load().ce_gemm(A, a_mn, B, b_mn, dtype, M, N, K, C, c_mode, bias, stream)
 
 
 def ce_scale_round(inp, grad_output, out, dtype, n, stream):

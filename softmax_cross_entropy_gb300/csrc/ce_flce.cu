@@ -5,15 +5,20 @@
 // fused_linear_cross_entropy, this kernel with the linear layer fused in).
 //
 // Per chunk of c rows, on the caller's stream:
-//   1. logits [c, V] fp32 = hidden_c @ W^T (+ bias): tensor-core GEMM
-//      (cuBLAS, or this library's tcgen05 kernel with GBCE_FLCE_GEMM=tcgen05;
-//      inputs in the storage type, fp32 accumulation);
+//   1. logits [c, V] fp32 = hidden_c @ W^T (+ bias): this library's
+//      tcgen05 GEMM (ce_gemm_tc.cu; inputs in the storage type, fp32
+//      accumulation in tensor memory);
 //   2. the fused forward of this library over the chunk, as one shard of
 //      the batch (the batch's D and counted rows from ce_count), writing
 //      the gradient of the batch's reduced loss in place over the logits;
 //   3. G = that gradient rounded to the storage type;
-//   4. grad_hidden_c = G @ W, grad_weight (+)= G^T @ hidden_c (fp32), and
-//      grad_bias (+)= the column sums of the fp32 gradient.
+//   4. grad_hidden_c = G @ W (the same GEMM kernel with W read MN-major,
+//      rounded to the storage type), grad_weight (+)= G^T @ hidden_c (both
+//      operands MN-major, fp32 written then added to), and grad_bias (+)=
+//      the column sums of the fp32 gradient (a column-per-thread kernel).
+// fp32 inputs, and 16-bit ones whose rows are not multiples of 8 elements
+// (16-byte rows for the TMA), take cuBLAS for the three GEMMs instead
+// (GBCE_FLCE_GEMM=cublas forces it for every input).
 // The chunks' scalar outputs are added in chunk order at the end, so the
 // results are deterministic.
 #include <algorithm>
@@ -37,6 +42,10 @@ bool tc_gemm_supported(const void* A, const void* B, int dtype, int64_t K);
 ce_status tc_gemm_abt_launch(const void* A, const void* B, int dtype, int64_t M, int64_t N,
                              int64_t K, float* C, const float* bias, unsigned* status,
                              unsigned* abort, cudaStream_t st);
+ce_status tc_gemm_launch(const void* A, bool a_mn, const void* B, bool b_mn, int dtype, int64_t M,
+                         int64_t N, int64_t K, void* C, int out, const float* bias,
+                         unsigned* status, unsigned* abort, cudaStream_t st);
+bool tc_operand_ok(const void* p, int dtype, int64_t row_elems);
 
 namespace {
 
@@ -71,10 +80,16 @@ flce_round(const float* in, T* out, int64_t n) {
         VT::store1(out, i, in[i]);
 }
 
-__global__ void flce_fill(float* p, float v, int64_t n) {
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        p[i] = v;
+// grad_bias[v] (+)= sum over the chunk's rows of g[r, v]: a thread a column
+// (consecutive threads, consecutive columns), the rows added in order.
+__global__ void __launch_bounds__(kFlceThreads)
+flce_colsum(const float* g, float* out, int64_t rows, int64_t V, int accumulate) {
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * kFlceThreads + threadIdx.x; v < V;
+         v += static_cast<int64_t>(gridDim.x) * kFlceThreads) {
+        float s = accumulate ? out[v] : 0.f;
+        for (int64_t r = 0; r < rows; ++r) s += g[r * V + v];
+        out[v] = s;
+    }
 }
 
 // out = in * g rounded into T, g one fp32 value read on the device.
@@ -136,11 +151,10 @@ cudaDataType_t blas_type(int dtype) {
 int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
 
 // Workspace layout: counts (2 doubles) | chunk scalars (3 floats a chunk) |
-// logits chunk (fp32) | rounded gradient chunk (storage type, not for fp32)
-// | ones (fp32, for the bias gradient).
+// logits chunk (fp32) | rounded gradient chunk (storage type, not for fp32).
 struct FlceLayout {
     int64_t chunk, nchunks;
-    int64_t off_counts, off_parts, off_logits, off_g, off_ones, total;
+    int64_t off_counts, off_parts, off_logits, off_g, total;
 };
 
 FlceLayout layout(int dtype, int64_t rows, int64_t V, int64_t chunk_rows) {
@@ -155,8 +169,7 @@ FlceLayout layout(int dtype, int64_t rows, int64_t V, int64_t chunk_rows) {
     L.off_parts = align256(16);
     L.off_logits = L.off_parts + align256(std::max<int64_t>(L.nchunks, 1) * 12);
     L.off_g = L.off_logits + align256(c * V * 4);
-    L.off_ones = L.off_g + (dtype == CE_F32 ? 0 : align256(c * V * b));
-    L.total = L.off_ones + align256(c * 4);
+    L.total = L.off_g + (dtype == CE_F32 ? 0 : align256(c * V * b));
     return L;
 }
 
@@ -204,18 +217,27 @@ extern "C" ce_status ce_flce(const void* hidden, const void* lm_weight, const fl
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return record_cuda_failure(e, "cudaDeviceGetAttribute");
+    // The three GEMMs on this library's tcgen05 kernel for 16-bit inputs
+    // with rows of multiples of 8 elements; cuBLAS otherwise (or with
+    // GBCE_FLCE_GEMM=cublas)
+    const char* genv = std::getenv("GBCE_FLCE_GEMM");
+    const bool use_tc = !(genv && std::strcmp(genv, "cublas") == 0) && dtype != CE_F32 &&
+                        tc_operand_ok(hidden, dtype, H) && tc_operand_ok(lm_weight, dtype, H) &&
+                        V % 8 == 0;
     cublasHandle_t blas = nullptr;
-    ce_status rc = blas_for(dev, &blas);
-    if (rc != CE_OK) return rc;
-    rc = blas_check(cublasSetStream(blas, st), "cublasSetStream");
-    if (rc != CE_OK) return rc;
+    ce_status rc = CE_OK;
+    if (!use_tc) {
+        rc = blas_for(dev, &blas);
+        if (rc != CE_OK) return rc;
+        rc = blas_check(cublasSetStream(blas, st), "cublasSetStream");
+        if (rc != CE_OK) return rc;
+    }
 
     char* ws = static_cast<char*>(workspace);
     double* counts = reinterpret_cast<double*>(ws + L.off_counts);
     float* parts = reinterpret_cast<float*>(ws + L.off_parts);
     float* logits = reinterpret_cast<float*>(ws + L.off_logits);
     void* gbuf = dtype == CE_F32 ? static_cast<void*>(logits) : static_cast<void*>(ws + L.off_g);
-    float* ones = reinterpret_cast<float*>(ws + L.off_ones);
     const int64_t b = dtype == CE_F32 ? 4 : 2;
     const cudaDataType_t dt = blas_type(dtype);
     const uint32_t tflag = flags & static_cast<uint32_t>(CE_FLAG_TARGET_I64);
@@ -224,17 +246,6 @@ extern "C" ce_status ce_flce(const void* hidden, const void* lm_weight, const fl
     // the batch's D and counted rows: every chunk is one shard of the batch
     rc = ce_count(target, class_weight, rows, V, ignore_index, tflag, counts, stream);
     if (rc != CE_OK) return rc;
-    if (grad && grad_bias) {
-        flce_fill<<<std::max<int64_t>(1, std::min<int64_t>((L.chunk + 255) / 256, sms)), 256, 0,
-                    st>>>(ones, 1.f, L.chunk);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return record_cuda_failure(e, "fill");
-    }
-    // The logits GEMM: cuBLAS, or with GBCE_FLCE_GEMM=tcgen05 this
-    // library's tensor-core kernel (ce_gemm_abt; bias added in its epilogue)
-    const char* genv = std::getenv("GBCE_FLCE_GEMM");
-    const bool use_tc = genv && std::strcmp(genv, "tcgen05") == 0 &&
-                        tc_gemm_supported(hidden, lm_weight, dtype, H);
     unsigned* status = nullptr;
     if (use_tc) {
         rc = library_status_word(st, &status);
@@ -290,7 +301,13 @@ extern "C" ce_status ce_flce(const void* hidden, const void* lm_weight, const fl
             if (e != cudaSuccess) return record_cuda_failure(e, "round");
         }
         // 4. gradients
-        if (grad_hidden) {
+        void* gh = grad_hidden ? static_cast<char*>(grad_hidden) + r0 * H * b : nullptr;
+        if (grad_hidden && use_tc) {
+            // G [c, V] (K-major) @ W [V, H] (MN-major), rounded to dtype
+            rc = tc_gemm_launch(gbuf, false, lm_weight, true, dtype, c, H, V, gh, CE_GEMM_16BIT,
+                                nullptr, status, status + 1, st);
+            if (rc != CE_OK) return rc;
+        } else if (grad_hidden) {
             rc = blas_check(cublasGemmEx(blas, CUBLAS_OP_N, CUBLAS_OP_N, static_cast<int>(H),
                                          static_cast<int>(c), static_cast<int>(V), &one, lm_weight,
                                          dt, static_cast<int>(H), gbuf, dt, static_cast<int>(V),
@@ -300,7 +317,14 @@ extern "C" ce_status ce_flce(const void* hidden, const void* lm_weight, const fl
                             "grad_hidden GEMM");
             if (rc != CE_OK) return rc;
         }
-        if (grad_weight) {
+        if (grad_weight && use_tc) {
+            // G^T [V, c] (G read MN-major) @ hidden_c [c, H] (MN-major), fp32,
+            // written by the first chunk and added to by the others
+            rc = tc_gemm_launch(gbuf, true, hc, true, dtype, V, H, c, grad_weight,
+                                k == 0 ? CE_GEMM_F32 : CE_GEMM_F32_ADD, nullptr, status,
+                                status + 1, st);
+            if (rc != CE_OK) return rc;
+        } else if (grad_weight) {
             rc = blas_check(cublasGemmEx(blas, CUBLAS_OP_N, CUBLAS_OP_T, static_cast<int>(H),
                                          static_cast<int>(V), static_cast<int>(c), &one, hc, dt,
                                          static_cast<int>(H), gbuf, dt, static_cast<int>(V),
@@ -311,14 +335,11 @@ extern "C" ce_status ce_flce(const void* hidden, const void* lm_weight, const fl
             if (rc != CE_OK) return rc;
         }
         if (grad_bias) {
-            rc = blas_check(cublasGemmEx(blas, CUBLAS_OP_N, CUBLAS_OP_N, static_cast<int>(V), 1,
-                                         static_cast<int>(c), &one, logits, CUDA_R_32F,
-                                         static_cast<int>(V), ones, CUDA_R_32F, static_cast<int>(c),
-                                         k == 0 ? &zero : &one, grad_bias, CUDA_R_32F,
-                                         static_cast<int>(V), CUBLAS_COMPUTE_32F,
-                                         CUBLAS_GEMM_DEFAULT),
-                            "grad_bias GEMV");
-            if (rc != CE_OK) return rc;
+            const int grid = static_cast<int>(std::min<int64_t>((V + kFlceThreads - 1) / kFlceThreads,
+                                                                8L * sms));
+            flce_colsum<<<grid, kFlceThreads, 0, st>>>(logits, grad_bias, c, V, k == 0 ? 0 : 1);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return record_cuda_failure(e, "grad_bias column sums");
         }
     }
     if (reduction != CE_RED_NONE) {

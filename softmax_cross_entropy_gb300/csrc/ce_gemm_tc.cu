@@ -1,30 +1,38 @@
-// C[M, N] (fp32, row-major) = A[M, K] @ B[N, K]^T (+ bias[N]), A and B bf16
-// or fp16, row-major (K contiguous): the logits GEMM of the fused linear
-// cross-entropy (hidden @ lm_weight^T), on the fifth-generation tensor
-// cores.
+// Tensor-core GEMMs of the fused linear cross-entropy on the fifth-
+// generation tensor cores: C[M, N] = A[M, K] @ B[K, N] with A and B bf16 or
+// fp16, each operand stored either K-major (rows of K contiguous elements:
+// A as [M, K], B as [N, K]) or MN-major (A as [K, M], B as [K, N]); C fp32
+// written, fp32 added to, or rounded to the operand type (+ bias[N] for the
+// fp32 store). The three GEMMs of ce_flce are the three layouts: logits =
+// hidden @ W^T (both K-major), grad_hidden = G @ W (B MN-major, 16-bit out),
+// grad_weight += G^T @ hidden (both MN-major, fp32 accumulate).
 //
-// One CTA of 4 warps computes a 128 x 256 tile of C:
-//  * lane 0 of warp 0 streams 128 x 64 tiles of A and 256 x 64 tiles of B
-//    into a 4-stage shared-memory ring with 2-D TMA copies (128-byte
-//    swizzle, the layout the tensor core reads), signalling `full`
-//    mbarriers;
-//  * lane 0 of warp 1 issues tcgen05.mma (M = 128, N = 256, K = 16, fp32
-//    accumulation) into a 256-column accumulator in tensor memory, four per
-//    stage, and frees each stage with tcgen05.commit on its `empty`
-//    mbarrier; a last commit signals `done`;
-//  * all four warps then read the accumulator with tcgen05.ld (warp w owns
-//    rows 32 w .. 32 w + 31 of the tile), add the bias and store fp32 rows.
-// CTAs run along M first, so the CTAs that share a 256-row slice of B
-// (the vocabulary) run together and read it from L2. Every mbarrier wait
-// is bounded; a wait that gives up records the timeout in the status word,
-// the kernel waits (bounded) for its copies in flight, frees its tensor
-// memory and returns.
+// A persistent kernel, one CTA an SM, warp-specialised (6 warps):
+//  * warp 0, lane 0: TMA producer. It walks the CTA's 128 x 256 tiles (tile
+//    t of the launch goes to CTA t mod grid; tiles run along M first, so
+//    concurrent CTAs share a slice of B through L2) and their 64-deep K
+//    blocks, and fills a 4-stage shared-memory ring with 2-D TMA copies
+//    (128-byte swizzle): one box a K-major operand tile, or boxes of 64
+//    MN elements x 64 K rows side by side for an MN-major one;
+//  * warp 1, lane 0: MMA issuer. tcgen05.mma (M 128, N 256, K 16, fp32
+//    accumulation) into one of two 256-column accumulators in tensor memory
+//    (512 columns: tile i uses accumulator i mod 2), freeing each stage with
+//    tcgen05.commit on its `empty` mbarrier and handing the finished
+//    accumulator to the epilogue with a commit on its `acc_full` mbarrier;
+//  * warps 2-5: epilogue. Each reads its 32 accumulator rows (tcgen05.ld)
+//    and writes them out while the tensor cores already work on the next
+//    tile in the other accumulator, then frees the accumulator
+//    (`acc_empty`, 128 arrivals).
+// Every mbarrier wait is bounded; a wait that gives up records the timeout
+// in the status word and sets the launch's abort word, the kernel waits
+// (bounded) for its copies in flight, frees its tensor memory and returns.
 #include <cuda.h>
 
 #include <algorithm>
 #include <cstdlib>
 #include <mutex>
 #include <string>
+#include <type_traits>
 
 #include "ce_kernels.cuh"
 #include "gbce.h"
@@ -39,17 +47,22 @@ namespace {
 // 4 stages of 128 x 64 + 256 x 64 tiles (192 KB, one CTA an SM): measured
 // best of 2 / 3 / 4 / 6 stages and 128- / 256-wide tiles on GB300
 constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 192;  // producer, MMA issuer, 4 epilogue warps
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kBBytes = kBN * kBK * 2;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kTmemCols = kBN;
+constexpr uint32_t kMnBox = 64 * kBK * 2;  // one 64 (MN) x 64 (K) box of an MN-major tile
+constexpr uint32_t kTmemCols = 2 * kBN;    // two accumulators
 constexpr size_t kTcSmem = static_cast<size_t>(kStages) * kStageBytes + 1024;
 
+// What the epilogue does with the accumulator.
+enum : int { kOutF32 = 0, kOutF32Add = 1, kOut16 = 2 };
+
 struct TcArgs {
-    float* C;
-    const float* bias;
+    void* C;            // [M, N] row-major: fp32, or the operand type for kOut16
+    const float* bias;  // [N] or nullptr (kOutF32 only)
     int64_t M, N, K;
+    int64_t tiles_m, tiles;
     uint64_t timeout_ns;
     unsigned* status;  // sticky error word of the scratch (ce_device_status)
     unsigned* abort;   // cleared before the launch; set when a CTA gives up
@@ -68,11 +81,26 @@ __device__ __forceinline__ uint64_t tc_smem_desc(uint32_t saddr) {
     return d;
 }
 
+// The same for an MN-major operand tile stored as boxes of 64 MN elements
+// (one 128-byte swizzled row) x 64 K rows, 8 KB each, side by side along
+// MN: 8-row (K) atoms of 1024 bytes, the stride between atoms along K (the
+// stride dimension offset) 1024 bytes, between 64-element blocks along MN
+// (the leading dimension offset) one box, 8 KB.
+__device__ __forceinline__ uint64_t tc_smem_desc_mn(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(kMnBox >> 4) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator, A and B of the
-// given type (0 fp16, 1 bf16), both K-major, N = kBN, M = kBM.
-__host__ __device__ constexpr uint32_t tc_idesc(uint32_t ab) {
-    return (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
-           (static_cast<uint32_t>(kBM >> 4) << 24);
+// given type (0 fp16, 1 bf16), A and B K-major (0) or MN-major (1, the
+// transpose bits 15 and 16), N = kBN, M = kBM.
+__host__ __device__ constexpr uint32_t tc_idesc(uint32_t ab, uint32_t a_mn = 0, uint32_t b_mn = 0) {
+    return (1u << 4) | (ab << 7) | (ab << 10) | (a_mn << 15) | (b_mn << 16) |
+           (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 }
 
 // Bounded wait for the producer and MMA threads of the tight GEMM pipeline:
@@ -142,14 +170,65 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <uint32_t AB>
+// Stores 32 accumulator columns (fp32 v) of row `row` from column n of C.
+template <int OUT, uint32_t AB>
+__device__ __forceinline__ void tc_store32(const TcArgs& a, int64_t row, int64_t n,
+                                           float (&v)[32]) {
+    if (OUT == kOutF32 && a.bias) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (n + i < a.N) v[i] += __ldg(a.bias + n + i);
+    }
+    const bool full = n + 32 <= a.N;
+    if constexpr (OUT == kOut16) {
+        using T = typename std::conditional<AB == 1u, __nv_bfloat16, __half>::type;
+        T* c = static_cast<T*>(a.C) + row * a.N + n;
+        if (full && (a.N & 7) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                const float f[8] = {v[i], v[i + 1], v[i + 2], v[i + 3],
+                                    v[i + 4], v[i + 5], v[i + 6], v[i + 7]};
+                *reinterpret_cast<uint4*>(c + i) = Vec<T>::pack(f);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (n + i < a.N) Vec<T>::store1(c, i, v[i]);
+        }
+    } else {
+        float* c = static_cast<float*>(a.C) + row * a.N + n;
+        if (full && (a.N & 3) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                float4 o = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                if (OUT == kOutF32Add) {
+                    const float4 p = *reinterpret_cast<const float4*>(c + i);
+                    o.x += p.x;
+                    o.y += p.y;
+                    o.z += p.z;
+                    o.w += p.w;
+                }
+                *reinterpret_cast<float4*>(c + i) = o;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (n + i < a.N) c[i] = OUT == kOutF32Add ? c[i] + v[i] : v[i];
+        }
+    }
+}
+
+// A_MN / B_MN: the operand is stored MN-major (A as [K, M], B as [K, N]).
+template <uint32_t AB, bool A_MN, bool B_MN, int OUT>
 __global__ void __launch_bounds__(kTcThreads, 1)
-tc_gemm_abt(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-            const __grid_constant__ TcArgs a) {
+tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+        const __grid_constant__ TcArgs a) {
     extern __shared__ unsigned char tc_smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
-    __shared__ __align__(8) uint64_t done_bar;
+    __shared__ __align__(8) uint64_t acc_full[2];
+    __shared__ __align__(8) uint64_t acc_empty[2];
+    __shared__ __align__(8) uint64_t done_bar;  // every MMA of the CTA completed
     __shared__ uint32_t tmem_base_sh;
     __shared__ uint32_t s_issued[kStages];  // 0, or 2 + parity of the last copy into the stage
     __shared__ int s_fail;
@@ -160,9 +239,8 @@ tc_gemm_abt(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CU
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t smem0 = (smem_u32(tc_smem_raw) + 1023u) & ~1023u;  // 1024-byte aligned
-    const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kBM;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kBN;
     const int nk = static_cast<int>((a.K + kBK - 1) / kBK);
+    const int64_t ntiles = a.tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -170,11 +248,15 @@ tc_gemm_abt(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CU
             mbar_init(smem_u32(&empty_bar[s]), 1);
             s_issued[s] = 0;
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 128);
+        }
         mbar_init(smem_u32(&done_bar), 1);
         s_fail = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == 1) {
         asm volatile(
             "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                 smem_u32(&tmem_base_sh)),
@@ -187,92 +269,136 @@ tc_gemm_abt(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CU
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == 0 && lane == 0) {
-        // ---- TMA producer
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t ph = static_cast<uint32_t>(kb / kStages) & 1u;
-            if (!tc_wait(smem_u32(&empty_bar[s]), ph ^ 1u, a.timeout_ns)) {
-                s_fail = 1;
-                break;
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer: every K block of every tile of this CTA
+            int it = 0;  // K blocks issued so far (ring position)
+            bool fail = false;
+            for (int64_t t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
+                const int m0 = static_cast<int>((t % a.tiles_m) * kBM);
+                const int n0 = static_cast<int>((t / a.tiles_m) * kBN);
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+                    if (!tc_wait(smem_u32(&empty_bar[s]), ph ^ 1u, a.timeout_ns) ||
+                        *reinterpret_cast<volatile unsigned*>(a.abort)) {
+                        fail = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full_bar[s]);
+                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    const uint32_t sa = smem0 + static_cast<uint32_t>(s) * kStageBytes;
+                    const int k0 = kb * kBK;
+                    if (A_MN) {
+                        for (int j = 0; j < kBM / 64; ++j)
+                            tma_load_2d(sa + j * kMnBox, &mapA, m0 + 64 * j, k0, fb);
+                    } else {
+                        tma_load_2d(sa, &mapA, k0, m0, fb);
+                    }
+                    if (B_MN) {
+                        for (int j = 0; j < kBN / 64; ++j)
+                            tma_load_2d(sa + kABytes + j * kMnBox, &mapB, n0 + 64 * j, k0, fb);
+                    } else {
+                        tma_load_2d(sa + kABytes, &mapB, k0, n0, fb);
+                    }
+                    s_issued[s] = 2u + ph;
+                }
             }
-            const uint32_t fb = smem_u32(&full_bar[s]);
-            mbar_arrive_expect_tx(fb, kStageBytes);
-            const uint32_t sa = smem0 + static_cast<uint32_t>(s) * kStageBytes;
-            tma_load_2d(sa, &mapA, kb * kBK, static_cast<int>(m0), fb);
-            tma_load_2d(sa + kABytes, &mapB, kb * kBK, static_cast<int>(n0), fb);
-            s_issued[s] = 2u + ph;
+            if (fail) s_fail = 1;
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer
-        constexpr uint32_t idesc = tc_idesc(AB);
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t ph = static_cast<uint32_t>(kb / kStages) & 1u;
-            if (!tc_wait(smem_u32(&full_bar[s]), ph, a.timeout_ns)) {
-                s_fail = 1;
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer: tile i into accumulator i mod 2
+            constexpr uint32_t idesc = tc_idesc(AB, A_MN ? 1u : 0u, B_MN ? 1u : 0u);
+            int it = 0;
+            int i = 0;  // tiles of this CTA so far
+            bool fail = false;
+            for (int64_t t = blockIdx.x; t < ntiles && !fail; t += gridDim.x, ++i) {
+                const int b = i & 1;
+                // the epilogue has drained this accumulator's previous tile
+                if (!tc_wait(smem_u32(&acc_empty[b]), (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u,
+                             a.timeout_ns)) {
+                    fail = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t acc = tmem + static_cast<uint32_t>(b * kBN);
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+                    if (!tc_wait(smem_u32(&full_bar[s]), ph, a.timeout_ns)) {
+                        fail = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem0 + static_cast<uint32_t>(s) * kStageBytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // K step of 16: 32 bytes inside a K-major swizzled row, two
+                        // 8-row atoms (2 KB) of an MN-major tile
+                        const uint64_t da = A_MN ? tc_smem_desc_mn(sa + 2048u * k)
+                                                 : tc_smem_desc(sa + 32u * k);
+                        const uint64_t db = B_MN ? tc_smem_desc_mn(sa + kABytes + 2048u * k)
+                                                 : tc_smem_desc(sa + kABytes + 32u * k);
+                        tc_mma(acc, da, db, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty_bar[s]));
+                }
+                // every MMA of the tile issued: the epilogue may read it once
+                // they complete (also after a failure, so that nothing waits)
+                tc_commit(smem_u32(&acc_full[b]));
+            }
+            if (fail) s_fail = 1;
+            tc_commit(smem_u32(&done_bar));  // after every MMA this thread issued
+        }
+    } else {
+        // ---- epilogue: warp w reads accumulator lanes 32 (w mod 4) ...
+        const int q = warp & 3;
+        int i = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int b = i & 1;
+            const bool ok = mbar_wait_bounded(smem_u32(&acc_full[b]),
+                                              static_cast<uint32_t>(i >> 1) & 1u, a.timeout_ns);
+            if (!ok || *reinterpret_cast<volatile int*>(&s_fail) ||
+                *reinterpret_cast<volatile unsigned*>(a.abort)) {
+                if (lane == 0) s_fail = 1;
                 break;
             }
             tc_fence_after();
-            const uint32_t sa = smem0 + static_cast<uint32_t>(s) * kStageBytes;
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-                // K step of 16 elements = 32 bytes inside the swizzled 128-byte rows
-                tc_mma(tmem, tc_smem_desc(sa + 32u * k), tc_smem_desc(sa + kABytes + 32u * k),
-                       idesc, (kb > 0 || k > 0) ? 1u : 0u);
-            }
-            tc_commit(smem_u32(&empty_bar[s]));
-        }
-        tc_commit(smem_u32(&done_bar));  // every MMA issued above, also after a failure
-    }
-    __syncwarp();
-
-    // ---- epilogue: accumulator rows -> fp32 C (+ bias)
-    bool ok = mbar_wait_bounded(smem_u32(&done_bar), 0u, a.timeout_ns);
-    tc_fence_after();
-    __syncthreads();  // s_fail is final
-    ok = ok && !s_fail;
-    if (ok && nk > 0) {
-        const int64_t row = m0 + warp * 32 + lane;
-        const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        float* crow = a.C + row * a.N;
-        const bool vec = (a.N & 3) == 0;
+            const int64_t m0 = (t % a.tiles_m) * kBM;
+            const int64_t n0 = (t / a.tiles_m) * kBN;
+            const int64_t row = m0 + q * 32 + lane;
+            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                  static_cast<uint32_t>(b * kBN);
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-            const int64_t n = n0 + c * 32;
-            if (n >= a.N) break;  // the same for every thread of the CTA
-            float v[32];
-            tc_ld32(trow + static_cast<uint32_t>(c * 32), v);
-            if (row < a.M) {
-                if (a.bias) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (n + i < a.N) v[i] += __ldg(a.bias + n + i);
-                }
-                if (vec && n + 32 <= a.N) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(crow + n + i) =
-                            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (n + i < a.N) crow[n + i] = v[i];
-                }
+            for (int c = 0; c < kBN / 32; ++c) {
+                const int64_t n = n0 + c * 32;
+                if (n >= a.N) break;  // the same for every thread of the warp
+                float v[32];
+                tc_ld32(trow + static_cast<uint32_t>(c * 32), v);
+                if (row < a.M) tc_store32<OUT, AB>(a, row, n, v);
             }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&acc_empty[b]));
         }
     }
-    if (!ok && threadIdx.x == 0) {
-        atomicOr(a.status, kDevErrTimeout);
-        atomicExch(a.abort, 1u);
-        // copies still in flight land before the shared memory is released
-        for (int s = 0; s < kStages; ++s)
-            if (s_issued[s])
-                (void)mbar_wait_bounded(smem_u32(&full_bar[s]), s_issued[s] & 1u, a.timeout_ns);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // every MMA completes before the tensor memory is freed
+        const bool done = mbar_wait_bounded(smem_u32(&done_bar), 0u, a.timeout_ns);
+        if (s_fail || !done) {
+            atomicOr(a.status, kDevErrTimeout);
+            atomicExch(a.abort, 1u);
+            // copies still in flight land before the shared memory is released
+            for (int s = 0; s < kStages; ++s)
+                if (s_issued[s])
+                    (void)mbar_wait_bounded(smem_u32(&full_bar[s]), s_issued[s] & 1u,
+                                            a.timeout_ns);
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0)
+    if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
@@ -303,16 +429,18 @@ ce_status encoder(EncodeTiled* out) {
     return CE_OK;
 }
 
-// 2-D map of a row-major [rows, K] matrix of 16-bit elements, boxes of
-// box_rows x 64 elements, 128-byte swizzle, zeros outside the matrix.
-ce_status make_map(CUtensorMap* map, const void* p, int dtype, int64_t rows, int64_t K,
-                   uint32_t box_rows) {
+// 2-D map of a row-major [outer, inner] matrix of 16-bit elements, boxes of
+// box_outer x 64 elements (128 bytes: the swizzle width), 128-byte
+// swizzle, zeros outside the matrix. A K-major operand is [MN, K] with boxes
+// of kBM or kBN rows; an MN-major one is [K, MN] with boxes of 64 K rows.
+ce_status make_map(CUtensorMap* map, const void* p, int dtype, int64_t outer, int64_t inner,
+                   uint32_t box_outer) {
     EncodeTiled enc = nullptr;
     ce_status rc = encoder(&enc);
     if (rc != CE_OK) return rc;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    const cuuint32_t box[2] = {64u, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map,
                            dtype == CE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -327,48 +455,76 @@ ce_status make_map(CUtensorMap* map, const void* p, int dtype, int64_t rows, int
     return CE_OK;
 }
 
-}  // namespace
-
-// Whether the tensor-core GEMM takes these operands: 16-bit types, 16-byte
-// aligned bases and K a multiple of 8 (16-byte row strides for the TMA).
-bool tc_gemm_supported(const void* A, const void* B, int dtype, int64_t K) {
-    return (dtype == CE_BF16 || dtype == CE_F16) && K % 8 == 0 && K > 0 &&
-           (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
+template <uint32_t AB>
+const void* gemm_fn(bool a_mn, bool b_mn, int out) {
+#define GBCE_TC(AM, BM)                                                   \
+    (out == kOutF32      ? (const void*)&tc_gemm<AB, AM, BM, kOutF32>    \
+     : out == kOutF32Add ? (const void*)&tc_gemm<AB, AM, BM, kOutF32Add> \
+                         : (const void*)&tc_gemm<AB, AM, BM, kOut16>)
+    if (!a_mn && !b_mn) return GBCE_TC(false, false);
+    if (!a_mn && b_mn) return GBCE_TC(false, true);
+    if (a_mn && !b_mn) return GBCE_TC(true, false);
+    return GBCE_TC(true, true);
+#undef GBCE_TC
 }
 
-// C = A @ B^T (+ bias) on `st`; status receives timeouts (device word),
-// abort is a device word this launch may use (cleared here first).
-ce_status tc_gemm_abt_launch(const void* A, const void* B, int dtype, int64_t M, int64_t N,
-                             int64_t K, float* C, const float* bias, unsigned* status,
-                             unsigned* abort, cudaStream_t st) {
+}  // namespace
+
+// Whether the tensor-core GEMM takes an operand: a 16-bit type, a 16-byte
+// aligned base and rows of a multiple of 8 elements (16-byte strides for
+// the TMA): K for a K-major operand, M or N for an MN-major one.
+bool tc_operand_ok(const void* p, int dtype, int64_t row_elems) {
+    return (dtype == CE_BF16 || dtype == CE_F16) && row_elems % 8 == 0 && row_elems > 0 &&
+           (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool tc_gemm_supported(const void* A, const void* B, int dtype, int64_t K) {
+    return tc_operand_ok(A, dtype, K) && tc_operand_ok(B, dtype, K);
+}
+
+// C = A @ B on `st` (layouts and outputs as ce_gemm); status receives
+// timeouts (device word), abort is a device word this launch may use
+// (cleared here first).
+ce_status tc_gemm_launch(const void* A, bool a_mn, const void* B, bool b_mn, int dtype, int64_t M,
+                         int64_t N, int64_t K, void* C, int out, const float* bias,
+                         unsigned* status, unsigned* abort, cudaStream_t st) {
     if (M <= 0 || N <= 0) return CE_OK;
-    if (!tc_gemm_supported(A, B, dtype, K)) return CE_ERR_UNSUPPORTED;
-    if (M > INT32_MAX || N > INT32_MAX) return CE_ERR_UNSUPPORTED;
+    if (K <= 0 || !tc_operand_ok(A, dtype, a_mn ? M : K) || !tc_operand_ok(B, dtype, b_mn ? N : K))
+        return CE_ERR_UNSUPPORTED;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return CE_ERR_UNSUPPORTED;
     CUtensorMap ma, mb;
-    ce_status rc = make_map(&ma, A, dtype, M, K, kBM);
+    ce_status rc = a_mn ? make_map(&ma, A, dtype, K, M, 64) : make_map(&ma, A, dtype, M, K, kBM);
     if (rc != CE_OK) return rc;
-    rc = make_map(&mb, B, dtype, N, K, kBN);
+    rc = b_mn ? make_map(&mb, B, dtype, K, N, 64) : make_map(&mb, B, dtype, N, K, kBN);
     if (rc != CE_OK) return rc;
-    const void* fn = dtype == CE_BF16 ? reinterpret_cast<const void*>(&tc_gemm_abt<1u>)
-                                      : reinterpret_cast<const void*>(&tc_gemm_abt<0u>);
-    static std::once_flag attr_once[2];
-    cudaError_t e = cudaSuccess;
-    std::call_once(attr_once[dtype == CE_BF16 ? 1 : 0], [&]() {
+    const void* fn = dtype == CE_BF16 ? gemm_fn<1u>(a_mn, b_mn, out) : gemm_fn<0u>(a_mn, b_mn, out);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kTcSmem));
-    });
-    if (e != cudaSuccess) return record_cuda_failure(e, "cudaFuncSetAttribute(tensor-core GEMM)");
+    if (e != cudaSuccess) return record_cuda_failure(e, "tensor-core GEMM attributes");
     const char* tenv = std::getenv("GBCE_WAIT_TIMEOUT_MS");
     const uint64_t tms = (tenv && *tenv) ? static_cast<uint64_t>(std::atoll(tenv)) : 2000ull;
     e = cudaMemsetAsync(abort, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return record_cuda_failure(e, "cudaMemsetAsync(abort word)");
-    TcArgs a{C, bias, M, N, K, tms * 1000000ull, status, abort};
-    const dim3 grid(static_cast<unsigned>((M + kBM - 1) / kBM),
-                    static_cast<unsigned>((N + kBN - 1) / kBN));
+    const int64_t tm = (M + kBM - 1) / kBM, tn = (N + kBN - 1) / kBN;
+    TcArgs a{C, out == kOutF32 ? bias : nullptr, M, N, K, tm, tm * tn, tms * 1000000ull, status,
+             abort};
+    // persistent: one CTA an SM at most
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tm * tn, std::max(sms, 1)));
     void* args[] = {&ma, &mb, &a};
-    e = cudaLaunchKernel(fn, grid, dim3(kTcThreads), args, kTcSmem, st);
+    e = cudaLaunchKernel(fn, dim3(grid), dim3(kTcThreads), args, kTcSmem, st);
     if (e != cudaSuccess) return record_cuda_failure(e, "tensor-core GEMM launch");
     return CE_OK;
+}
+
+// C = A @ B^T (+ bias), both K-major, fp32 C: the logits GEMM.
+ce_status tc_gemm_abt_launch(const void* A, const void* B, int dtype, int64_t M, int64_t N,
+                             int64_t K, float* C, const float* bias, unsigned* status,
+                             unsigned* abort, cudaStream_t st) {
+    return tc_gemm_launch(A, false, B, false, dtype, M, N, K, C, kOutF32, bias, status, abort, st);
 }
 
 }  // namespace gbce
@@ -390,4 +546,22 @@ extern "C" ce_status ce_gemm_abt(const void* A, const void* B, int dtype, int64_
     // launch's abort flag
     return tc_gemm_abt_launch(A, B, dtype, M, N, K, C, bias, status, status + 1,
                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" ce_status ce_gemm(const void* A, int a_mn, const void* B, int b_mn, int dtype,
+                             int64_t M, int64_t N, int64_t K, void* C, int c_mode,
+                             const float* bias, ce_stream_t stream) {
+    if (dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K <= 0) return CE_ERR_INVALID_ARG;
+    if (c_mode != kOutF32 && c_mode != kOutF32Add && c_mode != kOut16) return CE_ERR_INVALID_ARG;
+    if (bias && c_mode != kOutF32) return CE_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return CE_OK;
+    if (!A || !B || !C) return CE_ERR_INVALID_ARG;
+    if (!tc_operand_ok(A, dtype, a_mn ? M : K) || !tc_operand_ok(B, dtype, b_mn ? N : K))
+        return CE_ERR_UNSUPPORTED;
+    unsigned* status = nullptr;
+    ce_status rc = library_status_word(reinterpret_cast<cudaStream_t>(stream), &status);
+    if (rc != CE_OK) return rc;
+    return tc_gemm_launch(A, a_mn != 0, B, b_mn != 0, dtype, M, N, K, C, c_mode, bias, status,
+                          status + 1, reinterpret_cast<cudaStream_t>(stream));
 }

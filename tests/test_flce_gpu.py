@@ -242,8 +242,8 @@ def test_flce_rejects_small_workspace():
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("reduction", ["mean", "none"])
-def test_flce_with_tensor_core_logits(monkeypatch, dtype, reduction):
-    # the logits GEMM on this library's tcgen05 kernel (bias in its epilogue)
-    monkeypatch.setenv("GBCE_FLCE_GEMM", "tcgen05")
+def test_flce_with_cublas_gemms(monkeypatch, dtype, reduction):
+    # the three GEMMs on cuBLAS (the path fp32 and unaligned inputs take)
+    monkeypatch.setenv("GBCE_FLCE_GEMM", "cublas")
     h, w, t, b, cw = make_case(21, 300, 136, 5000, dtype, with_bias=True, class_weight=True)
     check(h, w, t, b, cw, dtype, reduction, 64, OPTS["smooth_z"])
