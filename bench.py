@@ -503,7 +503,7 @@ def measured_tensor_peak():
         return 1700.0, "fallback"
 
 
-def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5):
+def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5, chunk_rows=0):
     """Fused linear cross-entropy (ce_flce) forward + gradients on
     rows = 4096 (B=8, T=512), H = 4096, V = 128256 bf16, mean, its GEMMs on
     this library's tcgen05 kernel (and, beside it, on cuBLAS): time per step
@@ -521,7 +521,7 @@ def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5):
     loss = torch.empty(1, dtype=torch.float32, device=device)
     gh = torch.empty_like(hidden)
     gw = torch.empty(V, H, dtype=torch.float32, device=device)
-    nbytes = _lib.ce_flce_workspace_bytes(_lib.CE_BF16, rows, V, 0)
+    nbytes = _lib.ce_flce_workspace_bytes(_lib.CE_BF16, rows, V, chunk_rows)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
     st = torch.cuda.current_stream(device).cuda_stream
 
@@ -529,7 +529,7 @@ def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5):
         rc = _lib.ce_flce(hidden.data_ptr(), lm_w.data_ptr(), None, _lib.CE_BF16, rows, H, V,
                           target.data_ptr(), None, -100, 0.0, 0.0, 0.0, _lib.CE_RED_MEAN,
                           _lib.CE_FLAG_GRAD, loss.data_ptr(), None, None, None, gh.data_ptr(),
-                          gw.data_ptr(), None, 0, ws.data_ptr(), nbytes, st)
+                          gw.data_ptr(), None, chunk_rows, ws.data_ptr(), nbytes, st)
         if rc != 0:
             raise RuntimeError(f"ce_flce: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
 
@@ -562,7 +562,7 @@ def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5):
            "ms_per_step": round(t * 1e3, 3), "TFLOP/s": round(flops / t / 1e12, 1),
            "frac": round(flops / t / 1e12 / peak_t, 4), "peak_TFLOP/s": peak_t,
            "peak_kind": kind + " (bf16, sustained)",
-           "chunk_rows": max(1, (1 << 29) // (V * 4)),
+           "chunk_rows": chunk_rows or max(1, (1 << 29) // (V * 4)),
            "gemms": "this library's tcgen05 GEMM (ce_gemm: bf16 in, fp32 accumulation in "
                     "tensor memory) for the logits, grad_hidden and grad_weight",
            "cublas_gemms": {"ms_per_step": round(t_blas * 1e3, 3),

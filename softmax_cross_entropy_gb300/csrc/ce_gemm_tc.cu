@@ -30,6 +30,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <string>
 #include <type_traits>
@@ -53,7 +54,11 @@ constexpr uint32_t kBBytes = kBN * kBK * 2;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kMnBox = 64 * kBK * 2;  // one 64 (MN) x 64 (K) box of an MN-major tile
 constexpr uint32_t kTmemCols = 2 * kBN;    // two accumulators
-constexpr size_t kTcSmem = static_cast<size_t>(kStages) * kStageBytes + 1024;
+// epilogue staging for TMA stores: per epilogue warp two 32-row x 128-byte
+// boxes (4 KB each, 128-byte swizzle)
+constexpr uint32_t kStageOut = 4096;
+constexpr uint32_t kOutBytes = 4 * 2 * kStageOut;
+constexpr size_t kTcSmem = static_cast<size_t>(kStages) * kStageBytes + kOutBytes + 1024;
 
 // What the epilogue does with the accumulator.
 enum : int { kOutF32 = 0, kOutF32Add = 1, kOut16 = 2 };
@@ -62,7 +67,8 @@ struct TcArgs {
     void* C;            // [M, N] row-major: fp32, or the operand type for kOut16
     const float* bias;  // [N] or nullptr (kOutF32 only)
     int64_t M, N, K;
-    int64_t tiles_m, tiles;
+    int64_t tiles_m, tiles_n, tiles;
+    int m_first;  // tile t runs along M first (1) or along N first (0)
     uint64_t timeout_ns;
     unsigned* status;  // sticky error word of the scratch (ce_device_status)
     unsigned* abort;   // cleared before the launch; set when a CTA gives up
@@ -114,6 +120,37 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, uint64_t 
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 1023u) == 0 && global_timer_ns() - t0 > timeout_ns) return false;
     }
+}
+
+// TMA store and reduce-add of a 2-D box from this CTA's shared memory, in
+// a bulk group (commit, then wait for the reads before reusing the buffer)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x,
+                                                  int y) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// at most one bulk group still reading shared memory
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// this thread's shared-memory writes visible to the TMA (async proxy)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -218,11 +255,53 @@ __device__ __forceinline__ void tc_store32(const TcArgs& a, int64_t row, int64_t
     }
 }
 
+// Tile t's row and column of tiles.
+__device__ __forceinline__ int64_t tile_m(const TcArgs& a, int64_t t) {
+    return a.m_first ? t % a.tiles_m : t / a.tiles_n;
+}
+__device__ __forceinline__ int64_t tile_n(const TcArgs& a, int64_t t) {
+    return a.m_first ? t / a.tiles_m : t % a.tiles_n;
+}
+
+// Writes this thread's row of 32 fp32 columns (h = 0), or one half of 64
+// 16-bit columns (h = 0, 1), into a 32-row x 128-byte staging box laid out
+// as the TMA's 128-byte swizzle wants it: 16-byte chunk j of row r at
+// chunk position j ^ (r mod 8). Conflict-free: the 8 threads of a quarter
+// warp cover all 32 banks.
+template <int OUT, uint32_t AB>
+__device__ __forceinline__ void tc_stage32(uint32_t buf, int r, int h, const float (&v)[32]) {
+    const uint32_t row = buf + static_cast<uint32_t>(r) * 128u;
+    if constexpr (OUT == kOut16) {
+        using T = typename std::conditional<AB == 1u, __nv_bfloat16, __half>::type;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float f[8] = {v[8 * j], v[8 * j + 1], v[8 * j + 2], v[8 * j + 3],
+                                v[8 * j + 4], v[8 * j + 5], v[8 * j + 6], v[8 * j + 7]};
+            const uint4 p = Vec<T>::pack(f);
+            const uint32_t at = row + (static_cast<uint32_t>((4 * h + j) ^ (r & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(at), "r"(p.x), "r"(p.y),
+                         "r"(p.z), "r"(p.w)
+                         : "memory");
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t at = row + (static_cast<uint32_t>(j ^ (r & 7)) << 4);
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(at), "f"(v[4 * j]),
+                         "f"(v[4 * j + 1]), "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                         : "memory");
+        }
+    }
+}
+
 // A_MN / B_MN: the operand is stored MN-major (A as [K, M], B as [K, N]).
-template <uint32_t AB, bool A_MN, bool B_MN, int OUT>
+// TMAO: C leaves through shared memory with TMA stores (reduce-adds for
+// kOutF32Add) of 32-row x 128-byte boxes; else with plain stores (a C
+// whose base or row pitch is not a multiple of 16 bytes).
+template <uint32_t AB, bool A_MN, bool B_MN, int OUT, bool TMAO>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-        const __grid_constant__ TcArgs a) {
+        const __grid_constant__ CUtensorMap mapC, const __grid_constant__ TcArgs a) {
     extern __shared__ unsigned char tc_smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -275,8 +354,8 @@ tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtens
             int it = 0;  // K blocks issued so far (ring position)
             bool fail = false;
             for (int64_t t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
-                const int m0 = static_cast<int>((t % a.tiles_m) * kBM);
-                const int n0 = static_cast<int>((t / a.tiles_m) * kBN);
+                const int m0 = static_cast<int>(tile_m(a, t) * kBM);
+                const int n0 = static_cast<int>(tile_n(a, t) * kBN);
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
@@ -354,6 +433,10 @@ tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtens
     } else {
         // ---- epilogue: warp w reads accumulator lanes 32 (w mod 4) ...
         const int q = warp & 3;
+        // this warp's two staging boxes, used in turn
+        const uint32_t stg = smem0 + static_cast<uint32_t>(kStages) * kStageBytes +
+                             static_cast<uint32_t>(q) * 2u * kStageOut;
+        uint32_t nst = 0;  // boxes this warp has handed to the TMA
         int i = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
             const int b = i & 1;
@@ -365,22 +448,63 @@ tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtens
                 break;
             }
             tc_fence_after();
-            const int64_t m0 = (t % a.tiles_m) * kBM;
-            const int64_t n0 = (t / a.tiles_m) * kBN;
+            const int64_t m0 = tile_m(a, t) * kBM;
+            const int64_t n0 = tile_n(a, t) * kBN;
             const int64_t row = m0 + q * 32 + lane;
             const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                   static_cast<uint32_t>(b * kBN);
+            if constexpr (TMAO) {
+                constexpr int kBoxCols = OUT == kOut16 ? 64 : 32;
+                const bool rows_in = m0 + q * 32 < a.M;  // the same for the whole warp
 #pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                const int64_t n = n0 + c * 32;
-                if (n >= a.N) break;  // the same for every thread of the warp
-                float v[32];
-                tc_ld32(trow + static_cast<uint32_t>(c * 32), v);
-                if (row < a.M) tc_store32<OUT, AB>(a, row, n, v);
+                for (int c = 0; c < kBN / kBoxCols; ++c) {
+                    const int64_t n = n0 + c * kBoxCols;
+                    if (n >= a.N) break;  // the same for every thread of the warp
+                    const uint32_t buf = stg + (nst & 1u) * kStageOut;
+                    // the box written two turns ago has been read out of this buffer
+                    if (lane == 0) bulk_wait_read_1();
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < kBoxCols / 32; ++h) {
+                        float v[32];
+                        tc_ld32(trow + static_cast<uint32_t>(c * kBoxCols + h * 32), v);
+                        if (OUT == kOutF32 && a.bias) {
+                            const int64_t nb = n + h * 32;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (nb + j < a.N) v[j] += __ldg(a.bias + nb + j);
+                        }
+                        tc_stage32<OUT, AB>(buf, lane, h, v);
+                    }
+                    fence_proxy_async_smem();  // the writes, seen by the TMA
+                    __syncwarp();
+                    if (lane == 0 && rows_in) {
+                        // rows past M and columns past N are clipped by the TMA
+                        if (OUT == kOutF32Add)
+                            tma_reduce_add_2d(&mapC, buf, static_cast<int>(n),
+                                              static_cast<int>(m0 + q * 32));
+                        else
+                            tma_store_2d(&mapC, buf, static_cast<int>(n),
+                                         static_cast<int>(m0 + q * 32));
+                    }
+                    if (lane == 0) bulk_commit();
+                    ++nst;
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    const int64_t n = n0 + c * 32;
+                    if (n >= a.N) break;  // the same for every thread of the warp
+                    float v[32];
+                    tc_ld32(trow + static_cast<uint32_t>(c * 32), v);
+                    if (row < a.M) tc_store32<OUT, AB>(a, row, n, v);
+                }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&acc_empty[b]));
         }
+        // every box written out before the shared memory goes
+        if (TMAO && lane == 0) bulk_wait_all();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -455,17 +579,47 @@ ce_status make_map(CUtensorMap* map, const void* p, int dtype, int64_t outer, in
     return CE_OK;
 }
 
-template <uint32_t AB>
-const void* gemm_fn(bool a_mn, bool b_mn, int out) {
-#define GBCE_TC(AM, BM)                                                   \
-    (out == kOutF32      ? (const void*)&tc_gemm<AB, AM, BM, kOutF32>    \
-     : out == kOutF32Add ? (const void*)&tc_gemm<AB, AM, BM, kOutF32Add> \
-                         : (const void*)&tc_gemm<AB, AM, BM, kOut16>)
+// 2-D map of C [M, N] row-major (fp32, or 16-bit for kOut16) for the
+// epilogue's TMA stores: boxes of 32 rows x 128 bytes, 128-byte swizzle.
+ce_status make_map_c(CUtensorMap* map, void* C, int dtype, int out, int64_t M, int64_t N) {
+    EncodeTiled enc = nullptr;
+    ce_status rc = encoder(&enc);
+    if (rc != CE_OK) return rc;
+    const bool h = out == kOut16;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * (h ? 2 : 4)};
+    const cuuint32_t box[2] = {h ? 64u : 32u, 32u};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType t = !h ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : dtype == CE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = enc(map, t, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        record_message("cuTensorMapEncodeTiled (C) failed (" + std::to_string(static_cast<int>(r)) +
+                       ")");
+        return CE_ERR_UNSUPPORTED;
+    }
+    return CE_OK;
+}
+
+template <uint32_t AB, bool TMAO>
+const void* gemm_fn_t(bool a_mn, bool b_mn, int out) {
+#define GBCE_TC(AM, BM)                                                         \
+    (out == kOutF32      ? (const void*)&tc_gemm<AB, AM, BM, kOutF32, TMAO>    \
+     : out == kOutF32Add ? (const void*)&tc_gemm<AB, AM, BM, kOutF32Add, TMAO> \
+                         : (const void*)&tc_gemm<AB, AM, BM, kOut16, TMAO>)
     if (!a_mn && !b_mn) return GBCE_TC(false, false);
     if (!a_mn && b_mn) return GBCE_TC(false, true);
     if (a_mn && !b_mn) return GBCE_TC(true, false);
     return GBCE_TC(true, true);
 #undef GBCE_TC
+}
+
+template <uint32_t AB>
+const void* gemm_fn(bool a_mn, bool b_mn, int out, bool tmao) {
+    return tmao ? gemm_fn_t<AB, true>(a_mn, b_mn, out) : gemm_fn_t<AB, false>(a_mn, b_mn, out);
 }
 
 }  // namespace
@@ -497,7 +651,17 @@ ce_status tc_gemm_launch(const void* A, bool a_mn, const void* B, bool b_mn, int
     if (rc != CE_OK) return rc;
     rc = b_mn ? make_map(&mb, B, dtype, K, N, 64) : make_map(&mb, B, dtype, N, K, kBN);
     if (rc != CE_OK) return rc;
-    const void* fn = dtype == CE_BF16 ? gemm_fn<1u>(a_mn, b_mn, out) : gemm_fn<0u>(a_mn, b_mn, out);
+    // C through TMA stores when its base and row pitch are multiples of 16 bytes
+    const int64_t cpitch = N * (out == kOut16 ? 2 : 4);
+    const bool tmao = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && cpitch % 16 == 0;
+    CUtensorMap mc;
+    std::memset(&mc, 0, sizeof(mc));
+    if (tmao) {
+        rc = make_map_c(&mc, C, dtype, out, M, N);
+        if (rc != CE_OK) return rc;
+    }
+    const void* fn = dtype == CE_BF16 ? gemm_fn<1u>(a_mn, b_mn, out, tmao)
+                                      : gemm_fn<0u>(a_mn, b_mn, out, tmao);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -510,11 +674,16 @@ ce_status tc_gemm_launch(const void* A, bool a_mn, const void* B, bool b_mn, int
     e = cudaMemsetAsync(abort, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return record_cuda_failure(e, "cudaMemsetAsync(abort word)");
     const int64_t tm = (M + kBM - 1) / kBM, tn = (N + kBN - 1) / kBN;
-    TcArgs a{C, out == kOutF32 ? bias : nullptr, M, N, K, tm, tm * tn, tms * 1000000ull, status,
-             abort};
+    // consecutive tiles (the CTAs that run together) share a tile of the
+    // larger operand, which is then read from DRAM about once: along M first
+    // when B is the larger (its tile serves every row of tiles), along N
+    // first when A is
+    const int m_first = N >= M ? 1 : 0;
+    TcArgs a{C,  out == kOutF32 ? bias : nullptr, M, N, K, tm, tn, tm * tn, m_first,
+             tms * 1000000ull, status, abort};
     // persistent: one CTA an SM at most
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tm * tn, std::max(sms, 1)));
-    void* args[] = {&ma, &mb, &a};
+    void* args[] = {&ma, &mb, &mc, &a};
     e = cudaLaunchKernel(fn, dim3(grid), dim3(kTcThreads), args, kTcSmem, st);
     if (e != cudaSuccess) return record_cuda_failure(e, "tensor-core GEMM launch");
     return CE_OK;
