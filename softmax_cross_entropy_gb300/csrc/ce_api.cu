@@ -130,6 +130,31 @@ ce_status scratch_for(int dev, cudaStream_t st, Scratch** out) {
     return CE_OK;
 }
 
+// The split N-D forward's workspace for (device, stream): grown to `bytes`
+// when a call needs more (the old buffer is freed first, which waits for
+// the device), kept for later calls on the stream.
+std::map<std::pair<int, uintptr_t>, std::pair<void*, size_t>> g_nd_work;
+
+ce_status nd_work_for(int dev, cudaStream_t st, size_t bytes, void** out) {
+    const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(st));
+    auto it = g_nd_work.find(key);
+    if (it != g_nd_work.end() && it->second.second >= bytes) {
+        *out = it->second.first;
+        return CE_OK;
+    }
+    if (it != g_nd_work.end()) {
+        cudaError_t e = cudaFree(it->second.first);
+        g_nd_work.erase(it);
+        if (e != cudaSuccess) return cuda_failure(e, "cudaFree(N-D workspace)");
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaMalloc(N-D workspace)");
+    g_nd_work[key] = std::make_pair(p, bytes);
+    *out = p;
+    return CE_OK;
+}
+
 const void* staged_fn(int dtype, int cfg, bool softcap, bool wsmooth) {
     if (dtype == CE_F16) return nullptr;  // fp16 takes the streaming or the general kernel
     if (dtype == CE_BF16) {
@@ -458,11 +483,11 @@ ce_status make_plan(int devid, int dtype, int64_t V, bool softcap, bool sc_small
     // as fit in 8 warps. Its class weights are read as 16-byte vectors.
     const int64_t reg_max = env_int("GBCE_REG_MAX_BYTES", 65536);
     const int64_t vrow = V * bytes / 16;
-    // 8 vectors a thread while a row fits 8 warps (more rows in flight an
-    // SM; measured 2-4% faster at 8-32 KB rows), else 16
+    // 8 vectors a thread for rows of at most 8 KB, else 16: at 16 and 32 KB
+    // bf16 rows 16 vectors a thread (a warp for each 8 KB of the row)
+    // measured 3-6% faster than 8; at 8 KB the two are even
     const int nvl_env = env_int("GBCE_REG_NVL", 0);
-    const int nvl = (nvl_env == 8 || nvl_env == 16) ? nvl_env
-                    : (vrow <= 32 * 8 * kRegMaxWarps ? 8 : 16);
+    const int nvl = (nvl_env == 8 || nvl_env == 16) ? nvl_env : (vrow <= 512 ? 8 : 16);
     const int64_t wpr = (vrow + 32 * nvl - 1) / (32 * nvl);
     // Class-weighted smoothing: the weights in shared memory (one CTA of 16
     // warps an SM, 8 vectors a thread, teams of up to 16 warps) when they
@@ -1282,6 +1307,66 @@ ce_status nd_plan(int dev, const DeviceInfo& info, int dtype, int64_t C, bool ve
     return CE_OK;
 }
 
+// Occupancy (CTAs an SM) of a split N-D kernel, computed once.
+int nd_split_occ(const void* fn) {
+    static std::map<const void*, int> occ;
+    auto it = occ.find(fn);
+    if (it != occ.end()) return it->second;
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, kNdSplitThreads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        o = 1;
+    }
+    o = std::max(o, 1);
+    occ[fn] = o;
+    return o;
+}
+
+// The split N-D forward (ce_fwd_nd_split.cuh): class chunks of cc classes
+// so that the (tile, chunk) items number about GBCE_ND_ITEMS (default 4) per
+// SM, with at least GBCE_ND_MIN_CHUNK (default 64) classes a chunk; the
+// records, coefficients and counted targets in the stream's N-D workspace.
+ce_status nd_split_launch(int dev, const DeviceInfo& info, const FwdArgs& f, int dtype,
+                          bool vec_ok, bool softcap, bool argmax, cudaStream_t st) {
+    const int64_t b = dtype == CE_F32 ? 4 : 2;
+    const int64_t VP = vec_ok ? 16 / b : 1;
+    const int64_t P = 32 * VP;
+    const int64_t C = f.V;
+    NdSplitArgs s = {};
+    s.f = f;
+    s.tiles = (f.rows + P - 1) / P;
+    const int64_t want = std::max(1, env_int("GBCE_ND_ITEMS", 4)) * static_cast<int64_t>(info.sm_count);
+    const int64_t max_ch = std::max<int64_t>(1, C / std::max(8, env_int("GBCE_ND_MIN_CHUNK", 64)));
+    const int64_t nch0 = std::min<int64_t>(max_ch, std::max<int64_t>(1, (want + s.tiles - 1) / s.tiles));
+    const int64_t cc = (C + nch0 - 1) / nch0;
+    s.cc = static_cast<int>(cc);
+    s.nch = static_cast<int>((C + cc - 1) / cc);
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    const size_t rec_b = up(static_cast<size_t>(s.tiles * P) * s.nch * sizeof(NdRec));
+    const size_t coef_b = up(static_cast<size_t>(f.rows) * sizeof(NdCoef));
+    const size_t tpos_b = up(static_cast<size_t>(f.rows) * sizeof(int));
+    void* ws = nullptr;
+    ce_status rc = nd_work_for(dev, st, rec_b + coef_b + tpos_b, &ws);
+    if (rc != CE_OK) return rc;
+    s.rec = static_cast<NdRec*>(ws);
+    s.coef = reinterpret_cast<NdCoef*>(static_cast<char*>(ws) + rec_b);
+    s.tpos = reinterpret_cast<int*>(static_cast<char*>(ws) + rec_b + coef_b);
+    const NdSplitFns fns = nd_split_fns(dtype, vec_ok, softcap, argmax, f.eps > 0.f);
+    if (!fns.stats || !fns.merge || !fns.grad) return CE_ERR_INVALID_ARG;
+    const int64_t items = s.tiles * s.nch;
+    const int64_t g1 = std::min<int64_t>(items, nd_split_occ(fns.stats) * static_cast<int64_t>(info.sm_count));
+    rc = launch(fns.stats, static_cast<int>(g1), kNdSplitThreads, 0, 1, st, &s);
+    if (rc != CE_OK) return rc;
+    // one warp a position; the merge's CTAs take the partial-sum slots
+    const int64_t g2 = std::max<int64_t>(
+        1, std::min<int64_t>((f.rows + 7) / 8, std::min<int64_t>(8 * static_cast<int64_t>(info.sm_count),
+                                                                 kMaxUnits)));
+    rc = launch(fns.merge, static_cast<int>(g2), kNdSplitThreads, 0, 1, st, &s);
+    if (rc != CE_OK || !f.grad) return rc;
+    const int64_t g3 = std::min<int64_t>(items, nd_split_occ(fns.grad) * static_cast<int64_t>(info.sm_count));
+    return launch(fns.grad, static_cast<int>(g3), kNdSplitThreads, 0, 1, st, &s);
+}
+
 }  // namespace
 }  // namespace gbce
 
@@ -1360,6 +1445,14 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     a.nd_staged = p.staged ? 1 : 0;
     const int64_t P = p.vec ? 32 * (16 / b) : 32;
     const int64_t tiles = (rows + P - 1) / P;
+    // The single-kernel form reads a staged tile once, but runs one CTA a
+    // tile of every class; when its tile does not fit on chip (it would read
+    // the logits three times) or there are too few tiles for the SMs, the
+    // split form takes the call (GBCE_ND_SPLIT=0 / 1 forces one or the other)
+    const int split_env = env_int("GBCE_ND_SPLIT", -1);
+    const bool split = split_env == 1 || (split_env != 0 && env_int("GBCE_ND_MODE", 0) == 0 &&
+                                          (!p.staged || tiles < 2 * info.sm_count));
+    if (split) return nd_split_launch(dev, info, a, dtype, vec_ok, sc, argmax, st);
     const int64_t grid = std::min<int64_t>(tiles, std::min<int64_t>(p.max_ctas, kMaxUnits));
     return launch(p.fn, static_cast<int>(grid), kNdThreads, p.smem, 1, st, &a);
 }

@@ -1,11 +1,16 @@
 // N-D forward kernels (class dimension 1) for bf16 logits; one translation
 // unit per logit type so the variants compile in parallel.
 #include "ce_fwd_nd.cuh"
+#include "ce_fwd_nd_split.cuh"
 
 namespace gbce {
 
 const void* nd_kernel_bf16(bool vec, bool softcap, bool argmax) {
     return nd_kernel_of<__nv_bfloat16>(vec, softcap, argmax);
+}
+
+NdSplitFns nd_split_bf16(bool vec, bool softcap, bool argmax, bool smooth) {
+    return nd_split_of<__nv_bfloat16>(vec, softcap, argmax, smooth);
 }
 
 }  // namespace gbce

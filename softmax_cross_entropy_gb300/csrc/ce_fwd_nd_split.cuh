@@ -1,0 +1,420 @@
+// Forward for N-D logits [N, C, d1..dk] (class dimension 1) when one tile
+// of positions x all C classes does not fit on chip or there are too few
+// tiles to fill the GPU: the classes of each tile are split into chunks
+// that separate CTAs take (the tt-mlir pull request #9324 review comment:
+// the reductions run over every non-class dimension; row definitions, loss
+// terms and gradient as in the 2-D kernels: Liger-Kernel cross-entropy
+// profile, §Forward Pass, §Backward Pass, §Key Patterns).
+//
+// A position is one row of the 2-D definition; its C logits sit `inner`
+// elements apart. A tile is 32 * VP consecutive positions (VP = the
+// positions of one 16-byte vector, or 1), a work item one (tile, chunk of
+// classes). Three launches:
+//   nd_stats  every item, once over its logits: online statistics per
+//             position over the chunk's classes (running maximum m with
+//             S = sum exp(z - m) and SZ = sum w (z - m) rescaled when m
+//             grows, W = sum w, first raw argmax), merged over the CTA's
+//             warps in warp order, one record per (position, chunk);
+//   nd_merge  one warp per position merges its chunks' records (fixed lane
+//             split and butterfly: the same bits every call), writes the
+//             per-position outputs and the gradient's coefficients, and
+//             adds the reduced scalars (last-CTA epilogue);
+//   nd_grad   every item again, in reverse order (the last items' logits
+//             are the likeliest to still be in L2): the gradient in place.
+// Each element is read twice and written once.
+#pragma once
+
+#include <climits>
+#include <type_traits>
+
+#include "ce_fwd_nd.cuh"
+
+namespace gbce {
+
+constexpr int kNdSplitWarps = kNdSplitThreads / 32;
+
+// exp2 argument of z - m (m the running shift, mL = m log2 e): one FFMA
+// for 16-bit logits, the difference first for fp32 (as the 2-D kernels).
+template <typename T>
+__device__ __forceinline__ float nd_arg(float z, float m, float mL) {
+    if constexpr (sizeof(T) == 2)
+        return fmaf(z, kLog2e, -mL);
+    else
+        return (z - m) * kLog2e;
+}
+
+// Statistics of one chunk of classes for the tile's positions: each warp
+// takes every NW-th class of the chunk, U at a time (loads issued first);
+// the running maximum is checked once per U classes and position.
+// SMOOTH: the smoothing sums SZ and W are formed (label smoothing on).
+template <typename T, int VP, bool SOFTCAP, bool ARGMAX, bool SMOOTH>
+__global__ void __launch_bounds__(kNdSplitThreads, 2)
+ce_nd_stats(const __grid_constant__ NdSplitArgs s) {
+    using IO = NdIO<T, VP>;
+    using Raw = typename IO::Raw;
+    constexpr int NW = kNdSplitWarps;
+    constexpr int P = 32 * VP;
+    constexpr int U = VP > 1 ? 4 : 8;  // classes a step (loads in flight a thread)
+    __shared__ NdRec red[NW][P];
+    const FwdArgs& a = s.f;
+    const int tid = threadIdx.x, lane = tid & 31, wy = tid >> 5;
+    const int C = static_cast<int>(a.V);
+    const int64_t inner = a.inner;
+    const bool wsmooth = SMOOTH && a.weight != nullptr;
+    const int64_t items = s.tiles * s.nch;
+#pragma unroll 1
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t tile = it / s.nch;
+        const int ch = static_cast<int>(it - tile * s.nch);
+        const int c0 = ch * s.cc, c1 = min(C, c0 + s.cc);
+        const int64_t rl = tile * P + static_cast<int64_t>(lane) * VP;
+        const bool lane_ok = rl < a.rows;  // VP divides inner, hence rows
+        int64_t lb = 0;
+        if (lane_ok) {
+            const int64_t n = rl / inner;
+            lb = n * C * inner + (rl - n * inner);
+        }
+        float m[VP], S[VP], SZ[VP], xm[VP];
+        int xi[VP];
+#pragma unroll
+        for (int v = 0; v < VP; ++v) {
+            m[v] = -INFINITY;
+            S[v] = 0.f;
+            SZ[v] = 0.f;
+            xm[v] = -INFINITY;
+            xi[v] = INT_MAX;
+        }
+        float Wn = 0.f;
+        // n classes from c (step NW) whose raw values are in r
+        auto step = [&](int c, int n, const Raw (&r)[U]) {
+            float z[U][VP];
+            float wc[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (u < n) {
+                    IO::unpack(r[u], z[u]);
+                    wc[u] = wsmooth ? __ldg(a.weight + c + u * NW) : 1.f;
+                }
+            }
+            if (ARGMAX) {
+                // classes in increasing order: a later equal value never wins
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (u < n) {
+#pragma unroll
+                        for (int v = 0; v < VP; ++v)
+                            if (z[u][v] > xm[v]) {
+                                xm[v] = z[u][v];
+                                xi[v] = c + u * NW;
+                            }
+                    }
+            }
+            if (SOFTCAP) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (u < n) {
+#pragma unroll
+                        for (int v = 0; v < VP; ++v)
+                            z[u][v] = a.softcap * tanh_from_scaled(z[u][v] * a.sc_k2);
+                    }
+            }
+#pragma unroll
+            for (int v = 0; v < VP; ++v) {
+                float bm = z[0][v];
+#pragma unroll
+                for (int u = 1; u < U; ++u)
+                    if (u < n) bm = fmaxf(bm, z[u][v]);
+                if (bm > m[v]) {
+                    // the running maximum grows: rescale what was summed
+                    if (m[v] != -INFINITY) {
+                        const float d = m[v] - bm;
+                        S[v] *= ex2(d * kLog2e);
+                        if (SMOOTH) SZ[v] = fmaf(Wn, d, SZ[v]);
+                    }
+                    m[v] = bm;
+                }
+                const float ms = m[v] == -INFINITY ? 0.f : m[v];
+                const float mL = ms * kLog2e;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (u < n) {
+                        S[v] += ex2(nd_arg<T>(z[u][v], ms, mL));
+                        if (SMOOTH) SZ[v] = fmaf(wc[u], z[u][v] - ms, SZ[v]);
+                    }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (u < n) Wn += wc[u];
+        };
+        auto load = [&](int c) -> Raw {
+            return lane_ok ? IO::load(a.x, lb + static_cast<int64_t>(c) * inner) : Raw{};
+        };
+        int c = c0 + wy;
+#pragma unroll 1
+        for (; c + (U - 1) * NW < c1; c += U * NW) {
+            Raw r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) r[u] = load(c + u * NW);
+            step(c, U, r);
+        }
+        if (c < c1) {  // the chunk's last classes of this warp: fewer than U
+            Raw r[U];
+            const int n = (c1 - c + NW - 1) / NW;
+#pragma unroll
+            for (int u = 0; u < U; ++u) r[u] = u < n ? load(c + u * NW) : Raw{};
+            step(c, n, r);
+        }
+#pragma unroll
+        for (int v = 0; v < VP; ++v)
+            red[wy][lane * VP + v] = NdRec{m[v], S[v], SZ[v], Wn, xm[v], xi[v]};
+        __syncthreads();
+        for (int p = tid; p < P; p += kNdSplitThreads) {
+            const NdRec& r0 = red[0][p];
+            RowStats acc{r0.m, r0.S, r0.SZ, r0.Wn, r0.xmax, r0.idx};
+#pragma unroll
+            for (int w = 1; w < NW; ++w) {
+                const NdRec& r = red[w][p];
+                stats_merge(acc, RowStats{r.m, r.S, r.SZ, r.Wn, r.xmax, r.idx});
+            }
+            s.rec[(tile * P + p) * s.nch + ch] =
+                NdRec{acc.m, acc.S, acc.SZ, acc.Wn, acc.xmax, acc.idx};
+        }
+        __syncthreads();  // red is written again by the next item
+    }
+}
+
+// One warp a position: lane l merges chunks l, l + 32, ... in order, then a
+// fixed butterfly combines the lanes (stats_merge does not depend on the
+// order of its operands, so every lane ends with the same bits).
+template <typename T, bool SOFTCAP>
+__global__ void __launch_bounds__(kNdSplitThreads)
+ce_nd_merge(const __grid_constant__ NdSplitArgs s) {
+    const FwdArgs& a = s.f;
+    constexpr int NW = kNdSplitWarps;
+    __shared__ double red_d[2 * NW];
+    __shared__ long long red_n[NW];
+    __shared__ int s_flag;
+    const int tid = threadIdx.x, lane = tid & 31, wy = tid >> 5;
+    const int C = static_cast<int>(a.V);
+    const int64_t inner = a.inner;
+    const bool smooth = a.eps > 0.f;
+    const bool wsmooth = smooth && a.weight != nullptr;
+    float D = 0.f;
+    int n_valid = 0;
+    if (a.reduction != kRedNone) {
+        D = static_cast<float>(a.batch_counts[0]);
+        n_valid = static_cast<int>(a.batch_counts[1]);
+    }
+    float Wsum = static_cast<float>(C);
+    if (wsmooth) {
+        // W = sum of the class weights, the same order in every CTA
+        __shared__ float red_w[kNdSplitThreads / 32];
+        float w = 0.f;
+        for (int c = tid; c < C; c += kNdSplitThreads) w += __ldg(a.weight + c);
+        Wsum = block_sum_fixed<kNdSplitThreads>(w, red_w);
+        __syncthreads();
+    }
+    const float inv_C = 1.f / static_cast<float>(C);
+    const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;
+    const float Wf = wsmooth ? Wsum * inv_C : 1.f;
+    double accL = 0.0, accZ = 0.0;
+    long long accC = 0;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * NW;
+#pragma unroll 1
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * NW + wy; r < a.rows; r += nwarps) {
+        RowStats acc = empty_stats();
+        for (int c = lane; c < s.nch; c += 32) {
+            const NdRec q = s.rec[r * s.nch + c];
+            stats_merge(acc, RowStats{q.m, q.S, q.SZ, q.Wn, q.xmax, q.idx});
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const RowStats b = shfl_xor_stats(acc, o);
+            stats_merge(acc, b);
+        }
+        if (lane != 0) continue;
+        const int64_t t = load_target(a, r);
+        const bool counted = row_counts(a, t);
+        if (!counted && t != a.ignore_index) atomicOr(&a.scratch->status, kDevErrTarget);
+        NdCoef k{0.f, 0.f, 0.f, 0.f};
+        const float shift = acc.m == -INFINITY ? 0.f : acc.m;
+        k.shift = shift;
+        if (counted) {
+            const int64_t n = r / inner;
+            const float xt = Vec<T>::load1(a.x, n * C * inner + t * inner + (r - n * inner));
+            const float zt = SOFTCAP ? a.softcap * tanh_from_scaled(xt * a.sc_k2) : xt;
+            const float wt = a.weight ? __ldg(a.weight + t) : 1.f;
+            const float logS = logf(acc.S);
+            // the chunk records' SZ are relative to their own maxima, merged
+            // to the position's maximum; W of the smoothing term is the
+            // weights' sum (or C)
+            float zl;
+            const float l = row_loss(a, shift, logS, zt, wt, wsmooth ? Wsum : static_cast<float>(C),
+                                     acc.SZ, zl);
+            const bool correct = acc.idx == static_cast<int>(t);
+            if (a.reduction == kRedNone) {
+                a.loss[r] = l;
+                if (a.want_z) a.zloss[r] = zl;
+                if (a.want_acc) a.acc[r] = correct ? 1.f : 0.f;
+            } else {
+                accL += static_cast<double>(l);
+                accZ += static_cast<double>(zl);
+                accC += correct ? 1 : 0;
+            }
+            if (a.want_pred) a.pred[r] = acc.idx;
+            const float lse = shift + logS;
+            k.ac = scale * ((1.f - a.eps) * wt + a.eps * Wf + 2.f * a.lam * lse) / acc.S;
+            k.bc = -scale * a.eps * inv_C;
+            // the target's element: the one-hot term added
+            const float et = ex2((zt - shift) * kLog2e);
+            float gt = fmaf(k.ac, et, k.bc * (wsmooth ? wt : 1.f)) - scale * (1.f - a.eps) * wt;
+            if (SOFTCAP) {
+                const float th = tanh_from_scaled(xt * a.sc_k2);
+                gt *= fmaf(-th, th, 1.f);
+            }
+            k.gt = gt;
+        } else {
+            if (a.reduction == kRedNone) {
+                a.loss[r] = 0.f;
+                if (a.want_z) a.zloss[r] = 0.f;
+                if (a.want_acc) a.acc[r] = 0.f;
+            }
+            if (a.want_pred) a.pred[r] = -1;
+        }
+        s.coef[r] = k;
+        s.tpos[r] = counted ? static_cast<int>(t) : -1;
+    }
+    if (a.reduction != kRedNone) {
+        // lane 0 of each warp holds its positions' partials: warps in order
+        if (lane == 0) {
+            red_d[wy] = accL;
+            red_d[NW + wy] = accZ;
+            red_n[wy] = accC;
+        }
+        __syncthreads();
+        double L = 0.0, Z = 0.0;
+        long long Cn = 0;
+        if (tid == 0) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                L += red_d[w];
+                Z += red_d[NW + w];
+                Cn += red_n[w];
+            }
+        }
+        __syncthreads();  // red_d is the epilogue's scratch next
+        finish_scalars_cta(a, L, Z, Cn, D, n_valid, &s_flag, red_d, red_d + NW, red_n);
+    }
+}
+
+// The gradient of one chunk of classes for the tile's positions, classes
+// split over the warps as in ce_nd_stats; the target's element is then
+// overwritten with its whole gradient by the thread that wrote it.
+template <typename T, int VP, bool SOFTCAP>
+__global__ void __launch_bounds__(kNdSplitThreads)
+ce_nd_grad(const __grid_constant__ NdSplitArgs s) {
+    using IO = NdIO<T, VP>;
+    using Raw = typename IO::Raw;
+    constexpr int NW = kNdSplitWarps;
+    constexpr int P = 32 * VP;
+    constexpr int U = VP > 1 ? 8 : 16;  // loads in flight a thread
+    const FwdArgs& a = s.f;
+    const int tid = threadIdx.x, lane = tid & 31, wy = tid >> 5;
+    const int C = static_cast<int>(a.V);
+    const int64_t inner = a.inner;
+    const bool wsmooth = a.eps > 0.f && a.weight != nullptr;
+    const int64_t items = s.tiles * s.nch;
+#pragma unroll 1
+    for (int64_t i = blockIdx.x; i < items; i += gridDim.x) {
+        const int64_t it = items - 1 - i;
+        const int64_t tile = it / s.nch;
+        const int ch = static_cast<int>(it - tile * s.nch);
+        const int c0 = ch * s.cc, c1 = min(C, c0 + s.cc);
+        const int64_t rl = tile * P + static_cast<int64_t>(lane) * VP;
+        const bool lane_ok = rl < a.rows;
+        int64_t lb = 0;
+        float sh[VP], shL[VP], ac[VP], bc[VP], gt[VP];
+        int tv[VP];
+#pragma unroll
+        for (int v = 0; v < VP; ++v) {
+            sh[v] = shL[v] = ac[v] = bc[v] = gt[v] = 0.f;
+            tv[v] = -1;
+        }
+        if (lane_ok) {
+            const int64_t n = rl / inner;
+            lb = n * C * inner + (rl - n * inner);
+#pragma unroll
+            for (int v = 0; v < VP; ++v) {
+                const NdCoef k = s.coef[rl + v];
+                sh[v] = k.shift;
+                shL[v] = k.shift * kLog2e;
+                ac[v] = k.ac;
+                bc[v] = k.bc;
+                gt[v] = k.gt;
+                tv[v] = s.tpos[rl + v];
+            }
+        }
+        auto body = [&](int c, const Raw& r) {
+            float f[VP];
+            IO::unpack(r, f);
+            const float wc = wsmooth ? __ldg(a.weight + c) : 1.f;
+#pragma unroll
+            for (int v = 0; v < VP; ++v) {
+                float g;
+                if (SOFTCAP) {
+                    const float th = tanh_from_scaled(f[v] * a.sc_k2);
+                    const float z = th * a.softcap;
+                    g = fmaf(ac[v], ex2(nd_arg<T>(z, sh[v], shL[v])), bc[v] * wc) *
+                        fmaf(-th, th, 1.f);
+                } else {
+                    g = fmaf(ac[v], ex2(nd_arg<T>(f[v], sh[v], shL[v])), bc[v] * wc);
+                }
+                // positions that do not count get exact zeros
+                f[v] = tv[v] >= 0 ? g : 0.f;
+            }
+            if (lane_ok) IO::store(a.x, lb + static_cast<int64_t>(c) * inner, IO::pack(f));
+        };
+        nd_class_loop<U, Raw>(c0 + wy, NW, c1, [&](int c) -> Raw {
+            return lane_ok ? IO::load(a.x, lb + static_cast<int64_t>(c) * inner) : Raw{};
+        }, body);
+        if (lane_ok) {
+#pragma unroll
+            for (int v = 0; v < VP; ++v) {
+                const int t = tv[v];
+                if (t >= c0 && t < c1 && (t - c0) % NW == wy)
+                    Vec<T>::store1(a.x, lb + static_cast<int64_t>(t) * inner + v, gt[v]);
+            }
+        }
+    }
+}
+
+// Entry points of one logit type by (vector positions, softcap, argmax).
+template <typename T>
+NdSplitFns nd_split_of(bool vec, bool softcap, bool argmax, bool smooth) {
+    constexpr int VPV = Vec<T>::N;
+    NdSplitFns f{};
+#define GBCE_ND_SPLIT(VP, SC)                                                                 \
+    f.stats = argmax ? (smooth ? (const void*)&ce_nd_stats<T, VP, SC, true, true>              \
+                               : (const void*)&ce_nd_stats<T, VP, SC, true, false>)            \
+                     : (smooth ? (const void*)&ce_nd_stats<T, VP, SC, false, true>             \
+                               : (const void*)&ce_nd_stats<T, VP, SC, false, false>);          \
+    f.merge = (const void*)&ce_nd_merge<T, SC>;                                               \
+    f.grad = (const void*)&ce_nd_grad<T, VP, SC>;
+    if (vec) {
+        if (softcap) {
+            GBCE_ND_SPLIT(VPV, true)
+        } else {
+            GBCE_ND_SPLIT(VPV, false)
+        }
+    } else {
+        if (softcap) {
+            GBCE_ND_SPLIT(1, true)
+        } else {
+            GBCE_ND_SPLIT(1, false)
+        }
+    }
+#undef GBCE_ND_SPLIT
+    return f;
+}
+
+}  // namespace gbce

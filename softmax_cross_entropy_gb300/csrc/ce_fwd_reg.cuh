@@ -237,10 +237,15 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
                        : static_cast<int64_t>(blockIdx.x) * teams + team;
     PfQueue& Q = pfq[team];
     // leader only: copy the team's next counted row into buffer Q.k (its
-    // previous row has been read by every thread of the team)
-    auto prefetch_next = [&]() {
+    // previous row has been read by every thread of the team). hint_t is
+    // the target of row hint_row, already in a register: the common case
+    // (the next row of the team) then waits for no target load before its
+    // copy is issued.
+    auto prefetch_next = [&](int64_t hint_row, int64_t hint_t) {
         int64_t row = Q.next;
-        while (row < a.rows && !row_counts(a, load_target(a, row))) row += nteams;
+        while (row < a.rows &&
+               !row_counts(a, row == hint_row ? hint_t : load_target(a, row)))
+            row += nteams;
         if (row >= a.rows) {
             Q.next = row;
             return;
@@ -276,7 +281,7 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
     // (a CTA whose slice is empty copies and waits for nothing)
     const bool has_slice = row_bytes > 0;
     if (lead && has_slice)
-        for (int k = 0; k < NB; ++k) prefetch_next();
+        for (int k = 0; k < NB; ++k) prefetch_next(r, t_cur);
 #pragma unroll 1
     for (; r < a.rows; r += nteams) {
         const int64_t t = t_cur;
@@ -328,7 +333,9 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
             q[k] = 32 * k < vlim ? sb[vbase - cta_vec0 + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
         const int tvec = static_cast<int>(t / VE) - cta_vec0;  // in this CTA's slice
         const bool owner = tvec >= 0 && lane == (tvec & 31) && wr == tvec / (32 * NVL);
-        const float xt = owner ? VT::load1(xrow, t) : 0.f;
+        // x_t from the buffer (before it takes the next row), not from HBM
+        const float xt =
+            owner ? VT::load1(sb, t - static_cast<int64_t>(cta_vec0) * VE) : 0.f;
         const float wt = a.weight ? __ldg(a.weight + t) : 1.f;
 
         // ---- 1. maximum of the raw logits
@@ -348,7 +355,7 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
         // every thread of the team holds its vectors (the warp reduction
         // above, or the team barrier, follows every thread's buffer reads):
         // the buffer takes the team's next counted row
-        if (lead && has_slice && !failed) prefetch_next();
+        if (lead && has_slice && !failed) prefetch_next(rn, t_cur);
         if (CL > 1) {
             // the row's maximum over the cluster: lane i reads CTA i's
             if (tid == 0) cl_red[0] = X;
@@ -523,9 +530,9 @@ ce_fwd_reg(const __grid_constant__ FwdArgs a) {
                             gg = ffma2(make_float2(As4, As4), make_float2(ex2(ar.x), ex2(ar.y)), bc);
                             gg = fmul2(gg, ffma2(make_float2(-r.x, -r.y), r, r));
                         } else {
-                            const float2 ar = reg_arg2<T>(make_float2(f[j], f[j + 1]), Ms, ML);
                             const float2 bc = WS ? fmul2(make_float2(Bc, Bc), make_float2(w[j], w[j + 1]))
                                                  : make_float2(Bc, Bc);
+                            const float2 ar = reg_arg2<T>(make_float2(f[j], f[j + 1]), Ms, ML);
                             gg = ffma2(make_float2(As, As), make_float2(ex2(ar.x), ex2(ar.y)), bc);
                         }
                         g[j] = gg.x;

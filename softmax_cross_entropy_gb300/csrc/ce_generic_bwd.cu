@@ -288,6 +288,17 @@ const void* nd_kernel(int dtype, bool vec, bool softcap, bool argmax) {
     return nullptr;
 }
 
+NdSplitFns nd_split_f32(bool vec, bool softcap, bool argmax, bool smooth);
+NdSplitFns nd_split_bf16(bool vec, bool softcap, bool argmax, bool smooth);
+NdSplitFns nd_split_f16(bool vec, bool softcap, bool argmax, bool smooth);
+
+NdSplitFns nd_split_fns(int dtype, bool vec, bool softcap, bool argmax, bool smooth) {
+    if (dtype == 0) return nd_split_f32(vec, softcap, argmax, smooth);
+    if (dtype == 1) return nd_split_bf16(vec, softcap, argmax, smooth);
+    if (dtype == 2) return nd_split_f16(vec, softcap, argmax, smooth);
+    return NdSplitFns{nullptr, nullptr, nullptr};
+}
+
 const void* generic_kernel(int dtype, bool softcap) {
     if (dtype == 0)
         return softcap ? (const void*)&ce_fwd_generic<float, true>

@@ -570,6 +570,36 @@ constexpr size_t nd_fixed_smem(int positions) {
 }
 const void* nd_kernel(int dtype, bool vec, bool softcap, bool argmax);
 
+// The split N-D forward (ce_fwd_nd_split.cuh): the classes of each tile of
+// 32 * VP positions in chunks of cc that separate CTAs take. One record
+// per (position, chunk): the chunk's statistics of the position.
+struct NdRec {
+    float m, S, SZ, Wn, xmax;
+    int idx;
+};
+// The gradient's coefficients of one position (merge -> gradient):
+// g = (ac exp(z - shift) + bc w_c) dz/dx, and gt, the whole gradient at the
+// target class (the one-hot term included).
+struct NdCoef {
+    float shift, ac, bc, gt;
+};
+struct NdSplitArgs {
+    FwdArgs f;        // rows = N * inner, V = C, inner
+    int64_t tiles;    // ceil(rows / (32 VP))
+    int nch;          // class chunks a tile
+    int cc;           // classes a chunk (the last one may hold fewer)
+    NdRec* rec;       // [tiles * 32 VP][nch]
+    NdCoef* coef;     // [rows]
+    int* tpos;        // [rows]: the counted target, or -1
+};
+constexpr int kNdSplitThreads = 256;
+struct NdSplitFns {
+    const void* stats;  // per (tile, chunk): the records
+    const void* merge;  // per position: outputs, coefficients, reduced scalars
+    const void* grad;   // per (tile, chunk): the gradient in place
+};
+NdSplitFns nd_split_fns(int dtype, bool vec, bool softcap, bool argmax, bool smooth);
+
 struct NdBwdArgs {
     const float* g;  // one value, or one per position ([N, inner])
     int per_pos;

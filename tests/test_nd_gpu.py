@@ -184,6 +184,51 @@ def test_nd_many_classes(shape, dtype):
     check(case, want_pred=True)
 
 
+# The split form (GBCE_ND_SPLIT=1): the classes of a tile in chunks of at
+# least 64 that separate CTAs take, merged per position. Shapes with several
+# chunks, ragged last chunks and ragged tiles, vector and single positions.
+@pytest.mark.parametrize("opts", sorted(OPTION_SETS))
+@pytest.mark.parametrize("shape,dtype", [((2, 300, 40), "bf16"), ((3, 1000, 24), "f32"),
+                                         ((2, 517, 7, 3), "bf16"), ((1, 2049, 16), "f16")])
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_nd_split_every_option(monkeypatch, opts, shape, dtype, reduction):
+    monkeypatch.setenv("GBCE_ND_SPLIT", "1")
+    case = workloads.nd_case(13 + sum(shape), shape, dtype, std=3.0, reduction=reduction,
+                             **dict(OPTION_SETS[opts]))
+    check(case, want_z=case.lse_square_scale > 0, want_acc=True, want_pred=True)
+
+
+def test_nd_split_ties_across_chunks(monkeypatch):
+    # the top logit of every position tied at classes in different chunks:
+    # the prediction is the first of them
+    monkeypatch.setenv("GBCE_ND_SPLIT", "1")
+    case = workloads.nd_case(17, (2, 1000, 64), "bf16", reduction="mean")
+    x = case.x.copy()
+    top = workloads.f32_to_bf16_bits(np.array([60.0], np.float32))[0]
+    for c in (130, 640, 999):
+        x[:, c, :] = top
+    case = case.with_(x=x)
+    out, _ = check(case, want_pred=True, want_acc=True)
+    valid = case.target != case.ignore_index
+    assert np.all(out["pred"][valid] == 130)
+
+
+def test_nd_split_matches_single_kernel_layouts(monkeypatch):
+    # both forms on the same staged-size input, each against the oracle
+    case = workloads.nd_case(19, (4, 40, 96), "bf16", reduction="sum", label_smoothing=0.1)
+    for split in ("0", "1"):
+        monkeypatch.setenv("GBCE_ND_SPLIT", split)
+        check(case, want_acc=True, want_pred=True)
+
+
+def test_nd_split_large(monkeypatch):
+    # the N-D profile's class count at 2 x 32000 x 128 bf16 (8.2M logits),
+    # the whole gradient against the oracle
+    monkeypatch.delenv("GBCE_ND_SPLIT", raising=False)
+    case = workloads.nd_case(23, (2, 32000, 128), "bf16", std=3.0, reduction="mean")
+    check(case, want_acc=True, want_pred=True)
+
+
 def test_nd_inner_one_is_2d():
     case = workloads.nd_case(2, (33, 4096, 1), "bf16", reduction="sum")
     check(case, want_pred=True)
