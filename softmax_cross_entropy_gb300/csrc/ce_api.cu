@@ -1307,23 +1307,25 @@ ce_status nd_plan(int dev, const DeviceInfo& info, int dtype, int64_t C, bool ve
     return CE_OK;
 }
 
-// Occupancy (CTAs an SM) of a split N-D kernel, computed once.
-int nd_split_occ(const void* fn) {
+// Occupancy (CTAs an SM) of a split N-D kernel with `smem` bytes of
+// dynamic shared memory (its limit set on the first call), computed once.
+int nd_split_occ(const void* fn, size_t smem) {
     static std::map<const void*, int> occ;
     auto it = occ.find(fn);
     if (it != occ.end()) return it->second;
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, kNdSplitThreads, 0) != cudaSuccess) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, kNdSplitThreads, smem) != cudaSuccess) {
         cudaGetLastError();
-        o = 1;
+        o = 0;
     }
-    o = std::max(o, 1);
     occ[fn] = o;
     return o;
 }
 
 // The split N-D forward (ce_fwd_nd_split.cuh): class chunks of cc classes
-// so that the (tile, chunk) items number about GBCE_ND_ITEMS (default 4) per
+// so that the (tile, chunk) items number about GBCE_ND_ITEMS (default 2) per
 // SM, with at least GBCE_ND_MIN_CHUNK (default 64) classes a chunk; the
 // records, coefficients and counted targets in the stream's N-D workspace.
 ce_status nd_split_launch(int dev, const DeviceInfo& info, const FwdArgs& f, int dtype,
@@ -1335,7 +1337,7 @@ ce_status nd_split_launch(int dev, const DeviceInfo& info, const FwdArgs& f, int
     NdSplitArgs s = {};
     s.f = f;
     s.tiles = (f.rows + P - 1) / P;
-    const int64_t want = std::max(1, env_int("GBCE_ND_ITEMS", 4)) * static_cast<int64_t>(info.sm_count);
+    const int64_t want = std::max(1, env_int("GBCE_ND_ITEMS", 2)) * static_cast<int64_t>(info.sm_count);
     const int64_t max_ch = std::max<int64_t>(1, C / std::max(8, env_int("GBCE_ND_MIN_CHUNK", 64)));
     const int64_t nch0 = std::min<int64_t>(max_ch, std::max<int64_t>(1, (want + s.tiles - 1) / s.tiles));
     const int64_t cc = (C + nch0 - 1) / nch0;
@@ -1354,8 +1356,14 @@ ce_status nd_split_launch(int dev, const DeviceInfo& info, const FwdArgs& f, int
     const NdSplitFns fns = nd_split_fns(dtype, vec_ok, softcap, argmax, f.eps > 0.f);
     if (!fns.stats || !fns.merge || !fns.grad) return CE_ERR_INVALID_ARG;
     const int64_t items = s.tiles * s.nch;
-    const int64_t g1 = std::min<int64_t>(items, nd_split_occ(fns.stats) * static_cast<int64_t>(info.sm_count));
-    rc = launch(fns.stats, static_cast<int>(g1), kNdSplitThreads, 0, 1, st, &s);
+    const int o1 = nd_split_occ(fns.stats, fns.stats_smem);
+    const int o3 = nd_split_occ(fns.grad, 0);
+    if (o1 < 1 || o3 < 1) {
+        g_last_error = "the split N-D kernels do not fit on an SM";
+        return CE_ERR_UNSUPPORTED;
+    }
+    const int64_t g1 = std::min<int64_t>(items, o1 * static_cast<int64_t>(info.sm_count));
+    rc = launch(fns.stats, static_cast<int>(g1), kNdSplitThreads, fns.stats_smem, 1, st, &s);
     if (rc != CE_OK) return rc;
     // one warp a position; the merge's CTAs take the partial-sum slots
     const int64_t g2 = std::max<int64_t>(
@@ -1363,7 +1371,7 @@ ce_status nd_split_launch(int dev, const DeviceInfo& info, const FwdArgs& f, int
                                                                  kMaxUnits)));
     rc = launch(fns.merge, static_cast<int>(g2), kNdSplitThreads, 0, 1, st, &s);
     if (rc != CE_OK || !f.grad) return rc;
-    const int64_t g3 = std::min<int64_t>(items, nd_split_occ(fns.grad) * static_cast<int64_t>(info.sm_count));
+    const int64_t g3 = std::min<int64_t>(items, o3 * static_cast<int64_t>(info.sm_count));
     return launch(fns.grad, static_cast<int>(g3), kNdSplitThreads, 0, 1, st, &s);
 }
 

@@ -47,6 +47,31 @@ __device__ __forceinline__ float nd_arg(float z, float m, float mL) {
 // takes every NW-th class of the chunk, U at a time (loads issued first);
 // the running maximum is checked once per U classes and position.
 // SMOOTH: the smoothing sums SZ and W are formed (label smoothing on).
+// Vector positions (16 bytes a lane): each warp streams its classes
+// through its own ring of kNdRing stages of U class rows in shared memory
+// (cp.async, 16 bytes a lane, each lane reading back only what it copied),
+// so the bytes in flight do not hold registers. The ring is reused for the
+// merge over the warps at the end of each item.
+constexpr int kNdRing = 4;
+template <int VP>
+constexpr size_t nd_stats_smem() {
+    constexpr int U = VP > 1 ? 4 : 8;
+    const size_t ring = VP > 1 ? static_cast<size_t>(kNdSplitWarps) * kNdRing * U * 32 * 16 : 0;
+    const size_t red = static_cast<size_t>(kNdSplitWarps) * 32 * VP * sizeof(NdRec);
+    return ring > red ? ring : red;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 template <typename T, int VP, bool SOFTCAP, bool ARGMAX, bool SMOOTH>
 __global__ void __launch_bounds__(kNdSplitThreads, 2)
 ce_nd_stats(const __grid_constant__ NdSplitArgs s) {
@@ -54,8 +79,9 @@ ce_nd_stats(const __grid_constant__ NdSplitArgs s) {
     using Raw = typename IO::Raw;
     constexpr int NW = kNdSplitWarps;
     constexpr int P = 32 * VP;
-    constexpr int U = VP > 1 ? 4 : 8;  // classes a step (loads in flight a thread)
-    __shared__ NdRec red[NW][P];
+    constexpr int U = VP > 1 ? 4 : 8;  // classes a step
+    extern __shared__ __align__(16) unsigned char nd_dyn[];
+    NdRec (*red)[P] = reinterpret_cast<NdRec (*)[P]>(nd_dyn);  // after the item's loop
     const FwdArgs& a = s.f;
     const int tid = threadIdx.x, lane = tid & 31, wy = tid >> 5;
     const int C = static_cast<int>(a.V);
@@ -149,20 +175,57 @@ ce_nd_stats(const __grid_constant__ NdSplitArgs s) {
         auto load = [&](int c) -> Raw {
             return lane_ok ? IO::load(a.x, lb + static_cast<int64_t>(c) * inner) : Raw{};
         };
-        int c = c0 + wy;
+        if constexpr (VP > 1) {
+            // this warp's classes c0 + wy + NW j, j < ncw, in blocks of U
+            const int first = c0 + wy;
+            const int ncw = first < c1 ? (c1 - first + NW - 1) / NW : 0;
+            const int nb = (ncw + U - 1) / U;
+            const uint32_t ring =
+                smem_u32(nd_dyn) + static_cast<uint32_t>(wy * kNdRing * U * 32 + lane) * 16u;
+            auto issue = [&](int blk) {
+                if (blk < nb && lane_ok) {
+                    const int n = min(U, ncw - blk * U);
+                    const uint32_t slot = ring + static_cast<uint32_t>((blk % kNdRing) * U * 32) * 16u;
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (u < n)
+                            cp_async16(slot + static_cast<uint32_t>(u * 32) * 16u,
+                                       static_cast<const T*>(a.x) + lb +
+                                           static_cast<int64_t>(first + (blk * U + u) * NW) * inner);
+                }
+                cp_async_commit();  // (possibly empty: the group count stays uniform)
+            };
+#pragma unroll
+            for (int b = 0; b < kNdRing - 1; ++b) issue(b);
 #pragma unroll 1
-        for (; c + (U - 1) * NW < c1; c += U * NW) {
-            Raw r[U];
+            for (int blk = 0; blk < nb; ++blk) {
+                cp_async_wait<kNdRing - 2>();  // block blk has landed
+                Raw r[U];
+                const uint4* sl = reinterpret_cast<const uint4*>(nd_dyn) +
+                                  (wy * kNdRing + blk % kNdRing) * U * 32 + lane;
 #pragma unroll
-            for (int u = 0; u < U; ++u) r[u] = load(c + u * NW);
-            step(c, U, r);
-        }
-        if (c < c1) {  // the chunk's last classes of this warp: fewer than U
-            Raw r[U];
-            const int n = (c1 - c + NW - 1) / NW;
+                for (int u = 0; u < U; ++u) r[u] = sl[u * 32];
+                issue(blk + kNdRing - 1);  // into the slot read one block ago
+                step(first + blk * U * NW, min(U, ncw - blk * U), r);
+            }
+            cp_async_wait<0>();
+            __syncthreads();  // every warp is done with its ring: red takes the space
+        } else {
+            int c = c0 + wy;
+#pragma unroll 1
+            for (; c + (U - 1) * NW < c1; c += U * NW) {
+                Raw r[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) r[u] = u < n ? load(c + u * NW) : Raw{};
-            step(c, n, r);
+                for (int u = 0; u < U; ++u) r[u] = load(c + u * NW);
+                step(c, U, r);
+            }
+            if (c < c1) {  // the chunk's last classes of this warp: fewer than U
+                Raw r[U];
+                const int n = (c1 - c + NW - 1) / NW;
+#pragma unroll
+                for (int u = 0; u < U; ++u) r[u] = u < n ? load(c + u * NW) : Raw{};
+                step(c, n, r);
+            }
         }
 #pragma unroll
         for (int v = 0; v < VP; ++v)
@@ -399,7 +462,8 @@ NdSplitFns nd_split_of(bool vec, bool softcap, bool argmax, bool smooth) {
                      : (smooth ? (const void*)&ce_nd_stats<T, VP, SC, false, true>             \
                                : (const void*)&ce_nd_stats<T, VP, SC, false, false>);          \
     f.merge = (const void*)&ce_nd_merge<T, SC>;                                               \
-    f.grad = (const void*)&ce_nd_grad<T, VP, SC>;
+    f.grad = (const void*)&ce_nd_grad<T, VP, SC>;                                             \
+    f.stats_smem = nd_stats_smem<VP>();
     if (vec) {
         if (softcap) {
             GBCE_ND_SPLIT(VPV, true)

@@ -296,7 +296,7 @@ NdSplitFns nd_split_fns(int dtype, bool vec, bool softcap, bool argmax, bool smo
     if (dtype == 0) return nd_split_f32(vec, softcap, argmax, smooth);
     if (dtype == 1) return nd_split_bf16(vec, softcap, argmax, smooth);
     if (dtype == 2) return nd_split_f16(vec, softcap, argmax, smooth);
-    return NdSplitFns{nullptr, nullptr, nullptr};
+    return NdSplitFns{nullptr, nullptr, nullptr, 0};
 }
 
 const void* generic_kernel(int dtype, bool softcap) {

@@ -597,6 +597,7 @@ struct NdSplitFns {
     const void* stats;  // per (tile, chunk): the records
     const void* merge;  // per position: outputs, coefficients, reduced scalars
     const void* grad;   // per (tile, chunk): the gradient in place
+    size_t stats_smem;  // dynamic shared memory of a stats CTA
 };
 NdSplitFns nd_split_fns(int dtype, bool vec, bool softcap, bool argmax, bool smooth);
 
