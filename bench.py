@@ -525,30 +525,34 @@ def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5, chunk_ro
     ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
     st = torch.cuda.current_stream(device).cuda_stream
 
-    def step():
+    def step(ch):
         rc = _lib.ce_flce(hidden.data_ptr(), lm_w.data_ptr(), None, _lib.CE_BF16, rows, H, V,
                           target.data_ptr(), None, -100, 0.0, 0.0, 0.0, _lib.CE_RED_MEAN,
                           _lib.CE_FLAG_GRAD, loss.data_ptr(), None, None, None, gh.data_ptr(),
-                          gw.data_ptr(), None, chunk_rows, ws.data_ptr(), nbytes, st)
+                          gw.data_ptr(), None, ch, ws.data_ptr(), nbytes, st)
         if rc != 0:
             raise RuntimeError(f"ce_flce: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
 
-    def timed():
+    def timed(ch=chunk_rows):
         for _ in range(3):
-            step()
+            step(ch)
         torch.cuda.synchronize(device)
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(steps):
-            step()
+            step(ch)
         e1.record()
         torch.cuda.synchronize(device)
         barrier()
         return max_over_ranks(e0.elapsed_time(e1) / 1e3) / steps
 
     t = timed()  # every GEMM on this library's tcgen05 kernel (the default)
+    # the same with 1024-row chunks (512 MB of logits a chunk: four times
+    # the logits and gradient GEMMs over a quarter of the rows, and three
+    # fp32 read-add-writes of grad_weight)
+    t_small = timed(1024)
     # the same step with the three GEMMs on cuBLAS, for comparison
     os.environ["GBCE_FLCE_GEMM"] = "cublas"
     try:
@@ -562,9 +566,12 @@ def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5, chunk_ro
            "ms_per_step": round(t * 1e3, 3), "TFLOP/s": round(flops / t / 1e12, 1),
            "frac": round(flops / t / 1e12 / peak_t, 4), "peak_TFLOP/s": peak_t,
            "peak_kind": kind + " (bf16, sustained)",
-           "chunk_rows": chunk_rows or max(1, (1 << 29) // (V * 4)),
+           "chunk_rows": chunk_rows or min(rows, (1 << 31) // (V * 4) // 256 * 256),
            "gemms": "this library's tcgen05 GEMM (ce_gemm: bf16 in, fp32 accumulation in "
                     "tensor memory) for the logits, grad_hidden and grad_weight",
+           "chunks_of_1024_rows": {"ms_per_step": round(t_small * 1e3, 3),
+                                   "TFLOP/s": round(flops / t_small / 1e12, 1),
+                                   "frac": round(flops / t_small / 1e12 / peak_t, 4)},
            "cublas_gemms": {"ms_per_step": round(t_blas * 1e3, 3),
                             "TFLOP/s": round(flops / t_blas / 1e12, 1),
                             "gemms": "the same step with the three GEMMs on cuBLAS "

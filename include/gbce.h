@@ -284,7 +284,8 @@ ce_status ce_bwd_nd(const float* grad_output, int grad_per_position, void* dlogi
  * grad_hidden  [rows, H] in dtype;
  * grad_weight  [V, H] fp32 (overwritten, not accumulated into);
  * grad_bias    [V] fp32.
- * chunk_rows   rows per chunk (<= 0: about 512 MB of fp32 logits a chunk).
+ * chunk_rows   rows per chunk (<= 0: about 2 GB of fp32 logits a chunk, a
+ *              multiple of 256 rows when at least 256).
  * workspace    device memory of at least ce_flce_workspace_bytes(dtype,
  *              rows, V, chunk_rows) bytes, 256-byte aligned, owned by the
  *              caller; it holds one chunk of fp32 logits (and of the gradient

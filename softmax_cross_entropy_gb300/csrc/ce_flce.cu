@@ -160,7 +160,12 @@ struct FlceLayout {
 FlceLayout layout(int dtype, int64_t rows, int64_t V, int64_t chunk_rows) {
     FlceLayout L{};
     int64_t c = chunk_rows;
-    if (c <= 0) c = std::max<int64_t>(1, (int64_t{1} << 29) / (V * 4));  // about 512 MB of logits
+    // default: about 2 GB of fp32 logits (under 1% of this GPU's memory), in
+    // whole 256-row tiles of the tensor-core GEMMs when that leaves any
+    if (c <= 0) {
+        c = std::max<int64_t>(1, (int64_t{1} << 31) / (V * 4));
+        if (c >= 256) c = c / 256 * 256;
+    }
     c = std::max<int64_t>(1, std::min<int64_t>(c, std::max<int64_t>(rows, 1)));
     L.chunk = c;
     L.nchunks = rows == 0 ? 0 : (rows + c - 1) / c;

@@ -7,22 +7,24 @@
 // hidden @ W^T (both K-major), grad_hidden = G @ W (B MN-major, 16-bit out),
 // grad_weight += G^T @ hidden (both MN-major, fp32 accumulate).
 //
-// A persistent kernel, one CTA an SM, warp-specialised (6 warps):
-//  * warp 0, lane 0: TMA producer. It walks the CTA's 128 x 256 tiles (tile
-//    t of the launch goes to CTA t mod grid; tiles run along M first, so
-//    concurrent CTAs share a slice of B through L2) and their 64-deep K
-//    blocks, and fills a 4-stage shared-memory ring with 2-D TMA copies
-//    (128-byte swizzle): one box a K-major operand tile, or boxes of 64
-//    MN elements x 64 K rows side by side for an MN-major one;
+// A persistent kernel, one CTA an SM, warp-specialised (6 warps), on tiles
+// of 128 or 256 rows x 256 columns (TcTile):
+//  * warp 0, lane 0: TMA producer. It walks the CTA's tiles (tile t of the
+//    launch goes to CTA t mod grid; consecutive tiles share a tile of the
+//    larger operand through L2) and their 64-deep K blocks, and fills a
+//    3- or 4-stage shared-memory ring with 2-D TMA copies (128-byte
+//    swizzle): one box a K-major operand tile, or boxes of 64 MN elements x
+//    64 K rows side by side for an MN-major one;
 //  * warp 1, lane 0: MMA issuer. tcgen05.mma (M 128, N 256, K 16, fp32
-//    accumulation) into one of two 256-column accumulators in tensor memory
-//    (512 columns: tile i uses accumulator i mod 2), freeing each stage with
-//    tcgen05.commit on its `empty` mbarrier and handing the finished
-//    accumulator to the epilogue with a commit on its `acc_full` mbarrier;
-//  * warps 2-5: epilogue. Each reads its 32 accumulator rows (tcgen05.ld)
-//    and writes them out while the tensor cores already work on the next
-//    tile in the other accumulator, then frees the accumulator
-//    (`acc_empty`, 128 arrivals).
+//    accumulation, one a 128-row half) into tensor memory (512 columns: two
+//    256-column accumulators used by turns for 128-row tiles, the two
+//    halves of one for 256-row tiles), freeing each stage with
+//    tcgen05.commit on its `empty` mbarrier and handing the finished tile
+//    to the epilogue with a commit on its `acc_full` mbarrier;
+//  * warps 2-5: epilogue. Each reads its 32 accumulator rows of each half
+//    (tcgen05.ld), stages them in shared memory and hands them to TMA
+//    stores (or reduce-adds), then frees the accumulator (`acc_empty`, 128
+//    arrivals); with two accumulators this overlaps the next tile's MMAs.
 // Every mbarrier wait is bounded; a wait that gives up records the timeout
 // in the status word and sets the launch's abort word, the kernel waits
 // (bounded) for its copies in flight, frees its tensor memory and returns.
@@ -45,20 +47,36 @@ ce_status library_status_word(cudaStream_t st, unsigned** out);
 
 namespace {
 
-// 4 stages of 128 x 64 + 256 x 64 tiles (192 KB, one CTA an SM): measured
-// best of 2 / 3 / 4 / 6 stages and 128- / 256-wide tiles on GB300
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+// Tiles of BM x 256 (BM = 128 or 256) with K blocks of 64, one CTA an SM:
+//  * BM = 128: 4 stages of 128 x 64 + 256 x 64 (48 KB each); two 256-column
+//    accumulators, so the epilogue of a tile overlaps the next tile's MMAs;
+//  * BM = 256: 3 stages of 256 x 64 + 256 x 64 (64 KB each); the tile's two
+//    128-row halves take the 512 columns, the epilogue does not overlap,
+//    but each stage's bytes feed twice the MMA work (the TMA latency is
+//    what limits the 128-row tiles: a third fewer bytes a flop).
+constexpr int kMmaM = 128, kBN = 256, kBK = 64, kMaxStages = 4;
 constexpr int kTcThreads = 192;  // producer, MMA issuer, 4 epilogue warps
-constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kBBytes = kBN * kBK * 2;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kHalfA = kMmaM * kBK * 2;  // 128 rows of A (16 KB)
 constexpr uint32_t kMnBox = 64 * kBK * 2;  // one 64 (MN) x 64 (K) box of an MN-major tile
-constexpr uint32_t kTmemCols = 2 * kBN;    // two accumulators
+constexpr uint32_t kTmemCols = 2 * kBN;    // 512 columns
+template <int BM>
+struct TcTile {
+    static constexpr int kStages = BM == 256 ? 3 : 4;
+    static constexpr int kHalves = BM / kMmaM;      // 128-row MMAs a K step
+    static constexpr int kAccBufs = BM == 256 ? 1 : 2;
+    static constexpr uint32_t kABytes = BM * kBK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+};
+constexpr uint32_t kRingBytes = 4 * (kHalfA + kBBytes);  // the same for both BM
+static_assert(TcTile<128>::kStages * TcTile<128>::kStageBytes == kRingBytes &&
+                  TcTile<256>::kStages * TcTile<256>::kStageBytes == kRingBytes,
+              "both tile shapes use the same ring");
 // epilogue staging for TMA stores: per epilogue warp two 32-row x 128-byte
 // boxes (4 KB each, 128-byte swizzle)
 constexpr uint32_t kStageOut = 4096;
 constexpr uint32_t kOutBytes = 4 * 2 * kStageOut;
-constexpr size_t kTcSmem = static_cast<size_t>(kStages) * kStageBytes + kOutBytes + 1024;
+constexpr size_t kTcSmem = static_cast<size_t>(kRingBytes) + kOutBytes + 1024;
 
 // What the epilogue does with the accumulator.
 enum : int { kOutF32 = 0, kOutF32Add = 1, kOut16 = 2 };
@@ -103,10 +121,10 @@ __device__ __forceinline__ uint64_t tc_smem_desc_mn(uint32_t saddr) {
 
 // Instruction descriptor of kind::f16: fp32 accumulator, A and B of the
 // given type (0 fp16, 1 bf16), A and B K-major (0) or MN-major (1, the
-// transpose bits 15 and 16), N = kBN, M = kBM.
+// transpose bits 15 and 16), N = kBN, M = kMmaM.
 __host__ __device__ constexpr uint32_t tc_idesc(uint32_t ab, uint32_t a_mn = 0, uint32_t b_mn = 0) {
     return (1u << 4) | (ab << 7) | (ab << 10) | (a_mn << 15) | (b_mn << 16) |
-           (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+           (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(kMmaM >> 4) << 24);
 }
 
 // Bounded wait for the producer and MMA threads of the tight GEMM pipeline:
@@ -298,18 +316,25 @@ __device__ __forceinline__ void tc_stage32(uint32_t buf, int r, int h, const flo
 // TMAO: C leaves through shared memory with TMA stores (reduce-adds for
 // kOutF32Add) of 32-row x 128-byte boxes; else with plain stores (a C
 // whose base or row pitch is not a multiple of 16 bytes).
-template <uint32_t AB, bool A_MN, bool B_MN, int OUT, bool TMAO>
+// BM: the tile's rows (TcTile).
+template <uint32_t AB, bool A_MN, bool B_MN, int OUT, bool TMAO, int BM>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
         const __grid_constant__ CUtensorMap mapC, const __grid_constant__ TcArgs a) {
+    using TT = TcTile<BM>;
+    constexpr int kStages = TT::kStages;
+    constexpr uint32_t kABytes = TT::kABytes;
+    constexpr uint32_t kStageBytes = TT::kStageBytes;
+    constexpr int NACC = TT::kAccBufs;
+    constexpr int H = TT::kHalves;
     extern __shared__ unsigned char tc_smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kStages];
-    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
     __shared__ __align__(8) uint64_t acc_full[2];
     __shared__ __align__(8) uint64_t acc_empty[2];
     __shared__ __align__(8) uint64_t done_bar;  // every MMA of the CTA completed
     __shared__ uint32_t tmem_base_sh;
-    __shared__ uint32_t s_issued[kStages];  // 0, or 2 + parity of the last copy into the stage
+    __shared__ uint32_t s_issued[kMaxStages];  // 0, or 2 + parity of the last copy into the stage
     __shared__ int s_fail;
 
     // a CTA of this launch already gave up: the others return at once
@@ -354,7 +379,7 @@ tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtens
             int it = 0;  // K blocks issued so far (ring position)
             bool fail = false;
             for (int64_t t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
-                const int m0 = static_cast<int>(tile_m(a, t) * kBM);
+                const int m0 = static_cast<int>(tile_m(a, t) * BM);
                 const int n0 = static_cast<int>(tile_n(a, t) * kBN);
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % kStages;
@@ -369,7 +394,7 @@ tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtens
                     const uint32_t sa = smem0 + static_cast<uint32_t>(s) * kStageBytes;
                     const int k0 = kb * kBK;
                     if (A_MN) {
-                        for (int j = 0; j < kBM / 64; ++j)
+                        for (int j = 0; j < BM / 64; ++j)
                             tma_load_2d(sa + j * kMnBox, &mapA, m0 + 64 * j, k0, fb);
                     } else {
                         tma_load_2d(sa, &mapA, k0, m0, fb);
@@ -387,21 +412,22 @@ tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtens
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---- MMA issuer: tile i into accumulator i mod 2
+            // ---- MMA issuer: tile i into accumulator buffer i mod NACC
             constexpr uint32_t idesc = tc_idesc(AB, A_MN ? 1u : 0u, B_MN ? 1u : 0u);
             int it = 0;
             int i = 0;  // tiles of this CTA so far
             bool fail = false;
             for (int64_t t = blockIdx.x; t < ntiles && !fail; t += gridDim.x, ++i) {
-                const int b = i & 1;
-                // the epilogue has drained this accumulator's previous tile
-                if (!tc_wait(smem_u32(&acc_empty[b]), (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u,
-                             a.timeout_ns)) {
+                const int b = i % NACC;
+                // the epilogue has drained this buffer's previous tile
+                if (!tc_wait(smem_u32(&acc_empty[b]),
+                             (static_cast<uint32_t>(i / NACC) & 1u) ^ 1u, a.timeout_ns)) {
                     fail = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t acc = tmem + static_cast<uint32_t>(b * kBN);
+                // half h of the tile (rows 128 h ...) in columns (b H + h) 256
+                const uint32_t acc = tmem + static_cast<uint32_t>(b * H * kBN);
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
@@ -415,11 +441,18 @@ tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtens
                     for (int k = 0; k < kBK / 16; ++k) {
                         // K step of 16: 32 bytes inside a K-major swizzled row, two
                         // 8-row atoms (2 KB) of an MN-major tile
-                        const uint64_t da = A_MN ? tc_smem_desc_mn(sa + 2048u * k)
-                                                 : tc_smem_desc(sa + 32u * k);
                         const uint64_t db = B_MN ? tc_smem_desc_mn(sa + kABytes + 2048u * k)
                                                  : tc_smem_desc(sa + kABytes + 32u * k);
-                        tc_mma(acc, da, db, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int h = 0; h < H; ++h) {
+                            // rows 128 h of A: 16 KB on in either layout (128
+                            // swizzled rows, or two 64-wide boxes)
+                            const uint32_t ah = sa + static_cast<uint32_t>(h) * kHalfA;
+                            const uint64_t da = A_MN ? tc_smem_desc_mn(ah + 2048u * k)
+                                                     : tc_smem_desc(ah + 32u * k);
+                            tc_mma(acc + static_cast<uint32_t>(h * kBN), da, db, idesc,
+                                   (kb > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     tc_commit(smem_u32(&empty_bar[s]));
                 }
@@ -431,73 +464,76 @@ tc_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtens
             tc_commit(smem_u32(&done_bar));  // after every MMA this thread issued
         }
     } else {
-        // ---- epilogue: warp w reads accumulator lanes 32 (w mod 4) ...
+        // ---- epilogue: warp w reads accumulator lanes 32 (w mod 4) of
+        // each 128-row half of the tile
         const int q = warp & 3;
         // this warp's two staging boxes, used in turn
-        const uint32_t stg = smem0 + static_cast<uint32_t>(kStages) * kStageBytes +
-                             static_cast<uint32_t>(q) * 2u * kStageOut;
+        const uint32_t stg = smem0 + kRingBytes + static_cast<uint32_t>(q) * 2u * kStageOut;
         uint32_t nst = 0;  // boxes this warp has handed to the TMA
         int i = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-            const int b = i & 1;
+            const int b = i % NACC;
             const bool ok = mbar_wait_bounded(smem_u32(&acc_full[b]),
-                                              static_cast<uint32_t>(i >> 1) & 1u, a.timeout_ns);
+                                              static_cast<uint32_t>(i / NACC) & 1u, a.timeout_ns);
             if (!ok || *reinterpret_cast<volatile int*>(&s_fail) ||
                 *reinterpret_cast<volatile unsigned*>(a.abort)) {
                 if (lane == 0) s_fail = 1;
                 break;
             }
             tc_fence_after();
-            const int64_t m0 = tile_m(a, t) * kBM;
             const int64_t n0 = tile_n(a, t) * kBN;
-            const int64_t row = m0 + q * 32 + lane;
-            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                                  static_cast<uint32_t>(b * kBN);
-            if constexpr (TMAO) {
-                constexpr int kBoxCols = OUT == kOut16 ? 64 : 32;
-                const bool rows_in = m0 + q * 32 < a.M;  // the same for the whole warp
 #pragma unroll 1
-                for (int c = 0; c < kBN / kBoxCols; ++c) {
-                    const int64_t n = n0 + c * kBoxCols;
-                    if (n >= a.N) break;  // the same for every thread of the warp
-                    const uint32_t buf = stg + (nst & 1u) * kStageOut;
-                    // the box written two turns ago has been read out of this buffer
-                    if (lane == 0) bulk_wait_read_1();
-                    __syncwarp();
+            for (int hh = 0; hh < H; ++hh) {
+                const int64_t m0 = tile_m(a, t) * BM + hh * kMmaM;
+                const int64_t row = m0 + q * 32 + lane;
+                const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                      static_cast<uint32_t>((b * H + hh) * kBN);
+                if constexpr (TMAO) {
+                    constexpr int kBoxCols = OUT == kOut16 ? 64 : 32;
+                    const bool rows_in = m0 + q * 32 < a.M;  // the same for the whole warp
+#pragma unroll 1
+                    for (int c = 0; c < kBN / kBoxCols; ++c) {
+                        const int64_t n = n0 + c * kBoxCols;
+                        if (n >= a.N) break;  // the same for every thread of the warp
+                        const uint32_t buf = stg + (nst & 1u) * kStageOut;
+                        // the box written two turns ago has been read out of this buffer
+                        if (lane == 0) bulk_wait_read_1();
+                        __syncwarp();
 #pragma unroll
-                    for (int h = 0; h < kBoxCols / 32; ++h) {
-                        float v[32];
-                        tc_ld32(trow + static_cast<uint32_t>(c * kBoxCols + h * 32), v);
-                        if (OUT == kOutF32 && a.bias) {
-                            const int64_t nb = n + h * 32;
+                        for (int h = 0; h < kBoxCols / 32; ++h) {
+                            float v[32];
+                            tc_ld32(trow + static_cast<uint32_t>(c * kBoxCols + h * 32), v);
+                            if (OUT == kOutF32 && a.bias) {
+                                const int64_t nb = n + h * 32;
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (nb + j < a.N) v[j] += __ldg(a.bias + nb + j);
+                                for (int j = 0; j < 32; ++j)
+                                    if (nb + j < a.N) v[j] += __ldg(a.bias + nb + j);
+                            }
+                            tc_stage32<OUT, AB>(buf, lane, h, v);
                         }
-                        tc_stage32<OUT, AB>(buf, lane, h, v);
+                        fence_proxy_async_smem();  // the writes, seen by the TMA
+                        __syncwarp();
+                        if (lane == 0 && rows_in) {
+                            // rows past M and columns past N are clipped by the TMA
+                            if (OUT == kOutF32Add)
+                                tma_reduce_add_2d(&mapC, buf, static_cast<int>(n),
+                                                  static_cast<int>(m0 + q * 32));
+                            else
+                                tma_store_2d(&mapC, buf, static_cast<int>(n),
+                                             static_cast<int>(m0 + q * 32));
+                        }
+                        if (lane == 0) bulk_commit();
+                        ++nst;
                     }
-                    fence_proxy_async_smem();  // the writes, seen by the TMA
-                    __syncwarp();
-                    if (lane == 0 && rows_in) {
-                        // rows past M and columns past N are clipped by the TMA
-                        if (OUT == kOutF32Add)
-                            tma_reduce_add_2d(&mapC, buf, static_cast<int>(n),
-                                              static_cast<int>(m0 + q * 32));
-                        else
-                            tma_store_2d(&mapC, buf, static_cast<int>(n),
-                                         static_cast<int>(m0 + q * 32));
-                    }
-                    if (lane == 0) bulk_commit();
-                    ++nst;
-                }
-            } else {
+                } else {
 #pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
-                    const int64_t n = n0 + c * 32;
-                    if (n >= a.N) break;  // the same for every thread of the warp
-                    float v[32];
-                    tc_ld32(trow + static_cast<uint32_t>(c * 32), v);
-                    if (row < a.M) tc_store32<OUT, AB>(a, row, n, v);
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        const int64_t n = n0 + c * 32;
+                        if (n >= a.N) break;  // the same for every thread of the warp
+                        float v[32];
+                        tc_ld32(trow + static_cast<uint32_t>(c * 32), v);
+                        if (row < a.M) tc_store32<OUT, AB>(a, row, n, v);
+                    }
                 }
             }
             tc_fence_before();
@@ -556,7 +592,7 @@ ce_status encoder(EncodeTiled* out) {
 // 2-D map of a row-major [outer, inner] matrix of 16-bit elements, boxes of
 // box_outer x 64 elements (128 bytes: the swizzle width), 128-byte
 // swizzle, zeros outside the matrix. A K-major operand is [MN, K] with boxes
-// of kBM or kBN rows; an MN-major one is [K, MN] with boxes of 64 K rows.
+// of 128 or 256 rows; an MN-major one is [K, MN] with boxes of 64 K rows.
 ce_status make_map(CUtensorMap* map, const void* p, int dtype, int64_t outer, int64_t inner,
                    uint32_t box_outer) {
     EncodeTiled enc = nullptr;
@@ -604,12 +640,12 @@ ce_status make_map_c(CUtensorMap* map, void* C, int dtype, int out, int64_t M, i
     return CE_OK;
 }
 
-template <uint32_t AB, bool TMAO>
+template <uint32_t AB, bool TMAO, int TBM>
 const void* gemm_fn_t(bool a_mn, bool b_mn, int out) {
-#define GBCE_TC(AM, BM)                                                         \
-    (out == kOutF32      ? (const void*)&tc_gemm<AB, AM, BM, kOutF32, TMAO>    \
-     : out == kOutF32Add ? (const void*)&tc_gemm<AB, AM, BM, kOutF32Add, TMAO> \
-                         : (const void*)&tc_gemm<AB, AM, BM, kOut16, TMAO>)
+#define GBCE_TC(AM, BMN)                                                              \
+    (out == kOutF32      ? (const void*)&tc_gemm<AB, AM, BMN, kOutF32, TMAO, TBM>    \
+     : out == kOutF32Add ? (const void*)&tc_gemm<AB, AM, BMN, kOutF32Add, TMAO, TBM> \
+                         : (const void*)&tc_gemm<AB, AM, BMN, kOut16, TMAO, TBM>)
     if (!a_mn && !b_mn) return GBCE_TC(false, false);
     if (!a_mn && b_mn) return GBCE_TC(false, true);
     if (a_mn && !b_mn) return GBCE_TC(true, false);
@@ -617,9 +653,26 @@ const void* gemm_fn_t(bool a_mn, bool b_mn, int out) {
 #undef GBCE_TC
 }
 
+// The 256-row tiles only with the TMA-store epilogue (a C aligned for it).
 template <uint32_t AB>
-const void* gemm_fn(bool a_mn, bool b_mn, int out, bool tmao) {
-    return tmao ? gemm_fn_t<AB, true>(a_mn, b_mn, out) : gemm_fn_t<AB, false>(a_mn, b_mn, out);
+const void* gemm_fn(bool a_mn, bool b_mn, int out, bool tmao, int bm) {
+    if (!tmao) return gemm_fn_t<AB, false, 128>(a_mn, b_mn, out);
+    return bm == 256 ? gemm_fn_t<AB, true, 256>(a_mn, b_mn, out)
+                     : gemm_fn_t<AB, true, 128>(a_mn, b_mn, out);
+}
+
+// Tile rows for an M x N product on `sms` persistent CTAs: the shape with
+// the fewer rounds of tiles over the SMs, a round of 256-row tiles counted
+// as 1.6 of 128-row ones (measured: 1774 against 1440 TFLOP/s at 8192^3)
+// (GBCE_TC_BM = 128 or 256 forces one).
+int tile_rows(int64_t M, int64_t N, int sms, bool tmao) {
+    if (!tmao) return 128;
+    const char* v = std::getenv("GBCE_TC_BM");
+    if (v && *v) return std::atoi(v) == 256 ? 256 : 128;
+    const int64_t tn = (N + kBN - 1) / kBN, s = std::max(sms, 1);
+    const int64_t r256 = ((M + 255) / 256 * tn + s - 1) / s;
+    const int64_t r128 = ((M + 127) / 128 * tn + s - 1) / s;
+    return 16 * r256 < 10 * r128 ? 256 : 128;
 }
 
 }  // namespace
@@ -646,34 +699,36 @@ ce_status tc_gemm_launch(const void* A, bool a_mn, const void* B, bool b_mn, int
     if (K <= 0 || !tc_operand_ok(A, dtype, a_mn ? M : K) || !tc_operand_ok(B, dtype, b_mn ? N : K))
         return CE_ERR_UNSUPPORTED;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return CE_ERR_UNSUPPORTED;
-    CUtensorMap ma, mb;
-    ce_status rc = a_mn ? make_map(&ma, A, dtype, K, M, 64) : make_map(&ma, A, dtype, M, K, kBM);
-    if (rc != CE_OK) return rc;
-    rc = b_mn ? make_map(&mb, B, dtype, K, N, 64) : make_map(&mb, B, dtype, N, K, kBN);
-    if (rc != CE_OK) return rc;
     // C through TMA stores when its base and row pitch are multiples of 16 bytes
     const int64_t cpitch = N * (out == kOut16 ? 2 : 4);
     const bool tmao = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && cpitch % 16 == 0;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return record_cuda_failure(e, "tensor-core GEMM device");
+    const int bm = tile_rows(M, N, sms, tmao);
+    CUtensorMap ma, mb;
+    ce_status rc = a_mn ? make_map(&ma, A, dtype, K, M, 64)
+                        : make_map(&ma, A, dtype, M, K, static_cast<uint32_t>(bm));
+    if (rc != CE_OK) return rc;
+    rc = b_mn ? make_map(&mb, B, dtype, K, N, 64) : make_map(&mb, B, dtype, N, K, kBN);
+    if (rc != CE_OK) return rc;
     CUtensorMap mc;
     std::memset(&mc, 0, sizeof(mc));
     if (tmao) {
         rc = make_map_c(&mc, C, dtype, out, M, N);
         if (rc != CE_OK) return rc;
     }
-    const void* fn = dtype == CE_BF16 ? gemm_fn<1u>(a_mn, b_mn, out, tmao)
-                                      : gemm_fn<0u>(a_mn, b_mn, out, tmao);
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kTcSmem));
+    const void* fn = dtype == CE_BF16 ? gemm_fn<1u>(a_mn, b_mn, out, tmao, bm)
+                                      : gemm_fn<0u>(a_mn, b_mn, out, tmao, bm);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kTcSmem));
     if (e != cudaSuccess) return record_cuda_failure(e, "tensor-core GEMM attributes");
     const char* tenv = std::getenv("GBCE_WAIT_TIMEOUT_MS");
     const uint64_t tms = (tenv && *tenv) ? static_cast<uint64_t>(std::atoll(tenv)) : 2000ull;
     e = cudaMemsetAsync(abort, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return record_cuda_failure(e, "cudaMemsetAsync(abort word)");
-    const int64_t tm = (M + kBM - 1) / kBM, tn = (N + kBN - 1) / kBN;
+    const int64_t tm = (M + bm - 1) / bm, tn = (N + kBN - 1) / kBN;
     // consecutive tiles (the CTAs that run together) share a tile of the
     // larger operand, which is then read from DRAM about once: along M first
     // when B is the larger (its tile serves every row of tiles), along N

@@ -89,12 +89,15 @@ def _stored(x, dtype, transpose):
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 520, 136), (8, 24, 8),
                                    (1048, 2056, 1032)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_gemm_layouts_and_outputs(a_mn, b_mn, c_mode, M, N, K, dtype):
+@pytest.mark.parametrize("bm", ["128", "256"])
+def test_gemm_layouts_and_outputs(monkeypatch, a_mn, b_mn, c_mode, M, N, K, dtype, bm):
     # ce_gemm: A [M, K] and B [K, N] stored K-major or MN-major; C written
-    # in fp32, added to in fp32, or rounded to the operand type. The
-    # reference is the oracle's float64 product of the same bits.
+    # in fp32, added to in fp32, or rounded to the operand type; tiles of
+    # 128 or 256 rows (GBCE_TC_BM). The reference is the oracle's float64
+    # product of the same bits.
     import oracle
     from softmax_cross_entropy_gb300 import _lib
+    monkeypatch.setenv("GBCE_TC_BM", bm)
     seed = 7 * M + 3 * N + K + 11 * a_mn + 13 * b_mn + 17 * c_mode
     a = workloads.random_case(seed, M, K, dtype=dtype, std=1.0, ignore_frac=0.0).x   # [M, K]
     bt = workloads.random_case(seed + 1, N, K, dtype=dtype, std=1.0 / math.sqrt(K),
