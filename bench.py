@@ -481,6 +481,7 @@ def run_gpu(args):
                                    max_over_ranks, peak)}
 
         line["flce"] = measure_flce(device, torch, barrier, max_over_ranks, rank)
+        line["nd"] = measure_nd(device, torch, barrier, max_over_ranks, rank, peak)
 
     if clocks:
         line["clocks"] = clocks
@@ -578,6 +579,62 @@ def measure_flce(device, torch, barrier, max_over_ranks, rank, steps=5, chunk_ro
                                      "(GBCE_FLCE_GEMM=cublas)"}}
     del hidden, lm_w, gh, gw, ws
     torch.cuda.empty_cache()
+    return out
+
+
+ND_SHAPES = [(8, 32000, 512), (8, 4096, 1024), (16, 1000, 4096), (8, 19, 512, 512)]
+
+
+def measure_nd(device, torch, barrier, max_over_ranks, rank, peak, steps=6):
+    """N-D logits (class dimension 1) through ce_fwd_nd, forward with the
+    gradient in place, bf16, mean, 10% of positions ignored, N(0, 3^2):
+    each timed step on its own buffer of seeded logits (CUDA events over
+    `steps` steps), GB/s of one read and one write per element."""
+    import math
+    import numpy as np
+    from softmax_cross_entropy_gb300 import _lib
+    out = []
+    for shape in ND_SHAPES:
+        case = workloads.nd_case(rank, shape, "bf16", std=3.0, reduction="mean")
+        N, C = shape[0], shape[1]
+        inner = math.prod(shape[2:])
+        pristine = torch.from_numpy(np.ascontiguousarray(case.x).view(np.int16)).view(
+            torch.bfloat16).to(device)
+        t = torch.from_numpy(np.ascontiguousarray(case.target)).to(device)
+        loss = torch.empty(1, dtype=torch.float32, device=device)
+        bufs = [torch.empty_like(pristine) for _ in range(steps)]
+        st = torch.cuda.current_stream(device).cuda_stream
+
+        def run(x):
+            rc = _lib.ce_fwd_nd(x.data_ptr(), _lib.CE_BF16, N, C, inner, t.data_ptr(), None, -100,
+                                0.0, 0.0, 0.0, _lib.CE_RED_MEAN, _lib.CE_FLAG_GRAD,
+                                loss.data_ptr(), None, None, None, st)
+            if rc != 0:
+                raise RuntimeError(f"ce_fwd_nd: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
+
+        for b in bufs[:3]:
+            b.copy_(pristine)
+            run(b)  # warm-up (plans, workspace)
+        for b in bufs:
+            b.copy_(pristine)
+        torch.cuda.synchronize(device)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for b in bufs:
+            run(b)
+        e1.record()
+        torch.cuda.synchronize(device)
+        barrier()
+        if _lib.ce_device_status(st) != 0:
+            raise RuntimeError("device status after the N-D steps")
+        sec = max_over_ranks(e0.elapsed_time(e1) / 1e3) / steps
+        by = 2 * 2 * pristine.numel()
+        out.append({"shape": list(shape), "us_per_step": round(sec * 1e6, 1),
+                    "GB/s": round(by / sec / 1e9, 1), "frac": round(by / sec / 1e9 / peak, 4)})
+        del bufs, pristine
+        torch.cuda.empty_cache()
     return out
 
 
