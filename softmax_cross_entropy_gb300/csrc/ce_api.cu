@@ -833,7 +833,8 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
             DeviceInfo info;
             ce_status rc2 = device_info(dev, &info);
             if (rc2 != CE_OK) return rc2;
-            const int64_t want = (c.rows + kCountThreads * 4 - 1) / (kCountThreads * 4);
+            constexpr int64_t kPerCta = int64_t{kCountThreads} * kCountPerThread;
+            const int64_t want = (c.rows + kPerCta - 1) / kPerCta;
             const int64_t cgrid = std::max<int64_t>(1, std::min<int64_t>(want, info.sm_count));
             rc2 = launch(count_kernel(), static_cast<int>(cgrid), kCountThreads, 0, 1, st, &ca);
             if (rc2 != CE_OK) return rc2;
@@ -964,7 +965,8 @@ extern "C" ce_status ce_count(const void* target, const float* weight, int64_t r
     a.ignore_index = ignore_index;
     a.counts = counts;
     a.scratch = scratch;
-    const int64_t want = (rows + kCountThreads * 16 - 1) / (kCountThreads * 16);
+    constexpr int64_t kPerCta = int64_t{kCountThreads} * kCountPerThread;
+    const int64_t want = (rows + kPerCta - 1) / kPerCta;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, info.sm_count));
     return launch(count_kernel(), static_cast<int>(grid), kCountThreads, 0, 1, st, &a);
 }
@@ -1420,7 +1422,8 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
         ca.ignore_index = ignore_index;
         ca.counts = scratch->counts;
         ca.scratch = scratch;
-        const int64_t want = (rows + kCountThreads * 16 - 1) / (kCountThreads * 16);
+        constexpr int64_t kPerCta = int64_t{kCountThreads} * kCountPerThread;
+        const int64_t want = (rows + kPerCta - 1) / kPerCta;
         const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, info.sm_count));
         rc = launch(count_kernel(), static_cast<int>(grid), kCountThreads, 0, 1, st, &ca);
         if (rc != CE_OK) return rc;

@@ -11,7 +11,9 @@ namespace {
 
 // Grid-stride over the rows; each CTA adds its rows in double, the CTAs'
 // sums go through the scratch's partial slots and the last CTA (atomic
-// ticket) adds them in slot order with a fixed lane split and butterfly.
+// ticket) adds them in slot order with a fixed lane split and butterfly; a
+// launch of one CTA (up to kCountThreads * kCountPerThread rows) writes its
+// sums directly.
 __global__ void __launch_bounds__(kCountThreads) ce_count_kernel(const __grid_constant__ CountArgs a) {
     constexpr int NW = kCountThreads / 32;
     // a forward launched after this one may start now; it waits for these
@@ -22,15 +24,27 @@ __global__ void __launch_bounds__(kCountThreads) ce_count_kernel(const __grid_co
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     double d = 0.0;
     long long n = 0;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kCountThreads;
-#pragma unroll 4
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kCountThreads + tid; i < a.rows;
-         i += stride) {
-        const int64_t t = a.tgt64 ? reinterpret_cast<const int64_t*>(a.target)[i]
-                                  : static_cast<int64_t>(reinterpret_cast<const int32_t*>(a.target)[i]);
-        if (t != a.ignore_index && t >= 0 && t < a.V) {
-            d += a.weight ? static_cast<double>(__ldg(a.weight + t)) : 1.0;
-            ++n;
+    // kCountPerThread targets a thread, all loaded before any is used (one
+    // memory round trip a block of them)
+    constexpr int PT = kCountPerThread;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kCountThreads * PT;
+#pragma unroll 1
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kCountThreads * PT; base < a.rows;
+         base += stride) {
+        int64_t t[PT];
+#pragma unroll
+        for (int j = 0; j < PT; ++j) {
+            const int64_t i = base + static_cast<int64_t>(j) * kCountThreads + tid;
+            t[j] = i >= a.rows ? a.ignore_index
+                   : a.tgt64   ? reinterpret_cast<const int64_t*>(a.target)[i]
+                               : static_cast<int64_t>(reinterpret_cast<const int32_t*>(a.target)[i]);
+        }
+#pragma unroll
+        for (int j = 0; j < PT; ++j) {
+            if (t[j] != a.ignore_index && t[j] >= 0 && t[j] < a.V) {
+                d += a.weight ? static_cast<double>(__ldg(a.weight + t[j])) : 1.0;
+                ++n;
+            }
         }
     }
 #pragma unroll
@@ -44,6 +58,19 @@ __global__ void __launch_bounds__(kCountThreads) ce_count_kernel(const __grid_co
     }
     __syncthreads();
     if (warp != 0) return;
+    if (gridDim.x == 1) {  // one CTA: its sums are the totals
+        if (lane == 0) {
+            double cd = 0.0;
+            long long cn = 0;
+            for (int w = 0; w < NW; ++w) {
+                cd += s_d[w];
+                cn += s_n[w];
+            }
+            a.counts[0] = cd;
+            a.counts[1] = static_cast<double>(cn);
+        }
+        return;
+    }
     Scratch* s = a.scratch;
     int last = 0;
     if (lane == 0) {

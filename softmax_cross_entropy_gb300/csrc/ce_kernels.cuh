@@ -554,6 +554,7 @@ constexpr int kLsmGenericThreads = 512;
 constexpr int kNllThreads = 256;
 constexpr int kLsmBwdThreads = 1024;
 constexpr int kCountThreads = 256;
+constexpr int kCountPerThread = 16;  // targets a count thread loads at once
 const void* bwd_kernel(int dtype);
 
 // N-D logits [N, C, inner] (class dimension 1). The forward kernel takes one

@@ -137,6 +137,16 @@ def test_gemm_layouts_and_outputs(monkeypatch, a_mn, b_mn, c_mode, M, N, K, dtyp
                            f"{tuple(np.argwhere(bad)[0])}: got {got[bad][0]} want {want[bad][0]}")
 
 
+@pytest.mark.parametrize("bm", ["128", "256"])
+@pytest.mark.parametrize("c_mode", [0, 1, 2])
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (1, 1)])
+def test_gemm_many_rounds(monkeypatch, bm, c_mode, a_mn, b_mn):
+    # 2048 x 8192 with a ragged K: 256 or 512 tiles, so each persistent CTA
+    # runs two to four tiles and the stage ring and the accumulator
+    # barriers wrap their phases several times
+    test_gemm_layouts_and_outputs(monkeypatch, a_mn, b_mn, c_mode, 2048, 8192, 72, "bf16", bm)
+
+
 def test_gemm_rejects_bad_operands():
     from softmax_cross_entropy_gb300 import _lib
     a = torch.zeros(16, 12, dtype=torch.bfloat16, device="cuda")
