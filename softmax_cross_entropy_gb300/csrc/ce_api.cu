@@ -1309,20 +1309,29 @@ ce_status nd_plan(int dev, const DeviceInfo& info, int dtype, int64_t C, bool ve
     return CE_OK;
 }
 
-// Occupancy (CTAs an SM) of a split N-D kernel with `smem` bytes of
-// dynamic shared memory (its limit set on the first call), computed once.
-int nd_split_occ(const void* fn, size_t smem) {
-    static std::map<const void*, int> occ;
-    auto it = occ.find(fn);
+// Occupancy (CTAs an SM) of an N-D kernel of 256 threads with `smem`
+// bytes of dynamic shared memory; the kernel's limit is raised to
+// `smem_max` on its first use. Computed once for each (kernel, smem).
+int nd_split_occ(const void* fn, size_t smem, size_t smem_max = 0) {
+    static std::map<std::pair<const void*, size_t>, int> occ;
+    static std::map<const void*, size_t> limit;
+    const auto key = std::make_pair(fn, smem);
+    auto it = occ.find(key);
     if (it != occ.end()) return it->second;
     int o = 0;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
+    cudaError_t e = cudaSuccess;
+    const size_t want = std::max(smem, smem_max);
+    if (limit[fn] < want) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(want));
+        if (e == cudaSuccess) limit[fn] = want;
+    }
+    if (e != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, kNdSplitThreads, smem) != cudaSuccess) {
         cudaGetLastError();
         o = 0;
     }
-    occ[fn] = o;
+    occ[key] = o;
     return o;
 }
 
@@ -1463,6 +1472,22 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     const int split_env = env_int("GBCE_ND_SPLIT", -1);
     const bool split = split_env == 1 || (split_env != 0 && env_int("GBCE_ND_MODE", 0) == 0 &&
                                           (!p.staged || tiles < 2 * info.sm_count));
+    // Few classes with vector positions and enough tiles: a warp a tile
+    // (no CTA barrier between its phases; GBCE_ND_WARP=0 turns it off, 2
+    // takes it whatever the tile count)
+    const int warp_env = env_int("GBCE_ND_WARP", 1);
+    if ((warp_env == 2 || (!split && warp_env == 1)) && vec_ok && C <= kNdWarpClasses &&
+        env_int("GBCE_ND_MODE", 0) == 0 && split_env != 1) {
+        const void* fn = nd_warp_kernel(dtype, sc, argmax);
+        if (!fn) return CE_ERR_INVALID_ARG;
+        const size_t smem = static_cast<size_t>(8) * C * 512;
+        const int occ = nd_split_occ(fn, smem, static_cast<size_t>(8) * kNdWarpClasses * 512);
+        if (occ >= 1) {
+            const int64_t grid = std::min<int64_t>((tiles + 7) / 8,
+                                                   std::min<int64_t>(occ * int64_t{info.sm_count}, kMaxUnits));
+            return launch(fn, static_cast<int>(grid), 256, smem, 1, st, &a);
+        }
+    }
     if (split) return nd_split_launch(dev, info, a, dtype, vec_ok, sc, argmax, st);
     const int64_t grid = std::min<int64_t>(tiles, std::min<int64_t>(p.max_ctas, kMaxUnits));
     return launch(p.fn, static_cast<int>(grid), kNdThreads, p.smem, 1, st, &a);

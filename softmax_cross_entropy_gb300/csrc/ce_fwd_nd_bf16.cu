@@ -9,6 +9,8 @@ const void* nd_kernel_bf16(bool vec, bool softcap, bool argmax) {
     return nd_kernel_of<__nv_bfloat16>(vec, softcap, argmax);
 }
 
+const void* nd_warp_bf16(bool softcap, bool argmax) { return nd_warp_of<__nv_bfloat16>(softcap, argmax); }
+
 NdSplitFns nd_split_bf16(bool vec, bool softcap, bool argmax, bool smooth) {
     return nd_split_of<__nv_bfloat16>(vec, softcap, argmax, smooth);
 }

@@ -9,6 +9,8 @@ const void* nd_kernel_f16(bool vec, bool softcap, bool argmax) {
     return nd_kernel_of<__half>(vec, softcap, argmax);
 }
 
+const void* nd_warp_f16(bool softcap, bool argmax) { return nd_warp_of<__half>(softcap, argmax); }
+
 NdSplitFns nd_split_f16(bool vec, bool softcap, bool argmax, bool smooth) {
     return nd_split_of<__half>(vec, softcap, argmax, smooth);
 }

@@ -9,6 +9,8 @@ const void* nd_kernel_f32(bool vec, bool softcap, bool argmax) {
     return nd_kernel_of<float>(vec, softcap, argmax);
 }
 
+const void* nd_warp_f32(bool softcap, bool argmax) { return nd_warp_of<float>(softcap, argmax); }
+
 NdSplitFns nd_split_f32(bool vec, bool softcap, bool argmax, bool smooth) {
     return nd_split_of<float>(vec, softcap, argmax, smooth);
 }

@@ -33,14 +33,12 @@ namespace gbce {
 
 constexpr int kNdSplitWarps = kNdSplitThreads / 32;
 
-// exp2 argument of z - m (m the running shift, mL = m log2 e): one FFMA
-// for 16-bit logits, the difference first for fp32 (as the 2-D kernels).
+// exp2 argument of z - m (m the shift): the difference first, so the
+// maximum's term is exp2(0) = 1 exactly (a position whose other classes
+// are all -inf then has loss 0 exactly, as the definition gives).
 template <typename T>
-__device__ __forceinline__ float nd_arg(float z, float m, float mL) {
-    if constexpr (sizeof(T) == 2)
-        return fmaf(z, kLog2e, -mL);
-    else
-        return (z - m) * kLog2e;
+__device__ __forceinline__ float nd_arg(float z, float m, float /*mL*/) {
+    return (z - m) * kLog2e;
 }
 
 // Statistics of one chunk of classes for the tile's positions: each warp
@@ -449,6 +447,224 @@ ce_nd_grad(const __grid_constant__ NdSplitArgs s) {
             }
         }
     }
+}
+
+// Few classes (C <= 48) and vector positions: a warp owns a
+// whole tile of 32 VP positions and all C classes. It copies the tile into
+// its own C x 512 bytes of shared memory (cp.async, each lane its 16 bytes
+// a class, read back only by that lane), then takes the maximum and first
+// argmax, the sums and the gradient from there: no CTA barrier and no
+// merge across warps, so the CTA's warps run their tiles independently
+// and hide each other's HBM latency. One read and one write an element.
+constexpr int kNdWarpMaxC = 48;  // 8 warps x 48 x 512 bytes: 192 KB a CTA
+constexpr int kNdWarpThreads = 256;
+template <typename T, bool SOFTCAP, bool ARGMAX>
+__global__ void __launch_bounds__(kNdWarpThreads)
+ce_nd_warp(const __grid_constant__ FwdArgs a) {
+    constexpr int VP = Vec<T>::N;
+    constexpr int P = 32 * VP;
+    constexpr int NW = kNdWarpThreads / 32;
+    using IO = NdIO<T, VP>;
+    extern __shared__ __align__(16) unsigned char nd_dyn[];
+    __shared__ double red_d[2 * NW];
+    __shared__ long long red_n[NW];
+    __shared__ int s_flag;
+    const int tid = threadIdx.x, lane = tid & 31, wy = tid >> 5;
+    const int C = static_cast<int>(a.V);
+    const int64_t inner = a.inner;
+    const bool smooth = a.eps > 0.f;
+    const bool wsmooth = smooth && a.weight != nullptr;
+    // this lane's 16-byte slot of class c: tile + (c * 32 + lane) * 16
+    const uint32_t tile = smem_u32(nd_dyn) + static_cast<uint32_t>(wy * C * 32 + lane) * 16u;
+    const uint4* tl = reinterpret_cast<const uint4*>(nd_dyn) + wy * C * 32 + lane;
+    float D = 0.f;
+    int n_valid = 0;
+    if (a.reduction != kRedNone) {
+        D = static_cast<float>(a.batch_counts[0]);
+        n_valid = static_cast<int>(a.batch_counts[1]);
+    }
+    float Wsum = static_cast<float>(C);
+    if (wsmooth) {
+        // W = sum of the class weights, the same order in every thread
+        float w = 0.f;
+        for (int c = 0; c < C; ++c) w += __ldg(a.weight + c);
+        Wsum = w;
+    }
+    const float inv_C = 1.f / static_cast<float>(C);
+    const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;
+    const float Wf = wsmooth ? Wsum * inv_C : 1.f;
+    double accL = 0.0, accZ = 0.0;
+    long long accC = 0;
+    const int64_t ntiles = (a.rows + P - 1) / P;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * NW;
+#pragma unroll 1
+    for (int64_t ti = static_cast<int64_t>(blockIdx.x) * NW + wy; ti < ntiles; ti += nwarps) {
+        const int64_t rl = ti * P + static_cast<int64_t>(lane) * VP;
+        const bool lane_ok = rl < a.rows;  // VP divides inner, hence rows
+        int64_t lb = 0;
+        if (lane_ok) {
+            const int64_t n = rl / inner;
+            lb = n * C * inner + (rl - n * inner);
+            for (int c = 0; c < C; ++c)
+                cp_async16(tile + static_cast<uint32_t>(c * 32) * 16u,
+                           static_cast<const T*>(a.x) + lb + static_cast<int64_t>(c) * inner);
+        }
+        cp_async_commit();
+        int tv[VP];
+#pragma unroll
+        for (int v = 0; v < VP; ++v) {
+            int t = -1;
+            if (lane_ok) {
+                const int64_t tt = load_target(a, rl + v);
+                if (row_counts(a, tt))
+                    t = static_cast<int>(tt);
+                else if (tt != a.ignore_index)
+                    atomicOr(&a.scratch->status, kDevErrTarget);
+            }
+            tv[v] = t;
+        }
+        cp_async_wait<0>();
+        // ---- maximum of z and first argmax of x
+        float m[VP], xm[VP];
+        int xi[VP];
+#pragma unroll
+        for (int v = 0; v < VP; ++v) {
+            m[v] = -INFINITY;
+            xm[v] = -INFINITY;
+            xi[v] = -1;
+        }
+#pragma unroll 1
+        for (int c = 0; c < C; ++c) {
+            float f[VP];
+            IO::unpack(tl[c * 32], f);
+#pragma unroll
+            for (int v = 0; v < VP; ++v) {
+                if (ARGMAX && f[v] > xm[v]) {  // classes in increasing order
+                    xm[v] = f[v];
+                    xi[v] = c;
+                }
+                const float z = SOFTCAP ? a.softcap * tanh_from_scaled(f[v] * a.sc_k2) : f[v];
+                m[v] = fmaxf(m[v], z);
+            }
+        }
+        // ---- S = sum exp(z - M), SZ = sum w (z - M), z at the target
+        float S[VP], SZ[VP], zt[VP], sh[VP], shL[VP];
+#pragma unroll
+        for (int v = 0; v < VP; ++v) {
+            sh[v] = m[v] == -INFINITY ? 0.f : m[v];
+            shL[v] = sh[v] * kLog2e;
+            S[v] = 0.f;
+            SZ[v] = 0.f;
+            zt[v] = 0.f;
+        }
+#pragma unroll 1
+        for (int c = 0; c < C; ++c) {
+            float f[VP];
+            IO::unpack(tl[c * 32], f);
+            const float wc = wsmooth ? __ldg(a.weight + c) : 1.f;
+#pragma unroll
+            for (int v = 0; v < VP; ++v) {
+                const float z = SOFTCAP ? a.softcap * tanh_from_scaled(f[v] * a.sc_k2) : f[v];
+                S[v] += ex2(nd_arg<T>(z, sh[v], shL[v]));
+                if (smooth) SZ[v] = fmaf(wc, z - sh[v], SZ[v]);
+                if (c == tv[v]) zt[v] = z;
+            }
+        }
+        // ---- per-position outputs and the gradient's coefficients
+        float ac[VP], bc[VP], tf[VP];
+#pragma unroll
+        for (int v = 0; v < VP; ++v) {
+            ac[v] = bc[v] = tf[v] = 0.f;
+            if (!lane_ok) continue;
+            const int64_t r = rl + v;
+            if (tv[v] >= 0) {
+                const float wt = a.weight ? __ldg(a.weight + tv[v]) : 1.f;
+                const float logS = logf(S[v]);
+                float zl;
+                const float l = row_loss(a, sh[v], logS, zt[v], wt, Wsum, SZ[v], zl);
+                const bool correct = xi[v] == tv[v];
+                if (a.reduction == kRedNone) {
+                    a.loss[r] = l;
+                    if (a.want_z) a.zloss[r] = zl;
+                    if (a.want_acc) a.acc[r] = correct ? 1.f : 0.f;
+                } else {
+                    accL += static_cast<double>(l);
+                    accZ += static_cast<double>(zl);
+                    accC += correct ? 1 : 0;
+                }
+                if (a.want_pred) a.pred[r] = xi[v];
+                const float lse = sh[v] + logS;
+                ac[v] = scale * ((1.f - a.eps) * wt + a.eps * Wf + 2.f * a.lam * lse) / S[v];
+                bc[v] = -scale * a.eps * inv_C;
+                tf[v] = -scale * (1.f - a.eps) * wt;
+            } else {
+                if (a.reduction == kRedNone) {
+                    a.loss[r] = 0.f;
+                    if (a.want_z) a.zloss[r] = 0.f;
+                    if (a.want_acc) a.acc[r] = 0.f;
+                }
+                if (a.want_pred) a.pred[r] = -1;
+            }
+        }
+        // ---- the gradient in place
+        if (a.grad && lane_ok) {
+#pragma unroll 1
+            for (int c = 0; c < C; ++c) {
+                float f[VP];
+                IO::unpack(tl[c * 32], f);
+                const float wc = wsmooth ? __ldg(a.weight + c) : 1.f;
+#pragma unroll
+                for (int v = 0; v < VP; ++v) {
+                    float g, th = 0.f, z;
+                    if (SOFTCAP) {
+                        th = tanh_from_scaled(f[v] * a.sc_k2);
+                        z = th * a.softcap;
+                    } else {
+                        z = f[v];
+                    }
+                    g = fmaf(ac[v], ex2(nd_arg<T>(z, sh[v], shL[v])), bc[v] * wc);
+                    if (c == tv[v]) g += tf[v];
+                    if (SOFTCAP) g *= fmaf(-th, th, 1.f);
+                    f[v] = tv[v] >= 0 ? g : 0.f;  // exact zeros where a position does not count
+                }
+                IO::store(a.x, lb + static_cast<int64_t>(c) * inner, IO::pack(f));
+            }
+        }
+        __syncwarp();  // every lane done with the tile before the next copies
+    }
+    if (a.reduction != kRedNone) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            accL += __shfl_xor_sync(0xffffffffu, accL, o);
+            accZ += __shfl_xor_sync(0xffffffffu, accZ, o);
+            accC += __shfl_xor_sync(0xffffffffu, accC, o);
+        }
+        if (lane == 0) {
+            red_d[wy] = accL;
+            red_d[NW + wy] = accZ;
+            red_n[wy] = accC;
+        }
+        __syncthreads();
+        double L = 0.0, Z = 0.0;
+        long long Cn = 0;
+        if (tid == 0) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                L += red_d[w];
+                Z += red_d[NW + w];
+                Cn += red_n[w];
+            }
+        }
+        __syncthreads();  // red_d is the epilogue's scratch next
+        finish_scalars_cta(a, L, Z, Cn, D, n_valid, &s_flag, red_d, red_d + NW, red_n);
+    }
+}
+
+template <typename T>
+const void* nd_warp_of(bool softcap, bool argmax) {
+    if (softcap)
+        return argmax ? (const void*)&ce_nd_warp<T, true, true> : (const void*)&ce_nd_warp<T, true, false>;
+    return argmax ? (const void*)&ce_nd_warp<T, false, true> : (const void*)&ce_nd_warp<T, false, false>;
 }
 
 // Entry points of one logit type by (vector positions, softcap, argmax).

@@ -288,6 +288,17 @@ const void* nd_kernel(int dtype, bool vec, bool softcap, bool argmax) {
     return nullptr;
 }
 
+const void* nd_warp_f32(bool softcap, bool argmax);
+const void* nd_warp_bf16(bool softcap, bool argmax);
+const void* nd_warp_f16(bool softcap, bool argmax);
+
+const void* nd_warp_kernel(int dtype, bool softcap, bool argmax) {
+    if (dtype == 0) return nd_warp_f32(softcap, argmax);
+    if (dtype == 1) return nd_warp_bf16(softcap, argmax);
+    if (dtype == 2) return nd_warp_f16(softcap, argmax);
+    return nullptr;
+}
+
 NdSplitFns nd_split_f32(bool vec, bool softcap, bool argmax, bool smooth);
 NdSplitFns nd_split_bf16(bool vec, bool softcap, bool argmax, bool smooth);
 NdSplitFns nd_split_f16(bool vec, bool softcap, bool argmax, bool smooth);

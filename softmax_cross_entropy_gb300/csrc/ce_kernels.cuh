@@ -601,6 +601,11 @@ struct NdSplitFns {
     size_t stats_smem;  // dynamic shared memory of a stats CTA
 };
 NdSplitFns nd_split_fns(int dtype, bool vec, bool softcap, bool argmax, bool smooth);
+// A warp a tile of 32 vectors of positions and all C <= kNdWarpClasses
+// classes (ce_fwd_nd_split.cuh): FwdArgs as the N-D kernel, 256 threads,
+// dynamic shared memory 8 * C * 512 bytes.
+constexpr int kNdWarpClasses = 48;
+const void* nd_warp_kernel(int dtype, bool softcap, bool argmax);
 
 struct NdBwdArgs {
     const float* g;  // one value, or one per position ([N, inner])

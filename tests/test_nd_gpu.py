@@ -229,6 +229,36 @@ def test_nd_split_large(monkeypatch):
     check(case, want_acc=True, want_pred=True)
 
 
+# A warp a tile (few classes, vector positions): forced with GBCE_ND_WARP=2
+# on small shapes (ragged last tile, several tiles a warp), and taken by
+# default on one with enough tiles.
+@pytest.mark.parametrize("opts", sorted(OPTION_SETS))
+@pytest.mark.parametrize("shape,dtype", [((3, 19, 8, 16), "bf16"), ((2, 48, 40, 24), "f32"),
+                                         ((4, 7, 1000), "f16"), ((1, 1, 64), "bf16"),
+                                         ((2, 21, 64), "bf16")])
+@pytest.mark.parametrize("reduction", ["mean", "none", "sum"])
+def test_nd_warp_per_tile(monkeypatch, opts, shape, dtype, reduction):
+    monkeypatch.setenv("GBCE_ND_WARP", "2")
+    case = workloads.nd_case(29 + sum(shape), shape, dtype, std=3.0, reduction=reduction,
+                             **dict(OPTION_SETS[opts]))
+    check(case, want_z=case.lse_square_scale > 0, want_acc=True, want_pred=True)
+
+
+def test_nd_warp_per_tile_default_and_ties():
+    # 8 x 19 x 128 x 128 bf16: 512 tiles, the warp form by default; the top
+    # logit tied at classes 2, 9 and 18 of every position
+    case = workloads.nd_case(31, (8, 19, 128, 128), "bf16", std=3.0, reduction="mean",
+                             label_smoothing=0.1)
+    x = case.x.copy()
+    top = workloads.f32_to_bf16_bits(np.array([40.0], np.float32))[0]
+    for c in (2, 9, 18):
+        x[:, c] = top
+    case = case.with_(x=x)
+    out, _ = check(case, want_acc=True, want_pred=True)
+    valid = case.target != case.ignore_index
+    assert np.all(out["pred"][valid] == 2)
+
+
 def test_nd_inner_one_is_2d():
     case = workloads.nd_case(2, (33, 4096, 1), "bf16", reduction="sum")
     check(case, want_pred=True)
