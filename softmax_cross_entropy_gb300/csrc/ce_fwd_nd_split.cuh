@@ -327,8 +327,11 @@ ce_nd_merge(const __grid_constant__ NdSplitArgs s) {
             k.ac = scale * ((1.f - a.eps) * wt + a.eps * Wf + 2.f * a.lam * lse) / acc.S;
             k.bc = -scale * a.eps * inv_C;
             // the target's element: the one-hot term added
+            // the one-hot term added apart (no contraction into an FMA: with
+            // p_t = 1 the two cancel exactly)
             const float et = ex2((zt - shift) * kLog2e);
-            float gt = fmaf(k.ac, et, k.bc * (wsmooth ? wt : 1.f)) - scale * (1.f - a.eps) * wt;
+            const float tfix = -scale * (1.f - a.eps) * wt;
+            float gt = __fadd_rn(fmaf(k.ac, et, k.bc * (wsmooth ? wt : 1.f)), tfix);
             if (SOFTCAP) {
                 const float th = tanh_from_scaled(xt * a.sc_k2);
                 gt *= fmaf(-th, th, 1.f);
