@@ -247,3 +247,54 @@ def test_flce_with_cublas_gemms(monkeypatch, dtype, reduction):
     monkeypatch.setenv("GBCE_FLCE_GEMM", "cublas")
     h, w, t, b, cw = make_case(21, 300, 136, 5000, dtype, with_bias=True, class_weight=True)
     check(h, w, t, b, cw, dtype, reduction, 64, OPTS["smooth_z"])
+
+
+def test_flce_full_size_sampled_rows(monkeypatch):
+    """The bench's fused linear cross-entropy at full size, in its own launch
+    configuration (rows 4096, H 4096, V 128256 bf16, the default chunk):
+    reduction "none", so a row's loss, predicted token and grad_hidden row
+    depend on that row alone and the oracle computes 24 sampled rows one by
+    one, within the bounds of check(). grad_weight sums over every row, so
+    the oracle cannot sample it: it is compared element by element with the
+    same step on cuBLAS's GEMMs (GBCE_FLCE_GEMM=cublas), which consume the
+    same rounded gradient G_b; the two differ only in the order of fp32
+    accumulation over the 4096 rows, 2 rows 2^-23 (|G_b|^T |H|) an element
+    at most, which with random signs is about sqrt(rows) = 64 times |gw|:
+    3% relative. The test allows 2^-4 of |gw| plus 2^-2 of the column's
+    mean |gw| (a misplaced or transposed tile differs by the entries
+    themselves)."""
+    import oracle
+    rows, H, V = 4096, 4096, 128256
+    h, w, t, _, _ = make_case(4096, rows, H, V, "bf16", ignore_frac=0.05)
+    got = run_flce(h, w, t, None, None, "bf16", "none", 0, {})
+    rng = np.random.default_rng(4096)
+    sample = np.sort(rng.choice(rows, 24, replace=False))
+    ref = oracle.flce_forward(h[sample], w, t[sample], dtype="bf16", reduction="none",
+                              want_grad=False)
+    wa = np.abs(oracle.decode(w, "bf16"))
+    hv = oracle.decode(h[sample], "bf16")
+    delta = H * 2.0 ** -23 * (np.abs(hv) @ wa.T).max(axis=1)
+    counted = t[sample] != -100
+    bound = 4 * delta + 1e-4 * np.abs(ref["loss"]) + 1e-6
+    assert np.all(np.abs(got["loss"][sample] - ref["loss"]) <= bound), "row loss"
+    lg = ref["logits"]
+    top2 = np.sort(lg, axis=1)[:, -2:]
+    p = got["pred"][sample]
+    assert np.all(p[~counted] == -1)
+    idx = np.nonzero(counted)[0]
+    assert np.all(lg[idx, p[idx]] >= top2[idx, 1] - 2 * delta[idx])
+    clear = idx[(top2[idx, 1] - top2[idx, 0]) > 2 * delta[idx]]
+    assert np.array_equal(p[clear], ref["pred"][clear])
+    # grad_hidden rows: G (the oracle's, from these rows' float64 logits) @ W
+    G = oracle.forward(lg, t[sample], dtype="f64", reduction="none", want_grad=True)["grad"]
+    want = G @ oracle.decode(w, "bf16")
+    gbound = (U["bf16"] + 3 * delta[:, None] + V * 2.0 ** -23) * (np.abs(G) @ wa)
+    gbound += np.abs(want) * 2.0 ** -8 + 1e-6 * np.abs(G).max() * wa.sum(axis=0)
+    assert np.all(np.abs(got["grad_hidden"][sample] - want) <= gbound), "grad_hidden rows"
+    # grad_weight against the same step on cuBLAS's GEMMs
+    monkeypatch.setenv("GBCE_FLCE_GEMM", "cublas")
+    blas = run_flce(h, w, t, None, None, "bf16", "none", 0, {})
+    gw, gw_ref = got["grad_weight"], blas["grad_weight"]
+    assert np.all(np.isfinite(gw))
+    wbound = 2.0 ** -4 * np.abs(gw_ref) + 2.0 ** -2 * np.abs(gw_ref).mean(axis=0)[None, :]
+    assert np.all(np.abs(gw - gw_ref) <= wbound), "grad_weight against the cuBLAS GEMMs"
