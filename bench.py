@@ -297,6 +297,98 @@ class GpuRunner:
         if s != 0:
             raise RuntimeError(f"device status after warm-up: {self.lib.ce_status_string(s)}")
 
+    def e2e_pipelined(self, steps, barrier, nchunk=8, nbuf=3):
+        """Through the C ABI from pinned host memory, the copies overlapped:
+        per step the targets come in and ce_count forms the batch's mean
+        denominator; then for each of `nchunk` row chunks, on three
+        streams, the chunk's logits are copied in, ce_fwd_shard (the
+        gradient of the whole batch's mean) and ce_bwd run, and the
+        chunk's gradient is copied back, so that one chunk's copy in, the
+        previous one's compute and an earlier one's copy out run at the
+        same time (`nbuf` device chunk buffers in turn). The chunks' loss
+        shares come back at the end and add up to the batch loss."""
+        torch, L, c = self.torch, self.lib, self.case
+        rows, V = c.rows, c.V
+        cr = (rows + nchunk - 1) // nchunk
+        host_grad = torch.empty_like(self.host).pin_memory()
+        tdev = torch.empty_like(self.target)
+        counts = torch.zeros(2, dtype=torch.float64, device=self.dev)
+        bufs = [torch.empty((cr, V), dtype=self.pristine.dtype, device=self.dev)
+                for _ in range(nbuf)]
+        shares = torch.zeros(nchunk, dtype=torch.float32, device=self.dev)
+        out = torch.empty(nchunk, dtype=torch.float32).pin_memory()
+        s_in, s_cmp, s_out = torch.cuda.Stream(self.dev), self.stream, torch.cuda.Stream(self.dev)
+        ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_cmp = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_t = torch.cuda.Event()
+        tb = 4 if self.target.dtype == torch.int32 else 8
+        flags_t = L.CE_FLAG_TARGET_I64 if tb == 8 else 0
+
+        def chk(rc, what):
+            if rc != 0:
+                raise RuntimeError(f"{what}: {L.ce_status_string(rc)} {L.ce_last_error()}")
+
+        def step():
+            s_in.wait_stream(s_cmp)  # the previous step's shards have read the targets
+            with torch.cuda.stream(s_in):
+                tdev.copy_(self.host_t, non_blocking=True)
+                ev_t.record(s_in)
+            s_cmp.wait_event(ev_t)
+            chk(L.ce_count(tdev.data_ptr(), None if self.weight is None else self.weight.data_ptr(),
+                           rows, V, c.ignore_index, flags_t, counts.data_ptr(),
+                           s_cmp.cuda_stream), "ce_count")
+            for k in range(nchunk):
+                b = k % nbuf
+                r0, r1 = k * cr, min(rows, (k + 1) * cr)
+                n = r1 - r0
+                if n <= 0:
+                    break
+                s_in.wait_event(ev_out[b])  # the buffer's previous chunk has gone out
+                with torch.cuda.stream(s_in):
+                    bufs[b][:n].copy_(self.host[r0:r1], non_blocking=True)
+                    ev_in[b].record(s_in)
+                s_cmp.wait_event(ev_in[b])
+                x = bufs[b]
+                chk(L.ce_fwd_shard(x.data_ptr(), self.dtype, n, V, tdev.data_ptr() + r0 * tb,
+                                   None if self.weight is None else self.weight.data_ptr(),
+                                   c.ignore_index, c.label_smoothing, c.lse_square_scale,
+                                   c.softcap or 0.0, self.red, self.flags,
+                                   shares.data_ptr() + 4 * k, None, None, None,
+                                   counts.data_ptr(), s_cmp.cuda_stream), "ce_fwd_shard")
+                chk(L.ce_bwd(self.one.data_ptr(), 0, x.data_ptr(), self.dtype, n, V,
+                             s_cmp.cuda_stream), "ce_bwd")
+                ev_cmp[b].record(s_cmp)
+                s_out.wait_event(ev_cmp[b])
+                with torch.cuda.stream(s_out):
+                    host_grad[r0:r1].copy_(bufs[b][:n], non_blocking=True)
+                    ev_out[b].record(s_out)
+            s_out.wait_stream(s_cmp)
+            with torch.cuda.stream(s_out):
+                out.copy_(shares, non_blocking=True)
+
+        if self.red == 0:
+            raise ValueError("the pipelined end-to-end step takes 'sum' or 'mean'")
+        step()  # warm-up (plans, scratch of the streams)
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        s_cmp.wait_stream(s_in)
+        s_out.wait_stream(s_in)
+        for _ in range(steps):
+            step()
+        s_in.wait_stream(s_out)
+        s_in.wait_stream(s_cmp)
+        e1.record(s_in)
+        torch.cuda.synchronize(self.dev)
+        barrier()
+        loss = float(out.sum())  # the batch loss from the chunks' shares
+        h2d = self.host.numel() * self.elem + self.host_t.numel() * tb
+        d2h = 4 * nchunk + self.host.numel() * self.elem
+        return e0.elapsed_time(e1) / 1e3, h2d, d2h, loss
+
     def e2e(self, steps, barrier, read_grad=True):
         """Through the C ABI from pinned host memory: per step, copy the
         logits and targets in, run forward + backward, read the loss back
@@ -380,8 +472,14 @@ def run_gpu(args):
     runner.flags &= ~runner.lib.CE_FLAG_GRAD
     t_fo = max_over_ranks(runner.time_steps(K, lambda b, st: runner.fwd(b, st), barrier))
     runner.flags |= runner.lib.CE_FLAG_GRAD
-    t_e2e, h2d, d2h = runner.e2e(K, barrier)
+    t_e2e_seq, h2d_s, d2h_s = runner.e2e(K, barrier)
+    t_e2e_seq = max_over_ranks(t_e2e_seq)
+    loss_seq = float(runner.loss[0])
+    t_e2e, h2d, d2h, loss_pipe = runner.e2e_pipelined(K, barrier)
     t_e2e = max_over_ranks(t_e2e)
+    # the chunks' shares add up to the whole-batch loss of the one-call path
+    if not abs(loss_pipe - loss_seq) <= 1e-5 * abs(loss_seq) + 1e-6:
+        raise RuntimeError(f"pipelined end-to-end loss {loss_pipe} != {loss_seq}")
     t_e2e_loss, h2d_l, d2h_l = runner.e2e(K, barrier, read_grad=False)
     t_e2e_loss = max_over_ranks(t_e2e_loss)
 
@@ -416,8 +514,16 @@ def run_gpu(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(t_e2e / K * 1e3, 4),
                 "what": "per step: logits and targets copied in from pinned host memory, "
-                        "ce_fwd + ce_bwd through the C ABI, loss and the whole gradient "
-                        "copied back to pinned host memory"},
+                        "the whole gradient and the loss copied back to pinned host memory, "
+                        "through the C ABI (ce_count for the batch's mean denominator, then "
+                        "ce_fwd_shard + ce_bwd on 8 row chunks), each chunk's copy in, "
+                        "compute and copy out on three streams so that they overlap"},
+        "e2e_sequential": {"value": round(world * bytes_step * K / t_e2e_seq / 1e9, 1),
+                           "unit": "GB/s", "h2d_bytes_per_step": h2d_s,
+                           "d2h_bytes_per_step": d2h_s,
+                           "ms_per_step": round(t_e2e_seq / K * 1e3, 4),
+                           "what": "the same with one stream: copy in, ce_fwd + ce_bwd, "
+                                   "copy out, one after the other"},
         "e2e_loss_only": {"value": round(world * bytes_step * K / t_e2e_loss / 1e9, 1),
                           "unit": "GB/s", "h2d_bytes_per_step": h2d_l,
                           "d2h_bytes_per_step": d2h_l,
