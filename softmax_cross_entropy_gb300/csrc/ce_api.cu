@@ -773,6 +773,8 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
     a.timeout_ns = static_cast<uint64_t>(env_int("GBCE_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
     a.scratch = scratch;
     a.batch_counts = c.batch_counts;
+    a.gout = c.gout;
+    a.gout_bf16 = c.gout_dtype == CE_BF16 ? 1 : 0;
     // test hook: the streaming and register kernels leave one copy out, so
     // one bounded wait runs out (GBCE_TEST_STALL_COPY=1)
     a.test_stall = env_int("GBCE_TEST_STALL_COPY", 0) != 0 ? 1 : 0;
@@ -785,6 +787,32 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
         make_plan(dev, c.dtype, c.V, sc, sc && c.softcap <= kTmMaxSoftcap, wsmooth, aligned,
                   w_aligned, &p);
     if (rc != CE_OK) return rc;
+    // a separate 16-bit gradient: fp32 logits on the streaming kernel only
+    // (nothing launched otherwise; the caller takes the in-place path)
+    const void* gout_fn = nullptr;
+    if (c.gout) {
+        if (c.dtype != CE_F32 || p.kind != Kind::Stream || wsmooth || !(c.flags & CE_FLAG_GRAD) ||
+            (reinterpret_cast<uintptr_t>(c.gout) & 7u) ||
+            (c.gout_dtype != CE_BF16 && c.gout_dtype != CE_F16))
+            return CE_ERR_UNSUPPORTED;
+        const int nw = p.nt / 32 - 1;
+        gout_fn = stream_kernel_gout(sc, nw == 8 ? 8 : 4, nw);
+        if (!gout_fn) return CE_ERR_UNSUPPORTED;
+        static std::map<const void*, bool> ready;  // its shared-memory limit set
+        if (!ready[gout_fn]) {
+            DeviceInfo di;
+            rc = device_info(dev, &di);
+            if (rc != CE_OK) return rc;
+            cudaFuncAttributes fa;
+            cudaError_t e = cudaFuncGetAttributes(&fa, gout_fn);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(
+                    gout_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                    static_cast<int>(static_cast<size_t>(di.smem_optin) - fa.sharedSizeBytes));
+            if (e != cudaSuccess) return cuda_failure(e, "stream kernel attributes");
+            ready[gout_fn] = true;
+        }
+    }
     const int64_t units = c.rows == 0 ? 1 : std::min<int64_t>(c.rows, p.max_units);
     // the register kernel's clusters: a partial-sum slot for each CTA
     const int64_t slots =
@@ -810,7 +838,7 @@ ce_status run_fwd(int dev, const FwdCall& c, Scratch* scratch, int64_t max_slots
         a.chunk_vec = p.chunk_vec;
         a.nchunk = p.nchunk;
         a.resident = p.resident;
-        return launch(p.fn, static_cast<int>(units), p.nt, p.smem, 1, st, &a);
+        return launch(gout_fn ? gout_fn : p.fn, static_cast<int>(units), p.nt, p.smem, 1, st, &a);
     }
     if (p.kind == Kind::Reg) {
         bool pdl = false;
@@ -878,6 +906,19 @@ ce_status fwd_library_scratch(const FwdCall& c, ce_stream_t stream) {
 }
 
 }  // namespace
+
+// A shard's forward (ce_fwd_shard) whose gradient goes to gout in bf16 or
+// fp16 (gout_dtype) while the fp32 logits stay as they were: the fused
+// linear cross-entropy's G without a separate rounding pass.
+// CE_ERR_UNSUPPORTED, with nothing launched, when the plan is not the
+// streaming kernel.
+ce_status fwd_shard_gout(const FwdCall& c, void* gout, int gout_dtype, ce_stream_t stream) {
+    if (!c.batch_counts || !gout) return CE_ERR_INVALID_ARG;
+    FwdCall g = c;
+    g.gout = gout;
+    g.gout_dtype = gout_dtype;
+    return fwd_library_scratch(g, stream);
+}
 
 // The forward call with scratch that the caller provides (the static-scratch
 // entry point in ce_noalloc.cu): same checks, plan and launch as ce_fwd, the

@@ -46,6 +46,7 @@ ce_status tc_gemm_launch(const void* A, bool a_mn, const void* B, bool b_mn, int
                          int64_t N, int64_t K, void* C, int out, const float* bias,
                          unsigned* status, unsigned* abort, cudaStream_t st);
 bool tc_operand_ok(const void* p, int dtype, int64_t row_elems);
+ce_status fwd_shard_gout(const FwdCall& c, void* gout, int gout_dtype, ce_stream_t stream);
 
 namespace {
 
@@ -282,19 +283,35 @@ extern "C" ce_status ce_flce(const void* hidden, const void* lm_weight, const fl
                             "logits GEMM");
             if (rc != CE_OK) return rc;
         }
-        // 2. the fused forward over the chunk (one shard of the batch)
+        // 2. the fused forward over the chunk (one shard of the batch); with
+        // the tensor-core GEMMs and no grad_bias (which sums the fp32
+        // gradient) it writes G in the storage type directly, when its plan
+        // allows (the streaming kernel), saving the rounding pass's read
+        // and write of the fp32 gradient
         const bool none = reduction == CE_RED_NONE;
-        rc = ce_fwd_shard(logits, CE_F32, c, V, static_cast<const char*>(target) + r0 * tbytes,
-                          class_weight, ignore_index, label_smoothing, lse_square_scale, softcap,
-                          reduction, flags, none ? loss + r0 : parts + 3 * k,
-                          (flags & CE_FLAG_Z_LOSS) ? (none ? z_loss + r0 : parts + 3 * k + 1)
-                                                   : nullptr,
-                          (flags & CE_FLAG_ACC) ? (none ? acc + r0 : parts + 3 * k + 2) : nullptr,
-                          pred ? pred + r0 : nullptr, counts, stream);
-        if (rc != CE_OK) return rc;
+        const FwdCall fc{logits, CE_F32, c, V, static_cast<const char*>(target) + r0 * tbytes,
+                         class_weight, ignore_index, label_smoothing, lse_square_scale, softcap,
+                         reduction, flags, none ? loss + r0 : parts + 3 * k,
+                         (flags & CE_FLAG_Z_LOSS) ? (none ? z_loss + r0 : parts + 3 * k + 1)
+                                                  : nullptr,
+                         (flags & CE_FLAG_ACC) ? (none ? acc + r0 : parts + 3 * k + 2) : nullptr,
+                         pred ? pred + r0 : nullptr, counts};
+        bool g_done = false;
+        if (grad && use_tc && dtype != CE_F32 && !grad_bias &&
+            std::getenv("GBCE_FLCE_GOUT") == nullptr) {
+            rc = fwd_shard_gout(fc, gbuf, dtype, stream);
+            if (rc == CE_OK) g_done = true;
+            else if (rc != CE_ERR_UNSUPPORTED) return rc;
+        }
+        if (!g_done) {
+            rc = ce_fwd_shard(fc.logits, CE_F32, c, V, fc.target, class_weight, ignore_index,
+                              label_smoothing, lse_square_scale, softcap, reduction, flags,
+                              fc.loss, fc.z_loss, fc.acc, fc.pred, counts, stream);
+            if (rc != CE_OK) return rc;
+        }
         if (!grad) continue;
-        // 3. G in the storage type
-        if (dtype != CE_F32) {
+        // 3. G in the storage type (unless the forward wrote it)
+        if (dtype != CE_F32 && !g_done) {
             const int grid = static_cast<int>(std::min<int64_t>((c * V / 8 + 255) / 256 + 1, 8L * sms));
             if (dtype == CE_BF16)
                 flce_round<__nv_bfloat16><<<grid, kFlceThreads, 0, st>>>(

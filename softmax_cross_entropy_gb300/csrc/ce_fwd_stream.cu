@@ -21,4 +21,16 @@ const void* stream_kernel(int dtype, bool softcap, int vpt, int nw) {
     return nullptr;
 }
 
+// fp32 logits with the gradient to FwdArgs::gout in 16 bits, the same two
+// shapes.
+const void* stream_kernel_gout(bool softcap, int vpt, int nw) {
+#define GBCE_STREAM_GO(SC)                                                                 \
+    (nw == 8 && vpt == 8                                                                   \
+         ? (const void*)&ce_fwd_stream<float, SC, 8, 8, false, false, true>                \
+         : (nw == 16 && vpt == 4 ? (const void*)&ce_fwd_stream<float, SC, 4, 16, false, false, true> \
+                                 : nullptr))
+    return softcap ? GBCE_STREAM_GO(true) : GBCE_STREAM_GO(false);
+#undef GBCE_STREAM_GO
+}
+
 }  // namespace gbce

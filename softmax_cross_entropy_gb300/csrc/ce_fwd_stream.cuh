@@ -230,11 +230,28 @@ __device__ __forceinline__ RowSums warp_merge(float m, float S, float SZ, float 
 // With WS the constant term is Bc * w_k (class weights from shared memory;
 // vg0 is the row vector index of the thread's first vector of the slot).
 // spol: the L2 policy of the stores.
+// Four fp32 gradient values as four bf16 or fp16 (gout of FwdArgs).
+__device__ __forceinline__ uint2 pack4_16(const float (&g)[4], int bf16) {
+    uint2 o;
+    if (bf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(g[0], g[1]);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(g[2], g[3]);
+        o.x = *reinterpret_cast<const uint32_t*>(&lo);
+        o.y = *reinterpret_cast<const uint32_t*>(&hi);
+    } else {
+        const __half2 lo = __floats2half2_rn(g[0], g[1]);
+        const __half2 hi = __floats2half2_rn(g[2], g[3]);
+        o.x = *reinterpret_cast<const uint32_t*>(&lo);
+        o.y = *reinterpret_cast<const uint32_t*>(&hi);
+    }
+    return o;
+}
+
 template <typename T, bool SOFTCAP, int VPT, bool FULL, bool WS>
 __device__ __forceinline__ void grad_chunk(const uint4* ch, uint4* outv, int tg, int nv, int GT,
                                            float M, float ML, float As, float Bc,
                                            const FwdArgs& a, const float4* w4, int vrow,
-                                           int vg0, uint64_t spol) {
+                                           int vg0, uint64_t spol, uint2* gov) {
     using VT = Vec<T>;
     constexpr int VE = VT::N;
     // softcap (softcap_r2): exp2 argument c1 r + c0, constants times 4
@@ -270,6 +287,13 @@ __device__ __forceinline__ void grad_chunk(const uint4* ch, uint4* outv, int tg,
                 }
                 gr[j] = g.x;
                 gr[j + 1] = g.y;
+            }
+            if constexpr (VE == 4) {
+                if (gov) {  // 16-bit gradient output beside fp32 logits
+                    const float g4[4] = {gr[0], gr[1], gr[2], gr[3]};
+                    gov[k * GT] = pack4_16(g4, a.gout_bf16);
+                    continue;
+                }
             }
             st_v4_hint(outv + k * GT, VT::pack(gr), spol);
         }
@@ -330,7 +354,9 @@ struct RingPos {
 // LSM: the log-softmax of every row (the unfused _log_softmax), written to
 // a.out: no targets are read, no loss is formed, and pass 2 stores
 // (x - M) - log S instead of the gradient.
-template <typename T, bool SOFTCAP, int VPT, int NW, bool WS, bool LSM = false>
+// GO: fp32 logits whose gradient goes to a.gout in 16 bits (FwdArgs::gout);
+// a variant of its own, so that the plain kernels carry none of it.
+template <typename T, bool SOFTCAP, int VPT, int NW, bool WS, bool LSM = false, bool GO = false>
 __global__ void __launch_bounds__(32 * (NW + 1), 1)
 ce_fwd_stream(const __grid_constant__ FwdArgs a) {
     using VT = Vec<T>;
@@ -543,13 +569,21 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
             const bool counts = LSM || row_counts(a, t);
             T* xrow = reinterpret_cast<T*>(a.x) + r * a.V;
             uint4* rowv = reinterpret_cast<uint4*>(xrow);
+            // the 16-bit gradient's row (fp32 logits with gout only)
+            uint2* gorow = (GO && sizeof(T) == 4)
+                               ? reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.gout) + r * a.V)
+                               : nullptr;
             if (!LSM && gleader && t != a.ignore_index && !counts)
                 atomicOr(&a.scratch->status, kDevErrTarget);
             if (!counts) {
                 // Ignored row: exact +0 gradient, zero per-row outputs, pred -1.
                 if (a.grad)
-                    for (int v = tg; v < vrow; v += GT)
-                        st_v4_hint(rowv + v, make_uint4(0u, 0u, 0u, 0u), spol);
+                    for (int v = tg; v < vrow; v += GT) {
+                        if (gorow)
+                            gorow[v] = make_uint2(0u, 0u);
+                        else
+                            st_v4_hint(rowv + v, make_uint4(0u, 0u, 0u, 0u), spol);
+                    }
                 if (gleader) {
                     if (a.reduction == kRedNone) {
                         a.loss[r] = 0.f;
@@ -663,12 +697,15 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                             lsm_chunk<T, VPT, false>(ch, ov, tg, nv, GT, M, logS);
                     }
                 } else if (a.grad && !failed) {
+                    uint2* gov = gorow ? gorow + v0 + tg : nullptr;
                     if (nv == VPT * GT)
                         grad_chunk<T, SOFTCAP, VPT, true, WS>(ch, rowv + v0 + tg, tg, nv, GT, M,
-                                                              ML, As, Bc, a, w4, vrow_w, v0 + tg, spol);
+                                                              ML, As, Bc, a, w4, vrow_w, v0 + tg, spol,
+                                                              gov);
                     else
                         grad_chunk<T, SOFTCAP, VPT, false, WS>(ch, rowv + v0 + tg, tg, nv, GT, M,
-                                                               ML, As, Bc, a, w4, vrow_w, v0 + tg, spol);
+                                                               ML, As, Bc, a, w4, vrow_w, v0 + tg, spol,
+                                                               gov);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
@@ -684,7 +721,15 @@ ce_fwd_stream(const __grid_constant__ FwdArgs a) {
                     e = ex2((xt - M) * kLog2e);
                 }
                 const float gt = (fmaf(As, e, WS ? Bc * wt : Bc) - scale * (1.f - a.eps) * wt) * fac;
-                VT::store1(xrow, t, gt);
+                if (gorow) {
+                    uint16_t* go = reinterpret_cast<uint16_t*>(gorow);
+                    if (a.gout_bf16)
+                        go[t] = __bfloat16_as_ushort(__float2bfloat16_rn(gt));
+                    else
+                        go[t] = __half_as_ushort(__float2half_rn(gt));
+                } else {
+                    VT::store1(xrow, t, gt);
+                }
             }
         }
         if (gleader) {

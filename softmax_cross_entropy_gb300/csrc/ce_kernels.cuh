@@ -67,6 +67,11 @@ struct FwdArgs {
     uint64_t timeout_ns;
     Scratch* scratch;
     void* out;  // log-softmax mode: [rows, V] output (may equal x)
+    // fp32 logits, streaming kernel: the gradient goes to gout [rows, V] as
+    // bf16 (gout_bf16 = 1) or fp16, rounded once, and the logits stay as
+    // they were (the fused linear cross-entropy's G); nullptr: in place
+    void* gout;
+    int gout_bf16;
     // {D, n_valid} of the whole batch when this call is one shard of it
     // (the mean scale and the accuracy use them instead of this call's own
     // counts), or nullptr
@@ -103,6 +108,8 @@ struct FwdCall {
     float* acc;
     int64_t* pred;
     const double* batch_counts;
+    void* gout = nullptr;  // FwdArgs::gout (internal callers only)
+    int gout_dtype = 0;    // CE_BF16 or CE_F16 with gout
 };
 
 // Arguments of the unfused (aten-shaped) kernels.
@@ -517,6 +524,8 @@ const void* staged_kernel_f32_softcap_plain(int cfg);
 const void* staged_kernel_f32_softcap_wsmooth(int cfg);
 const void* stream_kernel(int dtype, bool softcap, int vpt, int nw);
 const void* stream_kernel_f16(bool softcap, int vpt, int nw);
+// fp32 logits, gradient to FwdArgs::gout (16-bit), the same shapes
+const void* stream_kernel_gout(bool softcap, int vpt, int nw);
 // class weights with label smoothing: 8 consumer warps, 8 vectors a thread
 const void* stream_kernel_ws(int dtype, bool softcap);
 constexpr int kStreamMaxSlots = 48;   // ring slots (all groups) of the streaming kernel
