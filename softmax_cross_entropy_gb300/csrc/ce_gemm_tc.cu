@@ -1,6 +1,9 @@
-// Tensor-core GEMMs of the fused linear cross-entropy on the fifth-
-// generation tensor cores: C[M, N] = A[M, K] @ B[K, N] with A and B bf16 or
-// fp16, each operand stored either K-major (rows of K contiguous elements:
+// Tensor-core GEMMs of the fused linear cross-entropy (the Liger-Kernel
+// cross-entropy kernel profile, §Classification: the closest existing
+// kernel is the fused linear cross-entropy, whose logits are hidden @
+// lm_head^T) on the fifth-generation tensor cores: C[M, N] = A[M, K] @
+// B[K, N] with A and B bf16 or fp16, each operand stored either K-major
+// (rows of K contiguous elements:
 // A as [M, K], B as [N, K]) or MN-major (A as [K, M], B as [K, N]); C fp32
 // written, fp32 added to, or rounded to the operand type (+ bias[N] for the
 // fp32 store). The three GEMMs of ce_flce are the three layouts: logits =
