@@ -143,6 +143,90 @@ struct TmRing {
 
 }  // namespace
 
+// The end of a CTA of the tensor-memory kernel: copies that may still be
+// in flight after a timed-out wait land, the TMEM columns are freed, and no
+// CTA leaves while another CTA of the cluster may still store into it.
+__device__ __forceinline__ void tm_teardown(const FwdArgs& a, uint32_t tmem, const int& s_failed,
+                                            const uint32_t* s_issued, uint64_t* full_bar, int sg,
+                                            int tid, int warp) {
+    __syncthreads();
+    if (s_failed && tid == kTmWarps * 32) {
+        for (int i = 0; i < sg; ++i) {
+            const uint32_t used = s_issued[i];
+            if (used) (void)mbar_wait_bounded(smem_u32(&full_bar[i]), used & 1u, a.timeout_ns);
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmCols)
+                     : "memory");
+    cluster_sync();
+}
+
+// The producer warp: its lanes read the targets of the cluster's next 32
+// rows; lane 0 copies this CTA's slice of each counted row into the ring,
+// slot by slot (1-D bulk async copies, completion on the slot's full
+// barrier), after the consumers have released the slot.
+template <typename T>
+__device__ __forceinline__ void tm_produce(const FwdArgs& a, unsigned char* ring,
+                                           uint64_t* full_bar, uint64_t* empty_bar,
+                                           uint32_t* s_issued, int* s_failed, int sg, int nvec,
+                                           int nchunk, int64_t v0c, int64_t clid, int64_t ncl,
+                                           int lane) {
+    constexpr int VE = Vec<T>::N;
+    const uint64_t pol = l2_evict_first_policy();
+    TmRing pos;
+    int failed = 0;
+    bool stall = a.test_stall && blockIdx.x == 0;  // test hook (FwdArgs::test_stall)
+    for (int64_t rb = clid; rb < a.rows && !failed; rb += 32 * ncl) {
+        const int64_t rl = rb + lane * ncl;
+        const bool lane_counts = rl < a.rows && row_counts(a, load_target(a, rl));
+        const uint32_t counted = __ballot_sync(0xffffffffu, lane_counts);
+        if (lane == 0) {
+            for (int j = 0; j < 32 && !failed; ++j) {
+                const int64_t r = rb + j * ncl;
+                if (r >= a.rows) break;
+                if (!((counted >> j) & 1u)) continue;
+                for (int c = 0; c < nchunk; ++c) {
+                    const int slot = pos.slot;
+                    if (!mbar_wait_bounded(smem_u32(&empty_bar[slot]), pos.phase ^ 1u,
+                                           a.timeout_ns)) {
+                        failed = 1;
+                        break;
+                    }
+                    const uint32_t ph = pos.phase;
+                    pos.next(sg);
+                    if (stall) {
+                        stall = false;
+                        continue;
+                    }
+                    const int64_t cv0 = static_cast<int64_t>(c) * kTmChunkVec;
+                    const uint32_t bytes =
+                        static_cast<uint32_t>(min(static_cast<int64_t>(kTmChunkVec),
+                                                  static_cast<int64_t>(nvec) - cv0)) *
+                        16u;
+                    const uint32_t fb = smem_u32(&full_bar[slot]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    const char* src = reinterpret_cast<const char*>(a.x) +
+                                      (r * a.V + (v0c + cv0) * VE) *
+                                          static_cast<int64_t>(sizeof(T));
+                    const uint32_t dst = smem_u32(ring + static_cast<size_t>(slot) * kTmChunkVec * 16);
+                    for (uint32_t off = 0; off < bytes; off += 32768u)
+                        bulk_g2s(dst + off, src + off, min(32768u, bytes - off), fb, pol);
+                    s_issued[slot] = 2u + ph;
+                }
+            }
+        }
+        failed = __shfl_sync(0xffffffffu, failed, 0);
+    }
+    if (failed && lane == 0) {
+        atomicOr(&a.scratch->status, kDevErrTimeout);
+        *s_failed = 1;
+    }
+}
+
 // One CTA an SM: kTmWarps consumer warps and one producer warp. The grid is
 // persistent: cluster k handles rows k, k + n_clusters, ...; CTA c of a
 // cluster owns the row's vectors [c * a.tm_slice_vec, (c + 1) *
@@ -213,58 +297,8 @@ ce_fwd_tmem(const __grid_constant__ FwdArgs a) {
     const uint32_t tmem = tmem_base_sh;
 
     if (warp == kTmWarps) {
-        // ------------------------------------------------------------ producer
-        // Lanes read the targets of the cluster's next 32 rows; lane 0 copies
-        // this CTA's slice of each counted one, slot by slot.
-        const uint64_t pol = l2_evict_first_policy();
-        TmRing pos;
-        int failed = 0;
-        bool stall = a.test_stall && blockIdx.x == 0;  // test hook (FwdArgs::test_stall)
-        for (int64_t rb = clid; rb < a.rows && !failed; rb += 32 * ncl) {
-            const int64_t rl = rb + lane * ncl;
-            const bool lane_counts = rl < a.rows && row_counts(a, load_target(a, rl));
-            const uint32_t counted = __ballot_sync(0xffffffffu, lane_counts);
-            if (lane == 0) {
-                for (int j = 0; j < 32 && !failed; ++j) {
-                    const int64_t r = rb + j * ncl;
-                    if (r >= a.rows) break;
-                    if (!((counted >> j) & 1u)) continue;
-                    for (int c = 0; c < nchunk; ++c) {
-                        const int slot = pos.slot;
-                        if (!mbar_wait_bounded(smem_u32(&empty_bar[slot]), pos.phase ^ 1u,
-                                               a.timeout_ns)) {
-                            failed = 1;
-                            break;
-                        }
-                        const uint32_t ph = pos.phase;
-                        pos.next(sg);
-                        if (stall) {
-                            stall = false;
-                            continue;
-                        }
-                        const int64_t cv0 = static_cast<int64_t>(c) * kTmChunkVec;
-                        const uint32_t bytes =
-                            static_cast<uint32_t>(min(static_cast<int64_t>(kTmChunkVec),
-                                                      static_cast<int64_t>(nvec) - cv0)) *
-                            16u;
-                        const uint32_t fb = smem_u32(&full_bar[slot]);
-                        mbar_arrive_expect_tx(fb, bytes);
-                        const char* src = reinterpret_cast<const char*>(a.x) +
-                                          (r * a.V + (v0c + cv0) * VE) *
-                                              static_cast<int64_t>(sizeof(T));
-                        const uint32_t dst = smem_u32(ring + static_cast<size_t>(slot) * kTmChunkVec * 16);
-                        for (uint32_t off = 0; off < bytes; off += 32768u)
-                            bulk_g2s(dst + off, src + off, min(32768u, bytes - off), fb, pol);
-                        s_issued[slot] = 2u + ph;
-                    }
-                }
-            }
-            failed = __shfl_sync(0xffffffffu, failed, 0);
-        }
-        if (failed && lane == 0) {
-            atomicOr(&a.scratch->status, kDevErrTimeout);
-            s_failed = 1;
-        }
+        tm_produce<T>(a, ring, full_bar, empty_bar, s_issued, &s_failed, sg, nvec, nchunk, v0c,
+                      clid, ncl, lane);
     } else {
         // ------------------------------------------------------------ consumers
         const NamedSync all_consumers{15, kTmNTC};
@@ -523,22 +557,7 @@ ce_fwd_tmem(const __grid_constant__ FwdArgs a) {
                            tid == 0 ? s_accZ : 0.0, tid == 0 ? s_accC : 0, s_D, s_nvalid);
         }
     }
-    __syncthreads();
-    if (s_failed && tid == kTmWarps * 32) {
-        // copies that may still be in flight land before the CTA exits
-        for (int i = 0; i < sg; ++i) {
-            const uint32_t used = s_issued[i];
-            if (used) (void)mbar_wait_bounded(smem_u32(&full_bar[i]), used & 1u, a.timeout_ns);
-        }
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kTmCols)
-                     : "memory");
-    // no CTA leaves while another CTA of the cluster may still store into it
-    cluster_sync();
+    tm_teardown(a, tmem, s_failed, s_issued, full_bar, sg, tid, warp);
 }
 
 }  // namespace gbce
