@@ -694,8 +694,9 @@ ND_SHAPES = [(8, 32000, 512), (8, 4096, 1024), (16, 1000, 4096), (8, 19, 512, 51
 def measure_nd(device, torch, barrier, max_over_ranks, rank, peak, steps=6):
     """N-D logits (class dimension 1) through ce_fwd_nd, forward with the
     gradient in place, bf16, mean, 10% of positions ignored, N(0, 3^2):
-    each timed step on its own buffer of seeded logits (CUDA events over
-    `steps` steps), GB/s of one read and one write per element."""
+    each timed step on its own buffer of seeded logits (`steps` steps
+    replayed from a CUDA graph, CUDA events on its stream), GB/s of one read
+    and one write per element."""
     import math
     import numpy as np
     from softmax_cross_entropy_gb300 import _lib
@@ -709,7 +710,8 @@ def measure_nd(device, torch, barrier, max_over_ranks, rank, peak, steps=6):
         t = torch.from_numpy(np.ascontiguousarray(case.target)).to(device)
         loss = torch.empty(1, dtype=torch.float32, device=device)
         bufs = [torch.empty_like(pristine) for _ in range(steps)]
-        st = torch.cuda.current_stream(device).cuda_stream
+        stream = torch.cuda.Stream(device)
+        st = stream.cuda_stream
 
         def run(x):
             rc = _lib.ce_fwd_nd(x.data_ptr(), _lib.CE_BF16, N, C, inner, t.data_ptr(), None, -100,
@@ -718,19 +720,27 @@ def measure_nd(device, torch, barrier, max_over_ranks, rank, peak, steps=6):
             if rc != 0:
                 raise RuntimeError(f"ce_fwd_nd: {_lib.ce_status_string(rc)} {_lib.ce_last_error()}")
 
-        for b in bufs[:3]:
-            b.copy_(pristine)
-            run(b)  # warm-up (plans, workspace)
+        with torch.cuda.stream(stream):
+            for b in bufs[:3]:
+                b.copy_(pristine)
+                run(b)  # warm-up on the timing stream (plans, scratch, workspace)
+        torch.cuda.synchronize(device)
+        # the steps replayed from a CUDA graph, as the other lines time them
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for b in bufs:
+                    run(b)
         for b in bufs:
             b.copy_(pristine)
         torch.cuda.synchronize(device)
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for b in bufs:
-            run(b)
-        e1.record()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
         torch.cuda.synchronize(device)
         barrier()
         if _lib.ce_device_status(st) != 0:

@@ -61,6 +61,8 @@ using PlanKey = std::tuple<int, int, int64_t, int, bool, bool, std::string>;
 // The tensor-memory kernel shifts exp(z) by the softcap s itself; exp(-2 s)
 // must stay a normal fp32
 constexpr float kTmMaxSoftcap = 40.f;
+// N-D logits with at least this many classes take the split form
+constexpr int64_t kNdSplitMinClasses = 768;
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
@@ -1377,11 +1379,13 @@ int nd_split_occ(const void* fn, size_t smem, size_t smem_max = 0) {
 }
 
 // The split N-D forward (ce_fwd_nd_split.cuh): class chunks of cc classes
-// so that the (tile, chunk) items number about GBCE_ND_ITEMS (default 2) per
-// SM, with at least GBCE_ND_MIN_CHUNK (default 64) classes a chunk; the
-// records, coefficients and counted targets in the stream's N-D workspace.
+// so that the (tile, chunk) items fill GBCE_ND_ITEMS (default 1) waves of
+// resident statistics CTAs without starting another, with at least
+// GBCE_ND_MIN_CHUNK (default 64) classes a chunk; the records, coefficients
+// and counted targets in the stream's N-D workspace.
 ce_status nd_split_launch(int dev, const DeviceInfo& info, const FwdArgs& f, int dtype,
-                          bool vec_ok, bool softcap, bool argmax, cudaStream_t st) {
+                          bool vec_ok, bool softcap, bool argmax, bool after_count,
+                          cudaStream_t st) {
     const int64_t b = dtype == CE_F32 ? 4 : 2;
     const int64_t VP = vec_ok ? 16 / b : 1;
     const int64_t P = 32 * VP;
@@ -1389,9 +1393,21 @@ ce_status nd_split_launch(int dev, const DeviceInfo& info, const FwdArgs& f, int
     NdSplitArgs s = {};
     s.f = f;
     s.tiles = (f.rows + P - 1) / P;
-    const int64_t want = std::max(1, env_int("GBCE_ND_ITEMS", 2)) * static_cast<int64_t>(info.sm_count);
+    const NdSplitFns fns = nd_split_fns(dtype, vec_ok, softcap, argmax, f.eps > 0.f);
+    if (!fns.stats || !fns.merge || !fns.grad) return CE_ERR_INVALID_ARG;
+    const int o1 = nd_split_occ(fns.stats, fns.stats_smem);
+    const int o3 = nd_split_occ(fns.grad, 0);
+    if (o1 < 1 || o3 < 1) {
+        g_last_error = "the split N-D kernels do not fit on an SM";
+        return CE_ERR_UNSUPPORTED;
+    }
+    // as many chunks a tile as keep the items within one wave of resident
+    // statistics CTAs (GBCE_ND_ITEMS waves; a partial second wave doubled
+    // the launch: 320 items on 304 CTAs at 8 x 4096 x 1024)
+    const int64_t want = std::max(1, env_int("GBCE_ND_ITEMS", 1)) * static_cast<int64_t>(o1) *
+                         static_cast<int64_t>(info.sm_count);
     const int64_t max_ch = std::max<int64_t>(1, C / std::max(8, env_int("GBCE_ND_MIN_CHUNK", 64)));
-    const int64_t nch0 = std::min<int64_t>(max_ch, std::max<int64_t>(1, (want + s.tiles - 1) / s.tiles));
+    const int64_t nch0 = std::min<int64_t>(max_ch, std::max<int64_t>(1, want / s.tiles));
     const int64_t cc = (C + nch0 - 1) / nch0;
     s.cc = static_cast<int>(cc);
     s.nch = static_cast<int>((C + cc - 1) / cc);
@@ -1405,17 +1421,12 @@ ce_status nd_split_launch(int dev, const DeviceInfo& info, const FwdArgs& f, int
     s.rec = static_cast<NdRec*>(ws);
     s.coef = reinterpret_cast<NdCoef*>(static_cast<char*>(ws) + rec_b);
     s.tpos = reinterpret_cast<int*>(static_cast<char*>(ws) + rec_b + coef_b);
-    const NdSplitFns fns = nd_split_fns(dtype, vec_ok, softcap, argmax, f.eps > 0.f);
-    if (!fns.stats || !fns.merge || !fns.grad) return CE_ERR_INVALID_ARG;
     const int64_t items = s.tiles * s.nch;
-    const int o1 = nd_split_occ(fns.stats, fns.stats_smem);
-    const int o3 = nd_split_occ(fns.grad, 0);
-    if (o1 < 1 || o3 < 1) {
-        g_last_error = "the split N-D kernels do not fit on an SM";
-        return CE_ERR_UNSUPPORTED;
-    }
     const int64_t g1 = std::min<int64_t>(items, o1 * static_cast<int64_t>(info.sm_count));
-    rc = launch(fns.stats, static_cast<int>(g1), kNdSplitThreads, fns.stats_smem, 1, st, &s);
+    // the statistics overlap the count kernel before them (they do not read
+    // its counts; the merge does, launched after both)
+    rc = launch(fns.stats, static_cast<int>(g1), kNdSplitThreads, fns.stats_smem, 1, st, &s,
+                after_count);
     if (rc != CE_OK) return rc;
     // one warp a position; the merge's CTAs take the partial-sum slots
     const int64_t g2 = std::max<int64_t>(
@@ -1508,11 +1519,16 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     const int64_t tiles = (rows + P - 1) / P;
     // The single-kernel form reads a staged tile once, but runs one CTA a
     // tile of every class; when its tile does not fit on chip (it would read
-    // the logits three times) or there are too few tiles for the SMs, the
-    // split form takes the call (GBCE_ND_SPLIT=0 / 1 forces one or the other)
+    // the logits three times), there are too few tiles for the SMs, or the
+    // classes are many (its serial pass over them then costs more than the
+    // split form's second read: at 16 x C x 4096 bf16, 80 against 94 us for
+    // C = 512, 163 against 136 for C = 1000, 199 against 124 for 4 x 2000 x
+    // 8192), the split form takes the call (GBCE_ND_SPLIT=0 / 1 forces one
+    // or the other)
     const int split_env = env_int("GBCE_ND_SPLIT", -1);
-    const bool split = split_env == 1 || (split_env != 0 && env_int("GBCE_ND_MODE", 0) == 0 &&
-                                          (!p.staged || tiles < 2 * info.sm_count));
+    const bool split =
+        split_env == 1 || (split_env != 0 && env_int("GBCE_ND_MODE", 0) == 0 &&
+                           (!p.staged || tiles < 2 * info.sm_count || C >= kNdSplitMinClasses));
     // Few classes with vector positions and enough tiles: a warp a tile
     // (no CTA barrier between its phases; GBCE_ND_WARP=0 turns it off, 2
     // takes it whatever the tile count)
@@ -1526,10 +1542,13 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
         if (occ >= 1) {
             const int64_t grid = std::min<int64_t>((tiles + 7) / 8,
                                                    std::min<int64_t>(occ * int64_t{info.sm_count}, kMaxUnits));
-            return launch(fn, static_cast<int>(grid), 256, smem, 1, st, &a);
+            return launch(fn, static_cast<int>(grid), 256, smem, 1, st, &a,
+                          reduction != CE_RED_NONE);
         }
     }
-    if (split) return nd_split_launch(dev, info, a, dtype, vec_ok, sc, argmax, st);
+    if (split)
+        return nd_split_launch(dev, info, a, dtype, vec_ok, sc, argmax, reduction != CE_RED_NONE,
+                               st);
     const int64_t grid = std::min<int64_t>(tiles, std::min<int64_t>(p.max_ctas, kMaxUnits));
     return launch(p.fn, static_cast<int>(grid), kNdThreads, p.smem, 1, st, &a);
 }

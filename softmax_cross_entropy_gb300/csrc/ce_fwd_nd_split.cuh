@@ -242,6 +242,10 @@ ce_nd_stats(const __grid_constant__ NdSplitArgs s) {
         }
         __syncthreads();  // red is written again by the next item
     }
+    // Launched as a programmatic dependent of the count kernel, it reads
+    // nothing that kernel writes; this wait keeps it from completing before
+    // the count kernel, so the merge launched after it sees the counts.
+    pdl_wait();
 }
 
 // One warp a position: lane l merges chunks l, l + 32, ... in order, then a
@@ -388,6 +392,9 @@ ce_nd_grad(const __grid_constant__ NdSplitArgs s) {
     const int64_t inner = a.inner;
     const bool wsmooth = a.eps > 0.f && a.weight != nullptr;
     const int64_t items = s.tiles * s.nch;
+    // a backward launched after this kernel may be scheduled now (it waits
+    // for this grid before reading anything)
+    pdl_launch_dependents();
 #pragma unroll 1
     for (int64_t i = blockIdx.x; i < items; i += gridDim.x) {
         const int64_t it = items - 1 - i;
@@ -480,12 +487,23 @@ ce_nd_warp(const __grid_constant__ FwdArgs a) {
     // this lane's 16-byte slot of class c: tile + (c * 32 + lane) * 16
     const uint32_t tile = smem_u32(nd_dyn) + static_cast<uint32_t>(wy * C * 32 + lane) * 16u;
     const uint4* tl = reinterpret_cast<const uint4*>(nd_dyn) + wy * C * 32 + lane;
+    // a backward launched after this kernel may be scheduled now (it waits
+    // for this grid before reading anything)
+    pdl_launch_dependents();
+    // D and the counted positions come from the count kernel launched just
+    // before, which this launch overlaps (programmatic dependent launch): read
+    // where first needed, after the first tile's statistics
     float D = 0.f;
     int n_valid = 0;
-    if (a.reduction != kRedNone) {
-        D = static_cast<float>(a.batch_counts[0]);
-        n_valid = static_cast<int>(a.batch_counts[1]);
-    }
+    bool have_counts = a.reduction == kRedNone;
+    auto need_counts = [&]() {
+        if (!have_counts) {
+            pdl_wait();
+            D = static_cast<float>(a.batch_counts[0]);
+            n_valid = static_cast<int>(a.batch_counts[1]);
+            have_counts = true;
+        }
+    };
     float Wsum = static_cast<float>(C);
     if (wsmooth) {
         // W = sum of the class weights, the same order in every thread
@@ -494,7 +512,6 @@ ce_nd_warp(const __grid_constant__ FwdArgs a) {
         Wsum = w;
     }
     const float inv_C = 1.f / static_cast<float>(C);
-    const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;
     const float Wf = wsmooth ? Wsum * inv_C : 1.f;
     double accL = 0.0, accZ = 0.0;
     long long accC = 0;
@@ -574,6 +591,8 @@ ce_nd_warp(const __grid_constant__ FwdArgs a) {
             }
         }
         // ---- per-position outputs and the gradient's coefficients
+        need_counts();
+        const float scale = a.reduction == kRedMean ? 1.f / D : 1.f;
         float ac[VP], bc[VP], tf[VP];
 #pragma unroll
         for (int v = 0; v < VP; ++v) {
@@ -636,6 +655,7 @@ ce_nd_warp(const __grid_constant__ FwdArgs a) {
         __syncwarp();  // every lane done with the tile before the next copies
     }
     if (a.reduction != kRedNone) {
+        need_counts();
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             accL += __shfl_xor_sync(0xffffffffu, accL, o);
