@@ -16,6 +16,12 @@
 #include "gbce.h"
 
 namespace gbce {
+
+// the single-read N-D tile kernel (ce_fwd_nd_tile.cu)
+ce_status nd_tile_launch(const FwdArgs& f, int dtype, int64_t N, int64_t C, int64_t inner,
+                         int sm_count, int smem_optin, int max_cluster, bool after_count,
+                         cudaStream_t st);
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -1514,6 +1520,7 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     a.scratch = scratch;
     a.batch_counts = reduction != CE_RED_NONE ? scratch->counts : nullptr;
     a.inner = inner;
+    a.timeout_ns = static_cast<uint64_t>(env_int("GBCE_WAIT_TIMEOUT_MS", 2000)) * 1000000ull;
     a.nd_staged = p.staged ? 1 : 0;
     const int64_t P = p.vec ? 32 * (16 / b) : 32;
     const int64_t tiles = (rows + P - 1) / P;
@@ -1526,6 +1533,22 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     // 8192), the split form takes the call (GBCE_ND_SPLIT=0 / 1 forces one
     // or the other)
     const int split_env = env_int("GBCE_ND_SPLIT", -1);
+    // The single-read tile kernel (a cluster holds a tile's classes in
+    // shared memory), no softcap and no class-weighted smoothing: by default
+    // where the split form would take the call and one or two CTAs hold a
+    // tile's classes, the range where it measured faster (16 x 1000 x 4096
+    // bf16 117.5 against 136.5 us, 4 x 2000 x 8192 120.3 against 127.3; with
+    // four CTAs a tile, 8 x 4096 x 1024, 79.7 against 71.2, and with 16,
+    // 8 x 32000 x 512, 463 against 170). GBCE_ND_TILE=0 turns it off, 2
+    // takes it for any class count and cluster size.
+    const int tile_env = env_int("GBCE_ND_TILE", 1);
+    if (tile_env != 0 && !sc && !(weight && label_smoothing > 0.f) &&
+        (tile_env == 2 || C >= kNdSplitMinClasses) && env_int("GBCE_ND_MODE", 0) == 0 &&
+        split_env < 0) {
+        rc = nd_tile_launch(a, dtype, N, C, inner, info.sm_count, info.smem_optin,
+                            tile_env == 2 ? 16 : 2, reduction != CE_RED_NONE, st);
+        if (rc != CE_ERR_UNSUPPORTED) return rc;
+    }
     const bool split =
         split_env == 1 || (split_env != 0 && env_int("GBCE_ND_MODE", 0) == 0 &&
                            (!p.staged || tiles < 2 * info.sm_count || C >= kNdSplitMinClasses));

@@ -680,6 +680,33 @@ int tile_rows(int64_t M, int64_t N, int sms, bool tmao) {
 
 }  // namespace
 
+// A 2-D map of a row-major [outer, inner] matrix of `dtype` elements (pitch
+// inner elements), boxes of box_inner x box_outer elements, no swizzle,
+// zeros outside the matrix (the N-D tile kernel's class rows).
+ce_status tensor_map_rows_2d(CUtensorMap* map, int dtype, const void* p, int64_t outer,
+                             int64_t inner, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiled enc = nullptr;
+    ce_status rc = encoder(&enc);
+    if (rc != CE_OK) return rc;
+    const int64_t b = dtype == CE_F32 ? 4 : 2;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner * b)};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType t = dtype == CE_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : dtype == CE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = enc(map, t, 2, const_cast<void*>(p), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        record_message("cuTensorMapEncodeTiled (rows) failed (" +
+                       std::to_string(static_cast<int>(r)) + ")");
+        return CE_ERR_UNSUPPORTED;
+    }
+    return CE_OK;
+}
+
 // Whether the tensor-core GEMM takes an operand: a 16-bit type, a 16-byte
 // aligned base and rows of a multiple of 8 elements (16-byte strides for
 // the TMA): K for a K-major operand, M or N for an MN-major one.

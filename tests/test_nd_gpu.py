@@ -259,6 +259,68 @@ def test_nd_warp_per_tile_default_and_ties():
     assert np.all(out["pred"][valid] == 2)
 
 
+# The single-read tile kernel (more than 48 classes, no softcap, no
+# class-weighted smoothing; GBCE_ND_TILE=2 forces it for any class count): a
+# cluster holds a tile's classes in shared memory. Shapes with one CTA, a few
+# and more than eight a tile (128- and 64-byte class rows), ragged class
+# slices, tiles past the end of `inner`, several N.
+TILE_OPTS = {"plain": dict(), "weight": dict(weight=True),
+             "smooth_z": dict(label_smoothing=0.1, lse_square_scale=1e-3)}
+
+
+@pytest.mark.parametrize("opts", sorted(TILE_OPTS))
+@pytest.mark.parametrize("shape,dtype", [((2, 300, 40), "bf16"), ((3, 1000, 24), "f32"),
+                                         ((1, 2049, 16), "f16"), ((2, 4096, 256), "bf16"),
+                                         ((4, 100, 8), "bf16"), ((2, 5, 3, 8), "f32"),
+                                         ((1, 7000, 72), "f32")])
+@pytest.mark.parametrize("reduction", ["mean", "none", "sum"])
+def test_nd_tile(monkeypatch, opts, shape, dtype, reduction):
+    monkeypatch.setenv("GBCE_ND_TILE", "2")
+    case = workloads.nd_case(37 + sum(shape), shape, dtype, std=3.0, reduction=reduction,
+                             **dict(TILE_OPTS[opts]))
+    check(case, want_z=case.lse_square_scale > 0, want_acc=True, want_pred=True)
+
+
+@pytest.mark.parametrize("shape,dtype", [((64, 200, 512), "bf16"), ((32, 2000, 256), "bf16"),
+                                         ((4, 32000, 128), "bf16"), ((48, 300, 256), "f32")])
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_nd_tile_several_tiles_a_cluster(monkeypatch, shape, dtype, reduction):
+    # more tiles than resident clusters: each cluster's producer reloads its
+    # blocks for the next tile as the consumers release them, and the
+    # cluster exchanges reuse their buffers by tile parity
+    monkeypatch.setenv("GBCE_ND_TILE", "2")
+    case = workloads.nd_case(47 + sum(shape), shape, dtype, std=3.0, reduction=reduction,
+                             label_smoothing=0.05)
+    check(case, want_acc=True, want_pred=True)
+
+
+def test_nd_tile_large_cluster_and_ties():
+    # 2 x 32000 x 128 bf16: more than eight CTAs a tile (64-byte class rows);
+    # the top logit tied at classes in different CTAs' slices
+    case = workloads.nd_case(41, (2, 32000, 128), "bf16", std=3.0, reduction="mean")
+    x = case.x.copy()
+    top = workloads.f32_to_bf16_bits(np.array([50.0], np.float32))[0]
+    for c in (7001, 15000, 31999):
+        x[:, c, :] = top
+    case = case.with_(x=x)
+    out, _ = check(case, want_acc=True, want_pred=True)
+    valid = case.target != case.ignore_index
+    assert np.all(out["pred"][valid] == 7001)
+
+
+def test_nd_tile_forward_only_and_all_ignored():
+    case = workloads.nd_case(43, (2, 700, 64), "bf16", std=3.0, reduction="mean")
+    x = _dev_logits(case)
+    before = x.clone()
+    out = run_nd(case, grad=False, want_pred=True, x=x)
+    assert torch.equal(x, before)
+    assert np.array_equal(out["pred"], oracle_nd(case, want_grad=False)["pred"])
+    none = case.with_(target=np.full_like(case.target, case.ignore_index))
+    m = run_nd(none, want_acc=True)
+    assert math.isnan(m["loss"]) and math.isnan(m["acc"])
+    assert bool((m["x"] == 0).all())
+
+
 def test_nd_inner_one_is_2d():
     case = workloads.nd_case(2, (33, 4096, 1), "bf16", reduction="sum")
     check(case, want_pred=True)
