@@ -19,8 +19,8 @@ namespace gbce {
 
 // the single-read N-D tile kernel (ce_fwd_nd_tile.cu)
 ce_status nd_tile_launch(const FwdArgs& f, int dtype, int64_t N, int64_t C, int64_t inner,
-                         int sm_count, int smem_optin, int max_cluster, bool after_count,
-                         cudaStream_t st);
+                         int sm_count, int smem_optin, int max_cluster, bool narrow_rows,
+                         bool after_count, cudaStream_t st);
 
 namespace {
 
@@ -1536,7 +1536,7 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     // The single-read tile kernel (a cluster holds a tile's classes in
     // shared memory), no softcap and no class-weighted smoothing: by default
     // where the split form would take the call and one or two CTAs hold a
-    // tile's classes, the range where it measured faster (16 x 1000 x 4096
+    // tile's classes in 128-byte rows, the range where it measured faster (16 x 1000 x 4096
     // bf16 117.5 against 136.5 us, 4 x 2000 x 8192 120.3 against 127.3; with
     // four CTAs a tile, 8 x 4096 x 1024, 79.7 against 71.2, and with 16,
     // 8 x 32000 x 512, 463 against 170). GBCE_ND_TILE=0 turns it off, 2
@@ -1546,7 +1546,7 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
         (tile_env == 2 || C >= kNdSplitMinClasses) && env_int("GBCE_ND_MODE", 0) == 0 &&
         split_env < 0) {
         rc = nd_tile_launch(a, dtype, N, C, inner, info.sm_count, info.smem_optin,
-                            tile_env == 2 ? 16 : 2, reduction != CE_RED_NONE, st);
+                            tile_env == 2 ? 16 : 2, tile_env == 2, reduction != CE_RED_NONE, st);
         if (rc != CE_ERR_UNSUPPORTED) return rc;
     }
     const bool split =

@@ -528,20 +528,21 @@ const void* nd_tile_kernel(int dtype, int tpr) {
 // The single-read N-D forward for the call in `f` (rows = N * inner
 // positions, V = C classes): plans the cluster (CTAs enough to hold a tile's
 // classes in shared memory, at most max_cluster; 128-byte class rows when a
-// cluster of at most 8 does, else 64-byte ones and up to 16; of the sizes
-// that fit, the one keeping the most SMs busy), encodes the class-row tensor
-// map and launches. Returns CE_ERR_UNSUPPORTED (nothing launched) when the
+// cluster of at most 8 does, else, with narrow_rows, 64-byte ones and up to
+// 16; of the sizes that fit, the one keeping the most SMs busy), encodes the
+// class-row tensor map and launches. Returns CE_ERR_UNSUPPORTED (nothing launched) when the
 // shape does not fit it; `after_count`: launched as a programmatic
 // dependent of the count kernel just before.
 ce_status nd_tile_launch(const FwdArgs& f, int dtype, int64_t N, int64_t C, int64_t inner,
-                         int sm_count, int smem_optin, int max_cluster, bool after_count,
-                         cudaStream_t st) {
+                         int sm_count, int smem_optin, int max_cluster, bool narrow_rows,
+                         bool after_count, cudaStream_t st) {
     const int64_t b = dtype == CE_F32 ? 4 : 2;
     const int E = static_cast<int>(4 / b);
     if (N * C > INT32_MAX || C > INT32_MAX / 2 || (inner * b) % 16 != 0 ||
         (reinterpret_cast<uintptr_t>(f.x) % 16) != 0)
         return CE_ERR_UNSUPPORTED;
     for (int tpr : {32, 16}) {
+        if (tpr == 16 && !narrow_rows) break;
         const void* fn = nd_tile_kernel(dtype, tpr);
         if (!fn) return CE_ERR_UNSUPPORTED;
         const int64_t P = static_cast<int64_t>(tpr) * E;
