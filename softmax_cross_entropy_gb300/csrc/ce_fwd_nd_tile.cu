@@ -246,6 +246,7 @@ ce_nd_tile(const __grid_constant__ CUtensorMap map, const __grid_constant__ NdTi
         const int rg = tid / TPR;    // row group: rows rg, rg + RG, ... of each block
         const uint64_t spol = l2_evict_first_policy();
         const bool smooth = a.eps > 0.f;
+        const bool want_arg = a.want_pred || a.want_acc;
         const float inv_C = 1.f / static_cast<float>(C);
         const bool outputs = crank == 0 && rg == 0;  // per-position outputs: rank 0, row group 0
         bool failed = false;
@@ -300,16 +301,26 @@ ce_nd_tile(const __grid_constant__ CUtensorMap map, const __grid_constant__ NdTi
                     atomicOr(&a.scratch->status, kDevErrTimeout);
                 }
                 const int rhi = min(ncls, (j + 1) * s.rb);
+                if (want_arg) {
 #pragma unroll 4
-                for (int r = j * s.rb + rg; r < rhi; r += RG) {
-                    float f[E];
-                    IO::unpack(*reinterpret_cast<const uint32_t*>(slice + r * kRowBytes + tcol * 4), f);
+                    for (int r = j * s.rb + rg; r < rhi; r += RG) {
+                        float f[E];
+                        IO::unpack(*reinterpret_cast<const uint32_t*>(slice + r * kRowBytes + tcol * 4), f);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        if (f[e] > m[e]) {  // rows in increasing order: the first maximum stays
-                            m[e] = f[e];
-                            mi[e] = c0 + r;
+                        for (int e = 0; e < E; ++e) {
+                            if (f[e] > m[e]) {  // rows in increasing order: the first maximum stays
+                                m[e] = f[e];
+                                mi[e] = c0 + r;
+                            }
                         }
+                    }
+                } else {
+#pragma unroll 8
+                    for (int r = j * s.rb + rg; r < rhi; r += RG) {
+                        float f[E];
+                        IO::unpack(*reinterpret_cast<const uint32_t*>(slice + r * kRowBytes + tcol * 4), f);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) m[e] = fmaxf(m[e], f[e]);
                     }
                 }
             }
@@ -365,7 +376,7 @@ ce_nd_tile(const __grid_constant__ CUtensorMap map, const __grid_constant__ NdTi
             for (int e = 0; e < E; ++e) S[e] = SZ[e] = zt[e] = fz[e] = 0.f;
             for (int j = 0; j < nbu; ++j) {
                 const int rhi = min(ncls, (j + 1) * s.rb);
-#pragma unroll 4
+#pragma unroll 8
                 for (int r = j * s.rb + rg; r < rhi; r += RG) {
                     float f[E];
                     IO::unpack(*reinterpret_cast<const uint32_t*>(slice + r * kRowBytes + tcol * 4), f);
@@ -374,10 +385,19 @@ ce_nd_tile(const __grid_constant__ CUtensorMap map, const __grid_constant__ NdTi
                         const float d = f[e] - sh[e];
                         S[e] += ex2(d * kLog2e);
                         if (smooth) SZ[e] += d;
-                        if (c0 + r == tv[e]) {
-                            zt[e] = f[e];
-                            fz[e] = 1.f;
-                        }
+                    }
+                }
+            }
+            // x at the target, read once by row group 0 when this CTA holds it
+            if (rg == 0) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int tr = tv[e] - c0;
+                    if (tv[e] >= 0 && tr >= 0 && tr < ncls) {
+                        float f[E];
+                        IO::unpack(*reinterpret_cast<const uint32_t*>(slice + tr * kRowBytes + tcol * 4), f);
+                        zt[e] = f[e];
+                        fz[e] = 1.f;
                     }
                 }
             }
@@ -460,23 +480,33 @@ ce_nd_tile(const __grid_constant__ CUtensorMap map, const __grid_constant__ NdTi
             // ---- pass C: the gradient, block by block; each block goes back
             // to the producer once every consumer warp is done with it
             T* xg = reinterpret_cast<T*>(a.x) + n * C * inner + sp0;
+            // the gradient of class row r for this thread's positions, with
+            // the one-hot term at their targets (added apart, no contraction
+            // into an FMA: with p_t = 1 the two cancel exactly)
+            auto grad_row = [&](int r, bool onehot) {
+                float f[E];
+                IO::unpack(*reinterpret_cast<const uint32_t*>(slice + r * kRowBytes + tcol * 4), f);
+                const int c = c0 + r;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    float g = fmaf(ac[e], ex2((f[e] - sh[e]) * kLog2e), bc[e]);
+                    if (onehot && c == tv[e]) g = __fadd_rn(g, tf[e]);
+                    f[e] = tv[e] >= 0 ? g : 0.f;  // exact zeros where a position does not count
+                }
+                nt_st_u32_hint(xg + static_cast<int64_t>(c) * inner, IO::pack(f), spol);
+            };
             for (int j = 0; j < nbu; ++j) {
                 if (a.grad && pos_ok) {
-                    const int rhi = min(ncls, (j + 1) * s.rb);
-#pragma unroll 4
-                    for (int r = j * s.rb + rg; r < rhi; r += RG) {
-                        float f[E];
-                        IO::unpack(*reinterpret_cast<const uint32_t*>(slice + r * kRowBytes + tcol * 4), f);
-                        const int c = c0 + r;
+                    const int rlo = j * s.rb, rhi = min(ncls, rlo + s.rb);
+#pragma unroll 8
+                    for (int r = rlo + rg; r < rhi; r += RG) grad_row(r, false);
+                    // the rows of this block holding a target of this
+                    // thread's positions, stored again by the same thread
 #pragma unroll
-                        for (int e = 0; e < E; ++e) {
-                            float g = fmaf(ac[e], ex2((f[e] - sh[e]) * kLog2e), bc[e]);
-                            // the one-hot term added apart (no contraction
-                            // into an FMA: with p_t = 1 the two cancel exactly)
-                            if (c == tv[e]) g = __fadd_rn(g, tf[e]);
-                            f[e] = tv[e] >= 0 ? g : 0.f;  // exact zeros where a position does not count
-                        }
-                        nt_st_u32_hint(xg + static_cast<int64_t>(c) * inner, IO::pack(f), spol);
+                    for (int e = 0; e < E; ++e) {
+                        const int tr = tv[e] - c0;
+                        if (tv[e] >= 0 && tr >= rlo + rg && tr < rhi && (tr - rlo - rg) % RG == 0)
+                            grad_row(tr, true);
                     }
                 }
                 __syncwarp();
