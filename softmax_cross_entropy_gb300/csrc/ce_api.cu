@@ -1526,12 +1526,13 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     const int64_t tiles = (rows + P - 1) / P;
     // The single-kernel form reads a staged tile once, but runs one CTA a
     // tile of every class; when its tile does not fit on chip (it would read
-    // the logits three times), there are too few tiles for the SMs, or the
-    // classes are many (its serial pass over them then costs more than the
-    // split form's second read: at 16 x C x 4096 bf16, 80 against 94 us for
-    // C = 512, 163 against 136 for C = 1000, 199 against 124 for 4 x 2000 x
-    // 8192), the split form takes the call (GBCE_ND_SPLIT=0 / 1 forces one
-    // or the other)
+    // the logits three times), there are very few tiles for the SMs (fewer
+    // than one for every two SMs; at 256 tiles of 16 x C x 4096 bf16 it was
+    // still faster: 23 against 61 us for C = 64, even at 256 and 512), or
+    // the classes are many (its serial pass over them then costs more than
+    // the split form's second read: 163 against 136 us for C = 1000, 199
+    // against 124 for 4 x 2000 x 8192), the split form takes the call
+    // (GBCE_ND_SPLIT=0 / 1 forces one or the other)
     const int split_env = env_int("GBCE_ND_SPLIT", -1);
     // The single-read tile kernel (a cluster holds a tile's classes in
     // shared memory), no softcap and no class-weighted smoothing: by default
@@ -1551,13 +1552,13 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     }
     const bool split =
         split_env == 1 || (split_env != 0 && env_int("GBCE_ND_MODE", 0) == 0 &&
-                           (!p.staged || tiles < 2 * info.sm_count || C >= kNdSplitMinClasses));
+                           (!p.staged || 2 * tiles < info.sm_count || C >= kNdSplitMinClasses));
     // Few classes with vector positions and enough tiles: a warp a tile
     // (no CTA barrier between its phases; GBCE_ND_WARP=0 turns it off, 2
     // takes it whatever the tile count)
     const int warp_env = env_int("GBCE_ND_WARP", 1);
-    if ((warp_env == 2 || (!split && warp_env == 1)) && vec_ok && C <= kNdWarpClasses &&
-        env_int("GBCE_ND_MODE", 0) == 0 && split_env != 1) {
+    if ((warp_env == 2 || (!split && warp_env == 1 && tiles >= 2 * info.sm_count)) && vec_ok &&
+        C <= kNdWarpClasses && env_int("GBCE_ND_MODE", 0) == 0 && split_env != 1) {
         const void* fn = nd_warp_kernel(dtype, sc, argmax);
         if (!fn) return CE_ERR_INVALID_ARG;
         const size_t smem = static_cast<size_t>(8) * C * 512;
