@@ -69,6 +69,9 @@ using PlanKey = std::tuple<int, int, int64_t, int, bool, bool, std::string>;
 constexpr float kTmMaxSoftcap = 40.f;
 // N-D logits with at least this many classes take the split form
 constexpr int64_t kNdSplitMinClasses = 768;
+// ... and the single-read tile form from this many, where one or two CTAs
+// hold a tile's classes
+constexpr int64_t kNdTileMinClasses = 512;
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
@@ -1536,15 +1539,17 @@ extern "C" ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, in
     const int split_env = env_int("GBCE_ND_SPLIT", -1);
     // The single-read tile kernel (a cluster holds a tile's classes in
     // shared memory), no softcap and no class-weighted smoothing: by default
-    // where the split form would take the call and one or two CTAs hold a
-    // tile's classes in 128-byte rows, the range where it measured faster (16 x 1000 x 4096
-    // bf16 117.5 against 136.5 us, 4 x 2000 x 8192 120.3 against 127.3; with
-    // four CTAs a tile, 8 x 4096 x 1024, 79.7 against 71.2, and with 16,
-    // 8 x 32000 x 512, 463 against 170). GBCE_ND_TILE=0 turns it off, 2
+    // from kNdTileMinClasses classes where one or two CTAs hold a tile's
+    // classes in 128-byte rows, the range where it measured faster (bf16,
+    // mean: 16 x 512 x 4096 69.9 against 80.3 us for the staged kernel,
+    // 16 x 1000 x 4096 98.4 against 135.9 for the split form, 4 x 2000 x
+    // 8192 111.8 against 124.6; at 256 classes 55.2 against 52.6, with four
+    // CTAs a tile, 8 x 4096 x 1024, 71.4 against 70.4, with sixteen,
+    // 8 x 32000 x 512, 445 against 171). GBCE_ND_TILE=0 turns it off, 2
     // takes it for any class count and cluster size.
     const int tile_env = env_int("GBCE_ND_TILE", 1);
     if (tile_env != 0 && !sc && !(weight && label_smoothing > 0.f) &&
-        (tile_env == 2 || C >= kNdSplitMinClasses) && env_int("GBCE_ND_MODE", 0) == 0 &&
+        (tile_env == 2 || C >= kNdTileMinClasses) && env_int("GBCE_ND_MODE", 0) == 0 &&
         split_env < 0) {
         rc = nd_tile_launch(a, dtype, N, C, inner, info.sm_count, info.smem_optin,
                             tile_env == 2 ? 16 : 2, tile_env == 2, reduction != CE_RED_NONE, st);

@@ -16,7 +16,7 @@
 //  * pass A: maximum and first argmax over the CTA's classes, reduced over
 //    the row groups in shared memory and over the cluster (each CTA stores
 //    its P records into every CTA's shared memory and arrives once on its
-//    exchange barrier; bounded waits);
+//    exchange barrier; bounded waits; a one-CTA tile keeps its records);
 //  * pass B: S = sum exp(x - M), the smoothing sum and x at the target, the
 //    same two reductions;
 //  * per-position outputs (rank 0 of the cluster) and the gradient's
@@ -339,19 +339,26 @@ ce_nd_tile(const __grid_constant__ CUtensorMap map, const __grid_constant__ NdTi
                         I = iq;
                     }
                 }
-                const uint32_t rec = smem_u32(&xA[(par * csize + crank) * P + tid]);
-                for (uint32_t q = 0; q < csize; ++q)
-                    nt_st_dsmem_f2(map_to_rank(rec, q), make_float2(M, __int_as_float(I)));
-                nt_fence_cluster();
+                if (csize == 1) {
+                    // one CTA a tile: the record stays in this CTA
+                    xA[par * P + tid] = make_float2(M, __int_as_float(I));
+                } else {
+                    const uint32_t rec = smem_u32(&xA[(par * csize + crank) * P + tid]);
+                    for (uint32_t q = 0; q < csize; ++q)
+                        nt_st_dsmem_f2(map_to_rank(rec, q), make_float2(M, __int_as_float(I)));
+                    nt_fence_cluster();
+                }
             }
             nt_consumer_sync();
-            if (tid == 0)
-                for (uint32_t q = 0; q < csize; ++q)
-                    nt_arrive_cluster(map_to_rank(smem_u32(&xbarA[par]), q));
-            if (!failed && !nt_wait_cluster(smem_u32(&xbarA[par]),
-                                            static_cast<uint32_t>(it >> 1) & 1u, a.timeout_ns)) {
-                failed = true;
-                atomicOr(&a.scratch->status, kDevErrTimeout);
+            if (csize > 1) {
+                if (tid == 0)
+                    for (uint32_t q = 0; q < csize; ++q)
+                        nt_arrive_cluster(map_to_rank(smem_u32(&xbarA[par]), q));
+                if (!failed && !nt_wait_cluster(smem_u32(&xbarA[par]),
+                                                static_cast<uint32_t>(it >> 1) & 1u, a.timeout_ns)) {
+                    failed = true;
+                    atomicOr(&a.scratch->status, kDevErrTimeout);
+                }
             }
             float sh[E];
             int xi[E];
@@ -416,18 +423,24 @@ ce_nd_tile(const __grid_constant__ CUtensorMap map, const __grid_constant__ NdTi
                         acc.w = 1.f;
                     }
                 }
-                const uint32_t rec = smem_u32(&xB[(par * csize + crank) * P + tid]);
-                for (uint32_t q = 0; q < csize; ++q) nt_st_dsmem_f4(map_to_rank(rec, q), acc);
-                nt_fence_cluster();
+                if (csize == 1) {
+                    xB[par * P + tid] = acc;
+                } else {
+                    const uint32_t rec = smem_u32(&xB[(par * csize + crank) * P + tid]);
+                    for (uint32_t q = 0; q < csize; ++q) nt_st_dsmem_f4(map_to_rank(rec, q), acc);
+                    nt_fence_cluster();
+                }
             }
             nt_consumer_sync();
-            if (tid == 0)
-                for (uint32_t q = 0; q < csize; ++q)
-                    nt_arrive_cluster(map_to_rank(smem_u32(&xbarB[par]), q));
-            if (!failed && !nt_wait_cluster(smem_u32(&xbarB[par]),
-                                            static_cast<uint32_t>(it >> 1) & 1u, a.timeout_ns)) {
-                failed = true;
-                atomicOr(&a.scratch->status, kDevErrTimeout);
+            if (csize > 1) {
+                if (tid == 0)
+                    for (uint32_t q = 0; q < csize; ++q)
+                        nt_arrive_cluster(map_to_rank(smem_u32(&xbarB[par]), q));
+                if (!failed && !nt_wait_cluster(smem_u32(&xbarB[par]),
+                                                static_cast<uint32_t>(it >> 1) & 1u, a.timeout_ns)) {
+                    failed = true;
+                    atomicOr(&a.scratch->status, kDevErrTimeout);
+                }
             }
             // ---- per-position outputs and the gradient's coefficients
             need_counts();
