@@ -247,7 +247,12 @@ ce_status ce_fwd_shard(void* logits, int dtype, int64_t rows, int64_t V,
  * enqueues a count kernel before the forward (D and the counted positions
  * land in the library scratch of (device, stream)). Vectorised loads need
  * a 16-byte aligned base and inner a multiple of 16 / sizeof(dtype); other
- * shapes take single-element loads with the same results.
+ * shapes take single-element loads with the same results. Many classes
+ * take a form that keeps per-position records in a workspace of (device,
+ * stream) that the library allocates on first use and grows when a call
+ * needs more (growing frees the old buffer, which waits for the device);
+ * a call that must not allocate passes a stream that has already run a
+ * call of the same shape.
  */
 ce_status ce_fwd_nd(void* logits, int dtype, int64_t N, int64_t C, int64_t inner,
                     const void* target, const float* weight, int64_t ignore_index,
