@@ -510,24 +510,22 @@ ce_fwd_tmem(const __grid_constant__ FwdArgs a) {
                 const float Bc = -scale * a.eps * inv_V;
                 const float2 As4 = make_float2(4.f * As, 4.f * As);
                 const float2 Bc4 = make_float2(4.f * Bc, 4.f * Bc);
-                // one vector's r values at a time (registers)
+                // one vector's r values at a time (registers; two or four
+                // at a time measured no faster, four spilled)
                 for (int c = 0; c < nchunk; ++c) {
 #pragma unroll
-                    for (int k0 = 0; k0 < kTmVecPerThread; ++k0) {
-                    uint32_t rv[1][VE];
-                    tm_load<VE>(tbase + static_cast<uint32_t>((c * kTmVecPerThread + k0) * VE),
-                                rv[0]);
-                    tm_wait_ld();
-#pragma unroll
-                    for (int h = 0; h < 1; ++h) {
-                        const int k = k0 + h;
+                    for (int k = 0; k < kTmVecPerThread; ++k) {
+                        uint32_t rv[VE];
+                        tm_load<VE>(tbase + static_cast<uint32_t>((c * kTmVecPerThread + k) * VE),
+                                    rv);
+                        tm_wait_ld();
                         const int vl = c * kTmChunkVec + k * kTmNTC + tid;
                         if (vl < nvec) {
                             float g[VE];
 #pragma unroll
                             for (int j = 0; j < VE; j += 2) {
-                                const float2 r2 = make_float2(__uint_as_float(rv[h][j]),
-                                                              __uint_as_float(rv[h][j + 1]));
+                                const float2 r2 =
+                                    make_float2(__uint_as_float(rv[j]), __uint_as_float(rv[j + 1]));
                                 const float2 ar = fmul2(r2, make_float2(c1, c1));
                                 float2 gg = ffma2(As4, make_float2(ex2(ar.x), ex2(ar.y)), Bc4);
                                 gg = fmul2(gg, ffma2(make_float2(-r2.x, -r2.y), r2, r2));
@@ -536,7 +534,6 @@ ce_fwd_tmem(const __grid_constant__ FwdArgs a) {
                             }
                             st_v4_hint(slice + vl, VT::pack(g), spol);
                         }
-                    }
                     }
                 }
                 if (t_owner) {
