@@ -13,16 +13,19 @@
 // 2-D TMA boxes of rb class rows (one mbarrier a block of rows). Sixteen
 // consumer warps, each thread E positions (4 bytes of a class row) and every
 // (512 / (P / E))-th row:
-//  * pass A: maximum and first argmax over the CTA's classes, reduced over
-//    the row groups in shared memory and over the cluster (each CTA stores
-//    its P records into every CTA's shared memory and arrives once on its
-//    exchange barrier; bounded waits; a one-CTA tile keeps its records);
-//  * pass B: S = sum exp(x - M), the smoothing sum and x at the target, the
-//    same two reductions;
+//  * pass A: maximum over the CTA's classes (and the first argmax when
+//    predictions or accuracy are asked for), reduced over the row groups
+//    in shared memory and over the cluster (each CTA stores its P records
+//    into every CTA's shared memory and arrives once on its exchange
+//    barrier; bounded waits; a one-CTA tile keeps its records);
+//  * pass B: S = sum exp(x - M) and the smoothing sum; x at the target
+//    read once from its row; the same two reductions;
 //  * per-position outputs (rank 0 of the cluster) and the gradient's
 //    coefficients; pass C: the gradient, stored to global memory from
-//    registers, each block of rows released to the producer as the warps
-//    finish it, so the next tile's loads overlap the rest of pass C.
+//    registers, the one-hot term added where a block holds a target by
+//    the thread that stored that row, each block of rows released to the
+//    producer as the warps finish it, so the next tile's loads overlap the
+//    rest of pass C.
 // One HBM read and one write an element; the class slices stay on chip
 // between the passes. Not for softcaps or class-weighted smoothing (the
 // split kernels take those).
@@ -573,9 +576,9 @@ const void* nd_tile_kernel(int dtype, int tpr) {
 // classes in shared memory, at most max_cluster; 128-byte class rows when a
 // cluster of at most 8 does, else, with narrow_rows, 64-byte ones and up to
 // 16; of the sizes that fit, the one keeping the most SMs busy), encodes the
-// class-row tensor map and launches. Returns CE_ERR_UNSUPPORTED (nothing launched) when the
-// shape does not fit it; `after_count`: launched as a programmatic
-// dependent of the count kernel just before.
+// class-row tensor map and launches. Returns CE_ERR_UNSUPPORTED (nothing
+// launched) when the shape does not fit it; `after_count`: launched as a
+// programmatic dependent of the count kernel just before.
 ce_status nd_tile_launch(const FwdArgs& f, int dtype, int64_t N, int64_t C, int64_t inner,
                          int sm_count, int smem_optin, int max_cluster, bool narrow_rows,
                          bool after_count, cudaStream_t st) {
